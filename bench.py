@@ -1,0 +1,420 @@
+"""Benchmark of the GEMM hot path: C = alpha * A @ B + beta * C at M = N = K = 4096.
+
+One step is one pass of the whole path on one batch of inputs: the f32 SIMT GEMM
+(phx_sgemm) and the f16-tensor-core / f32-accumulate GEMM (phx_gemm_f16tc_f32acc, i.e.
+its f32 -> f16 cast pass plus the tcgen05 GEMM), both with alpha = 1, beta = 0.5, on the
+same synthetic A and B (uniform [-1, 1), splitmix64, seed 0) and each on its own C.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line.  `value` is the whole job's GEMM throughput, sum of 2MNK over the
+GEMMs of all steps on all ranks divided by the slowest rank's summed device time of its
+steps (CUDA events on the launching stream; L2 flushed between steps, outside the events).
+`e2e` is the same metric through the public C ABI with host buffers: the pinned-host copies
+of the step's inputs in, the GEMMs, and the results back out, all inside the timed region.
+`roofline` places the dominant kernel (the f32 SIMT GEMM) against the FP32 issue rate of
+the SMs; `roofline_tc_gemm` and `roofline_cast` place the tensor-core GEMM kernel and the
+cast pass against the measured tensor and HBM peaks.  `cpu_baseline` times the CPU oracle
+on a bounded sample of the same workload.
+
+--impl reference times that oracle as the reference arm (there is no runnable reference
+implementation: the pages describe their kernels but ship no library).
+
+The path does not shard in this build, so with N GPUs each rank runs its own replica of
+the step (no collective on the data path) and `scaling` is "weak".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s (2MNK/t) at M=N=K=4096, f32 SIMT & f16-TC/f32-acc; % of peak"
+M = N = K = 4096
+ALPHA, BETA = 1.0, 0.5
+FLOPS_PER_GEMM = 2.0 * M * N * K
+GEMMS_PER_STEP = 2
+WORKLOAD = ("C = alpha*A@B + beta*C, M=N=K=4096, alpha=1, beta=0.5, row-major f32; "
+            "one step = phx_sgemm (f32 SIMT) + phx_gemm_f16tc_f32acc (f16 tensor cores, f32 acc)")
+DATA = "synthetic: A, B, C i.i.d. uniform[-1,1) f32 from splitmix64, seed 0 (no dataset involved)"
+FP32_LANES_PER_SM = 128  # FP32 multiply-add lanes per SM on sm_100-family GPUs
+
+
+def _dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "sm_max_mhz": float(p.get("sm_max_mhz", 2070.0)), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "sm_max_mhz": 2070.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self._t.join(timeout=5)
+
+    def summary(self):
+        sm, mx, pw, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+                pw.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "power_w_max": max(pw),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _oracle_sample(seconds_target: float, max_rows: int | None = None):
+    """Time the CPU oracle on leading row blocks of the workload (both variants) and return
+    (TFLOP/s, rows used, seconds, threads).  The oracle is used exactly as it stands."""
+    import oracle
+    from dense_gemm_04_gb300 import synth
+    oracle.build()
+    B = synth.matrix(K, N, seed=0, tensor=synth.TENSOR_B)
+    A_full = synth.matrix(M, K, seed=0, tensor=synth.TENSOR_A)
+    C_full = synth.matrix(M, N, seed=0, tensor=synth.TENSOR_C)
+
+    def run(rows):
+        t0 = time.perf_counter()
+        oracle.gemm(A_full[:rows], B, C_full[:rows], ALPHA, BETA, f16_inputs=False, want_mag=False)
+        oracle.gemm(A_full[:rows], B, C_full[:rows], ALPHA, BETA, f16_inputs=True, want_mag=False)
+        return time.perf_counter() - t0
+
+    probe_rows = 32
+    t = run(probe_rows)
+    rows = int(probe_rows * seconds_target / max(t, 1e-3))
+    rows = max(probe_rows, min(rows, max_rows or M, M))
+    t = run(rows)
+    flops = GEMMS_PER_STEP * 2.0 * rows * N * K
+    return flops / t / 1e12, rows, t, oracle.num_threads()
+
+
+def reference_arm(args):
+    ws, rank, _ = _dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    from dense_gemm_04_gb300 import synth
+    oracle.build()
+    B = synth.matrix(K, N, seed=0, tensor=synth.TENSOR_B)
+    A_full = synth.matrix(M, K, seed=0, tensor=synth.TENSOR_A)
+    C_full = synth.matrix(M, N, seed=0, tensor=synth.TENSOR_C)
+    rows = args.reference_rows
+
+    def step():
+        oracle.gemm(A_full[:rows], B, C_full[:rows], ALPHA, BETA, f16_inputs=False, want_mag=False)
+        oracle.gemm(A_full[:rows], B, C_full[:rows], ALPHA, BETA, f16_inputs=True, want_mag=False)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    t = time.perf_counter() - t0
+    flops = args.steps * GEMMS_PER_STEP * 2.0 * rows * N * K
+    value = flops / t / 1e12
+    sample = (f"each step: the oracle on the first {rows} of {M} rows of both GEMMs of the "
+              f"workload ({rows}x{N}x{K}, f32 and f16-rounded inputs, float64 sums)")
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+           "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": DATA,
+           "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "alpha": ALPHA, "beta": BETA,
+                      "reference": "CPU oracle (plain float64 triple loop, OpenMP over rows)"},
+           "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                            "kind": "oracle", "sample": sample},
+           "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+def _traffic_from_profiles(kernel: str):
+    """DRAM bytes per launch recorded from an ncu capture, if the kernel's source is
+    unchanged since (profiles/dram_traffic.txt: kernel, bytes per launch, source hash)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = {"sgemm": "sgemm_simt.cu", "tc_gemm": "gemm_f16tc.cu", "f16_cast": "gemm_f16tc.cu"}[kernel]
+    with open(os.path.join(ROOT, "dense_gemm_04_gb300", "csrc", src), "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    with open(path) as f:
+        for line in f:
+            p = line.split()
+            if len(p) >= 3 and not line.startswith("#") and p[0] == kernel and p[2] == h:
+                return float(p[1])
+    return None
+
+
+def gpu_arm(args):
+    import torch
+    import torch.distributed as dist
+    from dense_gemm_04_gb300 import phx, synth
+
+    ws, rank, local = _dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    props = torch.cuda.get_device_properties(local)
+    sms = props.multi_processor_count
+    peaks = _peaks()
+
+    # inputs resident in HBM before any timing
+    hA = synth.matrix(M, K, seed=0, tensor=synth.TENSOR_A)
+    hB = synth.matrix(K, N, seed=0, tensor=synth.TENSOR_B)
+    hC = synth.matrix(M, N, seed=0, tensor=synth.TENSOR_C)
+    A = torch.from_numpy(hA).to(dev)
+    B = torch.from_numpy(hB).to(dev)
+    C32 = torch.from_numpy(hC).to(dev)
+    C16 = C32.clone()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)   # > 129 MB L2
+
+    def step():
+        phx.check(phx.phx_sgemm(M, N, K, ALPHA, A.data_ptr(), B.data_ptr(), BETA, C32.data_ptr(), sh))
+        phx.check(phx.phx_gemm_f16tc_f32acc(M, N, K, ALPHA, A.data_ptr(), B.data_ptr(), BETA,
+                                            C16.data_ptr(), sh))
+
+    # settle the clocks under the same work, then the W warm-up steps (all untimed)
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < args.settle_s:
+        step()
+        torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        phx.profile_start()
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)                   # evict L2 (outside the step's events)
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+        prof = phx.profile_stop()
+    if ws > 1:
+        dist.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_s = sum(step_ms) / 1e3
+    total_t = torch.tensor([total_s], dtype=torch.float64, device=dev)
+    if ws > 1:
+        dist.all_reduce(total_t, op=dist.ReduceOp.MAX)
+    max_s = float(total_t.item())
+    launches = sum(n for n, _ in prof.values())
+    st = phx.check_device_status()
+    if st != phx.PHX_OK:
+        raise RuntimeError(f"device status after the timed steps: {phx.status_string(st)}")
+
+    # end to end through the public C ABI with host buffers: copies inside the timed region
+    pA, pB = torch.from_numpy(hA).pin_memory(), torch.from_numpy(hB).pin_memory()
+    pC = torch.from_numpy(hC).pin_memory()
+    out32 = torch.empty_like(pC).pin_memory()
+    out16 = torch.empty_like(pC).pin_memory()
+    dA, dB = torch.empty_like(A), torch.empty_like(B)
+    dC32, dC16 = torch.empty_like(C32), torch.empty_like(C32)
+
+    def e2e_step():
+        dA.copy_(pA, non_blocking=True)
+        dB.copy_(pB, non_blocking=True)
+        dC32.copy_(pC, non_blocking=True)
+        dC16.copy_(pC, non_blocking=True)
+        phx.check(phx.phx_sgemm(M, N, K, ALPHA, dA.data_ptr(), dB.data_ptr(), BETA, dC32.data_ptr(), sh))
+        phx.check(phx.phx_gemm_f16tc_f32acc(M, N, K, ALPHA, dA.data_ptr(), dB.data_ptr(), BETA,
+                                            dC16.data_ptr(), sh))
+        out32.copy_(dC32, non_blocking=True)
+        out16.copy_(dC16, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(3, min(args.steps, 10))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = e0.elapsed_time(e1) / 1e3
+    e2e_t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+    if ws > 1:
+        dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
+    h2d = M * K * 4 + K * N * 4 + 2 * M * N * 4
+    d2h = 2 * M * N * 4
+
+    if rank != 0:
+        if ws > 1:
+            dist.destroy_process_group()
+        return 0
+
+    flops_total = ws * args.steps * GEMMS_PER_STEP * FLOPS_PER_GEMM
+    value = flops_total / max_s / 1e12
+    clocks = clk.summary()
+    sm_max = clocks.get("sm_max_mhz") or peaks["sm_max_mhz"]
+
+    def per_launch_ms(kind):
+        n, ms = prof[kind]
+        return ms / n if n else None
+
+    sg_ms = per_launch_ms("sgemm")
+    tc_ms = per_launch_ms("tc_gemm")
+    cast_ms = per_launch_ms("f16_cast")
+    fp32_peak = sms * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
+    run_mhz = clocks.get("sm_mhz")
+    sg_tflops = FLOPS_PER_GEMM / (sg_ms / 1e3) / 1e12
+    roofline = {"bound": "alu", "kernel": "sgemm (f32 SIMT, FFMA)", "achieved": sg_tflops,
+                "peak": fp32_peak, "unit": "TFLOP/s", "frac": sg_tflops / fp32_peak,
+                "traffic": _traffic_from_profiles("sgemm"),
+                "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 FLOP x {sm_max:.0f} MHz (max SM clock)",
+                "algorithmic_bytes": 4.0 * (M * K + K * N + 2 * M * N)}
+    if run_mhz:
+        roofline["frac_at_run_clock"] = sg_tflops / (sms * FP32_LANES_PER_SM * 2 * run_mhz * 1e6 / 1e12)
+    tc_tflops = FLOPS_PER_GEMM / (tc_ms / 1e3) / 1e12
+    tc_peak = peaks["bf16_tflops_sustained"]
+    roofline_tc = {"bound": "tensor", "kernel": "tcgen05 f16 GEMM (f32 accumulate)", "achieved": tc_tflops,
+                   "peak": tc_peak, "unit": "TFLOP/s", "frac": tc_tflops / tc_peak,
+                   "traffic": _traffic_from_profiles("tc_gemm"),
+                   "peak_source": f"{peaks['source']} bf16 sustained (dense f16 = bf16 rate)",
+                   "algorithmic_bytes": 2.0 * (M * K + K * N) + 4.0 * 2 * M * N}
+    cast_bytes = 6.0 * (M * K + K * N)
+    cast_gbs = cast_bytes / (cast_ms / 1e3) / 1e9
+    roofline_cast = {"bound": "hbm", "kernel": "f32->f16 cast pass (A and B, 2 launches)", "achieved": cast_gbs,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": cast_gbs / peaks["hbm_gbs"],
+                     "traffic": _traffic_from_profiles("f16_cast"), "algorithmic_bytes": cast_bytes}
+    f16_ms = tc_ms + cast_ms
+    variants = {
+        "sgemm": {"tflops": sg_tflops, "ms": sg_ms, "config": phx.get_config(0, M, N, K)},
+        "f16tc_f32acc": {"tflops": FLOPS_PER_GEMM / (f16_ms / 1e3) / 1e12, "ms": f16_ms,
+                         "gemm_kernel_ms": tc_ms, "cast_ms": cast_ms,
+                         "frac_of_tensor_peak": FLOPS_PER_GEMM / (f16_ms / 1e3) / 1e12 / tc_peak,
+                         "config": phx.get_config(1, M, N, K)},
+    }
+    cpu = None
+    if ws == 1 and not args.no_cpu_baseline:
+        v, rows, t, cores = _oracle_sample(args.cpu_seconds)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": f"the oracle on the first {rows} of {M} rows of both GEMMs of the workload "
+                         f"({rows}x{N}x{K} each, f32 and f16-rounded inputs), {t:.1f} s"}
+    out = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * max_s / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32 (SIMT) + f16xf16->f32 (tensor cores)",
+        "data": DATA,
+        "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "alpha": ALPHA, "beta": BETA,
+                   "l2": "flushed between steps by a 512 MiB write outside the step's events",
+                   "settle_s": args.settle_s, "parallelism": f"replicas x{ws} (no collective)"},
+        "variants": variants,
+        "roofline": roofline,
+        "roofline_tc_gemm": roofline_tc,
+        "roofline_cast": roofline_cast,
+        "cpu_baseline": cpu,
+        "e2e": {"value": ws * e2e_steps * GEMMS_PER_STEP * FLOPS_PER_GEMM / float(e2e_t.item()) / 1e12,
+                "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps},
+        "clocks": clocks,
+        "gpu_launches": launches,
+        "kernel_launches": {k: v[0] for k, v in prof.items()},
+        "wall_s_timed_region": wall,
+        "peaks": peaks,
+    }
+    print(json.dumps(out), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["phx", "reference"], default="phx")
+    ap.add_argument("--settle-s", type=float, default=1.0, help="untimed settle time before warm-up")
+    ap.add_argument("--cpu-seconds", type=float, default=8.0, help="target CPU seconds of the oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--reference-rows", type=int, default=64,
+                    help="rows of the workload the reference arm's oracle evaluates per step")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return reference_arm(args)
+    return gpu_arm(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

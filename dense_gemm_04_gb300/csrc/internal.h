@@ -1,0 +1,82 @@
+// internal.h -- declarations shared by the translation units of libphx (not installed).
+//
+// The C ABI lives in include/phx.h; this header is the contract between phx_api.cu (argument
+// checks, dispatch, configuration, tuning) and the kernel files sgemm_simt.cu,
+// gemm_f16tc.cu and probes.cu.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace phx {
+
+// Status codes written into the per-device status word by kernels (0 = nothing to report).
+enum DeviceStatus : unsigned int {
+    kDevOk = 0,
+    kDevTimeout = 1,
+};
+
+// ---------------------------------------------------------------------------------------
+// f32 SIMT GEMM (sgemm_simt.cu)
+// ---------------------------------------------------------------------------------------
+struct SgemmConfig {
+    int tile_m, tile_n, tile_k, stages, fma2;
+};
+
+int sgemm_num_configs();
+const SgemmConfig& sgemm_config(int index);
+
+// True if the aligned (unmasked, 16-byte vector) kernel of config `index` may run on this
+// problem: every dimension a whole number of tiles and A, B, C 16-byte aligned.
+bool sgemm_is_aligned(int index, int64_t M, int64_t N, int64_t K, const float* A,
+                      const float* B, const float* C);
+
+// Enqueue config `index` (aligned or masked kernel as decided by sgemm_is_aligned).
+// Requires M, N > 0, K > 0 and alpha != 0 (the caller handles the degenerate cases).
+cudaError_t sgemm_launch(int index, int64_t M, int64_t N, int64_t K, float alpha,
+                         const float* A, const float* B, float beta, float* C,
+                         cudaStream_t stream);
+
+// C <- beta * C (beta == 0: C <- 0 without reading C).  Used for K == 0 or alpha == 0.
+cudaError_t scale_c_launch(int64_t M, int64_t N, float beta, float* C, cudaStream_t stream);
+
+// ---------------------------------------------------------------------------------------
+// f16 tensor-core GEMM with f32 accumulation (gemm_f16tc.cu)
+// ---------------------------------------------------------------------------------------
+struct F16Config {
+    int tile_m, tile_n, tile_k, stages;
+};
+
+int f16tc_num_configs();
+const F16Config& f16tc_config(int index);
+
+// Bytes of workspace for the rounded operands: A as M x Kp f16 and B transposed as
+// N x Kp f16, Kp = K rounded up to a multiple of 8, each part 256-byte aligned.
+size_t f16tc_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+// Enqueue the cast pass: A -> rounded f16 A (M x Kp) and B -> rounded, transposed f16 B
+// (N x Kp) in `workspace` (f16tc_workspace_bytes(M, N, K) bytes, 256-byte aligned).
+cudaError_t f16tc_cast_launch(int64_t M, int64_t N, int64_t K, const float* A, const float* B,
+                              void* workspace, int num_sms, cudaStream_t stream);
+
+// Enqueue the tcgen05 GEMM of config `index` on the cast operands in `workspace`;
+// `status` is the device status word; `num_sms` bounds the persistent grid.  Requires
+// M, N, K > 0 and alpha != 0.
+cudaError_t f16tc_gemm_launch(int index, int64_t M, int64_t N, int64_t K, float alpha, float beta,
+                              float* C, const void* workspace, unsigned int* status, int num_sms,
+                              cudaStream_t stream);
+
+// ---------------------------------------------------------------------------------------
+// Probes and self-tests (probes.cu)
+// ---------------------------------------------------------------------------------------
+cudaError_t probe_ffma_launch(int packed, int64_t blocks, int iters, float* out,
+                              cudaStream_t stream);
+cudaError_t probe_stream_read_launch(const float* x, int64_t n, float* sink, int64_t blocks,
+                                     cudaStream_t stream);
+cudaError_t probe_mma_f16_launch(int64_t ctas, int iters, int n, float* sink,
+                                 unsigned int* status, cudaStream_t stream);
+cudaError_t selftest_wait_launch(uint64_t limit_ns, unsigned int* status,
+                                 cudaStream_t stream);
+
+}  // namespace phx

@@ -1,0 +1,706 @@
+// phx_api.cu -- the C ABI of libphx (include/phx.h): argument checks, per-device state,
+// configuration choice, the autotuner, and the device status word.
+//
+// The operation and its argument list follow the kernel signature of "gemm, f32"
+// (phobos-lang.dev/docs/examples/gemm-fp32/): gemm(A: tensor<f32>[M, K], B: tensor<f32>[K, N],
+// C: tensor<f32>[M, N], alpha: f32, beta: f32).  The pages' launcher traps when the @aligned
+// promise is broken ("The attributes", @aligned row); this library instead checks every
+// argument on the host, returns an error code without launching anything, and sends
+// shapes that are not whole tiles to the masked kernels.  The tuner follows "gemm, f32",
+// section "Tuning" (two stages, finalists timed over rounds under the same clocks) and the
+// lab's stopwatches (settle the clock before timing; shuffle the order every round).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <chrono>
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <fstream>
+#include <functional>
+#include <map>
+#include <mutex>
+#include <numeric>
+#include <random>
+#include <sstream>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "../../include/phx.h"
+#include "internal.h"
+
+namespace {
+
+using phx::F16Config;
+using phx::SgemmConfig;
+
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+constexpr int64_t kMaxElems = int64_t(1) << 62;
+
+int log_level() {
+    static const int level = [] {
+        const char* v = std::getenv("PHX_LOG");
+        return v ? std::atoi(v) : 0;
+    }();
+    return level;
+}
+
+// ---------------------------------------------------------------------------------------
+// Per-device state: SM count, the status word, and the workspace pool.
+// ---------------------------------------------------------------------------------------
+struct DevState {
+    bool ready = false;
+    phx_status init_status = PHX_OK;
+    int sm_count = 0;
+    unsigned int* status = nullptr;  // device word written by kernels
+    cudaMemPool_t pool = nullptr;
+};
+
+std::mutex g_mu;
+std::map<int, DevState> g_dev;
+
+phx_status device_state(DevState** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return PHX_ERR_ARCH;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    DevState& d = g_dev[dev];
+    if (!d.ready) {
+        d.ready = true;
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            d.init_status = PHX_ERR_ARCH;
+        } else if (major != 10 || minor != 3) {
+            d.init_status = PHX_ERR_ARCH;  // the kernels are built for sm_103a only
+        } else if (cudaMalloc(&d.status, 256) != cudaSuccess ||
+                   cudaMemset(d.status, 0, 256) != cudaSuccess) {
+            cudaGetLastError();
+            d.init_status = PHX_ERR_NOMEM;
+        } else {
+            cudaMemPoolProps props;
+            std::memset(&props, 0, sizeof props);
+            props.allocType = cudaMemAllocationTypePinned;
+            props.location.type = cudaMemLocationTypeDevice;
+            props.location.id = dev;
+            if (cudaMemPoolCreate(&d.pool, &props) != cudaSuccess) {
+                cudaGetLastError();
+                d.init_status = PHX_ERR_NOMEM;
+            } else {
+                uint64_t keep = UINT64_MAX;  // keep freed workspace for reuse
+                cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+            }
+        }
+    }
+    *out = &d;
+    return d.init_status;
+}
+
+// ---------------------------------------------------------------------------------------
+// Argument checks
+// ---------------------------------------------------------------------------------------
+bool overlaps(const void* a, int64_t abytes, const void* b, int64_t bbytes) {
+    if (abytes <= 0 || bbytes <= 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + static_cast<uintptr_t>(bbytes) && b0 < a0 + static_cast<uintptr_t>(abytes);
+}
+
+phx_status validate_sizes(int64_t M, int64_t N, int64_t K) {
+    if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+        return PHX_ERR_INVALID;
+    if (M * K >= kMaxElems || K * N >= kMaxElems || M * N >= kMaxElems) return PHX_ERR_INVALID;
+    return PHX_OK;
+}
+
+phx_status validate(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C) {
+    if (validate_sizes(M, N, K) != PHX_OK) return PHX_ERR_INVALID;
+    if (M == 0 || N == 0) return PHX_OK;
+    auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) != 0; };
+    if (C == nullptr || misaligned(C)) return PHX_ERR_INVALID;
+    if (K > 0) {
+        if (A == nullptr || B == nullptr || misaligned(A) || misaligned(B)) return PHX_ERR_INVALID;
+        if (overlaps(A, M * K * 4, C, M * N * 4) || overlaps(B, K * N * 4, C, M * N * 4))
+            return PHX_ERR_INVALID;
+    }
+    return PHX_OK;
+}
+
+// ---------------------------------------------------------------------------------------
+// Configurations: names, parsing, pins, the tuning cache, defaults
+// ---------------------------------------------------------------------------------------
+int num_configs(int variant) {
+    if (variant == PHX_VARIANT_SGEMM) return phx::sgemm_num_configs();
+    if (variant == PHX_VARIANT_F16TC) return phx::f16tc_num_configs();
+    return -1;
+}
+
+std::string config_name(int variant, int i) {
+    char buf[128];
+    if (variant == PHX_VARIANT_SGEMM) {
+        const SgemmConfig& c = phx::sgemm_config(i);
+        std::snprintf(buf, sizeof buf, "TILE_M=%d TILE_N=%d TILE_K=%d STAGES=%d FMA2=%d", c.tile_m,
+                      c.tile_n, c.tile_k, c.stages, c.fma2);
+    } else {
+        const F16Config& c = phx::f16tc_config(i);
+        std::snprintf(buf, sizeof buf, "TILE_M=%d TILE_N=%d TILE_K=%d STAGES=%d", c.tile_m, c.tile_n,
+                      c.tile_k, c.stages);
+    }
+    return buf;
+}
+
+// Parse "KEY=value KEY=value ..." and return the first compiled config that matches every
+// given key (TILE_M, TILE_N, TILE_K required; STAGES and FMA2 optional), or -1.
+int parse_config(int variant, const char* spec) {
+    if (spec == nullptr) return -1;
+    std::map<std::string, int> kv;
+    std::istringstream in(spec);
+    std::string tok;
+    while (in >> tok) {
+        const size_t eq = tok.find('=');
+        if (eq == std::string::npos || eq == 0 || eq + 1 >= tok.size()) return -1;
+        const std::string key = tok.substr(0, eq);
+        const std::string val = tok.substr(eq + 1);
+        char* end = nullptr;
+        const long v = std::strtol(val.c_str(), &end, 10);
+        if (end == nullptr || *end != '\0') return -1;
+        if (key != "TILE_M" && key != "TILE_N" && key != "TILE_K" && key != "STAGES" && key != "FMA2")
+            return -1;
+        if (variant == PHX_VARIANT_F16TC && key == "FMA2") return -1;
+        kv[key] = static_cast<int>(v);
+    }
+    if (!kv.count("TILE_M") || !kv.count("TILE_N") || !kv.count("TILE_K")) return -1;
+    const int n = num_configs(variant);
+    for (int i = 0; i < n; ++i) {
+        int tm, tn, tk, st, f2 = 0;
+        if (variant == PHX_VARIANT_SGEMM) {
+            const SgemmConfig& c = phx::sgemm_config(i);
+            tm = c.tile_m; tn = c.tile_n; tk = c.tile_k; st = c.stages; f2 = c.fma2;
+        } else {
+            const F16Config& c = phx::f16tc_config(i);
+            tm = c.tile_m; tn = c.tile_n; tk = c.tile_k; st = c.stages;
+        }
+        if (kv["TILE_M"] != tm || kv["TILE_N"] != tn || kv["TILE_K"] != tk) continue;
+        if (kv.count("STAGES") && kv["STAGES"] != st) continue;
+        if (kv.count("FMA2") && kv["FMA2"] != f2) continue;
+        if (!kv.count("FMA2") && variant == PHX_VARIANT_SGEMM && f2 != 0) continue;
+        return i;
+    }
+    return -1;
+}
+
+using ShapeKey = std::tuple<int, int64_t, int64_t, int64_t>;
+std::map<ShapeKey, int> g_tuned;  // guarded by g_mu
+int g_pin[2] = {-1, -1};          // guarded by g_mu
+bool g_env_done = false;
+
+void load_env_once_locked() {
+    if (g_env_done) return;
+    g_env_done = true;
+    if (const char* s = std::getenv("PHX_CONFIG_SGEMM")) g_pin[0] = parse_config(PHX_VARIANT_SGEMM, s);
+    if (const char* s = std::getenv("PHX_CONFIG_F16TC")) g_pin[1] = parse_config(PHX_VARIANT_F16TC, s);
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Defaults when nothing is pinned or tuned: the largest tile that still gives every SM
+// work (the trade-off "gemm, f32" section "Tuning" describes: larger tiles reuse more,
+// but leave fewer CTAs to spread over the card).
+int default_config(int variant, int64_t M, int64_t N, int sms) {
+    if (variant == PHX_VARIANT_SGEMM) {
+        const int64_t slots = 2 * static_cast<int64_t>(sms);  // two CTAs per SM
+        if (ceil_div(M, 128) * ceil_div(N, 128) >= slots) return parse_config(variant, "TILE_M=128 TILE_N=128 TILE_K=16 STAGES=4 FMA2=1");
+        if (ceil_div(M, 128) * ceil_div(N, 64) >= slots) return parse_config(variant, "TILE_M=128 TILE_N=64 TILE_K=8 STAGES=4");
+        return parse_config(variant, "TILE_M=64 TILE_N=64 TILE_K=8 STAGES=4");
+    }
+    if (ceil_div(M, 128) * ceil_div(N, 256) >= sms) return parse_config(variant, "TILE_M=128 TILE_N=256 TILE_K=64 STAGES=4");
+    if (ceil_div(M, 128) * ceil_div(N, 128) >= sms) return parse_config(variant, "TILE_M=128 TILE_N=128 TILE_K=64 STAGES=6");
+    return parse_config(variant, "TILE_M=128 TILE_N=64 TILE_K=64 STAGES=8");
+}
+
+int choose_config(int variant, int64_t M, int64_t N, int64_t K, int sms) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    load_env_once_locked();
+    if (g_pin[variant] >= 0) return g_pin[variant];
+    auto it = g_tuned.find(ShapeKey(variant, M, N, K));
+    if (it != g_tuned.end()) return it->second;
+    return default_config(variant, M, N, sms);
+}
+
+// ---------------------------------------------------------------------------------------
+// The tuner's selection logic, shared by phx_autotune and phx_selftest_tuner.
+// measure(i) returns the seconds one launch of candidate i took, or a negative value if
+// the candidate failed (it is then dropped); elapsed() is the clock the settle phase uses.
+// ---------------------------------------------------------------------------------------
+struct TuneOutcome {
+    int picked = -1;
+    int64_t launches = 0;
+};
+
+double median(std::vector<double> v) {
+    std::sort(v.begin(), v.end());
+    const size_t n = v.size();
+    return n == 0 ? 0.0 : (n % 2 ? v[n / 2] : 0.5 * (v[n / 2 - 1] + v[n / 2]));
+}
+
+TuneOutcome tune_select(int n, const std::function<double(int)>& measure,
+                        const std::function<double()>& elapsed, int finalists, int rounds,
+                        double settle_s, uint64_t seed) {
+    TuneOutcome out;
+    auto run = [&](int i) {
+        ++out.launches;
+        return measure(i);
+    };
+    // Stage 1: every candidate, one warm-up launch and three timed ones; failures dropped.
+    std::vector<std::pair<double, int>> scored;
+    for (int i = 0; i < n; ++i) {
+        if (run(i) < 0) continue;
+        std::vector<double> t;
+        bool failed = false;
+        for (int r = 0; r < 3 && !failed; ++r) {
+            const double s = run(i);
+            if (s < 0) failed = true;
+            t.push_back(s);
+        }
+        if (!failed) scored.emplace_back(median(t), i);
+    }
+    if (scored.empty()) return out;
+    std::sort(scored.begin(), scored.end());
+    const int k = std::max(1, std::min<int>(finalists, static_cast<int>(scored.size())));
+    std::vector<int> fin;
+    for (int j = 0; j < k; ++j) fin.push_back(scored[j].second);
+    // Stage 2a: settle the clocks on the finalists' own work.
+    const double t0 = elapsed();
+    while (elapsed() - t0 < settle_s)
+        for (int i : fin) run(i);
+    // Stage 2b: `rounds` rounds, one launch of each finalist per round, shuffled each round.
+    std::mt19937_64 rng(seed);
+    std::map<int, std::vector<double>> times;
+    std::map<int, bool> dropped;
+    for (int r = 0; r < std::max(1, rounds); ++r) {
+        std::vector<int> order = fin;
+        std::shuffle(order.begin(), order.end(), rng);
+        for (int i : order) {
+            if (dropped[i]) continue;
+            const double s = run(i);
+            if (s < 0) dropped[i] = true;
+            else times[i].push_back(s);
+        }
+    }
+    double best = 0.0;
+    for (int i : fin) {
+        if (dropped[i] || times[i].empty()) continue;
+        const double m = median(times[i]);
+        if (out.picked < 0 || m < best) {
+            best = m;
+            out.picked = i;
+        }
+    }
+    return out;
+}
+
+// Fill n floats with small values (uniform-ish in [-1, 1)) for the tuner's scratch inputs.
+__global__ void tune_fill_kernel(float* p, int64_t n, uint32_t salt) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+        uint32_t h = static_cast<uint32_t>(i) * 2654435761u ^ salt;
+        h ^= h >> 15;
+        h *= 2246822519u;
+        h ^= h >> 13;
+        p[i] = static_cast<float>(h >> 8) * (1.0f / 8388608.0f) - 1.0f;
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// Per-kernel timing (phx_profile_start / phx_profile_stop): events recorded on the call's
+// stream around every kernel the library launches, summed per kernel kind at stop.
+// ---------------------------------------------------------------------------------------
+enum KernelKind { kKindSgemm = 0, kKindCast = 1, kKindTcGemm = 2, kKindScale = 3, kNumKinds = 4 };
+
+struct Profile {
+    bool on = false;
+    std::vector<std::tuple<int, cudaEvent_t, cudaEvent_t>> marks;  // kind, begin, end
+    std::vector<cudaEvent_t> spare;
+};
+std::mutex g_prof_mu;
+Profile g_prof;
+
+cudaEvent_t prof_event() {
+    if (!g_prof.spare.empty()) {
+        cudaEvent_t e = g_prof.spare.back();
+        g_prof.spare.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+
+// Runs `launch` on `stream`, bracketed by events when profiling is on.
+template <class F>
+cudaError_t timed(int kind, cudaStream_t stream, F&& launch) {
+    std::unique_lock<std::mutex> lock(g_prof_mu);
+    if (!g_prof.on) {
+        lock.unlock();
+        return launch();
+    }
+    cudaEvent_t b = prof_event(), e = prof_event();
+    cudaEventRecord(b, stream);
+    const cudaError_t err = launch();
+    cudaEventRecord(e, stream);
+    g_prof.marks.emplace_back(kind, b, e);
+    return err;
+}
+
+phx_status launch_variant(int variant, int cfg, int64_t M, int64_t N, int64_t K, float alpha,
+                          const float* A, const float* B, float beta, float* C, DevState* d,
+                          cudaStream_t stream) {
+    if (variant == PHX_VARIANT_SGEMM) {
+        return timed(kKindSgemm, stream, [&] {
+                   return phx::sgemm_launch(cfg, M, N, K, alpha, A, B, beta, C, stream);
+               }) == cudaSuccess
+                   ? PHX_OK : PHX_ERR_LAUNCH;
+    }
+    const size_t bytes = phx::f16tc_workspace_bytes(M, N, K);
+    void* ws = nullptr;
+    if (cudaMallocFromPoolAsync(&ws, bytes, d->pool, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return PHX_ERR_NOMEM;
+    }
+    cudaError_t err = timed(kKindCast, stream, [&] {
+        return phx::f16tc_cast_launch(M, N, K, A, B, ws, d->sm_count, stream);
+    });
+    if (err == cudaSuccess)
+        err = timed(kKindTcGemm, stream, [&] {
+            return phx::f16tc_gemm_launch(cfg, M, N, K, alpha, beta, C, ws, d->status, d->sm_count, stream);
+        });
+    cudaFreeAsync(ws, stream);
+    return err == cudaSuccess ? PHX_OK : PHX_ERR_LAUNCH;
+}
+
+phx_status gemm_entry(int variant, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+                      const float* B, float beta, float* C, cudaStream_t stream) {
+    phx_status st = validate(M, N, K, A, B, C);
+    if (st != PHX_OK) return st;
+    if (M == 0 || N == 0) return PHX_OK;
+    DevState* d = nullptr;
+    st = device_state(&d);
+    if (st != PHX_OK) return st;
+    if (K == 0 || alpha == 0.f) {
+        if (beta == 1.f) return PHX_OK;
+        return timed(kKindScale, stream, [&] { return phx::scale_c_launch(M, N, beta, C, stream); }) ==
+                       cudaSuccess
+                   ? PHX_OK : PHX_ERR_LAUNCH;
+    }
+    const int cfg = choose_config(variant, M, N, K, d->sm_count);
+    if (cfg < 0) return PHX_ERR_INTERNAL;
+    if (log_level() >= 2)
+        std::fprintf(stderr, "[phx] variant %d (%lld,%lld,%lld): %s\n", variant, (long long)M,
+                     (long long)N, (long long)K, config_name(variant, cfg).c_str());
+    return launch_variant(variant, cfg, M, N, K, alpha, A, B, beta, C, d, stream);
+}
+
+phx_status copy_name(const std::string& s, char* buf, size_t buflen) {
+    if (buf == nullptr || buflen == 0) return PHX_ERR_INVALID;
+    if (s.size() + 1 > buflen) return PHX_ERR_INVALID;
+    std::memcpy(buf, s.c_str(), s.size() + 1);
+    return PHX_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* phx_version(void) { return "phx 0.1 (sm_103a)"; }
+
+const char* phx_status_string(phx_status s) {
+    switch (s) {
+        case PHX_OK: return "PHX_OK";
+        case PHX_ERR_INVALID: return "PHX_ERR_INVALID: invalid argument";
+        case PHX_ERR_ARCH: return "PHX_ERR_ARCH: no sm_103 device";
+        case PHX_ERR_LAUNCH: return "PHX_ERR_LAUNCH: CUDA call or kernel launch failed";
+        case PHX_ERR_TIMEOUT: return "PHX_ERR_TIMEOUT: a device-side wait gave up";
+        case PHX_ERR_NOMEM: return "PHX_ERR_NOMEM: workspace allocation failed";
+        case PHX_ERR_INTERNAL: return "PHX_ERR_INTERNAL: library invariant failed";
+        case PHX_ERR_CONFIG: return "PHX_ERR_CONFIG: unknown or unparsable configuration";
+    }
+    return "unknown phx_status";
+}
+
+phx_status phx_validate_args(int64_t M, int64_t N, int64_t K, const void* A, const void* B,
+                             const void* C) {
+    return validate(M, N, K, A, B, C);
+}
+
+phx_status phx_sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float* A, const float* B,
+                     float beta, float* C, phx_stream_t stream) {
+    return gemm_entry(PHX_VARIANT_SGEMM, M, N, K, alpha, A, B, beta, C, stream);
+}
+
+phx_status phx_gemm_f16tc_f32acc(int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+                                 const float* B, float beta, float* C, phx_stream_t stream) {
+    return gemm_entry(PHX_VARIANT_F16TC, M, N, K, alpha, A, B, beta, C, stream);
+}
+
+phx_status phx_f16tc_workspace_bytes(int64_t M, int64_t N, int64_t K, size_t* bytes) {
+    if (bytes == nullptr || M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+        return PHX_ERR_INVALID;
+    *bytes = phx::f16tc_workspace_bytes(M, N, K);
+    return PHX_OK;
+}
+
+phx_status phx_check_device_status(phx_stream_t stream) {
+    DevState* d = nullptr;
+    phx_status st = device_state(&d);
+    if (st != PHX_OK) return st;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) {
+        cudaGetLastError();
+        return PHX_ERR_LAUNCH;
+    }
+    unsigned int word = 0;
+    if (cudaMemcpy(&word, d->status, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemset(d->status, 0, sizeof word) != cudaSuccess) {
+        cudaGetLastError();
+        return PHX_ERR_LAUNCH;
+    }
+    return (word & phx::kDevTimeout) ? PHX_ERR_TIMEOUT : PHX_OK;
+}
+
+phx_status phx_profile_start(void) {
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    for (auto& m : g_prof.marks) {
+        g_prof.spare.push_back(std::get<1>(m));
+        g_prof.spare.push_back(std::get<2>(m));
+    }
+    g_prof.marks.clear();
+    g_prof.on = true;
+    return PHX_OK;
+}
+
+phx_status phx_profile_stop(int64_t* launches, double* ms) {
+    if (launches == nullptr || ms == nullptr) return PHX_ERR_INVALID;
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    g_prof.on = false;
+    phx_status st = PHX_OK;
+    for (int k = 0; k < kNumKinds; ++k) {
+        launches[k] = 0;
+        ms[k] = 0.0;
+    }
+    for (auto& m : g_prof.marks) {
+        const int kind = std::get<0>(m);
+        float t = 0.f;
+        if (cudaEventSynchronize(std::get<2>(m)) != cudaSuccess ||
+            cudaEventElapsedTime(&t, std::get<1>(m), std::get<2>(m)) != cudaSuccess) {
+            cudaGetLastError();
+            st = PHX_ERR_LAUNCH;
+        }
+        launches[kind] += 1;
+        ms[kind] += t;
+        g_prof.spare.push_back(std::get<1>(m));
+        g_prof.spare.push_back(std::get<2>(m));
+    }
+    g_prof.marks.clear();
+    return st;
+}
+
+int phx_num_configs(int variant) { return num_configs(variant); }
+
+phx_status phx_config_name(int variant, int index, char* buf, size_t buflen) {
+    const int n = num_configs(variant);
+    if (n < 0 || index < 0 || index >= n) return PHX_ERR_INVALID;
+    return copy_name(config_name(variant, index), buf, buflen);
+}
+
+phx_status phx_set_config(int variant, const char* spec) {
+    if (num_configs(variant) < 0) return PHX_ERR_INVALID;
+    int idx = -1;
+    if (spec != nullptr && spec[0] != '\0') {
+        idx = parse_config(variant, spec);
+        if (idx < 0) return PHX_ERR_CONFIG;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    load_env_once_locked();
+    g_pin[variant] = idx;
+    return PHX_OK;
+}
+
+phx_status phx_get_config(int variant, int64_t M, int64_t N, int64_t K, char* buf, size_t buflen) {
+    if (num_configs(variant) < 0 || M < 0 || N < 0 || K < 0) return PHX_ERR_INVALID;
+    int sms = 148;
+    DevState* d = nullptr;
+    if (device_state(&d) == PHX_OK) sms = d->sm_count;
+    const int cfg = choose_config(variant, M, N, K, sms);
+    if (cfg < 0) return PHX_ERR_INTERNAL;
+    return copy_name(config_name(variant, cfg), buf, buflen);
+}
+
+phx_status phx_autotune(int variant, int64_t M, int64_t N, int64_t K, int finalists, int rounds,
+                        int settle_ms, phx_stream_t stream) {
+    const int n = num_configs(variant);
+    if (n < 0 || M <= 0 || N <= 0 || K <= 0) return PHX_ERR_INVALID;
+    if (validate_sizes(M, N, K) != PHX_OK) return PHX_ERR_INVALID;
+    DevState* d = nullptr;
+    phx_status st = device_state(&d);
+    if (st != PHX_OK) return st;
+    float *A = nullptr, *B = nullptr, *C = nullptr;
+    if (cudaMalloc(&A, 4 * M * K) != cudaSuccess || cudaMalloc(&B, 4 * K * N) != cudaSuccess ||
+        cudaMalloc(&C, 4 * M * N) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(A); cudaFree(B); cudaFree(C);
+        return PHX_ERR_NOMEM;
+    }
+    tune_fill_kernel<<<1024, 256, 0, stream>>>(A, M * K, 0x1234u);
+    tune_fill_kernel<<<1024, 256, 0, stream>>>(B, K * N, 0x5678u);
+    tune_fill_kernel<<<1024, 256, 0, stream>>>(C, M * N, 0x9abcu);
+    const char* inject = std::getenv("PHX_TUNE_FAIL");  // fault injection: this config "fails"
+    cudaEvent_t e0, e1;
+    cudaEventCreate(&e0);
+    cudaEventCreate(&e1);
+    auto measure = [&](int i) -> double {
+        if (inject != nullptr && config_name(variant, i) == inject) return -1.0;
+        cudaEventRecord(e0, stream);
+        const phx_status s = launch_variant(variant, i, M, N, K, 1.0f, A, B, 0.5f, C, d, stream);
+        cudaEventRecord(e1, stream);
+        if (s != PHX_OK || cudaEventSynchronize(e1) != cudaSuccess) {
+            cudaGetLastError();
+            return -1.0;
+        }
+        float ms = 0.f;
+        cudaEventElapsedTime(&ms, e0, e1);
+        return ms * 1e-3;
+    };
+    const auto start = std::chrono::steady_clock::now();
+    auto elapsed = [&]() {
+        return std::chrono::duration<double>(std::chrono::steady_clock::now() - start).count();
+    };
+    const TuneOutcome res = tune_select(n, measure, elapsed, finalists > 0 ? finalists : 4,
+                                        rounds > 0 ? rounds : 9, settle_ms > 0 ? settle_ms * 1e-3 : 0.25,
+                                        0x5eedull ^ static_cast<uint64_t>(M * 31 + N * 17 + K));
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    cudaStreamSynchronize(stream);
+    cudaFree(A);
+    cudaFree(B);
+    cudaFree(C);
+    // A timeout during tuning is reported, not hidden.
+    st = phx_check_device_status(stream);
+    if (st != PHX_OK) return st;
+    if (res.picked < 0) return PHX_ERR_LAUNCH;
+    if (log_level() >= 1)
+        std::fprintf(stderr, "[phx] tuned variant %d (%lld,%lld,%lld): %s (%lld launches)\n", variant,
+                     (long long)M, (long long)N, (long long)K, config_name(variant, res.picked).c_str(),
+                     (long long)res.launches);
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_tuned[ShapeKey(variant, M, N, K)] = res.picked;
+    return PHX_OK;
+}
+
+phx_status phx_tune_cache_save(const char* path) {
+    if (path == nullptr) return PHX_ERR_INVALID;
+    std::ofstream f(path);
+    if (!f) return PHX_ERR_INVALID;
+    std::lock_guard<std::mutex> lock(g_mu);
+    f << "# phx tuning cache: variant M N K config\n";
+    for (const auto& kv : g_tuned) {
+        f << std::get<0>(kv.first) << ' ' << std::get<1>(kv.first) << ' ' << std::get<2>(kv.first)
+          << ' ' << std::get<3>(kv.first) << ' ' << config_name(std::get<0>(kv.first), kv.second)
+          << '\n';
+    }
+    return f ? PHX_OK : PHX_ERR_INVALID;
+}
+
+phx_status phx_tune_cache_load(const char* path) {
+    if (path == nullptr) return PHX_ERR_INVALID;
+    std::ifstream f(path);
+    if (!f) return PHX_ERR_INVALID;
+    std::map<ShapeKey, int> loaded;
+    std::string line;
+    while (std::getline(f, line)) {
+        if (line.empty() || line[0] == '#') continue;
+        std::istringstream in(line);
+        int variant;
+        long long M, N, K;
+        if (!(in >> variant >> M >> N >> K)) return PHX_ERR_CONFIG;
+        std::string rest;
+        std::getline(in, rest);
+        if (num_configs(variant) < 0) return PHX_ERR_CONFIG;
+        const int idx = parse_config(variant, rest.c_str());
+        if (idx < 0) return PHX_ERR_CONFIG;
+        loaded[ShapeKey(variant, M, N, K)] = idx;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (const auto& kv : loaded) g_tuned[kv.first] = kv.second;
+    return PHX_OK;
+}
+
+phx_status phx_probe_ffma(int packed, int64_t blocks, int iters, float* out, phx_stream_t stream) {
+    if (blocks <= 0 || blocks > 0x7FFFFFFF || iters <= 0 || out == nullptr) return PHX_ERR_INVALID;
+    DevState* d = nullptr;
+    phx_status st = device_state(&d);
+    if (st != PHX_OK) return st;
+    return phx::probe_ffma_launch(packed, blocks, iters, out, stream) == cudaSuccess ? PHX_OK : PHX_ERR_LAUNCH;
+}
+
+phx_status phx_probe_stream_read(const float* x, int64_t n, float* sink, int64_t blocks,
+                                 phx_stream_t stream) {
+    if (x == nullptr || sink == nullptr || n <= 0 || n % 4 != 0 || blocks <= 0 || blocks > 0x7FFFFFFF ||
+        (reinterpret_cast<uintptr_t>(x) & 15u) != 0)
+        return PHX_ERR_INVALID;
+    DevState* d = nullptr;
+    phx_status st = device_state(&d);
+    if (st != PHX_OK) return st;
+    return phx::probe_stream_read_launch(x, n, sink, blocks, stream) == cudaSuccess ? PHX_OK : PHX_ERR_LAUNCH;
+}
+
+phx_status phx_probe_mma_f16(int64_t ctas, int iters, int n, float* sink, phx_stream_t stream) {
+    if (ctas <= 0 || ctas > 0x7FFFFFFF || iters <= 0 || sink == nullptr || (n != 64 && n != 128 && n != 256))
+        return PHX_ERR_INVALID;
+    DevState* d = nullptr;
+    phx_status st = device_state(&d);
+    if (st != PHX_OK) return st;
+    return phx::probe_mma_f16_launch(ctas, iters, n, sink, d->status, stream) == cudaSuccess ? PHX_OK
+                                                                                               : PHX_ERR_LAUNCH;
+}
+
+phx_status phx_selftest_bounded_wait(uint64_t limit_ns, phx_stream_t stream) {
+    DevState* d = nullptr;
+    phx_status st = device_state(&d);
+    if (st != PHX_OK) return st;
+    limit_ns = std::min<uint64_t>(std::max<uint64_t>(limit_ns, 1000), 1000000000ull);
+    return phx::selftest_wait_launch(limit_ns, d->status, stream) == cudaSuccess ? PHX_OK : PHX_ERR_LAUNCH;
+}
+
+phx_status phx_selftest_tuner(int n, const double* base_s, const int* fail, double noise,
+                              double drift, int finalists, int rounds, uint64_t seed, int* picked,
+                              int64_t* launches) {
+    if (n <= 0 || base_s == nullptr || picked == nullptr || launches == nullptr) return PHX_ERR_INVALID;
+    double clock = 0.0;
+    int64_t calls = 0;
+    auto measure = [&](int i) -> double {
+        ++calls;
+        if (fail != nullptr && fail[i]) return -1.0;
+        // deterministic noise in [-1, 1) from a hash of (seed, call)
+        uint64_t h = (seed + static_cast<uint64_t>(calls)) * 0x9E3779B97F4A7C15ull;
+        h ^= h >> 31;
+        h *= 0xBF58476D1CE4E5B9ull;
+        h ^= h >> 29;
+        const double u = static_cast<double>(h >> 11) * (1.0 / 9007199254740992.0) * 2.0 - 1.0;
+        const double s = base_s[i] * (1.0 + drift * static_cast<double>(calls)) * (1.0 + noise * u);
+        clock += s;
+        return s;
+    };
+    auto elapsed = [&]() { return clock; };
+    const double total = std::accumulate(base_s, base_s + n, 0.0);
+    const TuneOutcome res = tune_select(n, measure, elapsed, finalists, rounds, 2.0 * total, seed);
+    *picked = res.picked;
+    *launches = res.launches;
+    return PHX_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,378 @@
+// sgemm_simt.cu -- f32 GEMM on the CUDA cores for sm_103a.
+//
+// C <- alpha * A @ B + beta * C, row-major f32 ("gemm, f32", phobos-lang.dev/docs/examples/
+// gemm-fp32/: kernel listing; sections "One output tile per CTA", "The k loop",
+// "The epilogue").
+//
+// Design (one CTA of 256 threads per TILE_M x TILE_N output tile, as in "One output tile
+// per CTA" and @launch(256)):
+//   * The k loop walks K in steps of TILE_K.  Each step copies a TILE_M x TILE_K panel of
+//     A and a TILE_K x TILE_N panel of B into a STAGES-deep ring of shared-memory buffers
+//     with cp.async, so the copies of the next STAGES-1 panels overlap the math on the
+//     current one (the @pipeline double buffering, generalised to STAGES >= 2).
+//   * Aligned path: both panels move as 16-byte cp.async.cg copies (the @aligned promise:
+//     no masks, 16-byte vector loads).  Masked path: 4-byte cp.async.ca copies whose
+//     source size is 0 past an edge, which writes zeros ("extra 128-byte lines, masked
+//     elements"); stores past an edge are skipped.  Both paths compute the same values.
+//   * The output tile is split over 8 warps (4 x 2) and each warp's tile over its 32 lanes
+//     (4 x 8); every thread owns a TM x TN register micro-tile of accumulators, as the
+//     lab's register-tiling rung does (Part 2, "register tiling"; Part 2, "The register
+//     patch: reuse against occupancy").  The A panel lands row-major (as copied, 16 bytes
+//     at a time) and is rewritten once per k tile into a k-major buffer, so that at each k
+//     step a thread reads its TM values of A and its TN values of B as float4s.  Lanes that
+//     share rows or columns read the same shared-memory words (broadcast), so one warp's
+//     loads per k step touch 16 (or 32) rows of A and 64 (or 32) columns of B.
+//   * Optionally (FMA2 = 1) the multiply-adds are issued as packed f32x2 FMAs (__ffma2_rn),
+//     halving the FMA instructions the schedulers issue; each lane of the pair is an
+//     ordinary IEEE f32 fused multiply-add, so the values are the same.
+//   * Epilogue: C is read once (not at all when beta == 0) and written once, with 16-byte
+//     accesses on the aligned path.
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+#include "internal.h"
+
+namespace phx {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kLanesM = 4;  // lanes of a warp along M
+constexpr int kLanesN = 8;  // lanes of a warp along N
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 4-byte asynchronous copy; with pred false the source is not read and zeros are written.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const float* src, bool pred) {
+    const int bytes = pred ? 4 : 0;
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(bytes)
+                 : "memory");
+}
+
+// 16-byte asynchronous copy, bypassing L1 (the panel is used once per CTA).
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const float* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// Map a linear CTA index to (tile row, tile column), walking groups of 8 tile rows
+// column by column so that CTAs running together share panels of A and B in L2.
+__device__ __forceinline__ void tile_coords(int bid, int tiles_m, int tiles_n, int& pm, int& pn) {
+    constexpr int kGroup = 8;
+    const int per_group = kGroup * tiles_n;
+    const int group = bid / per_group;
+    const int first_m = group * kGroup;
+    const int rows = min(tiles_m - first_m, kGroup);
+    const int r = bid - group * per_group;
+    pm = first_m + r % rows;
+    pn = r / rows;
+}
+
+// Row stride (floats) of the k-major copy of the A panel: TILE_M plus 4, which keeps the
+// 16-byte fragment reads aligned and spreads the transposing stores over the banks.
+__host__ __device__ constexpr int at_row_stride(int bm) { return bm + 4; }
+
+// Shared-memory floats one CTA uses: the A staging ring (row-major, as copied), two
+// k-major A buffers, and the B ring.
+__host__ __device__ constexpr int sgemm_smem_floats(int bm, int bn, int bk, int stages) {
+    return stages * bm * bk + 2 * bk * at_row_stride(bm) + stages * bk * bn;
+}
+
+template <int BM, int BN, int BK, int STAGES, int TM, int TN, bool MASKED, bool FMA2>
+__global__ void __launch_bounds__(kThreads, 2)
+sgemm_kernel(const float* __restrict__ A, const float* __restrict__ B, float* __restrict__ C,
+             int M, int N, int K, float alpha, float beta) {
+    constexpr int WTM = kLanesM * TM;  // warp tile
+    constexpr int WTN = kLanesN * TN;
+    constexpr int WARPS_M = BM / WTM;
+    constexpr int WARPS_N = BN / WTN;
+    static_assert(WARPS_M * WARPS_N * 32 == kThreads, "8 warps must tile the CTA tile");
+    static_assert(TM % 4 == 0 && TN % 4 == 0 && BK % 4 == 0, "float4 fragments");
+    static_assert(STAGES >= 3, "the ring keeps one panel ahead of the transposed one");
+    constexpr int A_STAGE = BM * BK;        // staging, [m][k] as copied from A
+    constexpr int LDT = at_row_stride(BM);  // k-major copy, [k][m]
+    constexpr int AT_BUF = BK * LDT;
+    constexpr int B_STAGE = BK * BN;        // [k][n]
+
+    extern __shared__ __align__(16) float smem[];
+    float* As = smem;                        // STAGES x A_STAGE
+    float* At = As + STAGES * A_STAGE;       // 2 x AT_BUF
+    float* Bs = At + 2 * AT_BUF;             // STAGES x B_STAGE
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int wm = warp / WARPS_N;
+    const int wn = warp % WARPS_N;
+    const int lm = lane / kLanesN;
+    const int ln = lane % kLanesN;
+
+    const int tiles_m = (M + BM - 1) / BM;
+    const int tiles_n = (N + BN - 1) / BN;
+    int pm, pn;
+    tile_coords(blockIdx.x, tiles_m, tiles_n, pm, pn);
+    const int m0 = pm * BM;
+    const int n0 = pn * BN;
+    const int num_k_tiles = (K + BK - 1) / BK;
+
+    // Copy k tile `kt` of A (TILE_M x TILE_K) and B (TILE_K x TILE_N) into ring slot `stage`.
+    auto load_tile = [&](int kt, int stage) {
+        const int k0 = kt * BK;
+        float* as = As + stage * A_STAGE;
+        float* bs = Bs + stage * B_STAGE;
+        if constexpr (!MASKED) {
+#pragma unroll
+            for (int e = tid; e < BM * BK / 4; e += kThreads) {
+                const int m = e / (BK / 4);
+                const int k4 = e % (BK / 4);
+                cp_async_16(smem_addr(as + m * BK + k4 * 4),
+                            A + static_cast<int64_t>(m0 + m) * K + k0 + k4 * 4);
+            }
+#pragma unroll
+            for (int e = tid; e < BK * BN / 4; e += kThreads) {
+                const int k = e / (BN / 4);
+                const int n4 = e % (BN / 4);
+                cp_async_16(smem_addr(bs + k * BN + n4 * 4),
+                            B + static_cast<int64_t>(k0 + k) * N + n0 + n4 * 4);
+            }
+        } else {
+#pragma unroll
+            for (int e = tid; e < BM * BK; e += kThreads) {
+                const int m = e / BK;
+                const int k = e % BK;
+                const bool ok = (m0 + m < M) && (k0 + k < K);
+                const float* src = ok ? A + static_cast<int64_t>(m0 + m) * K + k0 + k : A;
+                cp_async_4(smem_addr(as + m * BK + k), src, ok);
+            }
+#pragma unroll
+            for (int e = tid; e < BK * BN; e += kThreads) {
+                const int k = e / BN;
+                const int n = e % BN;
+                const bool ok = (k0 + k < K) && (n0 + n < N);
+                const float* src = ok ? B + static_cast<int64_t>(k0 + k) * N + n0 + n : B;
+                cp_async_4(smem_addr(bs + k * BN + n), src, ok);
+            }
+        }
+    };
+
+    // Rewrite ring slot `stage` of A, [m][k], as the k-major buffer `buf`, [k][m].
+    auto transpose_a = [&](int stage, int buf) {
+        const float* as = As + stage * A_STAGE;
+        float* at = At + buf * AT_BUF;
+#pragma unroll
+        for (int e = tid; e < BM * BK / 4; e += kThreads) {
+            const int m = e / (BK / 4);
+            const int k4 = e % (BK / 4);
+            const float4 v = *reinterpret_cast<const float4*>(as + m * BK + k4 * 4);
+            at[(k4 * 4 + 0) * LDT + m] = v.x;
+            at[(k4 * 4 + 1) * LDT + m] = v.y;
+            at[(k4 * 4 + 2) * LDT + m] = v.z;
+            at[(k4 * 4 + 3) * LDT + m] = v.w;
+        }
+    };
+
+    // Accumulators: rows  wm*WTM + g*16 + lm*4 + r   (g < TM/4, r < 4)
+    //               cols  wn*WTN + h*32 + ln*4 + c   (h < TN/4, c < 4)
+    float acc[TM][TN];
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
+
+    // Prologue: panels 0 .. STAGES-2 in flight, panel 0 transposed.
+#pragma unroll
+    for (int s = 0; s < STAGES - 1; ++s) {
+        if (s < num_k_tiles) load_tile(s, s);
+        cp_async_commit();
+    }
+    cp_async_wait<STAGES - 2>();
+    __syncthreads();
+    transpose_a(0, 0);
+
+    for (int kt = 0; kt < num_k_tiles; ++kt) {
+        // Panels up to kt+1 have landed; after the barrier they and the transposed panel kt
+        // are visible to every thread, and everyone has finished reading the buffers of
+        // iteration kt-1 (ring slot (kt-1) % STAGES and k-major buffer (kt+1) % 2).
+        cp_async_wait<STAGES - 3>();
+        __syncthreads();
+        {
+            const int nk = kt + STAGES - 1;
+            if (nk < num_k_tiles) load_tile(nk, nk % STAGES);
+            cp_async_commit();
+        }
+        if (kt + 1 < num_k_tiles) transpose_a((kt + 1) % STAGES, (kt + 1) & 1);
+
+        const float* at = At + (kt & 1) * AT_BUF + wm * WTM + lm * 4;
+        const float* bs = Bs + (kt % STAGES) * B_STAGE + wn * WTN + ln * 4;
+#pragma unroll
+        for (int kk = 0; kk < BK; ++kk) {
+            float a[TM], b[TN];
+#pragma unroll
+            for (int g = 0; g < TM / 4; ++g) {
+                const float4 v = *reinterpret_cast<const float4*>(at + kk * LDT + g * (kLanesM * 4));
+                a[g * 4 + 0] = v.x;
+                a[g * 4 + 1] = v.y;
+                a[g * 4 + 2] = v.z;
+                a[g * 4 + 3] = v.w;
+            }
+#pragma unroll
+            for (int h = 0; h < TN / 4; ++h) {
+                const float4 v = *reinterpret_cast<const float4*>(bs + kk * BN + h * (kLanesN * 4));
+                b[h * 4 + 0] = v.x;
+                b[h * 4 + 1] = v.y;
+                b[h * 4 + 2] = v.z;
+                b[h * 4 + 3] = v.w;
+            }
+#pragma unroll
+            for (int i = 0; i < TM; ++i) {
+                if constexpr (FMA2) {
+                    const float2 aa = make_float2(a[i], a[i]);
+#pragma unroll
+                    for (int j = 0; j < TN; j += 2) {
+                        float2 c2 = make_float2(acc[i][j], acc[i][j + 1]);
+                        c2 = __ffma2_rn(aa, make_float2(b[j], b[j + 1]), c2);
+                        acc[i][j] = c2.x;
+                        acc[i][j + 1] = c2.y;
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+                }
+            }
+        }
+    }
+    cp_async_wait<0>();
+
+    // Epilogue: C <- alpha * acc + beta * C_old, C read only when beta != 0.
+    const bool read_c = beta != 0.f;
+#pragma unroll
+    for (int i = 0; i < TM; ++i) {
+        const int row = m0 + wm * WTM + (i / 4) * (kLanesM * 4) + lm * 4 + (i % 4);
+        if (MASKED && row >= M) continue;
+        float* crow = C + static_cast<int64_t>(row) * N;
+#pragma unroll
+        for (int h = 0; h < TN / 4; ++h) {
+            const int col = n0 + wn * WTN + h * (kLanesN * 4) + ln * 4;
+            if constexpr (!MASKED) {
+                float4* p = reinterpret_cast<float4*>(crow + col);
+                float4 o;
+                o.x = alpha * acc[i][h * 4 + 0];
+                o.y = alpha * acc[i][h * 4 + 1];
+                o.z = alpha * acc[i][h * 4 + 2];
+                o.w = alpha * acc[i][h * 4 + 3];
+                if (read_c) {
+                    const float4 c = *p;
+                    o.x = fmaf(beta, c.x, o.x);
+                    o.y = fmaf(beta, c.y, o.y);
+                    o.z = fmaf(beta, c.z, o.z);
+                    o.w = fmaf(beta, c.w, o.w);
+                }
+                *p = o;
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    if (col + c < N) {
+                        float o = alpha * acc[i][h * 4 + c];
+                        if (read_c) o = fmaf(beta, crow[col + c], o);
+                        crow[col + c] = o;
+                    }
+                }
+            }
+        }
+    }
+}
+
+// C <- beta * C over M*N elements (beta == 0 writes zeros without reading C).
+__global__ void scale_c_kernel(float* __restrict__ C, int64_t n, float beta) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
+        C[i] = beta == 0.f ? 0.f : beta * C[i];
+}
+
+// ---------------------------------------------------------------------------------------
+// The compiled configurations.  The pages' search space is TILE_M, TILE_N in
+// {32, 64, 128, 256} and TILE_K in {4, 8, 16, 32} ("gemm, f32", section "The attributes",
+// @autotune row); this build compiles the part of it that a 256-thread CTA with
+// 4x4..8x8 register micro-tiles covers, times STAGES in {3, 4} and the FMA2 switch.
+// ---------------------------------------------------------------------------------------
+using KernelFn = void (*)(const float*, const float*, float*, int, int, int, float, float);
+
+struct Entry {
+    SgemmConfig cfg;
+    KernelFn aligned;
+    KernelFn masked;
+    int smem_bytes;
+};
+
+template <int BM, int BN, int BK, int STAGES, int FMA2>
+constexpr Entry make_entry() {
+    constexpr int TM = BM / 16;  // 4 warps x 4 lanes along M
+    constexpr int TN = BN / 16;  // 2 warps x 8 lanes along N
+    return Entry{SgemmConfig{BM, BN, BK, STAGES, FMA2},
+                 &sgemm_kernel<BM, BN, BK, STAGES, TM, TN, false, FMA2 != 0>,
+                 &sgemm_kernel<BM, BN, BK, STAGES, TM, TN, true, FMA2 != 0>,
+                 sgemm_smem_floats(BM, BN, BK, STAGES) * 4};
+}
+
+const Entry kEntries[] = {
+    make_entry<128, 128, 8, 4, 0>(),  make_entry<128, 128, 8, 4, 1>(),
+    make_entry<128, 128, 16, 3, 0>(), make_entry<128, 128, 16, 3, 1>(),
+    make_entry<128, 128, 16, 4, 0>(), make_entry<128, 128, 16, 4, 1>(),
+    make_entry<128, 128, 8, 3, 0>(),  make_entry<128, 128, 8, 3, 1>(),
+    make_entry<128, 64, 8, 4, 0>(),   make_entry<128, 64, 16, 4, 1>(),
+    make_entry<64, 128, 8, 4, 0>(),   make_entry<64, 128, 16, 4, 1>(),
+    make_entry<64, 64, 8, 4, 0>(),    make_entry<64, 64, 16, 4, 0>(),
+};
+constexpr int kNumEntries = sizeof(kEntries) / sizeof(kEntries[0]);
+
+}  // namespace
+
+int sgemm_num_configs() { return kNumEntries; }
+
+const SgemmConfig& sgemm_config(int index) { return kEntries[index].cfg; }
+
+bool sgemm_is_aligned(int index, int64_t M, int64_t N, int64_t K, const float* A,
+                      const float* B, const float* C) {
+    const SgemmConfig& c = kEntries[index].cfg;
+    auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    return M % c.tile_m == 0 && N % c.tile_n == 0 && K % c.tile_k == 0 && al16(A) && al16(B) &&
+           al16(C);
+}
+
+cudaError_t sgemm_launch(int index, int64_t M, int64_t N, int64_t K, float alpha,
+                         const float* A, const float* B, float beta, float* C,
+                         cudaStream_t stream) {
+    const Entry& e = kEntries[index];
+    const bool aligned = sgemm_is_aligned(index, M, N, K, A, B, C);
+    KernelFn fn = aligned ? e.aligned : e.masked;
+    cudaError_t err = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           e.smem_bytes);
+    if (err != cudaSuccess) return err;
+    const int64_t tiles = ((M + e.cfg.tile_m - 1) / e.cfg.tile_m) * ((N + e.cfg.tile_n - 1) / e.cfg.tile_n);
+    if (tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    fn<<<static_cast<unsigned>(tiles), kThreads, e.smem_bytes, stream>>>(
+        A, B, C, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), alpha, beta);
+    return cudaGetLastError();
+}
+
+cudaError_t scale_c_launch(int64_t M, int64_t N, float beta, float* C, cudaStream_t stream) {
+    const int64_t n = M * N;
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    scale_c_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(C, n, beta);
+    return cudaGetLastError();
+}
+
+}  // namespace phx

@@ -1,0 +1,228 @@
+/*
+ * phx.h -- C ABI of libphx, a single-GPU GEMM library for GB300 (sm_103a).
+ *
+ * The one operation:   C <- alpha * A @ B + beta * C
+ *
+ * as stated in "gemm, f32" (phobos-lang.dev/docs/examples/gemm-fp32/): the kernel signature
+ * gemm(A: tensor<f32>[M, K], B: tensor<f32>[K, N], C: tensor<f32>[M, N], alpha: f32,
+ * beta: f32), section "The epilogue" (C is overwritten in place with alpha * acc +
+ * beta * c_old), and in "gemm on tensor cores" (phobos-lang.dev/docs/examples/
+ * gemm-fp16tc-fp32acc/), section "What changes" (operands rounded to f16, products summed
+ * in f32).
+ *
+ * Conventions shared by every entry point below
+ * ---------------------------------------------
+ * Layout     A, B and C are row-major and contiguous: A is M x K with leading dimension K,
+ *            B is K x N with leading dimension N, C is M x N with leading dimension N.
+ *            Element (i, j) of C is C[i * N + j].  No transposes.
+ * Pointers   A, B and C are DEVICE pointers (cudaMalloc, the caching allocator of a
+ *            framework, managed memory) on the current device, 4-byte aligned, and not
+ *            NULL whenever their matrix has at least one element.  The caller
+ *            owns them; the library keeps no reference after the call.  C is read (unless
+ *            beta == 0) and written in place.  A and B must not overlap C: an overlap is
+ *            rejected with PHX_ERR_INVALID.  A and B may alias each other.
+ * Stream     Work is enqueued on `stream` (NULL = the legacy default stream) and the call
+ *            returns once it is enqueued; results are visible to later work on that
+ *            stream.  The type phx_stream_t is cudaStream_t.
+ * Sizes      M, N, K >= 0 and each below 2^31; M*K, K*N and M*N below 2^62.
+ * Degenerate M == 0 or N == 0: nothing is read or written, PHX_OK.
+ *            K == 0 or alpha == 0: A and B are not read and C <- beta * C.
+ *            beta == 0: C is not read (NaN or Inf in C does not propagate), C <- alpha*A@B.
+ * Errors     Arguments are checked before anything is launched; on an error return nothing
+ *            was launched and no memory was touched.  The library never traps: a kernel
+ *            whose internal wait runs out of time records PHX_ERR_TIMEOUT in a per-device
+ *            status word and exits; phx_check_device_status() reports it.
+ * Threads    Entry points may be called from several host threads; configuration pins
+ *            and the tuning cache are process-wide and guarded by a lock.
+ */
+#ifndef PHX_H_
+#define PHX_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Every declaration below is part of the exported ABI, even when the library is built
+ * with hidden default visibility. */
+#if defined(__GNUC__)
+#pragma GCC visibility push(default)
+#endif
+
+typedef struct CUstream_st* phx_stream_t; /* identical to cudaStream_t */
+
+typedef enum phx_status {
+    PHX_OK = 0,
+    PHX_ERR_INVALID = 1,  /* bad size, null or overlapping pointer, bad variant        */
+    PHX_ERR_ARCH = 2,     /* no CUDA device, or the current device is not sm_103       */
+    PHX_ERR_LAUNCH = 3,   /* a CUDA runtime call or a kernel launch failed             */
+    PHX_ERR_TIMEOUT = 4,  /* a device-side bounded wait expired (see check_status)     */
+    PHX_ERR_NOMEM = 5,    /* the f16 workspace could not be allocated                  */
+    PHX_ERR_INTERNAL = 6, /* an invariant of the library itself failed                 */
+    PHX_ERR_CONFIG = 7    /* config string unparsable or not among the compiled configs */
+} phx_status;
+
+/* Variants, for the configuration and tuning calls. */
+enum { PHX_VARIANT_SGEMM = 0, PHX_VARIANT_F16TC = 1 };
+
+/* ---------------------------------------------------------------------------------------
+ * The GEMM calls
+ * ------------------------------------------------------------------------------------- */
+
+/* f32 GEMM on the CUDA cores ("gemm, f32", kernel listing and sections "One output tile
+ * per CTA", "The k loop", "The epilogue").  Every product and sum is an f32 fused
+ * multiply-add; the epilogue computes alpha * acc + beta * c_old in f32.  Tile-aligned
+ * shapes with 16-byte aligned pointers take the aligned fast path, all others a masked
+ * path (loads past an edge read zero, stores past an edge are skipped) that gives the
+ * same result.  No workspace is allocated. */
+phx_status phx_sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+                     const float* B, float beta, float* C, phx_stream_t stream);
+
+/* f16 tensor cores with f32 accumulation ("gemm on tensor cores", section "What
+ * changes"): every element of A and B is rounded to the nearest f16 (ties to even), the
+ * f16 x f16 products are summed in f32 by tcgen05.mma into tensor memory, and the
+ * epilogue computes alpha * acc + beta * c_old in f32.  The rounded operands go to a
+ * workspace of phx_f16tc_workspace_bytes(M, N, K) bytes taken, in stream order, from a
+ * memory pool the library owns for the current device, and returned to it after the
+ * GEMM (PHX_ERR_NOMEM if that fails). */
+phx_status phx_gemm_f16tc_f32acc(int64_t M, int64_t N, int64_t K, float alpha,
+                                 const float* A, const float* B, float beta, float* C,
+                                 phx_stream_t stream);
+
+/* Workspace bytes phx_gemm_f16tc_f32acc takes for this shape: the rounded A (M rows) and
+ * the rounded, transposed B (N rows), each row padded with zeros to a multiple of 8
+ * halves. */
+phx_status phx_f16tc_workspace_bytes(int64_t M, int64_t N, int64_t K, size_t* bytes);
+
+/* ---------------------------------------------------------------------------------------
+ * Status
+ * ------------------------------------------------------------------------------------- */
+
+/* A static, human-readable name for a status code. */
+const char* phx_status_string(phx_status s);
+
+/* Synchronise `stream`, then read and clear the current device's status word: PHX_OK,
+ * PHX_ERR_TIMEOUT if a kernel gave up a bounded wait since the last check, or
+ * PHX_ERR_LAUNCH if the stream reported an error. */
+phx_status phx_check_device_status(phx_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Per-kernel timing, for roofline reports
+ * ------------------------------------------------------------------------------------- */
+
+/* Kernel kinds counted by the profile. */
+enum { PHX_KIND_SGEMM = 0, PHX_KIND_F16_CAST = 1, PHX_KIND_TC_GEMM = 2, PHX_KIND_SCALE_C = 3,
+       PHX_NUM_KINDS = 4 };
+
+/* Start a profile: from now on every GEMM call records CUDA events on its stream around
+ * each kernel it launches (the f32 GEMM kernel; the f16 cast pass and the tensor-core GEMM
+ * kernel separately; the C-scaling kernel of the degenerate cases).  Restarting discards the
+ * previous marks. */
+phx_status phx_profile_start(void);
+
+/* Stop the profile: synchronise the recorded events and write, for each kind k in
+ * [0, PHX_NUM_KINDS), the number of launches[k] and their summed device time ms[k] in
+ * milliseconds.  Both arrays are caller-owned host arrays of PHX_NUM_KINDS elements. */
+phx_status phx_profile_stop(int64_t* launches, double* ms);
+
+/* ---------------------------------------------------------------------------------------
+ * Configurations and the autotuner
+ *
+ * A configuration is one compiled kernel shape, written as in "gemm, f32" section
+ * "Tuning": "TILE_M=128 TILE_N=128 TILE_K=8 STAGES=4" (f32 variant; an optional
+ * "FMA2=1" selects packed f32x2 multiply-adds) or "TILE_M=128 TILE_N=256 TILE_K=64
+ * STAGES=4" (f16 variant).  The order of keys does not matter.
+ * ------------------------------------------------------------------------------------- */
+
+/* Number of compiled configurations of a variant (or -1 for a bad variant). */
+int phx_num_configs(int variant);
+
+/* Canonical name of configuration `index` of `variant`, NUL-terminated in buf. */
+phx_status phx_config_name(int variant, int index, char* buf, size_t buflen);
+
+/* Pin one configuration for every later call of `variant` (spec as above), bypassing the
+ * tuned and default choices; spec == NULL or "" removes the pin.  PHX_ERR_CONFIG if the
+ * spec does not parse or names no compiled configuration. */
+phx_status phx_set_config(int variant, const char* spec);
+
+/* Name of the configuration a call of `variant` with this shape would use now. */
+phx_status phx_get_config(int variant, int64_t M, int64_t N, int64_t K, char* buf,
+                          size_t buflen);
+
+/* Tune `variant` for the shape (M, N, K), following "gemm, f32" section "Tuning":
+ * stage 1 times every configuration briefly on scratch inputs and skips any that fails;
+ * stage 2 runs the fastest `finalists` for `settle_ms` milliseconds to settle the clocks,
+ * then times them over `rounds` rounds, one launch each per round in a freshly shuffled
+ * order, and keeps the configuration with the lowest median.  The result goes into the
+ * process-wide tuning cache, which later calls with this exact shape consult.  Scratch
+ * inputs are allocated and freed inside the call; the call synchronises `stream`. */
+phx_status phx_autotune(int variant, int64_t M, int64_t N, int64_t K, int finalists,
+                        int rounds, int settle_ms, phx_stream_t stream);
+
+/* Save the tuning cache to a text file (one line per variant and shape) or merge one in. */
+phx_status phx_tune_cache_save(const char* path);
+phx_status phx_tune_cache_load(const char* path);
+
+/* ---------------------------------------------------------------------------------------
+ * Roof probes, after the lab's Part 1 (a kernel of nothing but independent multiply-adds,
+ * and a streaming read); used to measure the denominators of the roofline.
+ * ------------------------------------------------------------------------------------- */
+
+/* FP32 multiply-add probe: `blocks` CTAs of 256 threads, each thread running 8
+ * independent chains for `iters` iterations (packed = 1: 8 chains of f32x2 pairs).
+ * Floating-point operations performed: blocks * 256 * iters * 16 * (packed ? 2 : 1).
+ * `out` (device, blocks * 256 floats) receives one value per thread. */
+phx_status phx_probe_ffma(int packed, int64_t blocks, int iters, float* out,
+                          phx_stream_t stream);
+
+/* Streaming-read probe: sums n floats of x (device, 16-byte aligned, n % 4 == 0) with
+ * `blocks` CTAs of 256 threads; reads 4 * n bytes.  `sink` (device, 1 float) is written
+ * only if the sum equals a sentinel, so the read cannot be optimised away. */
+phx_status phx_probe_stream_read(const float* x, int64_t n, float* sink, int64_t blocks,
+                                 phx_stream_t stream);
+
+/* Tensor-core probe: `ctas` CTAs each issue `iters` rounds of 4 tcgen05.mma kind::f16
+ * (M = 128, N = n, K = 16, f32 accumulate) on shared-memory operands, with no global
+ * traffic.  Floating-point operations: ctas * iters * 4 * 2 * 128 * n * 16.  n is 64, 128
+ * or 256.  `sink` (device, ctas floats) receives one accumulator value per CTA. */
+phx_status phx_probe_mma_f16(int64_t ctas, int iters, int n, float* sink,
+                             phx_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Self-tests of host and device machinery that cannot be reached through a correct GEMM.
+ * ------------------------------------------------------------------------------------- */
+
+/* Launch one CTA whose thread waits on a shared-memory mbarrier that nothing ever
+ * arrives at, with a limit of `limit_ns` nanoseconds (clamped to [1e3, 1e9]).  The wait
+ * gives up, records PHX_ERR_TIMEOUT in the status word and the kernel exits normally;
+ * phx_check_device_status() then returns PHX_ERR_TIMEOUT.  No fault, trap or hang. */
+phx_status phx_selftest_bounded_wait(uint64_t limit_ns, phx_stream_t stream);
+
+/* Run the autotuner's selection logic (stages 1 and 2 of phx_autotune) on a simulated
+ * set of `n` candidates without any GPU: candidate i "takes" base_s[i] seconds scaled by
+ * (1 + drift * calls_so_far) plus deterministic noise of relative size `noise`, and
+ * fails if fail[i] != 0.  Writes the chosen index to *picked (-1 if every candidate
+ * failed) and the number of simulated launches to *launches. */
+phx_status phx_selftest_tuner(int n, const double* base_s, const int* fail, double noise,
+                              double drift, int finalists, int rounds, uint64_t seed,
+                              int* picked, int64_t* launches);
+
+/* Argument validation as the GEMM calls perform it, without launching anything and
+ * without touching the device: PHX_OK if (M, N, K, A, B, C) would be accepted. */
+phx_status phx_validate_args(int64_t M, int64_t N, int64_t K, const void* A, const void* B,
+                             const void* C);
+
+/* Library version string. */
+const char* phx_version(void);
+
+#if defined(__GNUC__)
+#pragma GCC visibility pop
+#endif
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PHX_H_ */

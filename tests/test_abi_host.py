@@ -1,0 +1,154 @@
+"""Host-side checks of the C-ABI library that need no GPU: it loads, it exports every
+function include/phx.h declares, and its argument checks, configuration table, config
+parsing and tuner selection logic behave as documented."""
+import ctypes
+
+import pytest
+
+from dense_gemm_04_gb300 import phx
+
+
+def test_every_declared_function_is_exported():
+    declared = phx.declared_functions()
+    assert len(declared) >= 15
+    lib = ctypes.CDLL(phx.LIB_PATH)
+    missing = [f for f in declared if not hasattr(lib, f)]
+    assert not missing, missing
+    # the binding wraps exactly the declared set
+    assert sorted(phx._SIGNATURES) == declared
+
+
+def test_status_strings():
+    for s in range(8):
+        assert phx.status_string(s).startswith("PHX_")
+    assert "unknown" in phx.status_string(99)
+
+
+def test_validate_args():
+    ok, bad = phx.PHX_OK, phx.PHX_ERR_INVALID
+    A, B, C = 0x1000, 0x100000, 0x200000
+    assert phx.validate_args(64, 64, 64, A, B, C) == ok
+    assert phx.validate_args(-1, 4, 4, A, B, C) == bad
+    assert phx.validate_args(4, -1, 4, A, B, C) == bad
+    assert phx.validate_args(4, 4, -1, A, B, C) == bad
+    assert phx.validate_args(1 << 31, 4, 4, A, B, C) == bad          # dimension too large
+    assert phx.validate_args(0, 4, 4, None, None, None) == ok          # empty: nothing touched
+    assert phx.validate_args(4, 0, 4, None, None, None) == ok
+    assert phx.validate_args(4, 4, 0, None, None, C) == ok             # K == 0: A, B unused
+    assert phx.validate_args(4, 4, 4, None, B, C) == bad               # null operand
+    assert phx.validate_args(4, 4, 4, A, B, None) == bad
+    assert phx.validate_args(4, 4, 4, A + 2, B, C) == bad              # not 4-byte aligned
+    assert phx.validate_args(4, 4, 4, A, B, A + 32) == bad             # C overlaps A
+    assert phx.validate_args(4, 4, 4, A, C - 16, C) == bad             # B overlaps C
+    assert phx.validate_args(4, 4, 4, A, A, C) == ok                   # A and B may alias
+
+
+def test_no_device_gives_arch_error_without_launch():
+    # On a machine without a GPU, a valid call reports PHX_ERR_ARCH; an invalid one is
+    # still rejected as invalid first (arguments are checked before the device).
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert phx.phx_sgemm(8, 8, 8, 1.0, 0x1000, 0x2000, 0.0, 0x3000, None) == phx.PHX_ERR_ARCH
+    assert phx.phx_sgemm(-8, 8, 8, 1.0, 0x1000, 0x2000, 0.0, 0x3000, None) == phx.PHX_ERR_INVALID
+    assert phx.phx_gemm_f16tc_f32acc(8, 8, 8, 1.0, 0x1000, 0x2000, 0.0, 0x1000, None) == phx.PHX_ERR_INVALID
+    assert phx.phx_sgemm(0, 8, 8, 1.0, None, None, 0.0, None, None) == phx.PHX_OK
+
+
+@pytest.mark.parametrize("variant", [phx.VARIANT_SGEMM, phx.VARIANT_F16TC])
+def test_config_names_round_trip(variant):
+    names = phx.config_names(variant)
+    assert len(names) == phx.num_configs(variant) > 0
+    assert len(set(names)) == len(names)
+    for name in names:
+        phx.set_config(variant, name)
+        assert phx.get_config(variant, 4096, 4096, 4096) == name
+        # keys in another order parse to the same configuration
+        phx.set_config(variant, " ".join(reversed(name.split())))
+        assert phx.get_config(variant, 512, 512, 512) == name
+    phx.set_config(variant, None)
+
+
+def test_config_parse_errors():
+    for spec in ("TILE_M=128", "TILE_M=128 TILE_N=128 TILE_K=7", "TILE_M=x TILE_N=1 TILE_K=1",
+                 "BOGUS=1 TILE_M=128 TILE_N=128 TILE_K=8", "TILE_M=128 TILE_N=128 TILE_K=8 STAGES=9"):
+        with pytest.raises(phx.PhxError) as e:
+            phx.set_config(phx.VARIANT_SGEMM, spec)
+        assert e.value.status == phx.PHX_ERR_CONFIG
+    with pytest.raises(phx.PhxError):
+        phx.set_config(phx.VARIANT_F16TC, "TILE_M=128 TILE_N=256 TILE_K=64 FMA2=1")
+    with pytest.raises(phx.PhxError):
+        phx.set_config(7, "TILE_M=128 TILE_N=128 TILE_K=8")
+    # the pages' own example pin parses (STAGES left open)
+    phx.set_config(phx.VARIANT_SGEMM, "TILE_M=128 TILE_N=128 TILE_K=8")
+    assert phx.get_config(0, 64, 64, 64).startswith("TILE_M=128 TILE_N=128 TILE_K=8 ")
+    phx.set_config(phx.VARIANT_SGEMM, "")
+
+
+def test_default_config_follows_grid_size():
+    phx.set_config(0, None)
+    phx.set_config(1, None)
+    big = phx.get_config(phx.VARIANT_SGEMM, 4096, 4096, 4096)
+    small = phx.get_config(phx.VARIANT_SGEMM, 1024, 1024, 16384)
+    assert big.startswith("TILE_M=128 TILE_N=128")
+    assert small.startswith("TILE_M=64 TILE_N=64")
+    assert phx.get_config(phx.VARIANT_F16TC, 4096, 4096, 4096).startswith("TILE_M=128 TILE_N=256")
+
+
+def test_workspace_bytes():
+    # A as M x Kp halves and B transposed as N x Kp halves, Kp = K rounded up to 8,
+    # each part rounded up to 256 bytes
+    def want(M, N, K):
+        Kp = (K + 7) // 8 * 8
+        r = lambda b: (b + 255) // 256 * 256
+        return r(M * Kp * 2) + r(N * Kp * 2)
+    for shape in [(4096, 4096, 4096), (4095, 4097, 4093), (1, 1, 1), (16384, 128, 4096)]:
+        assert phx.f16tc_workspace_bytes(*shape) == want(*shape)
+
+
+# ----------------------------------------------------------------------------------------
+# The tuner's selection logic on simulated candidates ("gemm, f32", section "Tuning")
+# ----------------------------------------------------------------------------------------
+
+def test_tuner_picks_fastest():
+    times = [3.0, 1.0, 2.0, 5.0, 1.5, 4.0]
+    picked, launches = phx.selftest_tuner(times, noise=0.02)
+    assert picked == 1
+    assert launches >= 4 * len(times)
+
+
+def test_tuner_skips_failing_candidates():
+    times = [3.0, 1.0, 2.0, 5.0]
+    picked, _ = phx.selftest_tuner(times, fail=[0, 1, 0, 0])
+    assert picked == 2
+    picked, _ = phx.selftest_tuner(times, fail=[1, 1, 1, 1])
+    assert picked == -1
+
+
+def test_tuner_second_stage_resists_drift():
+    # Two finalists 3 % apart while the card slows down over the run (drift): stage 2's
+    # shuffled rounds keep the faster one, whatever the order of the candidates.
+    for seed in range(1, 6):
+        picked, _ = phx.selftest_tuner([1.03, 1.0, 2.0], noise=0.005, drift=2e-3, seed=seed)
+        assert picked == 1, seed
+        picked, _ = phx.selftest_tuner([1.0, 1.03, 2.0], noise=0.005, drift=2e-3, seed=seed)
+        assert picked == 0, seed
+
+
+def test_tuner_cache_file_round_trip(tmp_path):
+    p = tmp_path / "tune.txt"
+    p.write_text("# variant M N K config\n0 4096 4096 4096 TILE_M=128 TILE_N=64 TILE_K=8 STAGES=4 FMA2=0\n"
+                 "1 8192 8192 1024 TILE_M=128 TILE_N=128 TILE_K=64 STAGES=6\n")
+    phx.set_config(0, None)
+    phx.set_config(1, None)
+    phx.tune_cache_load(str(p))
+    assert phx.get_config(0, 4096, 4096, 4096) == "TILE_M=128 TILE_N=64 TILE_K=8 STAGES=4 FMA2=0"
+    assert phx.get_config(1, 8192, 8192, 1024) == "TILE_M=128 TILE_N=128 TILE_K=64 STAGES=6"
+    out = tmp_path / "out.txt"
+    phx.tune_cache_save(str(out))
+    text = out.read_text()
+    assert "0 4096 4096 4096 TILE_M=128 TILE_N=64" in text
+    bad = tmp_path / "bad.txt"
+    bad.write_text("0 1 1 1 TILE_M=3 TILE_N=3 TILE_K=3\n")
+    with pytest.raises(phx.PhxError):
+        phx.tune_cache_load(str(bad))
