@@ -67,6 +67,10 @@ cudaError_t f16tc_gemm_launch(int index, int64_t M, int64_t N, int64_t K, float 
                               float* C, const void* workspace, unsigned int* status, int num_sms,
                               cudaStream_t stream);
 
+// The configuration index a call of `variant` with this shape would use now (pinned, tuned
+// or default), as phx_get_config reports it (phx_api.cu).
+int choose_config_for(int variant, int64_t M, int64_t N, int64_t K, int sms);
+
 // ---------------------------------------------------------------------------------------
 // Probes and self-tests (probes.cu)
 // ---------------------------------------------------------------------------------------

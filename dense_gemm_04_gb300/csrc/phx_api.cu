@@ -415,6 +415,14 @@ phx_status copy_name(const std::string& s, char* buf, size_t buflen) {
 
 }  // namespace
 
+namespace phx {
+// The configuration a call of `variant` with this shape would use (pin, tuned, default),
+// for entry points outside this file.
+int choose_config_for(int variant, int64_t M, int64_t N, int64_t K, int sms) {
+    return choose_config(variant, M, N, K, sms);
+}
+}  // namespace phx
+
 extern "C" {
 
 const char* phx_version(void) { return "phx 0.1 (sm_103a)"; }

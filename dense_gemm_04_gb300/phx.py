@@ -34,6 +34,7 @@ _vp, _cp, _sz = ctypes.c_void_p, ctypes.c_char_p, ctypes.c_size_t
 _SIGNATURES = {
     "phx_sgemm": (_i32, [_i64, _i64, _i64, _f32, _vp, _vp, _f32, _vp, _vp]),
     "phx_gemm_f16tc_f32acc": (_i32, [_i64, _i64, _i64, _f32, _vp, _vp, _f32, _vp, _vp]),
+    "phx_gemm_f16tc_f32acc_noalloc": (_i32, [_i64, _i64, _i64, _f32, _vp, _vp, _f32, _vp, _vp]),
     "phx_f16tc_workspace_bytes": (_i32, [_i64, _i64, _i64, ctypes.POINTER(_sz)]),
     "phx_status_string": (_cp, [_i32]),
     "phx_check_device_status": (_i32, [_vp]),

@@ -91,6 +91,27 @@ phx_status phx_gemm_f16tc_f32acc(int64_t M, int64_t N, int64_t K, float alpha,
                                  const float* A, const float* B, float beta, float* C,
                                  phx_stream_t stream);
 
+/* The same GEMM as phx_gemm_f16tc_f32acc for callers that cannot allocate device memory
+ * while they run: code in a latency-critical loop that must never wait on an allocator (an
+ * allocation can block, grow a pool or fail under memory pressure), or a plug-in whose host
+ * application owns the whole device-memory budget.  The paper has no counterpart; this is
+ * about this library's memory handling only.  Same arguments, rounding, kernels and
+ * results, but the f16 copies of A and B go to one array of static device memory inside the
+ * library, so the call allocates nothing:
+ *   - Limit: phx_f16tc_workspace_bytes(M, N, K) <= 64 MiB (M = N = K = 4096 fits exactly).
+ *     A larger problem returns PHX_ERR_NOMEM before anything is launched.
+ *   - Every GPU that loads this part of the library holds the 64 MiB until the process ends.
+ *   - The first call on each device looks up the array's device address (once per device,
+ *     with that device current); make that first call before any stream capture begins.
+ *   - All calls share the array.  Calls whose GPU work overlaps (different streams, or no
+ *     ordering between them) race and corrupt each other's results: keep them ordered.
+ *     Nothing needs clearing between calls: each call rewrites all the scratch it reads.
+ *   - A device-side wait that gives up records its code in a status word inside that array,
+ *     which phx_check_device_status does not read. */
+phx_status phx_gemm_f16tc_f32acc_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
+                                         const float* A, const float* B, float beta, float* C,
+                                         phx_stream_t stream);
+
 /* Workspace bytes phx_gemm_f16tc_f32acc takes for this shape: the rounded A (M rows) and
  * the rounded, transposed B (N rows), each row padded with zeros to a multiple of 8
  * halves. */
