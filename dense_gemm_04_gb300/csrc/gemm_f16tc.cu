@@ -7,8 +7,8 @@
 // per CTA", "The k loop", "The epilogue").
 //
 // Two passes:
-//   1. Cast (HBM-bound): A (M x K f32) -> Ah (M x Kp f16, row-major) and B (K x N f32) ->
-//      Bt (N x Kp f16, B transposed) with cvt.rn (round to nearest even); Kp = K rounded up
+//   1. Cast (HBM-bound, one launch): A (M x K f32) -> Ah (M x Kp f16, row-major) and B
+//      (K x N f32) -> Bt (N x Kp f16, B transposed) with cvt.rn (round to nearest even); Kp = K rounded up
 //      to a multiple of 8 so every row starts on 16 bytes, the TMA stride rule; the pad
 //      columns are written as zeros.  Both operands end up K-major, the layout the
 //      tensor-core descriptors below describe.
@@ -52,54 +52,77 @@ __host__ __device__ constexpr int64_t round_up(int64_t x, int64_t m) { return (x
 // Cast pass
 // ---------------------------------------------------------------------------------------
 
-// A (rows x K, f32) -> Ah (rows x Kp, f16), each thread writing 8 halves (16 bytes).
-__global__ void cast_rows_kernel(const float* __restrict__ A, __half* __restrict__ Ah,
-                                 int64_t rows, int64_t K, int64_t Kp, int vec) {
-    const int64_t chunks = Kp / 8;
-    const int64_t total = rows * chunks;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
-         idx += stride) {
-        const int64_t r = idx / chunks;
-        const int64_t c = (idx - r * chunks) * 8;
-        const float* src = A + r * K + c;
-        float v[8];
-        if (vec && c + 8 <= K) {
-            const float4 x = __ldcs(reinterpret_cast<const float4*>(src));
-            const float4 y = __ldcs(reinterpret_cast<const float4*>(src + 4));
-            v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
-            v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
-        } else {
-#pragma unroll
-            for (int q = 0; q < 8; ++q) v[q] = (c + q < K) ? src[q] : 0.f;
-        }
-        uint4 out;
-        __half2 h;
-        h = __floats2half2_rn(v[0], v[1]); out.x = *reinterpret_cast<uint32_t*>(&h);
-        h = __floats2half2_rn(v[2], v[3]); out.y = *reinterpret_cast<uint32_t*>(&h);
-        h = __floats2half2_rn(v[4], v[5]); out.z = *reinterpret_cast<uint32_t*>(&h);
-        h = __floats2half2_rn(v[6], v[7]); out.w = *reinterpret_cast<uint32_t*>(&h);
-        *reinterpret_cast<uint4*>(Ah + r * Kp + c) = out;
-    }
+// One launch for both operands.  Blocks [0, a_blocks) round A (rows x K, f32) into Ah
+// (rows x Kp, f16), each thread 8 halves (16 bytes) at a time; blocks from a_blocks on
+// each round and transpose one 64 x 64 tile of B (K x N, f32) into Bt (N x Kp, f16).
+// The B tile goes through shared memory with its columns XOR-swizzled per band of 8 rows,
+// so that both the row-wise 16-byte stores of the loaded tile and the column-wise reads
+// that build Bt's rows hit 32 different banks.
+constexpr int kTT = 64;
+
+__device__ __forceinline__ int tt_swizzle(int k) { return ((k >> 3) & 7) << 2; }
+
+__device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
+    uint4 out;
+    __half2 h;
+    h = __floats2half2_rn(v[0], v[1]); out.x = *reinterpret_cast<uint32_t*>(&h);
+    h = __floats2half2_rn(v[2], v[3]); out.y = *reinterpret_cast<uint32_t*>(&h);
+    h = __floats2half2_rn(v[4], v[5]); out.z = *reinterpret_cast<uint32_t*>(&h);
+    h = __floats2half2_rn(v[6], v[7]); out.w = *reinterpret_cast<uint32_t*>(&h);
+    return out;
 }
 
-// B (K x N, f32) -> Bt (N x Kp, f16): 64 x 64 tiles through shared memory.
-constexpr int kTT = 64;
-__global__ void __launch_bounds__(256) cast_transpose_kernel(const float* __restrict__ B,
-                                                             __half* __restrict__ Bt, int64_t K,
-                                                             int64_t N, int64_t Kp) {
-    __shared__ float tile[kTT][kTT + 1];  // [k][n]
-    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kTT;
-    const int64_t k0 = static_cast<int64_t>(blockIdx.y) * kTT;
+__global__ void __launch_bounds__(256) cast_kernel(const float* __restrict__ A, __half* __restrict__ Ah,
+                                                   int64_t M, int64_t K, int64_t Kp, int vec_a,
+                                                   const float* __restrict__ B, __half* __restrict__ Bt,
+                                                   int64_t N, int vec_b, int a_blocks, int b_tiles_n) {
+    // let the GEMM that follows start its prologue while the cast finishes
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int tid = threadIdx.x;
+    if (static_cast<int>(blockIdx.x) < a_blocks) {
+        const int64_t chunks = Kp / 8;
+        const int64_t total = M * chunks;
+        const int64_t stride = static_cast<int64_t>(a_blocks) * 256;
+        for (int64_t idx = static_cast<int64_t>(blockIdx.x) * 256 + tid; idx < total; idx += stride) {
+            const int64_t r = idx / chunks;
+            const int64_t c = (idx - r * chunks) * 8;
+            const float* src = A + r * K + c;
+            float v[8];
+            if (vec_a && c + 8 <= K) {
+                const float4 x = __ldcs(reinterpret_cast<const float4*>(src));
+                const float4 y = __ldcs(reinterpret_cast<const float4*>(src + 4));
+                v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+                v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
+            } else {
 #pragma unroll
-    for (int i = 0; i < kTT * kTT / 256; ++i) {
+                for (int q = 0; q < 8; ++q) v[q] = (c + q < K) ? src[q] : 0.f;
+            }
+            *reinterpret_cast<uint4*>(Ah + r * Kp + c) = pack8(v);
+        }
+        return;
+    }
+    __shared__ __align__(16) float tile[kTT][kTT];  // [k][n ^ swizzle(k)]
+    const int tb = static_cast<int>(blockIdx.x) - a_blocks;
+    const int64_t n0 = static_cast<int64_t>(tb % b_tiles_n) * kTT;
+    const int64_t k0 = static_cast<int64_t>(tb / b_tiles_n) * kTT;
+#pragma unroll
+    for (int i = 0; i < kTT * kTT / 4 / 256; ++i) {
         const int e = tid + i * 256;
-        const int k = e / kTT;
-        const int n = e % kTT;
+        const int k = e / (kTT / 4);
+        const int n4 = (e % (kTT / 4)) * 4;
         const int64_t gk = k0 + k;
-        const int64_t gn = n0 + n;
-        tile[k][n] = (gk < K && gn < N) ? __ldcs(B + gk * N + gn) : 0.f;
+        const int64_t gn = n0 + n4;
+        float4 v;
+        if (vec_b && gk < K && gn + 3 < N) {
+            v = __ldcs(reinterpret_cast<const float4*>(B + gk * N + gn));
+        } else {
+            const bool rk = gk < K;
+            v.x = (rk && gn + 0 < N) ? B[gk * N + gn + 0] : 0.f;
+            v.y = (rk && gn + 1 < N) ? B[gk * N + gn + 1] : 0.f;
+            v.z = (rk && gn + 2 < N) ? B[gk * N + gn + 2] : 0.f;
+            v.w = (rk && gn + 3 < N) ? B[gk * N + gn + 3] : 0.f;
+        }
+        *reinterpret_cast<float4*>(&tile[k][n4 ^ tt_swizzle(k)]) = v;
     }
     __syncthreads();
 #pragma unroll
@@ -110,13 +133,11 @@ __global__ void __launch_bounds__(256) cast_transpose_kernel(const float* __rest
         const int64_t gn = n0 + n;
         const int64_t gk = k0 + kc;
         if (gn < N && gk < Kp) {
-            uint4 out;
-            __half2 h;
-            h = __floats2half2_rn(tile[kc + 0][n], tile[kc + 1][n]); out.x = *reinterpret_cast<uint32_t*>(&h);
-            h = __floats2half2_rn(tile[kc + 2][n], tile[kc + 3][n]); out.y = *reinterpret_cast<uint32_t*>(&h);
-            h = __floats2half2_rn(tile[kc + 4][n], tile[kc + 5][n]); out.z = *reinterpret_cast<uint32_t*>(&h);
-            h = __floats2half2_rn(tile[kc + 6][n], tile[kc + 7][n]); out.w = *reinterpret_cast<uint32_t*>(&h);
-            *reinterpret_cast<uint4*>(Bt + gn * Kp + gk) = out;
+            const int col = n ^ tt_swizzle(kc);  // the same for the 8 rows kc .. kc+7
+            float v[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) v[q] = tile[kc + q][col];
+            *reinterpret_cast<uint4*>(Bt + gn * Kp + gk) = pack8(v);
         }
     }
 }
@@ -148,7 +169,11 @@ struct TcLayout {
     // offsets from the 1024-byte aligned base
     static constexpr uint32_t kA = 0;
     static constexpr uint32_t kB = STAGES * kABytes;
-    static constexpr uint32_t kBars = STAGES * kStageBytes;           // 8-byte aligned
+    // per epilogue warp, a 32 x 32 f32 chunk with rows padded to 36 floats
+    static constexpr uint32_t kEpiStride = 36;
+    static constexpr uint32_t kEpi = STAGES * kStageBytes;
+    static constexpr uint32_t kEpiBytes = kEpiWarps * 32 * kEpiStride * 4;
+    static constexpr uint32_t kBars = kEpi + kEpiBytes;               // 8-byte aligned
     static constexpr uint32_t kNumBars = 2 * STAGES + 4 + 1;          // full, empty, tfull, tempty, done
     static constexpr uint32_t kTmemSlot = kBars + 8 * kNumBars;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
@@ -161,8 +186,9 @@ struct TcLayout {
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(kThreadsTc, 1)
 gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                  float* __restrict__ C, int M, int N, int num_kb, float alpha, float beta,
-                  int tiles_m, int tiles_n, unsigned int* status) {
+                  const __grid_constant__ CUtensorMap tmB_half, float* __restrict__ C, int M, int N,
+                  int num_kb, float alpha, float beta, int tiles_m, int tiles_n, unsigned int* status,
+                  int full_tiles, int tail_split) {
     using L = TcLayout<BN, STAGES>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -182,11 +208,34 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
+    // Work items, dealt round-robin to the persistent CTAs: every whole tile of the full
+    // rounds, then each remaining (tail) tile as `tail_split` items of width TILE_N /
+    // tail_split, so that a last round with few tiles keeps more SMs busy.  A narrower
+    // item runs the same MMA sequence over K for each of its output elements.
     const int num_tiles = tiles_m * tiles_n;
+    const int num_items = full_tiles + (num_tiles - full_tiles) * tail_split;
+    constexpr int BN_HALF = BN / 2;
+    struct Item { int pm, pn, n0, width; };
+    auto decode = [&](int w) {
+        Item it;
+        int tile = w;
+        it.n0 = 0;
+        it.width = BN;
+        if (w >= full_tiles && tail_split > 1) {
+            const int q = w - full_tiles;
+            tile = full_tiles + q / tail_split;
+            it.width = BN_HALF;
+            it.n0 = (q % tail_split) * BN_HALF;
+        }
+        tc_tile_coords(tile, tiles_m, tiles_n, it.pm, it.pn);
+        it.n0 += it.pn * BN;
+        return it;
+    };
 
     if (warp == kProducerWarp && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmB_half);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
@@ -207,18 +256,23 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 
     if (warp == kProducerWarp) {
         if (lane == 0) {
+            // The operands come from the cast kernel just before this one, which may still be
+            // running (programmatic dependent launch): wait for its writes before loading.
+            asm volatile("griddepcontrol.wait;" ::: "memory");
             // issued[s]: bit 0 = a load was ever issued into slot s, bit 1 = its phase parity
             uint32_t issued_mask = 0, issued_phase = 0;
             uint32_t stage = 0, phase = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                int pm, pn;
-                tc_tile_coords(t, tiles_m, tiles_n, pm, pn);
+            for (int w = blockIdx.x; w < num_items && ok; w += gridDim.x) {
+                const Item it = decode(w);
+                const bool full = it.width == BN;
+                const uint32_t bytes = L::kABytes + (full ? L::kBBytes : L::kBBytes / 2);
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, status)) { ok = false; break; }
-                    mbar_arrive_expect_tx(full_bar(stage), L::kStageBytes);
-                    tma_load_2d(sA + stage * L::kABytes, &tmA, kb * kBK, pm * kBM, full_bar(stage));
-                    tma_load_2d(sB + stage * L::kBBytes, &tmB, kb * kBK, pn * BN, full_bar(stage));
+                    mbar_arrive_expect_tx(full_bar(stage), bytes);
+                    tma_load_2d(sA + stage * L::kABytes, &tmA, kb * kBK, it.pm * kBM, full_bar(stage));
+                    tma_load_2d(sB + stage * L::kBBytes, full ? &tmB : &tmB_half, kb * kBK, it.n0,
+                                full_bar(stage));
                     issued_mask |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -232,11 +286,13 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         }
     } else if (warp == kMmaWarp) {
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16_f32acc(kBM, BN);
+            constexpr uint32_t idesc_full = idesc_f16_f32acc(kBM, BN);
+            constexpr uint32_t idesc_half = idesc_f16_f32acc(kBM, BN_HALF);
             uint32_t stage = 0, phase = 0;
             uint32_t acc = 0, acc_phase = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            for (int w = blockIdx.x; w < num_items && ok; w += gridDim.x) {
+                const uint32_t idesc = decode(w).width == BN ? idesc_full : idesc_half;
                 if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, status)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
@@ -264,54 +320,80 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             mbar_wait_drain(done_bar, 0);
         }
     } else if (warp < kEpiWarps) {
+        float* epi = reinterpret_cast<float*>(base_ptr + L::kEpi) + warp * 32 * L::kEpiStride;
         uint32_t acc = 0, acc_phase = 0;
         const bool read_c = beta != 0.f;
         const bool vec = (N % 4 == 0) && ((reinterpret_cast<uintptr_t>(C) & 15u) == 0);
-        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-            int pm, pn;
-            tc_tile_coords(t, tiles_m, tiles_n, pm, pn);
+        for (int w = blockIdx.x; w < num_items; w += gridDim.x) {
+            const Item it = decode(w);
             // warp-uniform outcome: the tcgen05.ld below is .sync.aligned
             if (!__all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), acc_phase, abort_flag, status))) break;
             tc_fence_after();
-            const int row = pm * kBM + warp * 32 + lane;
-            float* crow = C + static_cast<int64_t>(row) * N;
+            // Each chunk of 32 rows x 32 columns goes from TMEM (lane = row) through this
+            // warp's shared-memory buffer, so that C is read and written along rows: four
+            // rows of 128 bytes per float4 instruction, or one row of 128 bytes per scalar
+            // instruction when N is not a multiple of 4.
+            const int row0 = it.pm * kBM + warp * 32;
             const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + acc * BN;
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
+            for (int c = 0; c < it.width / 32; ++c) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(t_addr + c * 32, r);
                 tmem_ld_wait();
-                const int col0 = pn * BN + c * 32;
-                if (row < M) {
-                    if (vec && col0 + 32 <= N) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    *reinterpret_cast<float4*>(epi + lane * L::kEpiStride + q * 4) =
+                        make_float4(__uint_as_float(r[q * 4 + 0]), __uint_as_float(r[q * 4 + 1]),
+                                    __uint_as_float(r[q * 4 + 2]), __uint_as_float(r[q * 4 + 3]));
+                __syncwarp();
+                const int col0 = it.n0 + c * 32;
+                if (vec) {
+                    const int cc = (lane % 8) * 4;
+                    const int col = col0 + cc;
+                    float4 cv[8];
+                    if (read_c) {
 #pragma unroll
                         for (int q = 0; q < 8; ++q) {
-                            float4* p = reinterpret_cast<float4*>(crow + col0 + q * 4);
-                            float4 o;
-                            o.x = alpha * __uint_as_float(r[q * 4 + 0]);
-                            o.y = alpha * __uint_as_float(r[q * 4 + 1]);
-                            o.z = alpha * __uint_as_float(r[q * 4 + 2]);
-                            o.w = alpha * __uint_as_float(r[q * 4 + 3]);
-                            if (read_c) {
-                                const float4 cv = *p;
-                                o.x = fmaf(beta, cv.x, o.x);
-                                o.y = fmaf(beta, cv.y, o.y);
-                                o.z = fmaf(beta, cv.z, o.z);
-                                o.w = fmaf(beta, cv.w, o.w);
-                            }
-                            *p = o;
+                            const int row = row0 + q * 4 + lane / 8;
+                            cv[q] = (row < M && col < N)
+                                        ? *reinterpret_cast<const float4*>(C + static_cast<int64_t>(row) * N + col)
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
                         }
-                    } else {
+                    }
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            if (col0 + j < N) {
-                                float o = alpha * __uint_as_float(r[j]);
-                                if (read_c) o = fmaf(beta, crow[col0 + j], o);
-                                crow[col0 + j] = o;
+                    for (int q = 0; q < 8; ++q) {
+                        const int rr = q * 4 + lane / 8;
+                        const int row = row0 + rr;
+                        if (row < M && col < N) {
+                            const float4 a = *reinterpret_cast<const float4*>(epi + rr * L::kEpiStride + cc);
+                            float4 o;
+                            o.x = alpha * a.x;
+                            o.y = alpha * a.y;
+                            o.z = alpha * a.z;
+                            o.w = alpha * a.w;
+                            if (read_c) {
+                                o.x = fmaf(beta, cv[q].x, o.x);
+                                o.y = fmaf(beta, cv[q].y, o.y);
+                                o.z = fmaf(beta, cv[q].z, o.z);
+                                o.w = fmaf(beta, cv[q].w, o.w);
                             }
+                            *reinterpret_cast<float4*>(C + static_cast<int64_t>(row) * N + col) = o;
+                        }
+                    }
+                } else {
+                    const int col = col0 + lane;
+#pragma unroll 4
+                    for (int rr = 0; rr < 32; ++rr) {
+                        const int row = row0 + rr;
+                        if (row < M && col < N) {
+                            float* p = C + static_cast<int64_t>(row) * N + col;
+                            float o = alpha * epi[rr * L::kEpiStride + lane];
+                            if (read_c) o = fmaf(beta, *p, o);
+                            *p = o;
                         }
                     }
                 }
+                __syncwarp();  // the buffer is rewritten by the next chunk
             }
             tc_fence_before();
             __syncwarp();
@@ -365,8 +447,8 @@ bool make_map(CUtensorMap* map, const __half* ptr, int64_t rows, int64_t Kp, int
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-using TcKernelFn = void (*)(CUtensorMap, CUtensorMap, float*, int, int, int, float, float, int,
-                            int, unsigned int*);
+using TcKernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, float*, int, int, int, float,
+                            float, int, int, unsigned int*, int, int);
 
 struct TcEntry {
     F16Config cfg;
@@ -402,17 +484,16 @@ cudaError_t f16tc_cast_launch(int64_t M, int64_t N, int64_t K, const float* A, c
     const int64_t Kp = round_up(K, 8);
     __half* Ah = static_cast<__half*>(workspace);
     __half* Bt = reinterpret_cast<__half*>(static_cast<char*>(workspace) + round_up(M * Kp * 2, 256));
-    const int vec = (K % 4 == 0) && ((reinterpret_cast<uintptr_t>(A) & 15u) == 0);
-    const int64_t total = M * (Kp / 8);
-    int64_t blocks = (total + 255) / 256;
-    const int64_t cap = static_cast<int64_t>(num_sms) * 16;
-    if (blocks > cap) blocks = cap;
-    cast_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(A, Ah, M, K, Kp, vec);
-    cudaError_t err = cudaGetLastError();
-    if (err != cudaSuccess) return err;
-    const dim3 grid(static_cast<unsigned>((N + kTT - 1) / kTT), static_cast<unsigned>((Kp + kTT - 1) / kTT));
-    if (grid.y > 65535u) return cudaErrorInvalidValue;
-    cast_transpose_kernel<<<grid, 256, 0, stream>>>(B, Bt, K, N, Kp);
+    const int vec_a = (K % 4 == 0) && ((reinterpret_cast<uintptr_t>(A) & 15u) == 0);
+    const int vec_b = (N % 4 == 0) && ((reinterpret_cast<uintptr_t>(B) & 15u) == 0);
+    int64_t a_blocks = (M * (Kp / 8) + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    if (a_blocks > cap) a_blocks = cap;
+    const int64_t b_tiles_n = (N + kTT - 1) / kTT;
+    const int64_t b_tiles = b_tiles_n * ((Kp + kTT - 1) / kTT);
+    if (a_blocks + b_tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    cast_kernel<<<static_cast<unsigned>(a_blocks + b_tiles), 256, 0, stream>>>(
+        A, Ah, M, K, Kp, vec_a, B, Bt, N, vec_b, static_cast<int>(a_blocks), static_cast<int>(b_tiles_n));
     return cudaGetLastError();
 }
 
@@ -424,8 +505,9 @@ cudaError_t f16tc_gemm_launch(int index, int64_t M, int64_t N, int64_t K, float 
     const __half* Ah = static_cast<const __half*>(workspace);
     const __half* Bt = reinterpret_cast<const __half*>(static_cast<const char*>(workspace) +
                                                        round_up(M * Kp * 2, 256));
-    CUtensorMap mapA, mapB;
-    if (!make_map(&mapA, Ah, M, Kp, kBM) || !make_map(&mapB, Bt, N, Kp, e.cfg.tile_n))
+    CUtensorMap mapA, mapB, mapB_half;
+    if (!make_map(&mapA, Ah, M, Kp, kBM) || !make_map(&mapB, Bt, N, Kp, e.cfg.tile_n) ||
+        !make_map(&mapB_half, Bt, N, Kp, e.cfg.tile_n / 2))
         return cudaErrorInvalidValue;
     cudaError_t err = cudaFuncSetAttribute(reinterpret_cast<const void*>(e.fn),
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -434,12 +516,38 @@ cudaError_t f16tc_gemm_launch(int index, int64_t M, int64_t N, int64_t K, float 
     const int tiles_m = static_cast<int>((M + kBM - 1) / kBM);
     const int tiles_n = static_cast<int>((N + e.cfg.tile_n - 1) / e.cfg.tile_n);
     const int64_t tiles = static_cast<int64_t>(tiles_m) * tiles_n;
-    const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
+    // Whole tiles for the full rounds of the persistent grid; the tiles of a last, partial
+    // round go out as two half-width items each when that still fits in one round.
+    const int64_t full = tiles >= num_sms ? tiles / num_sms * num_sms : 0;
+    const int64_t tail = tiles - full;
+    const int tail_split = (tail > 0 && 2 * tail <= num_sms) ? 2 : 1;
+    const int64_t items = full + tail * tail_split;
+    const int grid = static_cast<int>(items < num_sms ? items : num_sms);
     const int num_kb = static_cast<int>((K + kBK - 1) / kBK);
-    e.fn<<<grid, kThreadsTc, e.smem, stream>>>(mapA, mapB, C, static_cast<int>(M),
-                                               static_cast<int>(N), num_kb, alpha, beta, tiles_m,
-                                               tiles_n, status);
-    return cudaGetLastError();
+    // Launched as a programmatic dependent of the cast kernel, so that its prologue (barrier
+    // set-up, tensor-memory allocation, descriptor prefetch) overlaps the end of the cast;
+    // the producer warp waits for the cast's writes before its first load.
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(static_cast<unsigned>(grid));
+    lc.blockDim = dim3(kThreadsTc);
+    lc.dynamicSmemBytes = e.smem;
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    const int m32 = static_cast<int>(M), n32 = static_cast<int>(N), full32 = static_cast<int>(full);
+    err = cudaLaunchKernelEx(&lc, e.fn, mapA, mapB, mapB_half, C, m32, n32, num_kb, alpha, beta,
+                             tiles_m, tiles_n, status, full32, tail_split);
+    if (err != cudaSuccess) {
+        // a stream that does not take programmatic launches: launch normally
+        cudaGetLastError();
+        lc.numAttrs = 0;
+        err = cudaLaunchKernelEx(&lc, e.fn, mapA, mapB, mapB_half, C, m32, n32, num_kb, alpha, beta,
+                                 tiles_m, tiles_n, status, full32, tail_split);
+    }
+    return err;
 }
 
 }  // namespace phx

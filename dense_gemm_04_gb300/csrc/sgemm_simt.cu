@@ -89,8 +89,8 @@ __host__ __device__ constexpr int sgemm_smem_floats(int bm, int bn, int bk, int 
     return stages * bm * bk + 2 * bk * at_row_stride(bm) + stages * bk * bn;
 }
 
-template <int BM, int BN, int BK, int STAGES, int TM, int TN, bool MASKED, bool FMA2>
-__global__ void __launch_bounds__(kThreads, 2)
+template <int BM, int BN, int BK, int STAGES, int TM, int TN, bool MASKED, bool FMA2, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB)
 sgemm_kernel(const float* __restrict__ A, const float* __restrict__ B, float* __restrict__ C,
              int M, int N, int K, float alpha, float beta) {
     constexpr int WTM = kLanesM * TM;  // warp tile
@@ -304,7 +304,7 @@ __global__ void scale_c_kernel(float* __restrict__ C, int64_t n, float beta) {
 // The compiled configurations.  The pages' search space is TILE_M, TILE_N in
 // {32, 64, 128, 256} and TILE_K in {4, 8, 16, 32} ("gemm, f32", section "The attributes",
 // @autotune row); this build compiles the part of it that a 256-thread CTA with
-// 4x4..8x8 register micro-tiles covers, times STAGES in {3, 4} and the FMA2 switch.
+// 4x4..8x16 register micro-tiles covers, times STAGES in {3, 4} and the FMA2 switch.
 // ---------------------------------------------------------------------------------------
 using KernelFn = void (*)(const float*, const float*, float*, int, int, int, float, float);
 
@@ -319,9 +319,11 @@ template <int BM, int BN, int BK, int STAGES, int FMA2>
 constexpr Entry make_entry() {
     constexpr int TM = BM / 16;  // 4 warps x 4 lanes along M
     constexpr int TN = BN / 16;  // 2 warps x 8 lanes along N
+    // up to 64 accumulators a thread: two CTAs per SM (128 registers); 128: one CTA
+    constexpr int MINB = TM * TN > 64 ? 1 : 2;
     return Entry{SgemmConfig{BM, BN, BK, STAGES, FMA2},
-                 &sgemm_kernel<BM, BN, BK, STAGES, TM, TN, false, FMA2 != 0>,
-                 &sgemm_kernel<BM, BN, BK, STAGES, TM, TN, true, FMA2 != 0>,
+                 &sgemm_kernel<BM, BN, BK, STAGES, TM, TN, false, FMA2 != 0, MINB>,
+                 &sgemm_kernel<BM, BN, BK, STAGES, TM, TN, true, FMA2 != 0, MINB>,
                  sgemm_smem_floats(BM, BN, BK, STAGES) * 4};
 }
 
@@ -333,6 +335,9 @@ const Entry kEntries[] = {
     make_entry<128, 64, 8, 4, 0>(),   make_entry<128, 64, 16, 4, 1>(),
     make_entry<64, 128, 8, 4, 0>(),   make_entry<64, 128, 16, 4, 1>(),
     make_entry<64, 64, 8, 4, 0>(),    make_entry<64, 64, 16, 4, 0>(),
+    make_entry<128, 256, 8, 4, 1>(),  make_entry<128, 256, 16, 3, 1>(),
+    make_entry<128, 256, 16, 4, 1>(), make_entry<256, 128, 8, 4, 1>(),
+    make_entry<256, 128, 16, 3, 1>(),
 };
 constexpr int kNumEntries = sizeof(kEntries) / sizeof(kEntries[0]);
 

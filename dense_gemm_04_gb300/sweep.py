@@ -1,0 +1,200 @@
+"""Shape and arithmetic-intensity sweep of both GEMM precisions, placed on the roofline.
+
+    python -m dense_gemm_04_gb300.sweep [--out results.json] [--quick]
+
+For every shape of the workload sweep ((8192, 8192, 1024), (1024, 1024, 16384),
+(16384, 128, 4096), (4095, 4097, 4093) with alpha = 2, beta = -1; squares 512 .. 16384 with
+alpha = 1, beta = 0; and 4096^3 with alpha = 1, beta = 0.5) and both precisions, this measures
+the GEMM the way the matrix-multiplication lab's stopwatches do: settle the clock with synced
+calls, then take the median of CUDA-event timings ("steady"), with the shapes visited in a
+freshly shuffled order every round ("sweep").  Each result is placed on its roofline,
+min(peak, bandwidth x intensity), with intensity = 2MNK / minimum bytes (each f32 input
+read once, C written once and read when beta != 0), following the lab's minimum-traffic
+intensity (Part 5, the skinny-matrix sweep).
+
+The roofs are measured here as well: the FP32 multiply-add probe and the tensor-core probe
+run back to back for two seconds each while nvidia-smi samples the clocks (the lab's
+"sustained"), next to a streaming-read probe.  Inputs are synthetic uniform [-1, 1) matrices.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+from . import phx
+
+SHAPES = [
+    ("4096^3", 4096, 4096, 4096, 1.0, 0.5),
+    ("8192x8192x1024", 8192, 8192, 1024, 2.0, -1.0),
+    ("1024x1024x16384", 1024, 1024, 16384, 2.0, -1.0),
+    ("16384x128x4096", 16384, 128, 4096, 2.0, -1.0),
+    ("4095x4097x4093", 4095, 4097, 4093, 2.0, -1.0),
+] + [(f"{n}^3", n, n, n, 1.0, 0.0) for n in (512, 1024, 2048, 4096, 8192, 16384)]
+
+
+class Clocks:
+    """nvidia-smi SM clock and power samples every 200 ms while active."""
+
+    def __init__(self, gpu: int = 0):
+        self.gpu, self.samples, self._stop = gpu, [], threading.Event()
+
+    def _loop(self):
+        while not self._stop.is_set():
+            try:
+                out = subprocess.run(["nvidia-smi", "-i", str(self.gpu),
+                                      "--query-gpu=clocks.sm,power.draw,clocks_event_reasons.active",
+                                      "--format=csv,noheader,nounits"],
+                                     capture_output=True, text=True, timeout=5).stdout.strip()
+                p = [x.strip() for x in out.split(",")]
+                self.samples.append((float(p[0]), float(p[1]), p[2]))
+            except (OSError, ValueError, IndexError, subprocess.TimeoutExpired):
+                pass
+            self._stop.wait(0.2)
+
+    def __enter__(self):
+        self._t = threading.Thread(target=self._loop, daemon=True)
+        self._t.start()
+        return self
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        self._t.join()
+
+    def summary(self):
+        if not self.samples:
+            return {}
+        sm = sorted(s[0] for s in self.samples)
+        return {"sm_mhz_median": sm[len(sm) // 2], "power_w_max": max(s[1] for s in self.samples),
+                "samples": len(sm), "reasons": sorted({s[2] for s in self.samples})}
+
+
+def _sync():
+    import torch
+    torch.cuda.synchronize()
+
+
+def steady(fn, seconds=0.5, min_calls=3):
+    """Median seconds per call after settling for seconds/2 with one synced call at a time."""
+    import torch
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds / 2:
+        fn()
+        _sync()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ts, t0 = [], time.perf_counter()
+    while time.perf_counter() - t0 < seconds or len(ts) < min_calls:
+        s.record()
+        fn()
+        e.record()
+        e.synchronize()
+        ts.append(s.elapsed_time(e) / 1e3)
+    return float(np.median(ts))
+
+
+def sustained(fn, seconds=2.0):
+    """Seconds per call under continuous load, with the clocks it ran at."""
+    import torch
+    fn()
+    _sync()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks() as clk:
+        s.record()
+        n, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < seconds:
+            fn()
+            n += 1
+            if n % 4 == 0:
+                _sync()
+        e.record()
+        e.synchronize()
+    return s.elapsed_time(e) / 1e3 / n, clk.summary()
+
+
+def measure_roofs(seconds=2.0):
+    import torch
+    dev = torch.cuda.current_device()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    st = torch.cuda.current_stream().cuda_stream
+    roofs = {"sms": sms}
+    blocks, iters = sms * 8 * 8, 20000
+    out = torch.empty(blocks * 256, device="cuda")
+    for packed in (0, 1):
+        t, clk = sustained(lambda: phx.check(phx.phx_probe_ffma(packed, blocks, iters, out.data_ptr(), st)), seconds)
+        roofs["fp32_ffma2" if packed else "fp32_ffma"] = {
+            "tflops": blocks * 256 * iters * 16 * (2 if packed else 1) / t / 1e12, "clocks": clk}
+    sink = torch.empty(sms, device="cuda")
+    t, clk = sustained(lambda: phx.check(phx.phx_probe_mma_f16(sms, 4000, 256, sink.data_ptr(), st)), seconds)
+    roofs["f16_tensor"] = {"tflops": sms * 4000 * 4 * 2 * 128 * 256 * 16 / t / 1e12, "clocks": clk}
+    x = torch.ones(1 << 28, device="cuda")
+    t = steady(lambda: phx.check(phx.phx_probe_stream_read(x.data_ptr(), x.numel(), sink.data_ptr(), sms * 8, st)))
+    roofs["hbm_read_gbs"] = x.numel() * 4 / t / 1e9
+    del x
+    return roofs
+
+
+def run(quick=False, rounds=3, seed=0):
+    import torch
+    st = torch.cuda.current_stream().cuda_stream
+    roofs = measure_roofs(1.0 if quick else 2.0)
+    fp32 = max(roofs["fp32_ffma"]["tflops"], roofs["fp32_ffma2"]["tflops"])
+    tc = roofs["f16_tensor"]["tflops"]
+    bw = roofs["hbm_read_gbs"]
+    shapes = [s for s in SHAPES if not (quick and s[1] * s[2] * s[3] > 2 ** 40)]
+    cases = [(s, v) for s in shapes for v in ("sgemm", "f16tc")]
+    times = {c: [] for c in range(len(cases))}
+    rng = np.random.default_rng(seed)
+    for _ in range(rounds):
+        for ci in rng.permutation(len(cases)):
+            (name, M, N, K, alpha, beta), v = cases[ci]
+            A = torch.rand(M, K, device="cuda") * 2 - 1
+            B = torch.rand(K, N, device="cuda") * 2 - 1
+            C = torch.rand(M, N, device="cuda") * 2 - 1
+            fn = phx.phx_sgemm if v == "sgemm" else phx.phx_gemm_f16tc_f32acc
+            call = lambda: phx.check(fn(M, N, K, alpha, A.data_ptr(), B.data_ptr(), beta, C.data_ptr(), st))
+            times[ci].append(steady(call, seconds=0.3 if quick else 0.5))
+            del A, B, C
+            torch.cuda.empty_cache()
+    rows = []
+    for ci, ((name, M, N, K, alpha, beta), v) in enumerate(cases):
+        t = float(np.median(times[ci]))
+        flops = 2.0 * M * N * K
+        nbytes = 4.0 * (M * K + K * N + M * N * (2 if beta != 0 else 1))
+        ai = flops / nbytes
+        peak = fp32 if v == "sgemm" else tc
+        roof = min(peak * 1e12, bw * 1e9 * ai)
+        rows.append({"shape": name, "M": M, "N": N, "K": K, "alpha": alpha, "beta": beta, "variant": v,
+                     "config": phx.get_config(0 if v == "sgemm" else 1, M, N, K),
+                     "seconds": t, "tflops": flops / t / 1e12, "intensity": ai,
+                     "roof_tflops": roof / 1e12, "pct_of_roof": 100 * flops / t / roof,
+                     "bound": "compute" if roof >= peak * 1e12 else "hbm",
+                     "seconds_all": times[ci]})
+    return {"roofs": roofs, "rows": rows}
+
+
+def main():
+    ap = argparse.ArgumentParser(description="GEMM shape sweep on the roofline")
+    ap.add_argument("--out", default=None)
+    ap.add_argument("--quick", action="store_true", help="skip shapes above 2^40 MNK and shorten timings")
+    args = ap.parse_args()
+    res = run(quick=args.quick)
+    r = res["roofs"]
+    print(f"roofs: FP32 {r['fp32_ffma']['tflops']:.1f} / f32x2 {r['fp32_ffma2']['tflops']:.1f} TFLOP/s, "
+          f"f16 tensor {r['f16_tensor']['tflops']:.0f} TFLOP/s, HBM read {r['hbm_read_gbs']:.0f} GB/s")
+    for row in res["rows"]:
+        print(f"{row['shape']:>16s} {row['variant']:6s} {row['tflops']:8.1f} TFLOP/s  "
+              f"{row['pct_of_roof']:5.1f}% of {row['bound']} roof ({row['roof_tflops']:.0f})  [{row['config']}]")
+    if args.out:
+        with open(args.out, "w") as f:
+            json.dump(res, f, indent=1)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

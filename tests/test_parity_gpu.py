@@ -229,3 +229,53 @@ def test_lab_error_levels():
     lab_max, lab_fro = rows["f16_in_f32_acc"]
     assert st == phx.PHX_OK
     assert lab_fro / 1.5 <= e_fro <= lab_fro * 1.5 and lab_max / 2 <= e_max <= lab_max * 2, (e_max, e_fro)
+
+
+# ----------------------------------------------------------------------------------------
+# Tail waves: rows of tiles handed to a half-height launch (f32) and tiles dealt out as
+# half-width items (tensor cores) when the tile count leaves the last wave part-empty
+# ----------------------------------------------------------------------------------------
+
+TAIL_SHAPES = [(640, 512, 2048), (650, 500, 2000), (5000, 300, 700), (4224, 4096, 256), (129, 257, 4100)]
+
+
+@pytest.mark.parametrize("vname", list(VARIANTS))
+def test_tail_wave_paths(vname):
+    variant, _ = VARIANTS[vname]
+    for cfg in phx.config_names(variant):
+        phx.set_config(variant, cfg)
+        for M, N, K in TAIL_SHAPES[:2]:
+            _check(vname, M, N, K, 2.0, -1.0, "int3")
+            _check(vname, M, N, K, 2.0, -1.0, "uniform", seed=M + K)
+    phx.set_config(variant, None)
+    for M, N, K in TAIL_SHAPES[2:]:
+        _check(vname, M, N, K, 1.5, 0.5, "int3")
+        _check(vname, M, N, K, 1.5, 0.5, "uniform", seed=N)
+
+
+@pytest.mark.parametrize("vname", list(VARIANTS))
+def test_results_identical_run_to_run(vname):
+    variant, _ = VARIANTS[vname]
+    for M, N, K in [(640, 512, 2048), (4096, 4096, 4096)]:
+        A, B, C = synth.problem(M, N, K, seed=17)
+        outs = [run_cuda(variant, A, B, C, 1.0, 0.5)[1] for _ in range(3)]
+        for o in outs[1:]:
+            assert np.array_equal(o.view(np.uint32), outs[0].view(np.uint32)), (vname, M, N, K)
+
+
+def test_tiling_does_not_change_values():
+    # each output element is one k-ordered chain of multiply-adds (f32) or one k-ordered
+    # sequence of MMAs (f16 tensor cores) whatever the tile shape, so every configuration
+    # gives the same bits on the same inputs
+    M, N, K = 640, 512, 1000
+    A, B, C = synth.problem(M, N, K, seed=23)
+    for vname, (variant, _) in VARIANTS.items():
+        ref = None
+        for cfg in phx.config_names(variant):
+            phx.set_config(variant, cfg)
+            got = run_cuda(variant, A, B, C, 1.0, 0.5)[1]
+            if ref is None:
+                ref = got
+            else:
+                assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), (vname, cfg)
+        phx.set_config(variant, None)
