@@ -183,7 +183,11 @@ struct TcLayout {
     static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "swizzle atoms stay 1024-aligned");
 };
 
-template <int BN, int STAGES>
+// MC: the CTAs run in clusters of two that take vertically adjacent tiles with the same
+// B tile.  Each CTA loads one half of that B tile and multicasts it to both, so each SM
+// pulls half of B's bytes from L2; each MMA thread frees a ring slot in both CTAs (a
+// multicast commit), because both CTAs' loads land in both CTAs' slots.
+template <int BN, int STAGES, bool MC>
 __global__ void __launch_bounds__(kThreadsTc, 1)
 gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const __grid_constant__ CUtensorMap tmB_half, float* __restrict__ C, int M, int N,
@@ -208,11 +212,16 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
+    const uint32_t rank = MC ? cluster_ctarank() : 0u;          // position in the CTA pair
+    const int first_item = MC ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
+    const int item_stride = MC ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
+    // with MC a "tile" is a pair of vertically adjacent tiles; CTA `rank` takes one of them
+    const int tiles_rows = MC ? (tiles_m + 1) / 2 : tiles_m;
     // Work items, dealt round-robin to the persistent CTAs: every whole tile of the full
     // rounds, then each remaining (tail) tile as `tail_split` items of width TILE_N /
     // tail_split, so that a last round with few tiles keeps more SMs busy.  A narrower
     // item runs the same MMA sequence over K for each of its output elements.
-    const int num_tiles = tiles_m * tiles_n;
+    const int num_tiles = tiles_rows * tiles_n;
     const int num_items = full_tiles + (num_tiles - full_tiles) * tail_split;
     constexpr int BN_HALF = BN / 2;
     struct Item { int pm, pn, n0, width; };
@@ -227,7 +236,8 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             it.width = BN_HALF;
             it.n0 = (q % tail_split) * BN_HALF;
         }
-        tc_tile_coords(tile, tiles_m, tiles_n, it.pm, it.pn);
+        tc_tile_coords(tile, tiles_rows, tiles_n, it.pm, it.pn);
+        if (MC) it.pm = 2 * it.pm + static_cast<int>(rank);
         it.n0 += it.pn * BN;
         return it;
     };
@@ -238,7 +248,7 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         tma_prefetch_desc(&tmB_half);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
+            mbar_init(empty_bar(s), MC ? 2 : 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
@@ -251,6 +261,7 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     if (warp == 0) tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
     tc_fence_before();
     __syncthreads();
+    if (MC) cluster_sync();  // both CTAs' barriers exist before any multicast reaches them
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -263,7 +274,7 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             uint32_t issued_mask = 0, issued_phase = 0;
             uint32_t stage = 0, phase = 0;
             bool ok = true;
-            for (int w = blockIdx.x; w < num_items && ok; w += gridDim.x) {
+            for (int w = first_item; w < num_items && ok; w += item_stride) {
                 const Item it = decode(w);
                 const bool full = it.width == BN;
                 const uint32_t bytes = L::kABytes + (full ? L::kBBytes : L::kBBytes / 2);
@@ -271,8 +282,15 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, status)) { ok = false; break; }
                     mbar_arrive_expect_tx(full_bar(stage), bytes);
                     tma_load_2d(sA + stage * L::kABytes, &tmA, kb * kBK, it.pm * kBM, full_bar(stage));
-                    tma_load_2d(sB + stage * L::kBBytes, full ? &tmB : &tmB_half, kb * kBK, it.n0,
-                                full_bar(stage));
+                    if (MC && full) {
+                        // this CTA's half of the shared B tile, to both CTAs of the pair
+                        tma_load_2d_multicast(sB + stage * L::kBBytes + rank * (L::kBBytes / 2), &tmB_half,
+                                              kb * kBK, it.n0 + static_cast<int>(rank) * BN_HALF,
+                                              full_bar(stage), 0x3);
+                    } else {
+                        tma_load_2d(sB + stage * L::kBBytes, full ? &tmB : &tmB_half, kb * kBK, it.n0,
+                                    full_bar(stage));
+                    }
                     issued_mask |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -291,7 +309,7 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             uint32_t stage = 0, phase = 0;
             uint32_t acc = 0, acc_phase = 0;
             bool ok = true;
-            for (int w = blockIdx.x; w < num_items && ok; w += gridDim.x) {
+            for (int w = first_item; w < num_items && ok; w += item_stride) {
                 const uint32_t idesc = decode(w).width == BN ? idesc_full : idesc_half;
                 if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, status)) { ok = false; break; }
                 tc_fence_after();
@@ -307,7 +325,10 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                                    sw128_kmajor_desc(b0 + k * kUmmaK * 2), idesc,
                                    (kb | k) != 0 ? 1u : 0u);
                     }
-                    mma_commit(empty_bar(stage));
+                    if (MC)
+                        mma_commit_multicast(empty_bar(stage), 0x3);  // the slot is free in both CTAs
+                    else
+                        mma_commit(empty_bar(stage));
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
@@ -324,7 +345,7 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         uint32_t acc = 0, acc_phase = 0;
         const bool read_c = beta != 0.f;
         const bool vec = (N % 4 == 0) && ((reinterpret_cast<uintptr_t>(C) & 15u) == 0);
-        for (int w = blockIdx.x; w < num_items; w += gridDim.x) {
+        for (int w = first_item; w < num_items; w += item_stride) {
             const Item it = decode(w);
             // warp-uniform outcome: the tcgen05.ld below is .sync.aligned
             if (!__all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), acc_phase, abort_flag, status))) break;
@@ -405,6 +426,9 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 
     tc_fence_before();
     __syncthreads();
+    // with MC, neither CTA leaves while the other may still multicast into it or arrive on
+    // its barriers
+    if (MC) cluster_sync();
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem_base, L::kTmemCols);
@@ -456,15 +480,16 @@ struct TcEntry {
     uint32_t smem;
 };
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int CLUSTER>
 TcEntry make_tc_entry() {
-    return TcEntry{F16Config{kBM, BN, kBK, STAGES}, &gemm_f16tc_kernel<BN, STAGES>,
+    return TcEntry{F16Config{kBM, BN, kBK, STAGES, CLUSTER}, &gemm_f16tc_kernel<BN, STAGES, CLUSTER == 2>,
                    TcLayout<BN, STAGES>::kDynSmem};
 }
 
 const TcEntry kTcEntries[] = {
-    make_tc_entry<256, 4>(), make_tc_entry<256, 3>(), make_tc_entry<128, 6>(),
-    make_tc_entry<128, 4>(), make_tc_entry<64, 8>(),
+    make_tc_entry<256, 4, 1>(), make_tc_entry<256, 3, 1>(), make_tc_entry<128, 6, 1>(),
+    make_tc_entry<128, 4, 1>(), make_tc_entry<64, 8, 1>(),  make_tc_entry<256, 4, 2>(),
+    make_tc_entry<128, 6, 2>(),
 };
 constexpr int kNumTc = sizeof(kTcEntries) / sizeof(kTcEntries[0]);
 
@@ -515,14 +540,17 @@ cudaError_t f16tc_gemm_launch(int index, int64_t M, int64_t N, int64_t K, float 
     if (err != cudaSuccess) return err;
     const int tiles_m = static_cast<int>((M + kBM - 1) / kBM);
     const int tiles_n = static_cast<int>((N + e.cfg.tile_n - 1) / e.cfg.tile_n);
-    const int64_t tiles = static_cast<int64_t>(tiles_m) * tiles_n;
+    // With clusters of two, work is counted in pairs of tiles and in CTA pairs.
+    const bool mc = e.cfg.cluster == 2;
+    const int64_t workers = mc ? num_sms / 2 : num_sms;
+    const int64_t tiles = static_cast<int64_t>(mc ? (tiles_m + 1) / 2 : tiles_m) * tiles_n;
     // Whole tiles for the full rounds of the persistent grid; the tiles of a last, partial
     // round go out as two half-width items each when that still fits in one round.
-    const int64_t full = tiles >= num_sms ? tiles / num_sms * num_sms : 0;
+    const int64_t full = tiles >= workers ? tiles / workers * workers : 0;
     const int64_t tail = tiles - full;
-    const int tail_split = (tail > 0 && 2 * tail <= num_sms) ? 2 : 1;
+    const int tail_split = (tail > 0 && 2 * tail <= workers) ? 2 : 1;
     const int64_t items = full + tail * tail_split;
-    const int grid = static_cast<int>(items < num_sms ? items : num_sms);
+    const int grid = static_cast<int>((items < workers ? items : workers) * (mc ? 2 : 1));
     const int num_kb = static_cast<int>((K + kBK - 1) / kBK);
     // Launched as a programmatic dependent of the cast kernel, so that its prologue (barrier
     // set-up, tensor-memory allocation, descriptor prefetch) overlaps the end of the cast;
@@ -532,18 +560,22 @@ cudaError_t f16tc_gemm_launch(int index, int64_t M, int64_t N, int64_t K, float 
     lc.blockDim = dim3(kThreadsTc);
     lc.dynamicSmemBytes = e.smem;
     lc.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = mc ? 2 : 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     lc.attrs = attr;
-    lc.numAttrs = 1;
+    lc.numAttrs = 2;
     const int m32 = static_cast<int>(M), n32 = static_cast<int>(N), full32 = static_cast<int>(full);
     err = cudaLaunchKernelEx(&lc, e.fn, mapA, mapB, mapB_half, C, m32, n32, num_kb, alpha, beta,
                              tiles_m, tiles_n, status, full32, tail_split);
     if (err != cudaSuccess) {
         // a stream that does not take programmatic launches: launch normally
         cudaGetLastError();
-        lc.numAttrs = 0;
+        lc.numAttrs = 1;
         err = cudaLaunchKernelEx(&lc, e.fn, mapA, mapB, mapB_half, C, m32, n32, num_kb, alpha, beta,
                                  tiles_m, tiles_n, status, full32, tail_split);
     }

@@ -46,6 +46,7 @@ cudaError_t scale_c_launch(int64_t M, int64_t N, float beta, float* C, cudaStrea
 // ---------------------------------------------------------------------------------------
 struct F16Config {
     int tile_m, tile_n, tile_k, stages;
+    int cluster;  // 1, or 2: CTA pairs share their B tile through TMA multicast
 };
 
 int f16tc_num_configs();

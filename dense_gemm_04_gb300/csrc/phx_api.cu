@@ -149,14 +149,15 @@ std::string config_name(int variant, int i) {
                       c.tile_n, c.tile_k, c.stages, c.fma2);
     } else {
         const F16Config& c = phx::f16tc_config(i);
-        std::snprintf(buf, sizeof buf, "TILE_M=%d TILE_N=%d TILE_K=%d STAGES=%d", c.tile_m, c.tile_n,
-                      c.tile_k, c.stages);
+        std::snprintf(buf, sizeof buf, "TILE_M=%d TILE_N=%d TILE_K=%d STAGES=%d%s", c.tile_m, c.tile_n,
+                      c.tile_k, c.stages, c.cluster == 2 ? " CLUSTER=2" : "");
     }
     return buf;
 }
 
 // Parse "KEY=value KEY=value ..." and return the first compiled config that matches every
-// given key (TILE_M, TILE_N, TILE_K required; STAGES and FMA2 optional), or -1.
+// given key (TILE_M, TILE_N, TILE_K required; STAGES optional; FMA2 for the f32 variant and
+// CLUSTER for the f16 variant optional, default 0 and 1), or -1.
 int parse_config(int variant, const char* spec) {
     if (spec == nullptr) return -1;
     std::map<std::string, int> kv;
@@ -170,26 +171,29 @@ int parse_config(int variant, const char* spec) {
         char* end = nullptr;
         const long v = std::strtol(val.c_str(), &end, 10);
         if (end == nullptr || *end != '\0') return -1;
-        if (key != "TILE_M" && key != "TILE_N" && key != "TILE_K" && key != "STAGES" && key != "FMA2")
+        if (key != "TILE_M" && key != "TILE_N" && key != "TILE_K" && key != "STAGES" && key != "FMA2" &&
+            key != "CLUSTER")
             return -1;
         if (variant == PHX_VARIANT_F16TC && key == "FMA2") return -1;
+        if (variant == PHX_VARIANT_SGEMM && key == "CLUSTER") return -1;
         kv[key] = static_cast<int>(v);
     }
     if (!kv.count("TILE_M") || !kv.count("TILE_N") || !kv.count("TILE_K")) return -1;
     const int n = num_configs(variant);
     for (int i = 0; i < n; ++i) {
-        int tm, tn, tk, st, f2 = 0;
+        int tm, tn, tk, st, f2 = 0, cl = 1;
         if (variant == PHX_VARIANT_SGEMM) {
             const SgemmConfig& c = phx::sgemm_config(i);
             tm = c.tile_m; tn = c.tile_n; tk = c.tile_k; st = c.stages; f2 = c.fma2;
         } else {
             const F16Config& c = phx::f16tc_config(i);
-            tm = c.tile_m; tn = c.tile_n; tk = c.tile_k; st = c.stages;
+            tm = c.tile_m; tn = c.tile_n; tk = c.tile_k; st = c.stages; cl = c.cluster;
         }
         if (kv["TILE_M"] != tm || kv["TILE_N"] != tn || kv["TILE_K"] != tk) continue;
         if (kv.count("STAGES") && kv["STAGES"] != st) continue;
         if (kv.count("FMA2") && kv["FMA2"] != f2) continue;
         if (!kv.count("FMA2") && variant == PHX_VARIANT_SGEMM && f2 != 0) continue;
+        if ((kv.count("CLUSTER") ? kv["CLUSTER"] : 1) != cl) continue;
         return i;
     }
     return -1;

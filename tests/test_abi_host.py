@@ -152,3 +152,22 @@ def test_tuner_cache_file_round_trip(tmp_path):
     bad.write_text("0 1 1 1 TILE_M=3 TILE_N=3 TILE_K=3\n")
     with pytest.raises(phx.PhxError):
         phx.tune_cache_load(str(bad))
+
+
+def test_cluster_key():
+    names = phx.config_names(phx.VARIANT_F16TC)
+    clustered = [n for n in names if n.endswith(" CLUSTER=2")]
+    assert clustered, names
+    for n in clustered:
+        phx.set_config(phx.VARIANT_F16TC, n)
+        assert phx.get_config(phx.VARIANT_F16TC, 4096, 4096, 4096) == n
+    # without the key, the pair-free configuration of the same tile is meant
+    base = clustered[0].replace(" CLUSTER=2", "")
+    phx.set_config(phx.VARIANT_F16TC, base)
+    assert phx.get_config(phx.VARIANT_F16TC, 4096, 4096, 4096) == base
+    for bad in (base + " CLUSTER=3", ):
+        with pytest.raises(phx.PhxError):
+            phx.set_config(phx.VARIANT_F16TC, bad)
+    with pytest.raises(phx.PhxError):
+        phx.set_config(phx.VARIANT_SGEMM, "TILE_M=128 TILE_N=128 TILE_K=16 CLUSTER=2")
+    phx.set_config(phx.VARIANT_F16TC, None)
