@@ -159,10 +159,21 @@ __device__ __forceinline__ void tc_tile_coords(int t, int tiles_m, int tiles_n, 
     pn = r / rows;
 }
 
-template <int BN, int STAGES>
+// PAIR selects how CTAs cooperate:
+//   0  one CTA per tile;
+//   1  clusters of two CTAs take vertically adjacent tiles with the same B tile; each loads
+//      one half of that B tile and multicasts it to both (each SM pulls half of B's bytes
+//      from L2), and each MMA thread frees a ring slot in both CTAs (multicast commit);
+//   2  clusters of two CTAs run the 2-SM MMA (tcgen05.mma.cta_group::2, M = 256): each CTA
+//      stages its own 128 rows of A and its own half of the B tile, and the even CTA's MMA
+//      thread multiplies the pair's 256 x TILE_N tile, each CTA receiving its 128 rows of
+//      the accumulator.  A CTA stages 2/3 of the bytes per k block that PAIR 0 does for the
+//      same MMA work, so the same shared memory holds more k blocks in flight.
+template <int BN, int STAGES, int PAIR>
 struct TcLayout {
+    static constexpr int kBRows = PAIR == 2 ? BN / 2 : BN;   // B rows a CTA stages per k block
     static constexpr uint32_t kABytes = kBM * kBK * 2;
-    static constexpr uint32_t kBBytes = BN * kBK * 2;
+    static constexpr uint32_t kBBytes = kBRows * kBK * 2;
     static constexpr uint32_t kStageBytes = kABytes + kBBytes;
     static constexpr uint32_t kTmemCols = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64
                                           : (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
@@ -179,21 +190,19 @@ struct TcLayout {
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     static constexpr uint32_t kEnd = kAbort + 4;
     static constexpr uint32_t kDynSmem = kEnd + 1024;                 // + alignment slack
-    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "tcgen05 M=128 needs N % 16 == 0, N <= 256");
+    static_assert(BN % 16 == 0 && BN >= 32 && BN <= 256, "tcgen05 needs N % 16 == 0, N <= 256");
     static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "swizzle atoms stay 1024-aligned");
 };
 
-// MC: the CTAs run in clusters of two that take vertically adjacent tiles with the same
-// B tile.  Each CTA loads one half of that B tile and multicasts it to both, so each SM
-// pulls half of B's bytes from L2; each MMA thread frees a ring slot in both CTAs (a
-// multicast commit), because both CTAs' loads land in both CTAs' slots.
-template <int BN, int STAGES, bool MC>
+template <int BN, int STAGES, int PAIR>
 __global__ void __launch_bounds__(kThreadsTc, 1)
 gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                  const __grid_constant__ CUtensorMap tmB_half, float* __restrict__ C, int M, int N,
-                  int num_kb, float alpha, float beta, int tiles_m, int tiles_n, unsigned int* status,
-                  int full_tiles, int tail_split) {
-    using L = TcLayout<BN, STAGES>;
+                  const __grid_constant__ CUtensorMap tmB_half, const __grid_constant__ CUtensorMap tmB_quarter,
+                  float* __restrict__ C, int M, int N, int num_kb, float alpha, float beta, int tiles_m,
+                  int tiles_n, unsigned int* status, int full_tiles, int tail_split) {
+    using L = TcLayout<BN, STAGES, PAIR>;
+    constexpr bool kPair = PAIR != 0;
+    constexpr bool kTwoSm = PAIR == 2;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -212,15 +221,16 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    const uint32_t rank = MC ? cluster_ctarank() : 0u;          // position in the CTA pair
-    const int first_item = MC ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
-    const int item_stride = MC ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
-    // with MC a "tile" is a pair of vertically adjacent tiles; CTA `rank` takes one of them
-    const int tiles_rows = MC ? (tiles_m + 1) / 2 : tiles_m;
-    // Work items, dealt round-robin to the persistent CTAs: every whole tile of the full
-    // rounds, then each remaining (tail) tile as `tail_split` items of width TILE_N /
-    // tail_split, so that a last round with few tiles keeps more SMs busy.  A narrower
-    // item runs the same MMA sequence over K for each of its output elements.
+    const uint32_t rank = kPair ? cluster_ctarank() : 0u;  // position in the CTA pair
+    const bool leader = rank == 0;
+    const int first_item = kPair ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
+    const int item_stride = kPair ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
+    // with a pair, a "tile" is two vertically adjacent tiles; CTA `rank` takes one of them
+    const int tiles_rows = kPair ? (tiles_m + 1) / 2 : tiles_m;
+    // Work items, dealt round-robin to the persistent CTAs (or pairs): every whole tile of
+    // the full rounds, then each remaining (tail) tile as `tail_split` items of width
+    // TILE_N / tail_split, so that a last round with few tiles keeps more SMs busy.  A
+    // narrower item runs the same MMA sequence over K for each of its output elements.
     const int num_tiles = tiles_rows * tiles_n;
     const int num_items = full_tiles + (num_tiles - full_tiles) * tail_split;
     constexpr int BN_HALF = BN / 2;
@@ -237,7 +247,7 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             it.n0 = (q % tail_split) * BN_HALF;
         }
         tc_tile_coords(tile, tiles_rows, tiles_n, it.pm, it.pn);
-        if (MC) it.pm = 2 * it.pm + static_cast<int>(rank);
+        if (kPair) it.pm = 2 * it.pm + static_cast<int>(rank);
         it.n0 += it.pn * BN;
         return it;
     };
@@ -246,22 +256,29 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
         tma_prefetch_desc(&tmB_half);
+        tma_prefetch_desc(&tmB_quarter);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), MC ? 2 : 1);
+            mbar_init(empty_bar(s), PAIR == 1 ? 2 : 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
-            mbar_init(tempty_bar(a), kEpiWarps);
+            mbar_init(tempty_bar(a), kTwoSm ? 2 * kEpiWarps : kEpiWarps);
         }
         mbar_init(done_bar, 1);
         *abort_flag = 0;
         mbar_fence_init();
     }
-    if (warp == 0) tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
+    if (kTwoSm) cluster_sync();  // both CTAs present before the pair allocates tensor memory
+    if (warp == 0) {
+        if (kTwoSm)
+            tmem_alloc_2sm(smem_u32(tmem_slot), L::kTmemCols);
+        else
+            tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
+    }
     tc_fence_before();
     __syncthreads();
-    if (MC) cluster_sync();  // both CTAs' barriers exist before any multicast reaches them
+    if (kPair) cluster_sync();  // both CTAs' barriers exist before the other signals them
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -277,35 +294,49 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             for (int w = first_item; w < num_items && ok; w += item_stride) {
                 const Item it = decode(w);
                 const bool full = it.width == BN;
-                const uint32_t bytes = L::kABytes + (full ? L::kBBytes : L::kBBytes / 2);
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, status)) { ok = false; break; }
-                    mbar_arrive_expect_tx(full_bar(stage), bytes);
-                    tma_load_2d(sA + stage * L::kABytes, &tmA, kb * kBK, it.pm * kBM, full_bar(stage));
-                    if (MC && full) {
-                        // this CTA's half of the shared B tile, to both CTAs of the pair
-                        tma_load_2d_multicast(sB + stage * L::kBBytes + rank * (L::kBBytes / 2), &tmB_half,
-                                              kb * kBK, it.n0 + static_cast<int>(rank) * BN_HALF,
-                                              full_bar(stage), 0x3);
+                    const uint32_t a_dst = sA + stage * L::kABytes;
+                    const uint32_t b_dst = sB + stage * L::kBBytes;
+                    if constexpr (kTwoSm) {
+                        // each CTA: its 128 rows of A and its share of B, counted on the even
+                        // CTA's barrier, which expects the pair's bytes
+                        const uint32_t cta_bytes = L::kABytes + (full ? L::kBBytes : L::kBBytes / 2);
+                        const uint32_t lbar = map_to_rank(full_bar(stage), 0);
+                        if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * cta_bytes);
+                        tma_load_2d_2sm(a_dst, &tmA, kb * kBK, it.pm * kBM, lbar);
+                        if (full)
+                            tma_load_2d_2sm(b_dst, &tmB_half, kb * kBK, it.n0 + static_cast<int>(rank) * BN_HALF, lbar);
+                        else
+                            tma_load_2d_2sm(b_dst, &tmB_quarter, kb * kBK, it.n0 + static_cast<int>(rank) * (BN / 4), lbar);
                     } else {
-                        tma_load_2d(sB + stage * L::kBBytes, full ? &tmB : &tmB_half, kb * kBK, it.n0,
-                                    full_bar(stage));
+                        mbar_arrive_expect_tx(full_bar(stage), L::kABytes + (full ? L::kBBytes : L::kBBytes / 2));
+                        tma_load_2d(a_dst, &tmA, kb * kBK, it.pm * kBM, full_bar(stage));
+                        if (PAIR == 1 && full) {
+                            // this CTA's half of the shared B tile, to both CTAs of the pair
+                            tma_load_2d_multicast(b_dst + rank * (L::kBBytes / 2), &tmB_half, kb * kBK,
+                                                  it.n0 + static_cast<int>(rank) * BN_HALF, full_bar(stage), 0x3);
+                        } else {
+                            tma_load_2d(b_dst, full ? &tmB : &tmB_half, kb * kBK, it.n0, full_bar(stage));
+                        }
                     }
                     issued_mask |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
             }
-            if (!ok) {
-                // Aborted: let every load this thread issued land before the CTA exits.
+            if (!ok && (!kTwoSm || leader)) {
+                // Aborted: let every load issued into this CTA land before the CTA exits (in
+                // a 2-SM pair the even CTA's barriers count both CTAs' loads).
                 for (int s = 0; s < STAGES; ++s)
                     if (issued_mask & (1u << s)) mbar_wait_drain(full_bar(s), (issued_phase >> s) & 1u);
             }
         }
     } else if (warp == kMmaWarp) {
-        if (lane == 0) {
-            constexpr uint32_t idesc_full = idesc_f16_f32acc(kBM, BN);
-            constexpr uint32_t idesc_half = idesc_f16_f32acc(kBM, BN_HALF);
+        if (lane == 0 && (!kTwoSm || leader)) {
+            constexpr int kMmaM = kTwoSm ? 2 * kBM : kBM;
+            constexpr uint32_t idesc_full = idesc_f16_f32acc(kMmaM, BN);
+            constexpr uint32_t idesc_half = idesc_f16_f32acc(kMmaM, BN_HALF);
             uint32_t stage = 0, phase = 0;
             uint32_t acc = 0, acc_phase = 0;
             bool ok = true;
@@ -321,23 +352,36 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     const uint32_t b0 = sB + stage * L::kBBytes;
 #pragma unroll
                     for (int k = 0; k < kBK / kUmmaK; ++k) {
-                        mma_f16_ss(d_tmem, sw128_kmajor_desc(a0 + k * kUmmaK * 2),
-                                   sw128_kmajor_desc(b0 + k * kUmmaK * 2), idesc,
-                                   (kb | k) != 0 ? 1u : 0u);
+                        const uint64_t ad = sw128_kmajor_desc(a0 + k * kUmmaK * 2);
+                        const uint64_t bd = sw128_kmajor_desc(b0 + k * kUmmaK * 2);
+                        const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
+                        if constexpr (kTwoSm)
+                            mma_f16_ss_2sm(d_tmem, ad, bd, idesc, accum);
+                        else
+                            mma_f16_ss(d_tmem, ad, bd, idesc, accum);
                     }
-                    if (MC)
-                        mma_commit_multicast(empty_bar(stage), 0x3);  // the slot is free in both CTAs
+                    // the slot is free again (in both CTAs of a pair)
+                    if constexpr (kTwoSm)
+                        mma_commit_2sm_multicast(empty_bar(stage), 0x3);
+                    else if constexpr (PAIR == 1)
+                        mma_commit_multicast(empty_bar(stage), 0x3);
                     else
                         mma_commit(empty_bar(stage));
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                mma_commit(tfull_bar(acc));
+                if constexpr (kTwoSm)
+                    mma_commit_2sm_multicast(tfull_bar(acc), 0x3);
+                else
+                    mma_commit(tfull_bar(acc));
                 acc ^= 1u;
                 if (acc == 0) acc_phase ^= 1u;
             }
             // Every MMA this thread issued has completed once done_bar fires.
-            mma_commit(done_bar);
+            if constexpr (kTwoSm)
+                mma_commit_2sm(done_bar);
+            else
+                mma_commit(done_bar);
             mbar_wait_drain(done_bar, 0);
         }
     } else if (warp < kEpiWarps) {
@@ -418,7 +462,14 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(tempty_bar(acc));
+            if (lane == 0) {
+                // the accumulator buffer may be reused (in a 2-SM pair, the even CTA's MMA
+                // thread counts both CTAs' epilogue warps)
+                if constexpr (kTwoSm)
+                    mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
+                else
+                    mbar_arrive(tempty_bar(acc));
+            }
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
         }
@@ -426,12 +477,14 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 
     tc_fence_before();
     __syncthreads();
-    // with MC, neither CTA leaves while the other may still multicast into it or arrive on
-    // its barriers
-    if (MC) cluster_sync();
+    // with a pair, neither CTA leaves while the other may still write into it or signal it
+    if (kPair) cluster_sync();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, L::kTmemCols);
+        if (kTwoSm)
+            tmem_dealloc_2sm(tmem_base, L::kTmemCols);
+        else
+            tmem_dealloc(tmem_base, L::kTmemCols);
     }
 }
 
@@ -471,8 +524,8 @@ bool make_map(CUtensorMap* map, const __half* ptr, int64_t rows, int64_t Kp, int
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-using TcKernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, float*, int, int, int, float,
-                            float, int, int, unsigned int*, int, int);
+using TcKernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, float*, int, int, int,
+                            float, float, int, int, unsigned int*, int, int);
 
 struct TcEntry {
     F16Config cfg;
@@ -480,16 +533,19 @@ struct TcEntry {
     uint32_t smem;
 };
 
-template <int BN, int STAGES, int CLUSTER>
+// PAIR 0 and 1 run in the configuration names as CLUSTER=1 / CLUSTER=2 (TILE_M = 128 per CTA);
+// PAIR 2 as TILE_M=256 (the pair's 2-SM tile).
+template <int BN, int STAGES, int PAIR>
 TcEntry make_tc_entry() {
-    return TcEntry{F16Config{kBM, BN, kBK, STAGES, CLUSTER}, &gemm_f16tc_kernel<BN, STAGES, CLUSTER == 2>,
-                   TcLayout<BN, STAGES>::kDynSmem};
+    return TcEntry{F16Config{PAIR == 2 ? 2 * kBM : kBM, BN, kBK, STAGES, PAIR == 0 ? 1 : 2},
+                   &gemm_f16tc_kernel<BN, STAGES, PAIR>, TcLayout<BN, STAGES, PAIR>::kDynSmem};
 }
 
 const TcEntry kTcEntries[] = {
-    make_tc_entry<256, 4, 1>(), make_tc_entry<256, 3, 1>(), make_tc_entry<128, 6, 1>(),
-    make_tc_entry<128, 4, 1>(), make_tc_entry<64, 8, 1>(),  make_tc_entry<256, 4, 2>(),
-    make_tc_entry<128, 6, 2>(),
+    make_tc_entry<256, 4, 0>(), make_tc_entry<256, 3, 0>(), make_tc_entry<128, 6, 0>(),
+    make_tc_entry<128, 4, 0>(), make_tc_entry<64, 8, 0>(),  make_tc_entry<256, 4, 1>(),
+    make_tc_entry<128, 6, 1>(), make_tc_entry<256, 6, 2>(), make_tc_entry<256, 5, 2>(),
+    make_tc_entry<128, 8, 2>(),
 };
 constexpr int kNumTc = sizeof(kTcEntries) / sizeof(kTcEntries[0]);
 
@@ -530,18 +586,19 @@ cudaError_t f16tc_gemm_launch(int index, int64_t M, int64_t N, int64_t K, float 
     const __half* Ah = static_cast<const __half*>(workspace);
     const __half* Bt = reinterpret_cast<const __half*>(static_cast<const char*>(workspace) +
                                                        round_up(M * Kp * 2, 256));
-    CUtensorMap mapA, mapB, mapB_half;
+    CUtensorMap mapA, mapB, mapB_half, mapB_quarter;
     if (!make_map(&mapA, Ah, M, Kp, kBM) || !make_map(&mapB, Bt, N, Kp, e.cfg.tile_n) ||
-        !make_map(&mapB_half, Bt, N, Kp, e.cfg.tile_n / 2))
+        !make_map(&mapB_half, Bt, N, Kp, e.cfg.tile_n / 2) ||
+        !make_map(&mapB_quarter, Bt, N, Kp, e.cfg.tile_n / 4))
         return cudaErrorInvalidValue;
     cudaError_t err = cudaFuncSetAttribute(reinterpret_cast<const void*>(e.fn),
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(e.smem));
     if (err != cudaSuccess) return err;
-    const int tiles_m = static_cast<int>((M + kBM - 1) / kBM);
+    const int tiles_m = static_cast<int>((M + kBM - 1) / kBM);  // 128-row tiles (one per CTA)
     const int tiles_n = static_cast<int>((N + e.cfg.tile_n - 1) / e.cfg.tile_n);
     // With clusters of two, work is counted in pairs of tiles and in CTA pairs.
-    const bool mc = e.cfg.cluster == 2;
+    const bool mc = e.cfg.cluster == 2;  // CTA pairs (multicast, or the 2-SM MMA)
     const int64_t workers = mc ? num_sms / 2 : num_sms;
     const int64_t tiles = static_cast<int64_t>(mc ? (tiles_m + 1) / 2 : tiles_m) * tiles_n;
     // Whole tiles for the full rounds of the persistent grid; the tiles of a last, partial
@@ -570,14 +627,14 @@ cudaError_t f16tc_gemm_launch(int index, int64_t M, int64_t N, int64_t K, float 
     lc.attrs = attr;
     lc.numAttrs = 2;
     const int m32 = static_cast<int>(M), n32 = static_cast<int>(N), full32 = static_cast<int>(full);
-    err = cudaLaunchKernelEx(&lc, e.fn, mapA, mapB, mapB_half, C, m32, n32, num_kb, alpha, beta,
-                             tiles_m, tiles_n, status, full32, tail_split);
+    err = cudaLaunchKernelEx(&lc, e.fn, mapA, mapB, mapB_half, mapB_quarter, C, m32, n32, num_kb, alpha,
+                             beta, tiles_m, tiles_n, status, full32, tail_split);
     if (err != cudaSuccess) {
         // a stream that does not take programmatic launches: launch normally
         cudaGetLastError();
         lc.numAttrs = 1;
-        err = cudaLaunchKernelEx(&lc, e.fn, mapA, mapB, mapB_half, C, m32, n32, num_kb, alpha, beta,
-                                 tiles_m, tiles_n, status, full32, tail_split);
+        err = cudaLaunchKernelEx(&lc, e.fn, mapA, mapB, mapB_half, mapB_quarter, C, m32, n32, num_kb,
+                                 alpha, beta, tiles_m, tiles_n, status, full32, tail_split);
     }
     return err;
 }

@@ -149,8 +149,10 @@ std::string config_name(int variant, int i) {
                       c.tile_n, c.tile_k, c.stages, c.fma2);
     } else {
         const F16Config& c = phx::f16tc_config(i);
+        // CLUSTER=2 is written out for CTA pairs of 128-row tiles; a 256-row tile is always
+        // a 2-SM pair
         std::snprintf(buf, sizeof buf, "TILE_M=%d TILE_N=%d TILE_K=%d STAGES=%d%s", c.tile_m, c.tile_n,
-                      c.tile_k, c.stages, c.cluster == 2 ? " CLUSTER=2" : "");
+                      c.tile_k, c.stages, (c.cluster == 2 && c.tile_m == 128) ? " CLUSTER=2" : "");
     }
     return buf;
 }
@@ -193,7 +195,8 @@ int parse_config(int variant, const char* spec) {
         if (kv.count("STAGES") && kv["STAGES"] != st) continue;
         if (kv.count("FMA2") && kv["FMA2"] != f2) continue;
         if (!kv.count("FMA2") && variant == PHX_VARIANT_SGEMM && f2 != 0) continue;
-        if ((kv.count("CLUSTER") ? kv["CLUSTER"] : 1) != cl) continue;
+        const int cl_default = (variant == PHX_VARIANT_F16TC && tm == 256) ? 2 : 1;
+        if ((kv.count("CLUSTER") ? kv["CLUSTER"] : cl_default) != cl) continue;
         return i;
     }
     return -1;
@@ -223,6 +226,7 @@ int default_config(int variant, int64_t M, int64_t N, int sms) {
         if (ceil_div(M, 128) * ceil_div(N, 64) >= slots) return parse_config(variant, "TILE_M=128 TILE_N=64 TILE_K=8 STAGES=4");
         return parse_config(variant, "TILE_M=64 TILE_N=64 TILE_K=8 STAGES=4");
     }
+    if (ceil_div(M, 256) * ceil_div(N, 256) >= sms / 2) return parse_config(variant, "TILE_M=256 TILE_N=256 TILE_K=64 STAGES=6");
     if (ceil_div(M, 128) * ceil_div(N, 256) >= sms) return parse_config(variant, "TILE_M=128 TILE_N=256 TILE_K=64 STAGES=4");
     if (ceil_div(M, 128) * ceil_div(N, 128) >= sms) return parse_config(variant, "TILE_M=128 TILE_N=128 TILE_K=64 STAGES=6");
     return parse_config(variant, "TILE_M=128 TILE_N=64 TILE_K=64 STAGES=8");

@@ -92,7 +92,7 @@ def test_default_config_follows_grid_size():
     small = phx.get_config(phx.VARIANT_SGEMM, 1024, 1024, 16384)
     assert big.startswith("TILE_M=128 TILE_N=128")
     assert small.startswith("TILE_M=64 TILE_N=64")
-    assert phx.get_config(phx.VARIANT_F16TC, 4096, 4096, 4096).startswith("TILE_M=128 TILE_N=256")
+    assert phx.get_config(phx.VARIANT_F16TC, 4096, 4096, 4096).startswith("TILE_M=256 TILE_N=256")
 
 
 def test_workspace_bytes():
