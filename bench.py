@@ -367,7 +367,7 @@ def gpu_arm(args):
                    "algorithmic_bytes": 2.0 * (M * K + K * N) + 4.0 * 2 * M * N}
     cast_bytes = 6.0 * (M * K + K * N)
     cast_gbs = cast_bytes / (cast_ms / 1e3) / 1e9
-    roofline_cast = {"bound": "hbm", "kernel": "f32->f16 cast pass (A and B, 2 launches)", "achieved": cast_gbs,
+    roofline_cast = {"bound": "hbm", "kernel": "f32->f16 cast pass (A and B, one launch)", "achieved": cast_gbs,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": cast_gbs / peaks["hbm_gbs"],
                      "traffic": _traffic_from_profiles("f16_cast"), "algorithmic_bytes": cast_bytes}
     f16_ms = tc_ms + cast_ms

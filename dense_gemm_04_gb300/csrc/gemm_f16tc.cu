@@ -446,15 +446,23 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         }
                     }
                 } else {
+                    // all 32 rows' loads of C first, so they are in flight together
                     const int col = col0 + lane;
-#pragma unroll 4
+                    float cs[32];
+                    if (read_c) {
+#pragma unroll
+                        for (int rr = 0; rr < 32; ++rr) {
+                            const int row = row0 + rr;
+                            cs[rr] = (row < M && col < N) ? C[static_cast<int64_t>(row) * N + col] : 0.f;
+                        }
+                    }
+#pragma unroll
                     for (int rr = 0; rr < 32; ++rr) {
                         const int row = row0 + rr;
                         if (row < M && col < N) {
-                            float* p = C + static_cast<int64_t>(row) * N + col;
                             float o = alpha * epi[rr * L::kEpiStride + lane];
-                            if (read_c) o = fmaf(beta, *p, o);
-                            *p = o;
+                            if (read_c) o = fmaf(beta, cs[rr], o);
+                            C[static_cast<int64_t>(row) * N + col] = o;
                         }
                     }
                 }
