@@ -199,7 +199,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const __grid_constant__ CUtensorMap tmB_half, const __grid_constant__ CUtensorMap tmB_quarter,
                   float* __restrict__ C, int M, int N, int num_kb, float alpha, float beta, int tiles_m,
-                  int tiles_n, unsigned int* status, int full_tiles, int tail_split) {
+                  int tiles_n, unsigned int* status, int full_tiles, int tail_split, int ksplit,
+                  int kb_per_slice, float* __restrict__ partial) {
     using L = TcLayout<BN, STAGES, PAIR>;
     constexpr bool kPair = PAIR != 0;
     constexpr bool kTwoSm = PAIR == 2;
@@ -231,16 +232,27 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     // the full rounds, then each remaining (tail) tile as `tail_split` items of width
     // TILE_N / tail_split, so that a last round with few tiles keeps more SMs busy.  A
     // narrower item runs the same MMA sequence over K for each of its output elements.
+    // With ksplit > 1 (a grid too small for the GPU) every tile is instead `ksplit` items,
+    // one per k slice of kb_per_slice k blocks, each writing its partial product (alpha = 1,
+    // beta = 0) to its own M x N plane of `partial` for a separate reduction.
     const int num_tiles = tiles_rows * tiles_n;
-    const int num_items = full_tiles + (num_tiles - full_tiles) * tail_split;
+    const int num_items = ksplit > 1 ? num_tiles * ksplit : full_tiles + (num_tiles - full_tiles) * tail_split;
     constexpr int BN_HALF = BN / 2;
-    struct Item { int pm, pn, n0, width; };
+    struct Item { int pm, pn, n0, width, kb0, nkb, slice; };
     auto decode = [&](int w) {
         Item it;
         int tile = w;
         it.n0 = 0;
         it.width = BN;
-        if (w >= full_tiles && tail_split > 1) {
+        it.kb0 = 0;
+        it.nkb = num_kb;
+        it.slice = -1;
+        if (ksplit > 1) {
+            tile = w / ksplit;
+            it.slice = w - tile * ksplit;
+            it.kb0 = it.slice * kb_per_slice;
+            it.nkb = min(kb_per_slice, num_kb - it.kb0);
+        } else if (w >= full_tiles && tail_split > 1) {
             const int q = w - full_tiles;
             tile = full_tiles + q / tail_split;
             it.width = BN_HALF;
@@ -294,7 +306,7 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             for (int w = first_item; w < num_items && ok; w += item_stride) {
                 const Item it = decode(w);
                 const bool full = it.width == BN;
-                for (int kb = 0; kb < num_kb; ++kb) {
+                for (int kb = it.kb0; kb < it.kb0 + it.nkb; ++kb) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, status)) { ok = false; break; }
                     const uint32_t a_dst = sA + stage * L::kABytes;
                     const uint32_t b_dst = sB + stage * L::kBBytes;
@@ -341,11 +353,12 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             uint32_t acc = 0, acc_phase = 0;
             bool ok = true;
             for (int w = first_item; w < num_items && ok; w += item_stride) {
-                const uint32_t idesc = decode(w).width == BN ? idesc_full : idesc_half;
+                const Item it = decode(w);
+                const uint32_t idesc = it.width == BN ? idesc_full : idesc_half;
                 if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, status)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int kb = 0; kb < num_kb; ++kb) {
+                for (int kb = 0; kb < it.nkb; ++kb) {
                     if (!mbar_wait(full_bar(stage), phase, abort_flag, status)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t a0 = sA + stage * L::kABytes;
@@ -387,10 +400,15 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     } else if (warp < kEpiWarps) {
         float* epi = reinterpret_cast<float*>(base_ptr + L::kEpi) + warp * 32 * L::kEpiStride;
         uint32_t acc = 0, acc_phase = 0;
-        const bool read_c = beta != 0.f;
-        const bool vec = (N % 4 == 0) && ((reinterpret_cast<uintptr_t>(C) & 15u) == 0);
+        const bool vec = (N % 4 == 0) && ((reinterpret_cast<uintptr_t>(C) & 15u) == 0) &&
+                         (partial == nullptr || (reinterpret_cast<uintptr_t>(partial) & 15u) == 0);
         for (int w = first_item; w < num_items; w += item_stride) {
             const Item it = decode(w);
+            // a k slice writes its plane of partial products; a whole tile writes C
+            float* Cout = it.slice >= 0 ? partial + static_cast<int64_t>(it.slice) * M * N : C;
+            const float a_out = it.slice >= 0 ? 1.f : alpha;
+            const float b_out = it.slice >= 0 ? 0.f : beta;
+            const bool read_c = b_out != 0.f;
             // warp-uniform outcome: the tcgen05.ld below is .sync.aligned
             if (!__all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), acc_phase, abort_flag, status))) break;
             tc_fence_after();
@@ -421,7 +439,7 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         for (int q = 0; q < 8; ++q) {
                             const int row = row0 + q * 4 + lane / 8;
                             cv[q] = (row < M && col < N)
-                                        ? *reinterpret_cast<const float4*>(C + static_cast<int64_t>(row) * N + col)
+                                        ? *reinterpret_cast<const float4*>(Cout + static_cast<int64_t>(row) * N + col)
                                         : make_float4(0.f, 0.f, 0.f, 0.f);
                         }
                     }
@@ -432,17 +450,17 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         if (row < M && col < N) {
                             const float4 a = *reinterpret_cast<const float4*>(epi + rr * L::kEpiStride + cc);
                             float4 o;
-                            o.x = alpha * a.x;
-                            o.y = alpha * a.y;
-                            o.z = alpha * a.z;
-                            o.w = alpha * a.w;
+                            o.x = a_out * a.x;
+                            o.y = a_out * a.y;
+                            o.z = a_out * a.z;
+                            o.w = a_out * a.w;
                             if (read_c) {
-                                o.x = fmaf(beta, cv[q].x, o.x);
-                                o.y = fmaf(beta, cv[q].y, o.y);
-                                o.z = fmaf(beta, cv[q].z, o.z);
-                                o.w = fmaf(beta, cv[q].w, o.w);
+                                o.x = fmaf(b_out, cv[q].x, o.x);
+                                o.y = fmaf(b_out, cv[q].y, o.y);
+                                o.z = fmaf(b_out, cv[q].z, o.z);
+                                o.w = fmaf(b_out, cv[q].w, o.w);
                             }
-                            *reinterpret_cast<float4*>(C + static_cast<int64_t>(row) * N + col) = o;
+                            *reinterpret_cast<float4*>(Cout + static_cast<int64_t>(row) * N + col) = o;
                         }
                     }
                 } else {
@@ -453,16 +471,16 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 #pragma unroll
                         for (int rr = 0; rr < 32; ++rr) {
                             const int row = row0 + rr;
-                            cs[rr] = (row < M && col < N) ? C[static_cast<int64_t>(row) * N + col] : 0.f;
+                            cs[rr] = (row < M && col < N) ? Cout[static_cast<int64_t>(row) * N + col] : 0.f;
                         }
                     }
 #pragma unroll
                     for (int rr = 0; rr < 32; ++rr) {
                         const int row = row0 + rr;
                         if (row < M && col < N) {
-                            float o = alpha * epi[rr * L::kEpiStride + lane];
-                            if (read_c) o = fmaf(beta, cs[rr], o);
-                            C[static_cast<int64_t>(row) * N + col] = o;
+                            float o = a_out * epi[rr * L::kEpiStride + lane];
+                            if (read_c) o = fmaf(b_out, cs[rr], o);
+                            Cout[static_cast<int64_t>(row) * N + col] = o;
                         }
                     }
                 }
@@ -533,7 +551,7 @@ bool make_map(CUtensorMap* map, const __half* ptr, int64_t rows, int64_t Kp, int
 }
 
 using TcKernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, float*, int, int, int,
-                            float, float, int, int, unsigned int*, int, int);
+                            float, float, int, int, unsigned int*, int, int, int, int, float*);
 
 struct TcEntry {
     F16Config cfg;
@@ -586,9 +604,38 @@ cudaError_t f16tc_cast_launch(int64_t M, int64_t N, int64_t K, const float* A, c
     return cudaGetLastError();
 }
 
+namespace {
+
+constexpr int kTcMaxSplit = 8;
+constexpr int kTcMinKbPerSlice = 16;
+
+// K blocks per slice when a grid too small for the GPU is split along K; num_kb when not.
+int tc_kb_per_slice(const TcEntry& e, int64_t M, int64_t N, int64_t K, int num_sms) {
+    const bool mc = e.cfg.cluster == 2;
+    const int64_t workers = mc ? num_sms / 2 : num_sms;
+    const int64_t tiles_m = (M + kBM - 1) / kBM;
+    const int64_t tiles = (mc ? (tiles_m + 1) / 2 : tiles_m) * ((N + e.cfg.tile_n - 1) / e.cfg.tile_n);
+    const int64_t num_kb = (K + kBK - 1) / kBK;
+    if (workers <= 0 || 2 * tiles > workers) return static_cast<int>(num_kb);
+    int64_t split = workers / tiles;
+    if (split > kTcMaxSplit) split = kTcMaxSplit;
+    if (split > num_kb / kTcMinKbPerSlice) split = num_kb / kTcMinKbPerSlice;
+    if (split < 2) return static_cast<int>(num_kb);
+    return static_cast<int>((num_kb + split - 1) / split);
+}
+
+}  // namespace
+
+size_t f16tc_split_bytes(int index, int64_t M, int64_t N, int64_t K, int num_sms) {
+    const int64_t num_kb = (K + kBK - 1) / kBK;
+    const int kb = tc_kb_per_slice(kTcEntries[index], M, N, K, num_sms);
+    if (kb >= num_kb) return 0;
+    return static_cast<size_t>((num_kb + kb - 1) / kb) * static_cast<size_t>(M * N) * 4;
+}
+
 cudaError_t f16tc_gemm_launch(int index, int64_t M, int64_t N, int64_t K, float alpha, float beta,
-                              float* C, const void* workspace, unsigned int* status, int num_sms,
-                              cudaStream_t stream) {
+                              float* C, const void* workspace, void* split_ws, unsigned int* status,
+                              int num_sms, cudaStream_t stream) {
     const TcEntry& e = kTcEntries[index];
     const int64_t Kp = round_up(K, 8);
     const __half* Ah = static_cast<const __half*>(workspace);
@@ -613,8 +660,14 @@ cudaError_t f16tc_gemm_launch(int index, int64_t M, int64_t N, int64_t K, float 
     // round go out as two half-width items each when that still fits in one round.
     const int64_t full = tiles >= workers ? tiles / workers * workers : 0;
     const int64_t tail = tiles - full;
-    const int tail_split = (tail > 0 && 2 * tail <= workers) ? 2 : 1;
-    const int64_t items = full + tail * tail_split;
+    int tail_split = (tail > 0 && 2 * tail <= workers) ? 2 : 1;
+    // a grid too small for the GPU: split along K instead (when there is scratch for it)
+    const int64_t num_kb64 = (K + kBK - 1) / kBK;
+    int kb_per = tc_kb_per_slice(e, M, N, K, num_sms);
+    if (split_ws == nullptr) kb_per = static_cast<int>(num_kb64);
+    const int ksplit = static_cast<int>((num_kb64 + kb_per - 1) / kb_per);
+    if (ksplit > 1) tail_split = 1;
+    const int64_t items = ksplit > 1 ? tiles * ksplit : full + tail * tail_split;
     const int grid = static_cast<int>((items < workers ? items : workers) * (mc ? 2 : 1));
     const int num_kb = static_cast<int>((K + kBK - 1) / kBK);
     // Launched as a programmatic dependent of the cast kernel, so that its prologue (barrier
@@ -635,16 +688,19 @@ cudaError_t f16tc_gemm_launch(int index, int64_t M, int64_t N, int64_t K, float 
     lc.attrs = attr;
     lc.numAttrs = 2;
     const int m32 = static_cast<int>(M), n32 = static_cast<int>(N), full32 = static_cast<int>(full);
+    float* partial = ksplit > 1 ? static_cast<float*>(split_ws) : nullptr;
     err = cudaLaunchKernelEx(&lc, e.fn, mapA, mapB, mapB_half, mapB_quarter, C, m32, n32, num_kb, alpha,
-                             beta, tiles_m, tiles_n, status, full32, tail_split);
+                             beta, tiles_m, tiles_n, status, full32, tail_split, ksplit, kb_per, partial);
     if (err != cudaSuccess) {
         // a stream that does not take programmatic launches: launch normally
         cudaGetLastError();
         lc.numAttrs = 1;
         err = cudaLaunchKernelEx(&lc, e.fn, mapA, mapB, mapB_half, mapB_quarter, C, m32, n32, num_kb,
-                                 alpha, beta, tiles_m, tiles_n, status, full32, tail_split);
+                                 alpha, beta, tiles_m, tiles_n, status, full32, tail_split, ksplit, kb_per,
+                                 partial);
     }
-    return err;
+    if (err != cudaSuccess || ksplit == 1) return err;
+    return splitk_reduce_launch(partial, ksplit, M, N, alpha, beta, C, num_sms, stream);
 }
 
 }  // namespace phx

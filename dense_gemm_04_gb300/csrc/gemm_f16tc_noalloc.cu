@@ -104,7 +104,7 @@ extern "C" phx_status phx_gemm_f16tc_f32acc_noalloc(int64_t M, int64_t N, int64_
     void* workspace = d->base + kStatusBytes;
     cudaError_t err = phx::f16tc_cast_launch(M, N, K, A, B, workspace, d->sm_count, stream);
     if (err == cudaSuccess)
-        err = phx::f16tc_gemm_launch(cfg, M, N, K, alpha, beta, C, workspace, status_word,
+        err = phx::f16tc_gemm_launch(cfg, M, N, K, alpha, beta, C, workspace, nullptr, status_word,
                                      d->sm_count, stream);
     return err == cudaSuccess ? PHX_OK : PHX_ERR_LAUNCH;
 }

@@ -32,11 +32,23 @@ const SgemmConfig& sgemm_config(int index);
 bool sgemm_is_aligned(int index, int64_t M, int64_t N, int64_t K, const float* A,
                       const float* B, const float* C);
 
-// Enqueue config `index` (aligned or masked kernel as decided by sgemm_is_aligned).
+// Scratch bytes config `index` uses for this problem on `num_sms` SMs: the partial
+// products of the K slices when a grid too small for the GPU is split along K (0 if not).
+size_t sgemm_workspace_bytes(int index, int64_t M, int64_t N, int64_t K, const float* A,
+                             const float* B, const float* C, int num_sms);
+
+// Enqueue config `index` (aligned or masked kernel as decided by sgemm_is_aligned), split
+// along K when sgemm_workspace_bytes says so and `workspace` holds that many bytes (with
+// workspace == nullptr it never splits), followed by the reduction of the slices.
 // Requires M, N > 0, K > 0 and alpha != 0 (the caller handles the degenerate cases).
 cudaError_t sgemm_launch(int index, int64_t M, int64_t N, int64_t K, float alpha,
-                         const float* A, const float* B, float beta, float* C,
-                         cudaStream_t stream);
+                         const float* A, const float* B, float beta, float* C, void* workspace,
+                         int num_sms, cudaStream_t stream);
+
+// C <- alpha * (P[0] + ... + P[slices-1]) + beta * C, where P[s] is the s-th M x N plane of
+// `partial`, added in that order (beta == 0: C not read).  Finishes a GEMM split along K.
+cudaError_t splitk_reduce_launch(const float* partial, int slices, int64_t M, int64_t N, float alpha,
+                                 float beta, float* C, int num_sms, cudaStream_t stream);
 
 // C <- beta * C (beta == 0: C <- 0 without reading C).  Used for K == 0 or alpha == 0.
 cudaError_t scale_c_launch(int64_t M, int64_t N, float beta, float* C, cudaStream_t stream);
@@ -61,12 +73,17 @@ size_t f16tc_workspace_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t f16tc_cast_launch(int64_t M, int64_t N, int64_t K, const float* A, const float* B,
                               void* workspace, int num_sms, cudaStream_t stream);
 
-// Enqueue the tcgen05 GEMM of config `index` on the cast operands in `workspace`;
-// `status` is the device status word; `num_sms` bounds the persistent grid.  Requires
-// M, N, K > 0 and alpha != 0.
+// Scratch bytes config `index` uses on `num_sms` SMs for the partial products of the K
+// slices when a grid too small for the GPU is split along K (0 if it is not split).
+size_t f16tc_split_bytes(int index, int64_t M, int64_t N, int64_t K, int num_sms);
+
+// Enqueue the tcgen05 GEMM of config `index` on the cast operands in `workspace`, split
+// along K into `split_ws` (f16tc_split_bytes(...) bytes; nullptr: no split) and then
+// reduced; `status` is the device status word; `num_sms` bounds the persistent grid.
+// Requires M, N, K > 0 and alpha != 0.
 cudaError_t f16tc_gemm_launch(int index, int64_t M, int64_t N, int64_t K, float alpha, float beta,
-                              float* C, const void* workspace, unsigned int* status, int num_sms,
-                              cudaStream_t stream);
+                              float* C, const void* workspace, void* split_ws, unsigned int* status,
+                              int num_sms, cudaStream_t stream);
 
 // The configuration index a call of `variant` with this shape would use now (pinned, tuned
 // or default), as phx_get_config reports it (phx_api.cu).

@@ -222,11 +222,16 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int default_config(int variant, int64_t M, int64_t N, int sms) {
     if (variant == PHX_VARIANT_SGEMM) {
         const int64_t slots = 2 * static_cast<int64_t>(sms);  // two CTAs per SM
+        // 128 x 128 tiles whenever they exist: a grid too small for the GPU is then split
+        // along K, which keeps the larger, more efficient tile
+        if (M >= 128 && N >= 128) return parse_config(variant, "TILE_M=128 TILE_N=128 TILE_K=16 STAGES=4 FMA2=1");
         if (ceil_div(M, 128) * ceil_div(N, 128) >= slots) return parse_config(variant, "TILE_M=128 TILE_N=128 TILE_K=16 STAGES=4 FMA2=1");
         if (ceil_div(M, 128) * ceil_div(N, 64) >= slots) return parse_config(variant, "TILE_M=128 TILE_N=64 TILE_K=8 STAGES=4");
         return parse_config(variant, "TILE_M=64 TILE_N=64 TILE_K=8 STAGES=4");
     }
-    if (ceil_div(M, 256) * ceil_div(N, 256) >= sms / 2) return parse_config(variant, "TILE_M=256 TILE_N=256 TILE_K=64 STAGES=6");
+    // the 2-SM 256 x 256 tile whenever it fits the problem: a grid too small for the GPU is
+    // then split along K (when K is long enough), which keeps the efficient tile
+    if (M >= 256 && N >= 256) return parse_config(variant, "TILE_M=256 TILE_N=256 TILE_K=64 STAGES=6");
     if (ceil_div(M, 128) * ceil_div(N, 256) >= sms) return parse_config(variant, "TILE_M=128 TILE_N=256 TILE_K=64 STAGES=4");
     if (ceil_div(M, 128) * ceil_div(N, 128) >= sms) return parse_config(variant, "TILE_M=128 TILE_N=128 TILE_K=64 STAGES=6");
     return parse_config(variant, "TILE_M=128 TILE_N=64 TILE_K=64 STAGES=8");
@@ -370,23 +375,36 @@ phx_status launch_variant(int variant, int cfg, int64_t M, int64_t N, int64_t K,
                           const float* A, const float* B, float beta, float* C, DevState* d,
                           cudaStream_t stream) {
     if (variant == PHX_VARIANT_SGEMM) {
-        return timed(kKindSgemm, stream, [&] {
-                   return phx::sgemm_launch(cfg, M, N, K, alpha, A, B, beta, C, stream);
-               }) == cudaSuccess
-                   ? PHX_OK : PHX_ERR_LAUNCH;
+        // pooled scratch only when a small grid is split along K
+        const size_t bytes = phx::sgemm_workspace_bytes(cfg, M, N, K, A, B, C, d->sm_count);
+        void* ws = nullptr;
+        if (bytes > 0 && cudaMallocFromPoolAsync(&ws, bytes, d->pool, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return PHX_ERR_NOMEM;
+        }
+        const cudaError_t err = timed(kKindSgemm, stream, [&] {
+            return phx::sgemm_launch(cfg, M, N, K, alpha, A, B, beta, C, ws, d->sm_count, stream);
+        });
+        if (ws != nullptr) cudaFreeAsync(ws, stream);
+        return err == cudaSuccess ? PHX_OK : PHX_ERR_LAUNCH;
     }
-    const size_t bytes = phx::f16tc_workspace_bytes(M, N, K);
+    // one pooled block: the f16 operand copies, then (for a grid split along K) the partial
+    // products of the slices
+    const size_t cast_bytes = phx::f16tc_workspace_bytes(M, N, K);
+    const size_t split_bytes = phx::f16tc_split_bytes(cfg, M, N, K, d->sm_count);
     void* ws = nullptr;
-    if (cudaMallocFromPoolAsync(&ws, bytes, d->pool, stream) != cudaSuccess) {
+    if (cudaMallocFromPoolAsync(&ws, cast_bytes + split_bytes, d->pool, stream) != cudaSuccess) {
         cudaGetLastError();
         return PHX_ERR_NOMEM;
     }
+    void* split_ws = split_bytes > 0 ? static_cast<char*>(ws) + cast_bytes : nullptr;
     cudaError_t err = timed(kKindCast, stream, [&] {
         return phx::f16tc_cast_launch(M, N, K, A, B, ws, d->sm_count, stream);
     });
     if (err == cudaSuccess)
         err = timed(kKindTcGemm, stream, [&] {
-            return phx::f16tc_gemm_launch(cfg, M, N, K, alpha, beta, C, ws, d->status, d->sm_count, stream);
+            return phx::f16tc_gemm_launch(cfg, M, N, K, alpha, beta, C, ws, split_ws, d->status,
+                                          d->sm_count, stream);
         });
     cudaFreeAsync(ws, stream);
     return err == cudaSuccess ? PHX_OK : PHX_ERR_LAUNCH;

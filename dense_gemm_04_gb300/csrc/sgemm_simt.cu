@@ -33,6 +33,8 @@
 #include <cuda_fp16.h>
 
 #include <cstdint>
+#include <map>
+#include <mutex>
 
 #include "internal.h"
 
@@ -94,7 +96,7 @@ __host__ __device__ constexpr int sgemm_smem_floats(int bm, int bn, int bk, int 
 template <int BM, int BN, int BK, int STAGES, int TM, int TN, bool MASKED, bool FMA2, int MINB>
 __global__ void __launch_bounds__(kThreads, MINB)
 sgemm_kernel(const float* __restrict__ A, const float* __restrict__ B, float* __restrict__ C,
-             int M, int N, int K, float alpha, float beta) {
+             int M, int N, int K, float alpha, float beta, int k_slice, float* __restrict__ partial) {
     constexpr int WTM = kLanesM * TM;  // warp tile
     constexpr int WTN = kLanesN * TN;
     constexpr int WARPS_M = BM / WTM;
@@ -120,6 +122,20 @@ sgemm_kernel(const float* __restrict__ A, const float* __restrict__ B, float* __
     const int lm = lane / kLanesN;
     const int ln = lane % kLanesN;
 
+    // Split K (gridDim.y slices): slice y multiplies the k range [y * k_slice, ...) and
+    // writes its partial product, alpha = 1 and beta = 0, to its own M x N plane of
+    // `partial`; a separate pass adds the planes in slice order and applies alpha and beta.
+    const int lda = K;  // row stride of A
+    if (gridDim.y > 1) {
+        const int k0s = static_cast<int>(blockIdx.y) * k_slice;
+        A += k0s;
+        B += static_cast<int64_t>(k0s) * N;
+        K = min(K - k0s, k_slice);
+        C = partial + static_cast<int64_t>(blockIdx.y) * M * N;
+        alpha = 1.f;
+        beta = 0.f;
+    }
+
     const int tiles_m = (M + BM - 1) / BM;
     const int tiles_n = (N + BN - 1) / BN;
     int pm, pn;
@@ -139,7 +155,7 @@ sgemm_kernel(const float* __restrict__ A, const float* __restrict__ B, float* __
                 const int m = e / (BK / 4);
                 const int k4 = e % (BK / 4);
                 cp_async_16(smem_addr(as + m * BK + k4 * 4),
-                            A + static_cast<int64_t>(m0 + m) * K + k0 + k4 * 4);
+                            A + static_cast<int64_t>(m0 + m) * lda + k0 + k4 * 4);
             }
 #pragma unroll
             for (int e = tid; e < BK * BN / 4; e += kThreads) {
@@ -154,7 +170,7 @@ sgemm_kernel(const float* __restrict__ A, const float* __restrict__ B, float* __
                 const int m = e / BK;
                 const int k = e % BK;
                 const bool ok = (m0 + m < M) && (k0 + k < K);
-                const float* src = ok ? A + static_cast<int64_t>(m0 + m) * K + k0 + k : A;
+                const float* src = ok ? A + static_cast<int64_t>(m0 + m) * lda + k0 + k : A;
                 cp_async_4(smem_addr(as + m * BK + k), src, ok);
             }
 #pragma unroll
@@ -300,6 +316,39 @@ sgemm_kernel(const float* __restrict__ A, const float* __restrict__ B, float* __
     }
 }
 
+// C <- alpha * (P[0] + P[1] + ... + P[S-1]) + beta * C, the planes added in that order
+// (beta == 0: C not read).  float4 when N % 4 == 0 and the pointers are 16-byte aligned.
+__global__ void splitk_reduce_kernel(const float* __restrict__ P, int S, int64_t plane, float alpha,
+                                     float beta, float* __restrict__ C, int vec) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t start = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (vec) {
+        const int64_t n4 = plane / 4;
+        for (int64_t i = start; i < n4; i += stride) {
+            float4 acc = __ldcs(reinterpret_cast<const float4*>(P) + i);
+            for (int s = 1; s < S; ++s) {
+                const float4 v = __ldcs(reinterpret_cast<const float4*>(P + s * plane) + i);
+                acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+            }
+            float4 o = make_float4(alpha * acc.x, alpha * acc.y, alpha * acc.z, alpha * acc.w);
+            if (beta != 0.f) {
+                const float4 c = reinterpret_cast<const float4*>(C)[i];
+                o.x = fmaf(beta, c.x, o.x); o.y = fmaf(beta, c.y, o.y);
+                o.z = fmaf(beta, c.z, o.z); o.w = fmaf(beta, c.w, o.w);
+            }
+            reinterpret_cast<float4*>(C)[i] = o;
+        }
+        return;
+    }
+    for (int64_t i = start; i < plane; i += stride) {
+        float acc = P[i];
+        for (int s = 1; s < S; ++s) acc += P[s * plane + i];
+        float o = alpha * acc;
+        if (beta != 0.f) o = fmaf(beta, C[i], o);
+        C[i] = o;
+    }
+}
+
 // C <- beta * C over M*N elements (beta == 0 writes zeros without reading C).
 __global__ void scale_c_kernel(float* __restrict__ C, int64_t n, float beta) {
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -313,7 +362,7 @@ __global__ void scale_c_kernel(float* __restrict__ C, int64_t n, float beta) {
 // @autotune row); this build compiles the part of it that a 256-thread CTA with
 // 4x4..8x16 register micro-tiles covers, times STAGES in {3, 4} and the FMA2 switch.
 // ---------------------------------------------------------------------------------------
-using KernelFn = void (*)(const float*, const float*, float*, int, int, int, float, float);
+using KernelFn = void (*)(const float*, const float*, float*, int, int, int, float, float, int, float*);
 
 struct Entry {
     SgemmConfig cfg;
@@ -362,9 +411,57 @@ bool sgemm_is_aligned(int index, int64_t M, int64_t N, int64_t K, const float* A
            al16(C);
 }
 
+namespace {
+
+// CTAs of `fn` that fit on one SM at once (cached per kernel).
+int ctas_per_sm(KernelFn fn, int smem) {
+    static std::mutex mu;
+    static std::map<KernelFn, int> cache;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(fn);
+    if (it != cache.end()) return it->second;
+    int n = 0;
+    if (cudaFuncSetAttribute(reinterpret_cast<const void*>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreads, smem) != cudaSuccess) {
+        cudaGetLastError();
+        n = 1;
+    }
+    if (n < 1) n = 1;
+    cache[fn] = n;
+    return n;
+}
+
+constexpr int kMaxSplit = 8;
+constexpr int kMinKTilesPerSlice = 16;
+
+// Elements of K per slice when a grid too small for the GPU is split along K (the grid
+// gets one row of CTAs per slice); K itself when it is not split.
+int64_t k_per_slice(const Entry& e, bool aligned, int64_t M, int64_t N, int64_t K, int num_sms) {
+    const int64_t tiles = ((M + e.cfg.tile_m - 1) / e.cfg.tile_m) * ((N + e.cfg.tile_n - 1) / e.cfg.tile_n);
+    const int64_t slots = static_cast<int64_t>(ctas_per_sm(aligned ? e.aligned : e.masked, e.smem_bytes)) * num_sms;
+    const int64_t k_tiles = (K + e.cfg.tile_k - 1) / e.cfg.tile_k;
+    if (num_sms <= 0 || 2 * tiles > slots) return K;
+    int64_t split = slots / tiles;
+    if (split > kMaxSplit) split = kMaxSplit;
+    if (split > k_tiles / kMinKTilesPerSlice) split = k_tiles / kMinKTilesPerSlice;
+    if (split < 2) return K;
+    return (k_tiles + split - 1) / split * e.cfg.tile_k;
+}
+
+}  // namespace
+
+size_t sgemm_workspace_bytes(int index, int64_t M, int64_t N, int64_t K, const float* A,
+                             const float* B, const float* C, int num_sms) {
+    const Entry& e = kEntries[index];
+    const int64_t ks = k_per_slice(e, sgemm_is_aligned(index, M, N, K, A, B, C), M, N, K, num_sms);
+    if (ks >= K) return 0;
+    return static_cast<size_t>((K + ks - 1) / ks) * static_cast<size_t>(M * N) * 4;
+}
+
 cudaError_t sgemm_launch(int index, int64_t M, int64_t N, int64_t K, float alpha,
-                         const float* A, const float* B, float beta, float* C,
-                         cudaStream_t stream) {
+                         const float* A, const float* B, float beta, float* C, void* workspace,
+                         int num_sms, cudaStream_t stream) {
     const Entry& e = kEntries[index];
     const bool aligned = sgemm_is_aligned(index, M, N, K, A, B, C);
     KernelFn fn = aligned ? e.aligned : e.masked;
@@ -374,8 +471,28 @@ cudaError_t sgemm_launch(int index, int64_t M, int64_t N, int64_t K, float alpha
     if (err != cudaSuccess) return err;
     const int64_t tiles = ((M + e.cfg.tile_m - 1) / e.cfg.tile_m) * ((N + e.cfg.tile_n - 1) / e.cfg.tile_n);
     if (tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
-    fn<<<static_cast<unsigned>(tiles), kThreads, e.smem_bytes, stream>>>(
-        A, B, C, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), alpha, beta);
+    int64_t ks = k_per_slice(e, aligned, M, N, K, num_sms);
+    if (workspace == nullptr) ks = K;
+    const int64_t slices = (K + ks - 1) / ks;
+    float* partial = slices > 1 ? static_cast<float*>(workspace) : nullptr;
+    fn<<<dim3(static_cast<unsigned>(tiles), static_cast<unsigned>(slices)), kThreads, e.smem_bytes, stream>>>(
+        A, B, C, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), alpha, beta,
+        static_cast<int>(ks), partial);
+    err = cudaGetLastError();
+    if (err != cudaSuccess || slices == 1) return err;
+    return splitk_reduce_launch(partial, static_cast<int>(slices), M, N, alpha, beta, C, num_sms, stream);
+}
+
+cudaError_t splitk_reduce_launch(const float* partial, int slices, int64_t M, int64_t N, float alpha,
+                                 float beta, float* C, int num_sms, cudaStream_t stream) {
+    const int64_t plane = M * N;
+    const int vec = (N % 4 == 0) && ((reinterpret_cast<uintptr_t>(C) & 15u) == 0) &&
+                    ((reinterpret_cast<uintptr_t>(partial) & 15u) == 0);
+    int64_t blocks = (plane / (vec ? 4 : 1) + 255) / 256;
+    if (blocks > static_cast<int64_t>(num_sms) * 8) blocks = static_cast<int64_t>(num_sms) * 8;
+    if (blocks < 1) blocks = 1;
+    splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(partial, slices, plane, alpha,
+                                                                             beta, C, vec);
     return cudaGetLastError();
 }
 

@@ -90,8 +90,10 @@ def test_default_config_follows_grid_size():
     phx.set_config(1, None)
     big = phx.get_config(phx.VARIANT_SGEMM, 4096, 4096, 4096)
     small = phx.get_config(phx.VARIANT_SGEMM, 1024, 1024, 16384)
+    skinny = phx.get_config(phx.VARIANT_SGEMM, 64, 4096, 4096)
     assert big.startswith("TILE_M=128 TILE_N=128")
-    assert small.startswith("TILE_M=64 TILE_N=64")
+    assert small.startswith("TILE_M=128 TILE_N=128")   # a small grid is split along K instead
+    assert skinny.startswith("TILE_M=64 TILE_N=64")
     assert phx.get_config(phx.VARIANT_F16TC, 4096, 4096, 4096).startswith("TILE_M=256 TILE_N=256")
 
 

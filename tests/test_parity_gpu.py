@@ -232,8 +232,8 @@ def test_lab_error_levels():
 
 
 # ----------------------------------------------------------------------------------------
-# Tail waves: rows of tiles handed to a half-height launch (f32) and tiles dealt out as
-# half-width items (tensor cores) when the tile count leaves the last wave part-empty
+# Small grids split along K (the slices' partial products added in slice order) and tiles
+# of a last, partial round dealt out as half-width items (tensor cores)
 # ----------------------------------------------------------------------------------------
 
 TAIL_SHAPES = [(640, 512, 2048), (650, 500, 2000), (5000, 300, 700), (4224, 4096, 256), (129, 257, 4100)]
@@ -264,10 +264,10 @@ def test_results_identical_run_to_run(vname):
 
 
 def test_tiling_does_not_change_values():
-    # each output element is one k-ordered chain of multiply-adds (f32) or one k-ordered
-    # sequence of MMAs (f16 tensor cores) whatever the tile shape, so every configuration
-    # gives the same bits on the same inputs
-    M, N, K = 640, 512, 1000
+    # on a grid large enough not to be split along K, each output element is one k-ordered
+    # chain of multiply-adds (f32) or one k-ordered sequence of MMAs (f16 tensor cores)
+    # whatever the tile shape, so every configuration gives the same bits on the same inputs
+    M, N, K = 2048, 2048, 1000
     A, B, C = synth.problem(M, N, K, seed=23)
     for vname, (variant, _) in VARIANTS.items():
         ref = None
