@@ -58,6 +58,24 @@ def _dist_env():
     return ws, rank, local
 
 
+def reduce_max(x: float, ws: int, device=None) -> float:
+    """The largest x over all ranks (the slowest rank's time); x itself on one rank."""
+    if ws == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(ws: int, steps: int, flops_per_step: float, max_seconds: float) -> float:
+    """Throughput of the whole job: the work of every rank over the slowest rank's time.
+    Each rank runs its own replica of the step (the path is not sharded), so the work grows
+    with the number of ranks (weak scaling)."""
+    return ws * steps * flops_per_step / max_seconds / 1e12
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -285,11 +303,7 @@ def gpu_arm(args):
     torch.cuda.synchronize()
     prof = phx.profile_stop()
     launches_per_step = sum(n for n, _ in prof.values()) / prof_steps
-    total_s = sum(step_ms) / 1e3
-    total_t = torch.tensor([total_s], dtype=torch.float64, device=dev)
-    if ws > 1:
-        dist.all_reduce(total_t, op=dist.ReduceOp.MAX)
-    max_s = float(total_t.item())
+    max_s = reduce_max(sum(step_ms) / 1e3, ws, dev)
     launches = int(round(launches_per_step * args.steps))
     st = phx.check_device_status()
     if st != phx.PHX_OK:
@@ -325,9 +339,7 @@ def gpu_arm(args):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_s = e0.elapsed_time(e1) / 1e3
-    e2e_t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-    if ws > 1:
-        dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
+    e2e_max_s = reduce_max(e2e_s, ws, dev)
     h2d = M * K * 4 + K * N * 4 + 2 * M * N * 4
     d2h = 2 * M * N * 4
 
@@ -336,8 +348,7 @@ def gpu_arm(args):
             dist.destroy_process_group()
         return 0
 
-    flops_total = ws * args.steps * GEMMS_PER_STEP * FLOPS_PER_GEMM
-    value = flops_total / max_s / 1e12
+    value = whole_job_tflops(ws, args.steps, GEMMS_PER_STEP * FLOPS_PER_GEMM, max_s)
     clocks = clk.summary()
     sm_max = clocks.get("sm_max_mhz") or peaks["sm_max_mhz"]
 
@@ -397,7 +408,7 @@ def gpu_arm(args):
         "roofline_tc_gemm": roofline_tc,
         "roofline_cast": roofline_cast,
         "cpu_baseline": cpu,
-        "e2e": {"value": ws * e2e_steps * GEMMS_PER_STEP * FLOPS_PER_GEMM / float(e2e_t.item()) / 1e12,
+        "e2e": {"value": whole_job_tflops(ws, e2e_steps, GEMMS_PER_STEP * FLOPS_PER_GEMM, e2e_max_s),
                 "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps},
         "clocks": clocks,
