@@ -8,7 +8,8 @@
 //
 // Two passes:
 //   1. Cast (HBM-bound, one launch): A (M x K f32) -> Ah (M x Kp f16, row-major) and B
-//      (K x N f32) -> Bt (N x Kp f16, B transposed) with cvt.rn (round to nearest even); Kp = K rounded up
+//      (K x N f32) -> Bt (N x Kp f16, B transposed) with cvt.rn (round to nearest even);
+//      operands given transposed are read in their stored order; Kp = K rounded up
 //      to a multiple of 8 so every row starts on 16 bytes, the TMA stride rule; the pad
 //      columns are written as zeros.  Both operands end up K-major, the layout the
 //      tensor-core descriptors below describe.
@@ -52,13 +53,25 @@ __host__ __device__ constexpr int64_t round_up(int64_t x, int64_t m) { return (x
 // Cast pass
 // ---------------------------------------------------------------------------------------
 
-// One launch for both operands.  Blocks [0, a_blocks) round A (rows x K, f32) into Ah
-// (rows x Kp, f16), each thread 8 halves (16 bytes) at a time; blocks from a_blocks on
-// each round and transpose one 64 x 64 tile of B (K x N, f32) into Bt (N x Kp, f16).
-// The B tile goes through shared memory with its columns XOR-swizzled per band of 8 rows,
-// so that both the row-wise 16-byte stores of the loaded tile and the column-wise reads
-// that build Bt's rows hit 32 different banks.
+// One launch casts both operands.  Each operand is a job: its f32 values, as rows x K,
+// become rows x Kp halves (K-major), rounded to nearest even.  A job whose source is
+// stored row by row (trans = 0) is cast 8 halves (16 bytes) per thread, grid-stride; a
+// job whose source is stored transposed (trans = 1: K x rows) goes through 64 x 64 tiles
+// of shared memory, one tile per block, with the tile's columns XOR-swizzled per band of
+// 8 rows so that both the row-wise 16-byte stores of the loaded tile and the column-wise
+// reads that build the output rows hit 32 different banks.  A of a plain GEMM is a row
+// job and B a transposed one (B is K x N, its K-major form N x K).
 constexpr int kTT = 64;
+
+struct CastJob {
+    const float* src;
+    __half* dst;
+    int64_t rows;   // rows of the K-major result
+    int trans;      // source stored K x rows
+    int vec;        // 16-byte source loads allowed
+    int blocks;     // blocks of the launch this job takes
+    int tiles_r;    // trans: 64-row tiles along rows
+};
 
 __device__ __forceinline__ int tt_swizzle(int k) { return ((k >> 3) & 7) << 2; }
 
@@ -72,23 +85,23 @@ __device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
     return out;
 }
 
-__global__ void __launch_bounds__(256) cast_kernel(const float* __restrict__ A, __half* __restrict__ Ah,
-                                                   int64_t M, int64_t K, int64_t Kp, int vec_a,
-                                                   const float* __restrict__ B, __half* __restrict__ Bt,
-                                                   int64_t N, int vec_b, int a_blocks, int b_tiles_n) {
+__global__ void __launch_bounds__(256) cast_kernel(CastJob j0, CastJob j1, int64_t K, int64_t Kp) {
     // let the GEMM that follows start its prologue while the cast finishes
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int tid = threadIdx.x;
-    if (static_cast<int>(blockIdx.x) < a_blocks) {
+    int b = static_cast<int>(blockIdx.x);
+    const CastJob j = b < j0.blocks ? j0 : j1;
+    if (b >= j0.blocks) b -= j0.blocks;
+    if (!j.trans) {
         const int64_t chunks = Kp / 8;
-        const int64_t total = M * chunks;
-        const int64_t stride = static_cast<int64_t>(a_blocks) * 256;
-        for (int64_t idx = static_cast<int64_t>(blockIdx.x) * 256 + tid; idx < total; idx += stride) {
+        const int64_t total = j.rows * chunks;
+        const int64_t stride = static_cast<int64_t>(j.blocks) * 256;
+        for (int64_t idx = static_cast<int64_t>(b) * 256 + tid; idx < total; idx += stride) {
             const int64_t r = idx / chunks;
             const int64_t c = (idx - r * chunks) * 8;
-            const float* src = A + r * K + c;
+            const float* src = j.src + r * K + c;
             float v[8];
-            if (vec_a && c + 8 <= K) {
+            if (j.vec && c + 8 <= K) {
                 const float4 x = __ldcs(reinterpret_cast<const float4*>(src));
                 const float4 y = __ldcs(reinterpret_cast<const float4*>(src + 4));
                 v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
@@ -97,47 +110,47 @@ __global__ void __launch_bounds__(256) cast_kernel(const float* __restrict__ A, 
 #pragma unroll
                 for (int q = 0; q < 8; ++q) v[q] = (c + q < K) ? src[q] : 0.f;
             }
-            *reinterpret_cast<uint4*>(Ah + r * Kp + c) = pack8(v);
+            *reinterpret_cast<uint4*>(j.dst + r * Kp + c) = pack8(v);
         }
         return;
     }
-    __shared__ __align__(16) float tile[kTT][kTT];  // [k][n ^ swizzle(k)]
-    const int tb = static_cast<int>(blockIdx.x) - a_blocks;
-    const int64_t n0 = static_cast<int64_t>(tb % b_tiles_n) * kTT;
-    const int64_t k0 = static_cast<int64_t>(tb / b_tiles_n) * kTT;
+    __shared__ __align__(16) float tile[kTT][kTT];  // [k][r ^ swizzle(k)]
+    const int64_t R = j.rows;
+    const int64_t r0 = static_cast<int64_t>(b % j.tiles_r) * kTT;
+    const int64_t k0 = static_cast<int64_t>(b / j.tiles_r) * kTT;
 #pragma unroll
     for (int i = 0; i < kTT * kTT / 4 / 256; ++i) {
         const int e = tid + i * 256;
         const int k = e / (kTT / 4);
-        const int n4 = (e % (kTT / 4)) * 4;
+        const int r4 = (e % (kTT / 4)) * 4;
         const int64_t gk = k0 + k;
-        const int64_t gn = n0 + n4;
+        const int64_t gr = r0 + r4;
         float4 v;
-        if (vec_b && gk < K && gn + 3 < N) {
-            v = __ldcs(reinterpret_cast<const float4*>(B + gk * N + gn));
+        if (j.vec && gk < K && gr + 3 < R) {
+            v = __ldcs(reinterpret_cast<const float4*>(j.src + gk * R + gr));
         } else {
             const bool rk = gk < K;
-            v.x = (rk && gn + 0 < N) ? B[gk * N + gn + 0] : 0.f;
-            v.y = (rk && gn + 1 < N) ? B[gk * N + gn + 1] : 0.f;
-            v.z = (rk && gn + 2 < N) ? B[gk * N + gn + 2] : 0.f;
-            v.w = (rk && gn + 3 < N) ? B[gk * N + gn + 3] : 0.f;
+            v.x = (rk && gr + 0 < R) ? j.src[gk * R + gr + 0] : 0.f;
+            v.y = (rk && gr + 1 < R) ? j.src[gk * R + gr + 1] : 0.f;
+            v.z = (rk && gr + 2 < R) ? j.src[gk * R + gr + 2] : 0.f;
+            v.w = (rk && gr + 3 < R) ? j.src[gk * R + gr + 3] : 0.f;
         }
-        *reinterpret_cast<float4*>(&tile[k][n4 ^ tt_swizzle(k)]) = v;
+        *reinterpret_cast<float4*>(&tile[k][r4 ^ tt_swizzle(k)]) = v;
     }
     __syncthreads();
 #pragma unroll
     for (int i = 0; i < kTT * (kTT / 8) / 256; ++i) {
         const int e = tid + i * 256;
-        const int n = e / (kTT / 8);
+        const int r = e / (kTT / 8);
         const int kc = (e % (kTT / 8)) * 8;
-        const int64_t gn = n0 + n;
+        const int64_t gr = r0 + r;
         const int64_t gk = k0 + kc;
-        if (gn < N && gk < Kp) {
-            const int col = n ^ tt_swizzle(kc);  // the same for the 8 rows kc .. kc+7
+        if (gr < R && gk < Kp) {
+            const int col = r ^ tt_swizzle(kc);  // the same for the 8 rows kc .. kc+7
             float v[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q) v[q] = tile[kc + q][col];
-            *reinterpret_cast<uint4*>(Bt + gn * Kp + gk) = pack8(v);
+            *reinterpret_cast<uint4*>(j.dst + gr * Kp + gk) = pack8(v);
         }
     }
 }
@@ -586,22 +599,45 @@ size_t f16tc_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     return static_cast<size_t>(round_up(M * Kp * 2, 256) + round_up(N * Kp * 2, 256));
 }
 
-cudaError_t f16tc_cast_launch(int64_t M, int64_t N, int64_t K, const float* A, const float* B,
-                              void* workspace, int num_sms, cudaStream_t stream) {
+cudaError_t f16tc_cast_launch_ex(int trans_a, int trans_b, int64_t M, int64_t N, int64_t K,
+                                 const float* A, const float* B, void* workspace, int num_sms,
+                                 cudaStream_t stream) {
     const int64_t Kp = round_up(K, 8);
     __half* Ah = static_cast<__half*>(workspace);
     __half* Bt = reinterpret_cast<__half*>(static_cast<char*>(workspace) + round_up(M * Kp * 2, 256));
-    const int vec_a = (K % 4 == 0) && ((reinterpret_cast<uintptr_t>(A) & 15u) == 0);
-    const int vec_b = (N % 4 == 0) && ((reinterpret_cast<uintptr_t>(B) & 15u) == 0);
-    int64_t a_blocks = (M * (Kp / 8) + 255) / 256;
-    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
-    if (a_blocks > cap) a_blocks = cap;
-    const int64_t b_tiles_n = (N + kTT - 1) / kTT;
-    const int64_t b_tiles = b_tiles_n * ((Kp + kTT - 1) / kTT);
-    if (a_blocks + b_tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
-    cast_kernel<<<static_cast<unsigned>(a_blocks + b_tiles), 256, 0, stream>>>(
-        A, Ah, M, K, Kp, vec_a, B, Bt, N, vec_b, static_cast<int>(a_blocks), static_cast<int>(b_tiles_n));
+    auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    // K-major A is A itself unless A is given transposed; K-major B is the transpose of B
+    // unless B is given transposed.
+    auto make_job = [&](const float* src, __half* dst, int64_t rows, int trans) {
+        CastJob j;
+        j.src = src;
+        j.dst = dst;
+        j.rows = rows;
+        j.trans = trans;
+        j.vec = (trans ? rows % 4 == 0 : K % 4 == 0) && al16(src);
+        j.tiles_r = static_cast<int>((rows + kTT - 1) / kTT);
+        int64_t blocks;
+        if (trans) {
+            blocks = static_cast<int64_t>(j.tiles_r) * ((Kp + kTT - 1) / kTT);
+        } else {
+            blocks = (rows * (Kp / 8) + 255) / 256;
+            const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+            if (blocks > cap) blocks = cap;
+        }
+        j.blocks = static_cast<int>(blocks < 0x3FFFFFFF ? blocks : 0x3FFFFFFF);
+        return j;
+    };
+    const CastJob ja = make_job(A, Ah, M, trans_a ? 1 : 0);
+    const CastJob jb = make_job(B, Bt, N, trans_b ? 0 : 1);
+    const int64_t blocks = static_cast<int64_t>(ja.blocks) + jb.blocks;
+    if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    cast_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(ja, jb, K, Kp);
     return cudaGetLastError();
+}
+
+cudaError_t f16tc_cast_launch(int64_t M, int64_t N, int64_t K, const float* A, const float* B,
+                              void* workspace, int num_sms, cudaStream_t stream) {
+    return f16tc_cast_launch_ex(0, 0, M, N, K, A, B, workspace, num_sms, stream);
 }
 
 namespace {

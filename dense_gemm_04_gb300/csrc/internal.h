@@ -50,6 +50,10 @@ cudaError_t sgemm_launch(int index, int64_t M, int64_t N, int64_t K, float alpha
 cudaError_t splitk_reduce_launch(const float* partial, int slices, int64_t M, int64_t N, float alpha,
                                  float beta, float* C, int num_sms, cudaStream_t stream);
 
+// dst (cols x rows) <- the transpose of src (rows x cols), both row-major f32.
+cudaError_t transpose_f32_launch(const float* src, float* dst, int64_t rows, int64_t cols,
+                                 cudaStream_t stream);
+
 // C <- beta * C (beta == 0: C <- 0 without reading C).  Used for K == 0 or alpha == 0.
 cudaError_t scale_c_launch(int64_t M, int64_t N, float beta, float* C, cudaStream_t stream);
 
@@ -72,6 +76,12 @@ size_t f16tc_workspace_bytes(int64_t M, int64_t N, int64_t K);
 // (N x Kp) in `workspace` (f16tc_workspace_bytes(M, N, K) bytes, 256-byte aligned).
 cudaError_t f16tc_cast_launch(int64_t M, int64_t N, int64_t K, const float* A, const float* B,
                               void* workspace, int num_sms, cudaStream_t stream);
+
+// The same for operands given transposed: with trans_a, A is stored K x M; with trans_b, B
+// is stored N x K.  The result in `workspace` is the same K-major pair.
+cudaError_t f16tc_cast_launch_ex(int trans_a, int trans_b, int64_t M, int64_t N, int64_t K,
+                                 const float* A, const float* B, void* workspace, int num_sms,
+                                 cudaStream_t stream);
 
 // Scratch bytes config `index` uses on `num_sms` SMs for the partial products of the K
 // slices when a grid too small for the GPU is split along K (0 if it is not split).

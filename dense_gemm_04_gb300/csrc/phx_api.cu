@@ -334,7 +334,8 @@ __global__ void tune_fill_kernel(float* p, int64_t n, uint32_t salt) {
 // Per-kernel timing (phx_profile_start / phx_profile_stop): events recorded on the call's
 // stream around every kernel the library launches, summed per kernel kind at stop.
 // ---------------------------------------------------------------------------------------
-enum KernelKind { kKindSgemm = 0, kKindCast = 1, kKindTcGemm = 2, kKindScale = 3, kNumKinds = 4 };
+enum KernelKind { kKindSgemm = 0, kKindCast = 1, kKindTcGemm = 2, kKindScale = 3, kKindTranspose = 4,
+                  kNumKinds = 5 };
 
 struct Profile {
     bool on = false;
@@ -371,9 +372,18 @@ cudaError_t timed(int kind, cudaStream_t stream, F&& launch) {
     return err;
 }
 
+// An f32 operand given transposed is copied into its plain layout first (pooled scratch);
+// the copies start on 256-byte boundaries so that the aligned kernels apply whenever the
+// shape allows.
+phx_status launch_sgemm_transposed(int cfg, int trans_a, int trans_b, int64_t M, int64_t N, int64_t K,
+                                   float alpha, const float* A, const float* B, float beta, float* C,
+                                   DevState* d, cudaStream_t stream);
+
 phx_status launch_variant(int variant, int cfg, int64_t M, int64_t N, int64_t K, float alpha,
                           const float* A, const float* B, float beta, float* C, DevState* d,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, int trans_a = 0, int trans_b = 0) {
+    if (variant == PHX_VARIANT_SGEMM && (trans_a || trans_b))
+        return launch_sgemm_transposed(cfg, trans_a, trans_b, M, N, K, alpha, A, B, beta, C, d, stream);
     if (variant == PHX_VARIANT_SGEMM) {
         // pooled scratch only when a small grid is split along K
         const size_t bytes = phx::sgemm_workspace_bytes(cfg, M, N, K, A, B, C, d->sm_count);
@@ -399,7 +409,7 @@ phx_status launch_variant(int variant, int cfg, int64_t M, int64_t N, int64_t K,
     }
     void* split_ws = split_bytes > 0 ? static_cast<char*>(ws) + cast_bytes : nullptr;
     cudaError_t err = timed(kKindCast, stream, [&] {
-        return phx::f16tc_cast_launch(M, N, K, A, B, ws, d->sm_count, stream);
+        return phx::f16tc_cast_launch_ex(trans_a, trans_b, M, N, K, A, B, ws, d->sm_count, stream);
     });
     if (err == cudaSuccess)
         err = timed(kKindTcGemm, stream, [&] {
@@ -410,8 +420,35 @@ phx_status launch_variant(int variant, int cfg, int64_t M, int64_t N, int64_t K,
     return err == cudaSuccess ? PHX_OK : PHX_ERR_LAUNCH;
 }
 
+phx_status launch_sgemm_transposed(int cfg, int trans_a, int trans_b, int64_t M, int64_t N, int64_t K,
+                                   float alpha, const float* A, const float* B, float beta, float* C,
+                                   DevState* d, cudaStream_t stream) {
+    auto r256 = [](int64_t b) { return (b + 255) / 256 * 256; };
+    const int64_t a_bytes = trans_a ? r256(M * K * 4) : 0;
+    const int64_t b_bytes = trans_b ? r256(K * N * 4) : 0;
+    void* ws = nullptr;
+    if (cudaMallocFromPoolAsync(&ws, static_cast<size_t>(a_bytes + b_bytes), d->pool, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return PHX_ERR_NOMEM;
+    }
+    float* At = trans_a ? static_cast<float*>(ws) : nullptr;
+    float* Bt = trans_b ? reinterpret_cast<float*>(static_cast<char*>(ws) + a_bytes) : nullptr;
+    cudaError_t err = cudaSuccess;
+    if (trans_a)  // A stored K x M
+        err = timed(kKindTranspose, stream, [&] { return phx::transpose_f32_launch(A, At, K, M, stream); });
+    if (err == cudaSuccess && trans_b)  // B stored N x K
+        err = timed(kKindTranspose, stream, [&] { return phx::transpose_f32_launch(B, Bt, N, K, stream); });
+    phx_status st = err == cudaSuccess ? PHX_OK : PHX_ERR_LAUNCH;
+    if (st == PHX_OK)
+        st = launch_variant(PHX_VARIANT_SGEMM, cfg, M, N, K, alpha, trans_a ? At : A, trans_b ? Bt : B, beta,
+                            C, d, stream);
+    cudaFreeAsync(ws, stream);
+    return st;
+}
+
 phx_status gemm_entry(int variant, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
-                      const float* B, float beta, float* C, cudaStream_t stream) {
+                      const float* B, float beta, float* C, cudaStream_t stream, int trans_a = 0,
+                      int trans_b = 0) {
     phx_status st = validate(M, N, K, A, B, C);
     if (st != PHX_OK) return st;
     if (M == 0 || N == 0) return PHX_OK;
@@ -429,7 +466,12 @@ phx_status gemm_entry(int variant, int64_t M, int64_t N, int64_t K, float alpha,
     if (log_level() >= 2)
         std::fprintf(stderr, "[phx] variant %d (%lld,%lld,%lld): %s\n", variant, (long long)M,
                      (long long)N, (long long)K, config_name(variant, cfg).c_str());
-    return launch_variant(variant, cfg, M, N, K, alpha, A, B, beta, C, d, stream);
+    return launch_variant(variant, cfg, M, N, K, alpha, A, B, beta, C, d, stream, trans_a, trans_b);
+}
+
+bool valid_op(phx_op op) {
+    const int v = static_cast<int>(op);
+    return v == PHX_OP_N || v == PHX_OP_T;
 }
 
 phx_status copy_name(const std::string& s, char* buf, size_t buflen) {
@@ -480,6 +522,21 @@ phx_status phx_sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float* 
 phx_status phx_gemm_f16tc_f32acc(int64_t M, int64_t N, int64_t K, float alpha, const float* A,
                                  const float* B, float beta, float* C, phx_stream_t stream) {
     return gemm_entry(PHX_VARIANT_F16TC, M, N, K, alpha, A, B, beta, C, stream);
+}
+
+phx_status phx_sgemm_ex(phx_op op_a, phx_op op_b, int64_t M, int64_t N, int64_t K, float alpha,
+                        const float* A, const float* B, float beta, float* C, phx_stream_t stream) {
+    if (!valid_op(op_a) || !valid_op(op_b)) return PHX_ERR_INVALID;
+    return gemm_entry(PHX_VARIANT_SGEMM, M, N, K, alpha, A, B, beta, C, stream, op_a == PHX_OP_T,
+                      op_b == PHX_OP_T);
+}
+
+phx_status phx_gemm_f16tc_f32acc_ex(phx_op op_a, phx_op op_b, int64_t M, int64_t N, int64_t K,
+                                    float alpha, const float* A, const float* B, float beta, float* C,
+                                    phx_stream_t stream) {
+    if (!valid_op(op_a) || !valid_op(op_b)) return PHX_ERR_INVALID;
+    return gemm_entry(PHX_VARIANT_F16TC, M, N, K, alpha, A, B, beta, C, stream, op_a == PHX_OP_T,
+                      op_b == PHX_OP_T);
 }
 
 phx_status phx_f16tc_workspace_bytes(int64_t M, int64_t N, int64_t K, size_t* bytes) {

@@ -349,6 +349,27 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ P, int S, int64_t
     }
 }
 
+// dst (cols x rows) <- src (rows x cols) transposed, through 32 x 32 tiles of shared
+// memory padded by one column (conflict-free in both directions).
+__global__ void __launch_bounds__(256) transpose_f32_kernel(const float* __restrict__ src, float* __restrict__ dst,
+                                                            int64_t rows, int64_t cols, int64_t tiles_c) {
+    __shared__ float t[32][33];
+    const int64_t c0 = (static_cast<int64_t>(blockIdx.x) % tiles_c) * 32;
+    const int64_t r0 = (static_cast<int64_t>(blockIdx.x) / tiles_c) * 32;
+    const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;  // 32 x 8
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int64_t r = r0 + ty + i * 8, c = c0 + tx;
+        if (r < rows && c < cols) t[ty + i * 8][tx] = __ldcs(src + r * cols + c);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int64_t c = c0 + ty + i * 8, r = r0 + tx;
+        if (c < cols && r < rows) dst[c * rows + r] = t[tx][ty + i * 8];
+    }
+}
+
 // C <- beta * C over M*N elements (beta == 0 writes zeros without reading C).
 __global__ void scale_c_kernel(float* __restrict__ C, int64_t n, float beta) {
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -493,6 +514,14 @@ cudaError_t splitk_reduce_launch(const float* partial, int slices, int64_t M, in
     if (blocks < 1) blocks = 1;
     splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(partial, slices, plane, alpha,
                                                                              beta, C, vec);
+    return cudaGetLastError();
+}
+
+cudaError_t transpose_f32_launch(const float* src, float* dst, int64_t rows, int64_t cols,
+                                 cudaStream_t stream) {
+    const int64_t gx = (cols + 31) / 32, gy = (rows + 31) / 32;
+    if (gx * gy > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    transpose_f32_kernel<<<static_cast<unsigned>(gx * gy), 256, 0, stream>>>(src, dst, rows, cols, gx);
     return cudaGetLastError();
 }
 

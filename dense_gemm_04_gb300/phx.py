@@ -35,6 +35,8 @@ _SIGNATURES = {
     "phx_sgemm": (_i32, [_i64, _i64, _i64, _f32, _vp, _vp, _f32, _vp, _vp]),
     "phx_gemm_f16tc_f32acc": (_i32, [_i64, _i64, _i64, _f32, _vp, _vp, _f32, _vp, _vp]),
     "phx_gemm_f16tc_f32acc_noalloc": (_i32, [_i64, _i64, _i64, _f32, _vp, _vp, _f32, _vp, _vp]),
+    "phx_sgemm_ex": (_i32, [_i32, _i32, _i64, _i64, _i64, _f32, _vp, _vp, _f32, _vp, _vp]),
+    "phx_gemm_f16tc_f32acc_ex": (_i32, [_i32, _i32, _i64, _i64, _i64, _f32, _vp, _vp, _f32, _vp, _vp]),
     "phx_f16tc_workspace_bytes": (_i32, [_i64, _i64, _i64, ctypes.POINTER(_sz)]),
     "phx_status_string": (_cp, [_i32]),
     "phx_check_device_status": (_i32, [_vp]),
@@ -102,35 +104,62 @@ def _stream_handle(stream) -> int:
     return stream.cuda_stream
 
 
+OP_N, OP_T = 0, 1
+
+
+def _operand_op(t, name):
+    """PHX_OP_N for a contiguous matrix, PHX_OP_T for the transpose view of one."""
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be a 2-D tensor")
+    if t.is_contiguous():
+        return OP_N
+    if t.t().is_contiguous():
+        return OP_T
+    raise ValueError(f"{name} must be contiguous or the transpose of a contiguous matrix")
+
+
 def _check_operands(A, B, C):
+    """Shapes (M, N, K) and storage orders (op_a, op_b) of the GEMM's operands.  A or B may
+    be the transpose view (t.t() or t.T) of a contiguous matrix; C must be contiguous."""
     import torch
     for name, t in (("A", A), ("B", B), ("C", C)):
         if t.dtype != torch.float32:
             raise TypeError(f"{name} must be float32, got {t.dtype}")
         if not t.is_cuda:
             raise TypeError(f"{name} must be a CUDA tensor")
-        if t.dim() != 2 or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous 2-D tensor")
+    op_a, op_b = _operand_op(A, "A"), _operand_op(B, "B")
+    if C.dim() != 2 or not C.is_contiguous():
+        raise ValueError("C must be a contiguous 2-D tensor")
     M, K = A.shape
     K2, N = B.shape
     if K2 != K or tuple(C.shape) != (M, N):
         raise ValueError(f"shapes do not match: A {tuple(A.shape)}, B {tuple(B.shape)}, C {tuple(C.shape)}")
-    return M, N, K
+    return M, N, K, op_a, op_b
 
 
 def sgemm(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
-    """C <- alpha * A @ B + beta * C in f32 on the CUDA cores (in place; returns C)."""
-    M, N, K = _check_operands(A, B, C)
-    check(phx_sgemm(M, N, K, alpha, A.data_ptr(), B.data_ptr(), beta, C.data_ptr(),
-                    _stream_handle(stream)), "phx_sgemm")
+    """C <- alpha * A @ B + beta * C in f32 on the CUDA cores (in place; returns C).  A or B
+    may be a transpose view of a contiguous matrix (stored transposed)."""
+    M, N, K, op_a, op_b = _check_operands(A, B, C)
+    if op_a == OP_N and op_b == OP_N:
+        check(phx_sgemm(M, N, K, alpha, A.data_ptr(), B.data_ptr(), beta, C.data_ptr(),
+                        _stream_handle(stream)), "phx_sgemm")
+    else:
+        check(phx_sgemm_ex(op_a, op_b, M, N, K, alpha, A.data_ptr(), B.data_ptr(), beta, C.data_ptr(),
+                           _stream_handle(stream)), "phx_sgemm_ex")
     return C
 
 
 def gemm_f16tc_f32acc(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
-    """C <- alpha * f16(A) @ f16(B) + beta * C with f32 accumulation on the tensor cores."""
-    M, N, K = _check_operands(A, B, C)
-    check(phx_gemm_f16tc_f32acc(M, N, K, alpha, A.data_ptr(), B.data_ptr(), beta, C.data_ptr(),
-                                _stream_handle(stream)), "phx_gemm_f16tc_f32acc")
+    """C <- alpha * f16(A) @ f16(B) + beta * C with f32 accumulation on the tensor cores.  A or
+    B may be a transpose view of a contiguous matrix (stored transposed)."""
+    M, N, K, op_a, op_b = _check_operands(A, B, C)
+    if op_a == OP_N and op_b == OP_N:
+        check(phx_gemm_f16tc_f32acc(M, N, K, alpha, A.data_ptr(), B.data_ptr(), beta, C.data_ptr(),
+                                    _stream_handle(stream)), "phx_gemm_f16tc_f32acc")
+    else:
+        check(phx_gemm_f16tc_f32acc_ex(op_a, op_b, M, N, K, alpha, A.data_ptr(), B.data_ptr(), beta,
+                                       C.data_ptr(), _stream_handle(stream)), "phx_gemm_f16tc_f32acc_ex")
     return C
 
 
@@ -196,8 +225,8 @@ def selftest_tuner(base_s, fail=None, noise=0.0, drift=0.0, finalists=4, rounds=
     return picked.value, launches.value
 
 
-KIND_SGEMM, KIND_F16_CAST, KIND_TC_GEMM, KIND_SCALE_C = 0, 1, 2, 3
-KIND_NAMES = ("sgemm", "f16_cast", "tc_gemm", "scale_c")
+KIND_SGEMM, KIND_F16_CAST, KIND_TC_GEMM, KIND_SCALE_C, KIND_TRANSPOSE = 0, 1, 2, 3, 4
+KIND_NAMES = ("sgemm", "f16_cast", "tc_gemm", "scale_c", "transpose")
 
 
 def profile_start() -> None:
@@ -206,10 +235,11 @@ def profile_start() -> None:
 
 def profile_stop():
     """Stop the profile; returns {kind name: (launches, total device ms)}."""
-    n = (_i64 * 4)()
-    ms = (ctypes.c_double * 4)()
+    kinds = len(KIND_NAMES)
+    n = (_i64 * kinds)()
+    ms = (ctypes.c_double * kinds)()
     check(phx_profile_stop(n, ms), "phx_profile_stop")
-    return {KIND_NAMES[k]: (int(n[k]), float(ms[k])) for k in range(4)}
+    return {KIND_NAMES[k]: (int(n[k]), float(ms[k])) for k in range(kinds)}
 
 
 def validate_args(M, N, K, A, B, C) -> int:

@@ -1,6 +1,6 @@
 """Shape and arithmetic-intensity sweep of both GEMM precisions, placed on the roofline.
 
-    python -m dense_gemm_04_gb300.sweep [--out results.json] [--quick]
+    python -m dense_gemm_04_gb300.sweep [--out results.json] [--quick] [--layouts]
 
 For every shape of the workload sweep ((8192, 8192, 1024), (1024, 1024, 16384),
 (16384, 128, 4096), (4095, 4097, 4093) with alpha = 2, beta = -1; squares 512 .. 16384 with
@@ -178,11 +178,50 @@ def run(quick=False, rounds=3, seed=0):
     return {"roofs": roofs, "rows": rows}
 
 
+def run_layouts(n=4096, rounds=3, seed=0, seconds=0.5):
+    """The lab's layout sweep (Part 5): A @ B with A, B or both stored transposed, n^3,
+    alpha = 1, beta = 0, both precisions; median seconds over shuffled rounds."""
+    import torch
+    st = torch.cuda.current_stream().cuda_stream
+    A = torch.rand(n, n, device="cuda") * 2 - 1
+    B = torch.rand(n, n, device="cuda") * 2 - 1
+    C = torch.zeros(n, n, device="cuda")
+    At, Bt = A.t().contiguous(), B.t().contiguous()
+    cases = [(v, oa, ob) for v in ("sgemm", "f16tc") for oa in (phx.OP_N, phx.OP_T) for ob in (phx.OP_N, phx.OP_T)]
+    times = {c: [] for c in cases}
+    rng = np.random.default_rng(seed)
+    for _ in range(rounds):
+        for ci in rng.permutation(len(cases)):
+            v, oa, ob = cases[ci]
+            fn = phx.phx_sgemm_ex if v == "sgemm" else phx.phx_gemm_f16tc_f32acc_ex
+            a = (At if oa == phx.OP_T else A).data_ptr()
+            b = (Bt if ob == phx.OP_T else B).data_ptr()
+            times[cases[ci]].append(steady(lambda: phx.check(fn(oa, ob, n, n, n, 1.0, a, b, 0.0, C.data_ptr(), st)),
+                                           seconds=seconds))
+    rows = []
+    for v, oa, ob in cases:
+        t = float(np.median(times[(v, oa, ob)]))
+        plain = float(np.median(times[(v, phx.OP_N, phx.OP_N)]))
+        name = ("A.T" if oa == phx.OP_T else "A") + " @ " + ("B.T" if ob == phx.OP_T else "B")
+        rows.append({"variant": v, "layout": name, "seconds": t, "tflops": 2.0 * n ** 3 / t / 1e12,
+                     "vs_plain": plain / t})
+    return rows
+
+
 def main():
     ap = argparse.ArgumentParser(description="GEMM shape sweep on the roofline")
     ap.add_argument("--out", default=None)
     ap.add_argument("--quick", action="store_true", help="skip shapes above 2^40 MNK and shorten timings")
+    ap.add_argument("--layouts", action="store_true", help="time the four storage orders at 4096^3 only")
     args = ap.parse_args()
+    if args.layouts:
+        rows = run_layouts()
+        for row in rows:
+            print(f"{row['variant']:6s} {row['layout']:>11s} {row['tflops']:8.1f} TFLOP/s  {row['vs_plain']:.3f}x of A @ B")
+        if args.out:
+            with open(args.out, "w") as f:
+                json.dump({"layouts": rows}, f, indent=1)
+        return 0
     res = run(quick=args.quick)
     r = res["roofs"]
     print(f"roofs: FP32 {r['fp32_ffma']['tflops']:.1f} / f32x2 {r['fp32_ffma2']['tflops']:.1f} TFLOP/s, "

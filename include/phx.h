@@ -14,7 +14,8 @@
  * ---------------------------------------------
  * Layout     A, B and C are row-major and contiguous: A is M x K with leading dimension K,
  *            B is K x N with leading dimension N, C is M x N with leading dimension N.
- *            Element (i, j) of C is C[i * N + j].  No transposes.
+ *            Element (i, j) of C is C[i * N + j].  The _ex calls also take A or B stored
+ *            transposed (see phx_op).
  * Pointers   A, B and C are DEVICE pointers (cudaMalloc, the caching allocator of a
  *            framework, managed memory) on the current device, 4-byte aligned, and not
  *            NULL whenever their matrix has at least one element.  The caller
@@ -76,7 +77,11 @@ enum { PHX_VARIANT_SGEMM = 0, PHX_VARIANT_F16TC = 1 };
  * multiply-add; the epilogue computes alpha * acc + beta * c_old in f32.  Tile-aligned
  * shapes with 16-byte aligned pointers take the aligned fast path, all others a masked
  * path (loads past an edge read zero, stores past an edge are skipped) that gives the
- * same result.  No workspace is allocated. */
+ * same result.  A grid too small to fill the GPU is split along K: each slice of K writes
+ * its partial products to scratch taken, in stream order, from the library's pooled device
+ * memory (PHX_ERR_NOMEM if that fails), and one more kernel sums the slices in slice order
+ * and applies the epilogue, so results do not depend on timing.  Other shapes allocate
+ * nothing. */
 phx_status phx_sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float* A,
                      const float* B, float beta, float* C, phx_stream_t stream);
 
@@ -112,6 +117,32 @@ phx_status phx_gemm_f16tc_f32acc_noalloc(int64_t M, int64_t N, int64_t K, float 
                                          const float* A, const float* B, float beta, float* C,
                                          phx_stream_t stream);
 
+/* Storage order of an operand for the _ex calls, after the matrix-multiplication lab's
+ * layout sweep (Part 5: the same products with A, B or both stored transposed).  The
+ * product is always C (M x N) <- alpha * op(A) @ op(B) + beta * C with op(A) M x K and
+ * op(B) K x N, both contiguous:
+ *   PHX_OP_N   A stored M x K (A[i * K + k]);  B stored K x N (B[k * N + j]);
+ *   PHX_OP_T   A stored K x M (A[k * M + i]);  B stored N x K (B[j * K + k]). */
+typedef enum phx_op { PHX_OP_N = 0, PHX_OP_T = 1 } phx_op;
+
+/* phx_sgemm with either operand stored transposed.  An operand given as PHX_OP_T is first
+ * transposed into scratch taken, in stream order, from the library's pooled device memory
+ * (M*K or K*N floats; PHX_ERR_NOMEM if that fails), then the same kernels run, so the
+ * result is bit-identical to phx_sgemm on the transposed copy.  With PHX_OP_N for both
+ * this is phx_sgemm.  An op outside {PHX_OP_N, PHX_OP_T} is PHX_ERR_INVALID. */
+phx_status phx_sgemm_ex(phx_op op_a, phx_op op_b, int64_t M, int64_t N, int64_t K,
+                        float alpha, const float* A, const float* B, float beta, float* C,
+                        phx_stream_t stream);
+
+/* phx_gemm_f16tc_f32acc with either operand stored transposed.  The rounding pass reads
+ * each operand in its stored order and writes the same K-major f16 copies as for the plain
+ * layout (a row-wise rounding for A as PHX_OP_N and B as PHX_OP_T, a tiled transposing
+ * rounding for the other two), so no extra pass or workspace is needed and the result is
+ * bit-identical to phx_gemm_f16tc_f32acc on op(A), op(B). */
+phx_status phx_gemm_f16tc_f32acc_ex(phx_op op_a, phx_op op_b, int64_t M, int64_t N,
+                                    int64_t K, float alpha, const float* A, const float* B,
+                                    float beta, float* C, phx_stream_t stream);
+
 /* Workspace bytes phx_gemm_f16tc_f32acc takes for this shape: the rounded A (M rows) and
  * the rounded, transposed B (N rows), each row padded with zeros to a multiple of 8
  * halves. */
@@ -135,7 +166,7 @@ phx_status phx_check_device_status(phx_stream_t stream);
 
 /* Kernel kinds counted by the profile. */
 enum { PHX_KIND_SGEMM = 0, PHX_KIND_F16_CAST = 1, PHX_KIND_TC_GEMM = 2, PHX_KIND_SCALE_C = 3,
-       PHX_NUM_KINDS = 4 };
+       PHX_KIND_TRANSPOSE = 4, PHX_NUM_KINDS = 5 };
 
 /* Start a profile: from now on every GEMM call records CUDA events on its stream around
  * each kernel it launches (the f32 GEMM kernel; the f16 cast pass and the tensor-core GEMM

@@ -173,3 +173,27 @@ def test_cluster_key():
     with pytest.raises(phx.PhxError):
         phx.set_config(phx.VARIANT_SGEMM, "TILE_M=128 TILE_N=128 TILE_K=16 CLUSTER=2")
     phx.set_config(phx.VARIANT_F16TC, None)
+
+
+def test_ex_calls_check_the_op_first():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    for fn in (phx.phx_sgemm_ex, phx.phx_gemm_f16tc_f32acc_ex):
+        assert fn(2, 0, 8, 8, 8, 1.0, 0x1000, 0x2000, 0.0, 0x3000, None) == phx.PHX_ERR_INVALID
+        assert fn(0, -1, 8, 8, 8, 1.0, 0x1000, 0x2000, 0.0, 0x3000, None) == phx.PHX_ERR_INVALID
+        assert fn(1, 1, 8, 8, 8, 1.0, 0x1000, 0x2000, 0.0, 0x3000, None) == phx.PHX_ERR_ARCH
+        assert fn(1, 0, 8, 8, 8, 1.0, 0x1000, 0x2000, 0.0, 0x1000, None) == phx.PHX_ERR_INVALID
+        assert fn(1, 1, 0, 8, 8, 1.0, None, None, 0.0, None, None) == phx.PHX_OK
+
+
+def test_binding_storage_order():
+    import torch
+    x = torch.zeros(5, 3)
+    assert phx._operand_op(x, "A") == phx.OP_N
+    assert phx._operand_op(x.t(), "A") == phx.OP_T
+    assert phx._operand_op(torch.zeros(1, 4), "A") == phx.OP_N
+    with pytest.raises(ValueError):
+        phx._operand_op(torch.zeros(6, 6)[::2, ::2], "A")
+    with pytest.raises(ValueError):
+        phx._operand_op(torch.zeros(2, 3, 4), "A")
