@@ -102,6 +102,13 @@ extern "C" phx_status phx_gemm_f16tc_f32acc_noalloc(int64_t M, int64_t N, int64_
     if (cfg < 0) return PHX_ERR_INTERNAL;
     unsigned int* status_word = reinterpret_cast<unsigned int*>(d->base);
     void* workspace = d->base + kStatusBytes;
+    if (phx::is_skinny_config(PHX_VARIANT_F16TC, cfg)) {
+        // few rows of A: no rounded copies; the scratch holds the K slices' partial sums
+        if (phx::skinny_workspace_bytes(1, M, N, K, B, d->sm_count) > kNoAllocScratchBytes) return PHX_ERR_NOMEM;
+        return phx::skinny_launch(1, 0, M, N, K, alpha, A, B, beta, C, workspace, d->sm_count, stream) ==
+                       cudaSuccess
+                   ? PHX_OK : PHX_ERR_LAUNCH;
+    }
     cudaError_t err = phx::f16tc_cast_launch(M, N, K, A, B, workspace, d->sm_count, stream);
     if (err == cudaSuccess)
         err = phx::f16tc_gemm_launch(cfg, M, N, K, alpha, beta, C, workspace, nullptr, status_word,

@@ -54,6 +54,21 @@ cudaError_t splitk_reduce_launch(const float* partial, int slices, int64_t M, in
 cudaError_t transpose_f32_launch(const float* src, float* dst, int64_t rows, int64_t cols,
                                  cudaStream_t stream);
 
+// ---------------------------------------------------------------------------------------
+// Few rows of A (gemm_skinny.cu): B streamed once, CUDA-core arithmetic, both precisions
+// ---------------------------------------------------------------------------------------
+// Scratch bytes skinny_launch needs for this problem (the partial planes of its K slices;
+// 0 when it does not split K).
+size_t skinny_workspace_bytes(int f16, int64_t M, int64_t N, int64_t K, const float* B, int num_sms);
+
+// C <- alpha * op(A) @ B + beta * C for M, N, K > 0 and alpha != 0, A in blocks of 16 rows
+// (meant for few rows: every block re-reads B, from L2 when it can); with f16
+// both operands are rounded to f16 (ties to even) as they are loaded.  a_trans: A stored
+// K x M.  `workspace` holds skinny_workspace_bytes bytes (may be null when that is 0).
+cudaError_t skinny_launch(int f16, int a_trans, int64_t M, int64_t N, int64_t K, float alpha,
+                          const float* A, const float* B, float beta, float* C, void* workspace,
+                          int num_sms, cudaStream_t stream);
+
 // C <- beta * C (beta == 0: C <- 0 without reading C).  Used for K == 0 or alpha == 0.
 cudaError_t scale_c_launch(int64_t M, int64_t N, float beta, float* C, cudaStream_t stream);
 
@@ -98,6 +113,9 @@ cudaError_t f16tc_gemm_launch(int index, int64_t M, int64_t N, int64_t K, float 
 // The configuration index a call of `variant` with this shape would use now (pinned, tuned
 // or default), as phx_get_config reports it (phx_api.cu).
 int choose_config_for(int variant, int64_t M, int64_t N, int64_t K, int sms);
+
+// True if configuration `cfg` of `variant` is the skinny kernel rather than a GEMM tile.
+bool is_skinny_config(int variant, int cfg);
 
 // ---------------------------------------------------------------------------------------
 // Probes and self-tests (probes.cu)

@@ -135,14 +135,29 @@ phx_status validate(int64_t M, int64_t N, int64_t K, const void* A, const void* 
 // ---------------------------------------------------------------------------------------
 // Configurations: names, parsing, pins, the tuning cache, defaults
 // ---------------------------------------------------------------------------------------
-int num_configs(int variant) {
+// Configurations of a variant: its compiled GEMM tiles, then "SKINNY", the kernel for few
+// rows of A (gemm_skinny.cu), which takes any M as blocks of 16 rows.
+int tile_configs(int variant) {
     if (variant == PHX_VARIANT_SGEMM) return phx::sgemm_num_configs();
     if (variant == PHX_VARIANT_F16TC) return phx::f16tc_num_configs();
     return -1;
 }
 
+int num_configs(int variant) {
+    const int n = tile_configs(variant);
+    return n < 0 ? -1 : n + 1;
+}
+
+int skinny_index(int variant) { return tile_configs(variant); }
+
+// Largest M for which the skinny kernel is the default: measured crossovers at K = N = 4096
+// on GB300 (f32: skinny 55 us against 94 us for the tiles at M = 48, 78 against 70 at M = 64;
+// f16: 27 against 31 us at M = 16, 47 against 33 at M = 32, where the tensor cores win).
+int64_t skinny_default_max_m(int variant) { return variant == PHX_VARIANT_SGEMM ? 48 : 16; }
+
 std::string config_name(int variant, int i) {
     char buf[128];
+    if (i == skinny_index(variant)) return "SKINNY";
     if (variant == PHX_VARIANT_SGEMM) {
         const SgemmConfig& c = phx::sgemm_config(i);
         std::snprintf(buf, sizeof buf, "TILE_M=%d TILE_N=%d TILE_K=%d STAGES=%d FMA2=%d", c.tile_m,
@@ -161,10 +176,15 @@ std::string config_name(int variant, int i) {
 // given key (TILE_M, TILE_N, TILE_K required; STAGES optional; FMA2 for the f32 variant and
 // CLUSTER for the f16 variant optional, default 0 and 1), or -1.
 int parse_config(int variant, const char* spec) {
-    if (spec == nullptr) return -1;
+    if (spec == nullptr || num_configs(variant) < 0) return -1;
     std::map<std::string, int> kv;
     std::istringstream in(spec);
     std::string tok;
+    {
+        std::istringstream words(spec);
+        std::string w, extra;
+        if (words >> w && w == "SKINNY") return (words >> extra) ? -1 : skinny_index(variant);
+    }
     while (in >> tok) {
         const size_t eq = tok.find('=');
         if (eq == std::string::npos || eq == 0 || eq + 1 >= tok.size()) return -1;
@@ -181,7 +201,7 @@ int parse_config(int variant, const char* spec) {
         kv[key] = static_cast<int>(v);
     }
     if (!kv.count("TILE_M") || !kv.count("TILE_N") || !kv.count("TILE_K")) return -1;
-    const int n = num_configs(variant);
+    const int n = tile_configs(variant);
     for (int i = 0; i < n; ++i) {
         int tm, tn, tk, st, f2 = 0, cl = 1;
         if (variant == PHX_VARIANT_SGEMM) {
@@ -220,6 +240,7 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // work (the trade-off "gemm, f32" section "Tuning" describes: larger tiles reuse more,
 // but leave fewer CTAs to spread over the card).
 int default_config(int variant, int64_t M, int64_t N, int sms) {
+    if (M <= skinny_default_max_m(variant)) return skinny_index(variant);
     if (variant == PHX_VARIANT_SGEMM) {
         const int64_t slots = 2 * static_cast<int64_t>(sms);  // two CTAs per SM
         // 128 x 128 tiles whenever they exist: a grid too small for the GPU is then split
@@ -335,7 +356,7 @@ __global__ void tune_fill_kernel(float* p, int64_t n, uint32_t salt) {
 // stream around every kernel the library launches, summed per kernel kind at stop.
 // ---------------------------------------------------------------------------------------
 enum KernelKind { kKindSgemm = 0, kKindCast = 1, kKindTcGemm = 2, kKindScale = 3, kKindTranspose = 4,
-                  kNumKinds = 5 };
+                  kKindSkinny = 5, kNumKinds = 6 };
 
 struct Profile {
     bool on = false;
@@ -379,9 +400,50 @@ phx_status launch_sgemm_transposed(int cfg, int trans_a, int trans_b, int64_t M,
                                    float alpha, const float* A, const float* B, float beta, float* C,
                                    DevState* d, cudaStream_t stream);
 
+// The skinny kernel reads A in either storage order; B stored transposed is copied into its
+// plain layout first (pooled scratch).
+phx_status launch_skinny(int variant, int trans_a, int trans_b, int64_t M, int64_t N, int64_t K,
+                         float alpha, const float* A, const float* B, float beta, float* C,
+                         DevState* d, cudaStream_t stream) {
+    const int f16 = variant == PHX_VARIANT_F16TC ? 1 : 0;
+    void* bt = nullptr;
+    if (trans_b) {
+        if (cudaMallocFromPoolAsync(&bt, static_cast<size_t>(K * N * 4), d->pool, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return PHX_ERR_NOMEM;
+        }
+        const cudaError_t err = timed(kKindTranspose, stream, [&] {
+            return phx::transpose_f32_launch(B, static_cast<float*>(bt), N, K, stream);
+        });
+        if (err != cudaSuccess) {
+            cudaFreeAsync(bt, stream);
+            return PHX_ERR_LAUNCH;
+        }
+        B = static_cast<const float*>(bt);
+    }
+    const size_t bytes = phx::skinny_workspace_bytes(f16, M, N, K, B, d->sm_count);
+    void* ws = nullptr;
+    phx_status st = PHX_OK;
+    if (bytes > 0 && cudaMallocFromPoolAsync(&ws, bytes, d->pool, stream) != cudaSuccess) {
+        cudaGetLastError();
+        st = PHX_ERR_NOMEM;
+    }
+    if (st == PHX_OK) {
+        const cudaError_t err = timed(kKindSkinny, stream, [&] {
+            return phx::skinny_launch(f16, trans_a, M, N, K, alpha, A, B, beta, C, ws, d->sm_count, stream);
+        });
+        if (err != cudaSuccess) st = PHX_ERR_LAUNCH;
+    }
+    if (ws != nullptr) cudaFreeAsync(ws, stream);
+    if (bt != nullptr) cudaFreeAsync(bt, stream);
+    return st;
+}
+
 phx_status launch_variant(int variant, int cfg, int64_t M, int64_t N, int64_t K, float alpha,
                           const float* A, const float* B, float beta, float* C, DevState* d,
                           cudaStream_t stream, int trans_a = 0, int trans_b = 0) {
+    if (cfg == skinny_index(variant))
+        return launch_skinny(variant, trans_a, trans_b, M, N, K, alpha, A, B, beta, C, d, stream);
     if (variant == PHX_VARIANT_SGEMM && (trans_a || trans_b))
         return launch_sgemm_transposed(cfg, trans_a, trans_b, M, N, K, alpha, A, B, beta, C, d, stream);
     if (variant == PHX_VARIANT_SGEMM) {
@@ -489,6 +551,8 @@ namespace phx {
 int choose_config_for(int variant, int64_t M, int64_t N, int64_t K, int sms) {
     return choose_config(variant, M, N, K, sms);
 }
+
+bool is_skinny_config(int variant, int cfg) { return cfg == skinny_index(variant); }
 }  // namespace phx
 
 extern "C" {

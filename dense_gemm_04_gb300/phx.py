@@ -225,8 +225,8 @@ def selftest_tuner(base_s, fail=None, noise=0.0, drift=0.0, finalists=4, rounds=
     return picked.value, launches.value
 
 
-KIND_SGEMM, KIND_F16_CAST, KIND_TC_GEMM, KIND_SCALE_C, KIND_TRANSPOSE = 0, 1, 2, 3, 4
-KIND_NAMES = ("sgemm", "f16_cast", "tc_gemm", "scale_c", "transpose")
+KIND_SGEMM, KIND_F16_CAST, KIND_TC_GEMM, KIND_SCALE_C, KIND_TRANSPOSE, KIND_SKINNY = 0, 1, 2, 3, 4, 5
+KIND_NAMES = ("sgemm", "f16_cast", "tc_gemm", "scale_c", "transpose", "skinny")
 
 
 def profile_start() -> None:

@@ -1,6 +1,7 @@
 """Shape and arithmetic-intensity sweep of both GEMM precisions, placed on the roofline.
 
-    python -m dense_gemm_04_gb300.sweep [--out results.json] [--quick] [--layouts]
+    python -m dense_gemm_04_gb300.sweep [--out results.json] [--quick] [--layouts] [--skinny]
+    python -m dense_gemm_04_gb300.sweep --one M,N,K [--variant sgemm|f16tc] [--calls 5]
 
 For every shape of the workload sweep ((8192, 8192, 1024), (1024, 1024, 16384),
 (16384, 128, 4096), (4095, 4097, 4093) with alpha = 2, beta = -1; squares 512 .. 16384 with
@@ -208,12 +209,85 @@ def run_layouts(n=4096, rounds=3, seed=0, seconds=0.5):
     return rows
 
 
+def run_skinny(rounds=3, seed=0, seconds=0.3, queue=50):
+    """The lab's skinny-matrix sweep (Part 5): (M x 4096) @ (4096 x 4096) for M = 1 .. 2048,
+    both precisions, alpha = 1, beta = 0, with the default configuration (the skinny kernel
+    for small M).  Times are the median over shuffled rounds of `queue` back-to-back calls
+    between two events (the GPU time per call, without the host's launch gaps), and the
+    least traffic 4 (MK + KN + MN) bytes gives the bandwidth each call reached."""
+    import torch
+    st = torch.cuda.current_stream().cuda_stream
+    K = N = 4096
+    Ms = [1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024, 2048]
+    B = torch.rand(K, N, device="cuda") * 2 - 1
+    X = {M: (torch.rand(M, K, device="cuda") * 2 - 1, torch.zeros(M, N, device="cuda")) for M in Ms}
+    cases = [(v, M) for v in ("sgemm", "f16tc") for M in Ms]
+    times = {c: [] for c in cases}
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    rng = np.random.default_rng(seed)
+    for _ in range(rounds):
+        for ci in rng.permutation(len(cases)):
+            v, M = cases[ci]
+            A, C = X[M]
+            fn = phx.phx_sgemm if v == "sgemm" else phx.phx_gemm_f16tc_f32acc
+            call = lambda: phx.check(fn(M, N, K, 1.0, A.data_ptr(), B.data_ptr(), 0.0, C.data_ptr(), st))
+            t0 = time.perf_counter()
+            while time.perf_counter() - t0 < seconds / 2:
+                call()
+                _sync()
+            ev0.record()
+            for _ in range(queue):
+                call()
+            ev1.record()
+            ev1.synchronize()
+            times[cases[ci]].append(ev0.elapsed_time(ev1) / 1e3 / queue)
+    rows = []
+    for v, M in cases:
+        t = float(np.median(times[(v, M)]))
+        nbytes = 4.0 * (M * K + K * N + M * N)
+        rows.append({"variant": v, "M": M, "seconds": t, "tflops": 2.0 * M * N * K / t / 1e12,
+                     "gbs": nbytes / t / 1e9, "intensity": 2.0 * M * N * K / nbytes,
+                     "config": phx.get_config(0 if v == "sgemm" else 1, M, N, K)})
+    return rows
+
+
+def run_one(M, N, K, variant, calls=5, alpha=1.0, beta=0.0):
+    """A handful of calls of one shape with the default configuration, for profilers."""
+    import torch
+    st = torch.cuda.current_stream().cuda_stream
+    A = torch.rand(M, K, device="cuda") * 2 - 1
+    B = torch.rand(K, N, device="cuda") * 2 - 1
+    C = torch.zeros(M, N, device="cuda")
+    fn = phx.phx_sgemm if variant == "sgemm" else phx.phx_gemm_f16tc_f32acc
+    for _ in range(calls):
+        phx.check(fn(M, N, K, alpha, A.data_ptr(), B.data_ptr(), beta, C.data_ptr(), st))
+    torch.cuda.synchronize()
+    return phx.get_config(0 if variant == "sgemm" else 1, M, N, K)
+
+
 def main():
     ap = argparse.ArgumentParser(description="GEMM shape sweep on the roofline")
     ap.add_argument("--out", default=None)
     ap.add_argument("--quick", action="store_true", help="skip shapes above 2^40 MNK and shorten timings")
     ap.add_argument("--layouts", action="store_true", help="time the four storage orders at 4096^3 only")
+    ap.add_argument("--skinny", action="store_true", help="time M = 1 .. 2048 rows against K = N = 4096 only")
+    ap.add_argument("--one", default=None, metavar="M,N,K", help="only run a few calls of this shape (for profilers)")
+    ap.add_argument("--variant", default="sgemm", choices=("sgemm", "f16tc"), help="with --one")
+    ap.add_argument("--calls", type=int, default=5, help="with --one")
     args = ap.parse_args()
+    if args.one:
+        M, N, K = (int(x) for x in args.one.split(","))
+        print(f"{args.variant} {(M, N, K)} x{args.calls}: {run_one(M, N, K, args.variant, args.calls)}")
+        return 0
+    if args.skinny:
+        rows = run_skinny()
+        for row in rows:
+            print(f"{row['variant']:6s} M={row['M']:5d} {row['seconds'] * 1e6:9.1f} us {row['tflops']:8.2f} TFLOP/s "
+                  f"{row['gbs']:7.0f} GB/s  I={row['intensity']:7.1f}  [{row['config']}]")
+        if args.out:
+            with open(args.out, "w") as f:
+                json.dump({"skinny": rows}, f, indent=1)
+        return 0
     if args.layouts:
         rows = run_layouts()
         for row in rows:

@@ -166,7 +166,7 @@ phx_status phx_check_device_status(phx_stream_t stream);
 
 /* Kernel kinds counted by the profile. */
 enum { PHX_KIND_SGEMM = 0, PHX_KIND_F16_CAST = 1, PHX_KIND_TC_GEMM = 2, PHX_KIND_SCALE_C = 3,
-       PHX_KIND_TRANSPOSE = 4, PHX_NUM_KINDS = 5 };
+       PHX_KIND_TRANSPOSE = 4, PHX_KIND_SKINNY = 5, PHX_NUM_KINDS = 6 };
 
 /* Start a profile: from now on every GEMM call records CUDA events on its stream around
  * each kernel it launches (the f32 GEMM kernel; the f16 cast pass and the tensor-core GEMM
@@ -185,7 +185,12 @@ phx_status phx_profile_stop(int64_t* launches, double* ms);
  * A configuration is one compiled kernel shape, written as in "gemm, f32" section
  * "Tuning": "TILE_M=128 TILE_N=128 TILE_K=8 STAGES=4" (f32 variant; an optional
  * "FMA2=1" selects packed f32x2 multiply-adds) or "TILE_M=128 TILE_N=256 TILE_K=64
- * STAGES=4" (f16 variant).  The order of keys does not matter.
+ * STAGES=4" (f16 variant).  The order of keys does not matter.  The last configuration of
+ * each variant, "SKINNY", is the kernel for few rows of A (the lab's skinny-matrix sweep,
+ * Part 5): B is streamed once from HBM with 16-byte loads and the products are summed with
+ * f32 multiply-adds on the CUDA cores (for the f16 variant, of operands rounded to f16 as
+ * they are loaded: the same rounded products, summed in f32).  It takes any M, in blocks
+ * of 16 rows, and is the default for M <= 48 (f32) and M <= 16 (f16).
  * ------------------------------------------------------------------------------------- */
 
 /* Number of compiled configurations of a variant (or -1 for a bad variant). */

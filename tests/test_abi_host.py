@@ -69,6 +69,18 @@ def test_config_names_round_trip(variant):
     phx.set_config(variant, None)
 
 
+def test_skinny_config_name():
+    for variant in (phx.VARIANT_SGEMM, phx.VARIANT_F16TC):
+        names = phx.config_names(variant)
+        assert names[-1] == "SKINNY" and names.count("SKINNY") == 1
+        phx.set_config(variant, "  SKINNY ")
+        assert phx.get_config(variant, 4096, 4096, 4096) == "SKINNY"
+        for bad in ("SKINNY TILE_M=128", "SKINNY=1", "skinny"):
+            with pytest.raises(phx.PhxError):
+                phx.set_config(variant, bad)
+        phx.set_config(variant, None)
+
+
 def test_config_parse_errors():
     for spec in ("TILE_M=128", "TILE_M=128 TILE_N=128 TILE_K=7", "TILE_M=x TILE_N=1 TILE_K=1",
                  "BOGUS=1 TILE_M=128 TILE_N=128 TILE_K=8", "TILE_M=128 TILE_N=128 TILE_K=8 STAGES=9"):
@@ -95,6 +107,12 @@ def test_default_config_follows_grid_size():
     assert small.startswith("TILE_M=128 TILE_N=128")   # a small grid is split along K instead
     assert skinny.startswith("TILE_M=64 TILE_N=64")
     assert phx.get_config(phx.VARIANT_F16TC, 4096, 4096, 4096).startswith("TILE_M=256 TILE_N=256")
+    # few rows of A: the skinny kernel (B streamed once) up to 48 rows (f32) and 16 (f16)
+    assert phx.get_config(phx.VARIANT_SGEMM, 1, 4096, 4096) == "SKINNY"
+    assert phx.get_config(phx.VARIANT_SGEMM, 48, 4096, 4096) == "SKINNY"
+    assert phx.get_config(phx.VARIANT_SGEMM, 49, 4096, 4096) != "SKINNY"
+    assert phx.get_config(phx.VARIANT_F16TC, 16, 4096, 4096) == "SKINNY"
+    assert phx.get_config(phx.VARIANT_F16TC, 17, 4096, 4096) != "SKINNY"
 
 
 def test_workspace_bytes():

@@ -267,11 +267,14 @@ def test_tiling_does_not_change_values():
     # on a grid large enough not to be split along K, each output element is one k-ordered
     # chain of multiply-adds (f32) or one k-ordered sequence of MMAs (f16 tensor cores)
     # whatever the tile shape, so every configuration gives the same bits on the same inputs
+    # (the skinny kernel, whose warps split K, sums in another order and is left out)
     M, N, K = 2048, 2048, 1000
     A, B, C = synth.problem(M, N, K, seed=23)
     for vname, (variant, _) in VARIANTS.items():
         ref = None
         for cfg in phx.config_names(variant):
+            if cfg == "SKINNY":
+                continue
             phx.set_config(variant, cfg)
             got = run_cuda(variant, A, B, C, 1.0, 0.5)[1]
             if ref is None:

@@ -1,0 +1,149 @@
+"""The skinny kernel (few rows of A; the matrix-multiplication lab's skinny-matrix sweep,
+Part 5), both precisions, through the C ABI on a GB300, against the oracle.
+
+It is the default for small M and can be pinned ("SKINNY") for any M.  Covered here: M from
+1 to 64 at the sweep's K = N = 4096 in both precisions; ragged N (scalar loads, partial
+column strips), K shorter than one slice and K split into many slices; A stored transposed
+(read in place) and B stored transposed (copied first); a B pointer only 4-byte aligned;
+M beyond one block of 16 rows; the degenerate cases; run-to-run determinism.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from dense_gemm_04_gb300 import phx, synth
+from tests.gpu_util import VARIANTS, assert_bits_equal, assert_within_bound, run_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _pin_skinny():
+    for v in (phx.VARIANT_SGEMM, phx.VARIANT_F16TC):
+        phx.set_config(v, "SKINNY")
+    yield
+    for v in (phx.VARIANT_SGEMM, phx.VARIANT_F16TC):
+        phx.set_config(v, None)
+    assert phx.check_device_status() == phx.PHX_OK
+
+
+def _check(vname, M, N, K, alpha, beta, dist, seed=0):
+    variant, f16 = VARIANTS[vname]
+    A, B, C = synth.problem(M, N, K, seed=seed, dist=dist)
+    want, mag = oracle.gemm(A, B, C, alpha, beta, f16_inputs=f16)
+    st, got = run_cuda(variant, A, B, C, alpha, beta)
+    assert st == phx.PHX_OK, phx.status_string(st)
+    what = f"skinny {vname} {(M, N, K)} {dist}"
+    if dist == "int3":
+        assert_bits_equal(got, want, what)
+    else:
+        assert_within_bound(got, want, mag, C, K, alpha, beta, what)
+    return got
+
+
+@pytest.mark.parametrize("vname", list(VARIANTS))
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8, 13, 16, 17, 32, 33, 64])
+def test_skinny_sweep_shapes(vname, M):
+    # the lab's sweep: K = N = 4096
+    _check(vname, M, 4096, 4096, 1.0, 0.0, "int3", seed=M)
+    _check(vname, M, 4096, 4096, 2.0, -1.0, "uniform", seed=M)
+
+
+@pytest.mark.parametrize("vname", list(VARIANTS))
+@pytest.mark.parametrize("shape", [(1, 1, 1), (3, 5, 7), (7, 4095, 300), (16, 130, 513), (2, 129, 12345),
+                                   (9, 1, 4096), (4, 4100, 64), (64, 200, 8), (20, 384, 1000)])
+def test_skinny_ragged(vname, shape):
+    M, N, K = shape
+    _check(vname, M, N, K, 1.5, 0.5, "int3", seed=1)
+    _check(vname, M, N, K, 1.5, 0.5, "uniform", seed=2)
+
+
+@pytest.mark.parametrize("vname", list(VARIANTS))
+def test_skinny_large_m(vname):
+    # any M, as blocks of 16 rows (the pinned configuration of every test of the suite)
+    _check(vname, 301, 263, 197, 2.0, -1.0, "int3")
+    _check(vname, 256, 256, 256, 1.5, 0.5, "uniform")
+
+
+@pytest.mark.parametrize("vname", list(VARIANTS))
+def test_skinny_transposed_operands(vname):
+    import torch
+    variant, f16 = VARIANTS[vname]
+    fn = phx.phx_sgemm_ex if variant == phx.VARIANT_SGEMM else phx.phx_gemm_f16tc_f32acc_ex
+    for M, N, K in ((1, 4096, 4096), (13, 333, 777)):
+        A, B, C = synth.problem(M, N, K, seed=9, dist="int3")
+        want, _ = oracle.gemm(A, B, C, 1.0, 1.0, f16_inputs=f16)
+        for op_a in (phx.OP_N, phx.OP_T):
+            for op_b in (phx.OP_N, phx.OP_T):
+                a = np.ascontiguousarray(A.T if op_a == phx.OP_T else A)
+                b = np.ascontiguousarray(B.T if op_b == phx.OP_T else B)
+                dA, dB = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
+                dC = torch.from_numpy(C.copy()).cuda()
+                st = fn(op_a, op_b, M, N, K, 1.0, dA.data_ptr(), dB.data_ptr(), 1.0, dC.data_ptr(),
+                        torch.cuda.current_stream().cuda_stream)
+                torch.cuda.synchronize()
+                assert st == phx.PHX_OK
+                assert_bits_equal(dC.cpu().numpy(), want, f"{vname} ops ({op_a},{op_b}) {(M, N, K)}")
+
+
+@pytest.mark.parametrize("vname", list(VARIANTS))
+def test_skinny_unaligned_b(vname):
+    import torch
+    variant, f16 = VARIANTS[vname]
+    M, N, K = 6, 1024, 1024
+    A, B, C = synth.problem(M, N, K, seed=10, dist="int3")
+    want, _ = oracle.gemm(A, B, C, 1.0, 0.0, f16_inputs=f16)
+    flat = torch.zeros(K * N + 1)
+    flat[1:] = torch.from_numpy(B.reshape(-1))
+    dB = flat.cuda()
+    dA = torch.from_numpy(A).cuda()
+    dC = torch.zeros(M, N, device="cuda")
+    fn = phx.phx_sgemm if variant == phx.VARIANT_SGEMM else phx.phx_gemm_f16tc_f32acc
+    st = fn(M, N, K, 1.0, dA.data_ptr(), dB.data_ptr() + 4, 0.0, dC.data_ptr(),
+            torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert st == phx.PHX_OK
+    assert_bits_equal(dC.cpu().numpy(), want, f"{vname} unaligned B")
+
+
+@pytest.mark.parametrize("vname", list(VARIANTS))
+def test_skinny_degenerate_and_special_values(vname):
+    variant, f16 = VARIANTS[vname]
+    M, N, K = 4, 300, 600
+    A, B, C = synth.problem(M, N, K, seed=11, dist="int3")
+    # beta == 0 with NaN in C: C is not read
+    st, got = run_cuda(variant, A, B, np.full_like(C, np.nan), 1.0, 0.0)
+    want, _ = oracle.gemm(A, B, C, 1.0, 0.0, f16_inputs=f16)
+    assert st == phx.PHX_OK
+    assert_bits_equal(got, want, "beta = 0, C = NaN")
+    # an Inf in row 0 of A reaches row 0 of C only
+    A2 = A.copy()
+    A2[0, 5] = np.inf
+    B2 = np.abs(B) + 1
+    st, got = run_cuda(variant, A2, B2, C, 1.0, 0.0)
+    assert st == phx.PHX_OK
+    assert np.isinf(got[0]).all() and np.isfinite(got[1:]).all()
+    # f16 variant: values beyond the f16 range round to infinity, as the pages' rounding does
+    if f16:
+        A3 = np.zeros((1, 1), np.float32)
+        A3[0, 0] = 70000.0
+        B3 = np.ones((1, 3), np.float32)
+        st, got = run_cuda(variant, A3, B3, np.zeros((1, 3), np.float32), 1.0, 0.0)
+        assert st == phx.PHX_OK and np.isinf(got).all()
+
+
+@pytest.mark.parametrize("vname", list(VARIANTS))
+def test_skinny_is_deterministic(vname):
+    variant, _ = VARIANTS[vname]
+    A, B, C = synth.problem(24, 4096, 4096, seed=12, dist="uniform")
+    _, r1 = run_cuda(variant, A, B, C, 1.0, 0.5)
+    _, r2 = run_cuda(variant, A, B, C, 1.0, 0.5)
+    assert_bits_equal(r1, r2, "two runs")
+
+
+def test_default_routes_small_m_to_skinny():
+    for v in (phx.VARIANT_SGEMM, phx.VARIANT_F16TC):
+        phx.set_config(v, None)
+    assert phx.get_config(phx.VARIANT_SGEMM, 8, 4096, 4096) == "SKINNY"
+    _check("sgemm", 8, 4096, 4096, 1.0, 0.5, "int3", seed=13)
+    _check("f16tc", 8, 4096, 4096, 1.0, 0.5, "int3", seed=13)

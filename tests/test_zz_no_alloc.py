@@ -39,6 +39,8 @@ def test_noalloc_matches_the_pooled_entry_point_call_after_call():
         (1000, 900, 700, 1.5, 0.5, 11),      # ragged in every dimension
         (2048, 1536, 2048, 1.0, 0.5, 12),    # a larger problem reusing the same scratch
         (1000, 900, 700, 1.5, 0.5, 13),      # back to the first shape: stale scratch is harmless
+        (8, 4096, 4096, 1.0, 0.5, 14),       # few rows of A: the skinny kernel, K split in a cluster
+        (2, 128, 65536, 1.0, 0.5, 15),       # ... and in planes of partial sums in the scratch
     ]
     for M, N, K, alpha, beta, seed in problems:
         A, B, C = synth.problem(M, N, K, seed=seed)
