@@ -7,7 +7,9 @@ from .oracle import (  # noqa: F401
     build,
     f16_bits_to_f32,
     f32_to_f16_bits,
+    f64_to_f16_bits,
     gemm,
+    gemm_f16out,
     gemm_at,
     num_threads,
     round_f16,

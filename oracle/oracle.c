@@ -29,6 +29,11 @@
  *   float64 product of the same inputs; this oracle is that float64 product, plus alpha,
  *   beta and C.
  *
+ *   The same lab, Part 4 ("precision") and Part 5, times cuBLAS's f16 GEMM: f16 operands
+ *   and an f16 result, accumulated in f32.  oracle_gemm_f16out is that product's
+ *   definition: the float64 sum and epilogue as above, then one rounding straight to f16
+ *   (to nearest, ties to even) instead of to f32.
+ *
  * Readings of points the pages leave open:
  *   - beta == 0: C is not read (the BLAS reading), so NaN in C does not propagate.
  *   - alpha == 0: A and B are not read; C' = round(beta * C).
@@ -119,6 +124,34 @@ float oracle_f16_bits_to_f32(uint16_t h) {
     return sign ? -out : out;
 }
 
+/* f64 -> f16, round to nearest with ties to even, in one step (no intermediate f32).
+ * |x| lies in [2^e, 2^(e+1)); the f16 spacing there is 2^(e-10) for e >= -14 (normal) and
+ * 2^-24 below (subnormal).  x / spacing is rounded to an integer q, ties to even; q = 2048
+ * (normal) carries into the exponent, q = 1024 (subnormal) is the smallest normal, and an
+ * exponent past 15 is infinity.  Scaling by a power of two is exact in float64. */
+uint16_t oracle_f64_to_f16_bits(double x) {
+    const uint16_t sign = signbit(x) ? 0x8000u : 0u;
+    if (isnan(x)) return (uint16_t)(sign | 0x7E00u);
+    const double a = fabs(x);
+    if (isinf(a)) return (uint16_t)(sign | 0x7C00u);
+    if (a == 0.0) return sign;
+    int fe;
+    (void)frexp(a, &fe);                       /* a = m * 2^fe, 0.5 <= m < 1 */
+    const int e = fe - 1;                      /* 2^e <= a < 2^(e+1) */
+    const int spacing = e < -14 ? -24 : e - 10;
+    const double scaled = ldexp(a, -spacing);  /* exact */
+    const double fl = floor(scaled);
+    const double rem = scaled - fl;            /* exact */
+    if (fl >= 4096.0) return (uint16_t)(sign | 0x7C00u);    /* only when e > 15 */
+    uint32_t q = (uint32_t)fl;
+    if (rem > 0.5 || (rem == 0.5 && (q & 1u))) q += 1u;
+    if (e < -14) return (uint16_t)(sign | q);  /* q <= 1024: 1024 is the smallest normal */
+    int be = e + 15;                           /* biased exponent, >= 1 */
+    if (q == 2048u) { q = 1024u; be += 1; }
+    if (be >= 31) return (uint16_t)(sign | 0x7C00u);
+    return (uint16_t)(sign | ((uint32_t)be << 10) | (q - 1024u));
+}
+
 void oracle_f32_to_f16(const float* x, uint16_t* h, int64_t n) {
     for (int64_t i = 0; i < n; ++i) h[i] = oracle_f32_to_f16_bits(x[i]);
 }
@@ -149,9 +182,11 @@ void oracle_set_num_threads(int n) {
 }
 
 /* Row i of the result: D[i, :] and, if mag_out is not NULL, sum_k |a_ik| |b_kj| for the
- * error bound.  `a` is row i of A (length K), already rounded if the f16 variant asked. */
+ * error bound.  `a` is row i of A (length K), already rounded if the f16 variant asked.
+ * The one final rounding of alpha * acc + beta * c goes to f32 (d) or, when d16 is not
+ * NULL, straight from float64 to f16 bits (d16). */
 static void gemm_row(int64_t N, int64_t K, double alpha, const float* a, const float* B,
-                     double beta, const float* c, float* d, double* mag_out,
+                     double beta, const float* c, float* d, uint16_t* d16, double* mag_out,
                      double* acc, double* mag) {
     for (int64_t j = 0; j < N; ++j) { acc[j] = 0.0; if (mag) mag[j] = 0.0; }
     if (alpha != 0.0) {
@@ -168,7 +203,10 @@ static void gemm_row(int64_t N, int64_t K, double alpha, const float* a, const f
     for (int64_t j = 0; j < N; ++j) {
         double v = alpha * acc[j];
         if (beta != 0.0) v += beta * (double)c[j];
-        d[j] = (float)v;
+        if (d16)
+            d16[j] = oracle_f64_to_f16_bits(v);
+        else
+            d[j] = (float)v;
         if (mag_out) mag_out[j] = mag ? mag[j] : 0.0;
     }
 }
@@ -180,8 +218,9 @@ static void gemm_row(int64_t N, int64_t K, double alpha, const float* a, const f
  * tensor-core variant: A and B are rounded to f16 (to nearest, ties to even) first.
  * Returns 0, or -1 if memory ran out or a size is negative.
  */
-int oracle_gemm(int64_t M, int64_t N, int64_t K, float alpha, const float* A, const float* B,
-                float beta, const float* C, float* D, double* mag, int round_inputs_f16) {
+static int gemm_impl(int64_t M, int64_t N, int64_t K, float alpha, const float* A, const float* B,
+                     float beta, const float* C, float* D, uint16_t* D16, double* mag,
+                     int round_inputs_f16) {
     if (M < 0 || N < 0 || K < 0) return -1;
     if (M == 0 || N == 0) return 0;
     const double a64 = (double)alpha, b64 = (double)beta;
@@ -209,8 +248,8 @@ int oracle_gemm(int64_t M, int64_t N, int64_t K, float alpha, const float* A, co
         } else {
 #pragma omp for schedule(dynamic, 1)
             for (int64_t i = 0; i < M; ++i) {
-                gemm_row(N, K, a64, Ause + i * K, Buse, b64, C ? C + i * N : NULL, D + i * N,
-                         mag ? mag + i * N : NULL, acc, mg);
+                gemm_row(N, K, a64, Ause + i * K, Buse, b64, C ? C + i * N : NULL, D ? D + i * N : NULL,
+                         D16 ? D16 + i * N : NULL, mag ? mag + i * N : NULL, acc, mg);
             }
         }
         free(acc);
@@ -219,6 +258,22 @@ int oracle_gemm(int64_t M, int64_t N, int64_t K, float alpha, const float* A, co
     free(Ar);
     free(Br);
     return failed ? -1 : 0;
+}
+
+int oracle_gemm(int64_t M, int64_t N, int64_t K, float alpha, const float* A, const float* B,
+                float beta, const float* C, float* D, double* mag, int round_inputs_f16) {
+    return gemm_impl(M, N, K, alpha, A, B, beta, C, D, NULL, mag, round_inputs_f16);
+}
+
+/*
+ * The same product with an f16 result, as a GEMM with half-precision output computes it:
+ * D16 = round_f16(alpha * (A @ B) + beta * C) with one rounding, straight from float64 (the
+ * values of A, B and C are given as f32; for half-precision operands they are f16 values
+ * held exactly).  mag and round_inputs_f16 as in oracle_gemm.
+ */
+int oracle_gemm_f16out(int64_t M, int64_t N, int64_t K, float alpha, const float* A, const float* B,
+                       float beta, const float* C, uint16_t* D16, double* mag, int round_inputs_f16) {
+    return gemm_impl(M, N, K, alpha, A, B, beta, C, NULL, D16, mag, round_inputs_f16);
 }
 
 /*

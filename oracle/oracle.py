@@ -50,6 +50,10 @@ def _load():
             lib.oracle_gemm_at.argtypes = [i64, i64, i64, f32, vp, vp, f32, vp, vp, vp, i64,
                                            vp, vp, ci]
             lib.oracle_gemm_at.restype = ci
+            lib.oracle_gemm_f16out.argtypes = [i64, i64, i64, f32, vp, vp, f32, vp, vp, vp, ci]
+            lib.oracle_gemm_f16out.restype = ci
+            lib.oracle_f64_to_f16_bits.argtypes = [ctypes.c_double]
+            lib.oracle_f64_to_f16_bits.restype = ctypes.c_uint16
             lib.oracle_f32_to_f16.argtypes = [vp, vp, i64]
             lib.oracle_f32_to_f16.restype = None
             lib.oracle_round_f16.argtypes = [vp, vp, i64]
@@ -123,6 +127,37 @@ def gemm(A, B, C, alpha: float, beta: float, f16_inputs: bool = False,
                              1 if f16_inputs else 0)
     if rc != 0:
         raise MemoryError("oracle_gemm failed")
+    return D, mag
+
+
+def f64_to_f16_bits(x) -> np.ndarray:
+    """float64 values rounded to the nearest f16 (ties to even) in one step, as f16 bit
+    patterns (uint16)."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    fn = _load().oracle_f64_to_f16_bits
+    out = np.fromiter((fn(float(v)) for v in x.reshape(-1)), dtype=np.uint16, count=x.size)
+    return out.reshape(x.shape)
+
+
+def gemm_f16out(A, B, C, alpha: float, beta: float, f16_inputs: bool = False, want_mag: bool = True):
+    """Return (D16, mag): D16 = round_f16(alpha * A @ B + beta * C) as f16 bit patterns
+    (uint16), summed in float64 with one final rounding; mag as in gemm.  A, B and C are
+    given as f32 values (f16 operands held exactly)."""
+    A, B = _f32(A), _f32(B)
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K:
+        raise ValueError(f"inner dimensions differ: A is {A.shape}, B is {B.shape}")
+    Cp = _f32(C) if C is not None else np.zeros((M, N), np.float32)
+    if Cp.shape != (M, N):
+        raise ValueError(f"C is {Cp.shape}, expected {(M, N)}")
+    D = np.empty((M, N), dtype=np.uint16)
+    mag = np.empty((M, N), dtype=np.float64) if want_mag else None
+    rc = _load().oracle_gemm_f16out(M, N, K, np.float32(alpha), _ptr(A), _ptr(B), np.float32(beta),
+                                    _ptr(Cp), _ptr(D), _ptr(mag) if want_mag else None,
+                                    1 if f16_inputs else 0)
+    if rc != 0:
+        raise MemoryError("oracle_gemm_f16out failed")
     return D, mag
 
 

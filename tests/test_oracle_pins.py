@@ -283,3 +283,105 @@ def test_f16_variant_error_level_matches_lab(oracle_mod):
     # and without the rounding step the error is at the f32 level, far below the band
     D32, _ = oracle_mod.gemm(A, B, None, 1.0, 0.0, f16_inputs=False, want_mag=False)
     assert _errors(D32, ref)[1] < want_fro / 50
+
+
+# ----------------------------------------------------------------------------------------
+# f64 -> f16 in one rounding, and the GEMM with an f16 result (the lab's cuBLAS f16 GEMM,
+# Part 4 "precision": f16 operands and output, f32 accumulation)
+# ----------------------------------------------------------------------------------------
+
+def _np_f16_bits_from_f64(x):
+    # numpy converts float64 to binary16 directly, rounding to nearest with ties to even
+    with np.errstate(over="ignore"):
+        return np.asarray(x, dtype=np.float64).astype(np.float16).view(np.uint16)
+
+
+def test_f64_to_f16_golden_cases(oracle_mod):
+    cases = [
+        (0.0, 0x0000), (-0.0, 0x8000), (1.0, 0x3C00), (-2.0, 0xC000),
+        (65504.0, 0x7BFF),                       # largest finite
+        (65519.99999999999, 0x7BFF),             # just below the overflow tie
+        (65520.0, 0x7C00),                       # the tie rounds to even: infinity
+        (1e300, 0x7C00), (-1e300, 0xFC00), (float("inf"), 0x7C00),
+        (2.0 ** -24, 0x0001),                    # smallest subnormal
+        (2.0 ** -25, 0x0000),                    # tie between 0 and 2^-24: even is 0
+        (3 * 2.0 ** -25, 0x0002),                # tie between 1 and 2 units: even is 2
+        (2.0 ** -25 + 2.0 ** -60, 0x0001),       # just above the tie: an f32 step would lose it
+        (2.0 ** -14 - 2.0 ** -26, 0x0400),       # rounds up into the smallest normal
+        (1.0 + 2.0 ** -11, 0x3C00),              # tie at 1: even
+        (1.0 + 3 * 2.0 ** -11, 0x3C02),          # tie at 1 + 2^-10: even is 1 + 2^-9
+        (1.0 + 2.0 ** -11 + 2.0 ** -40, 0x3C01), # a float64 tail an f32 rounding would drop
+        (2047.0, 0x67FF), (2047.5, 0x6800),      # tie between 2047 and 2048: even is 2048
+        (2048.5, 0x6800), (2049.0, 0x6800), (2051.0, 0x6802),
+        (1e-300, 0x0000), (-1e-300, 0x8000),
+    ]
+    for x, want in cases:
+        got = int(oracle_mod.f64_to_f16_bits(np.array([x]))[0])
+        assert got == want, (x, hex(got), hex(want))
+    assert (int(oracle_mod.f64_to_f16_bits(np.array([float("nan")]))[0]) & 0x7FFF) > 0x7C00
+
+
+def test_f64_to_f16_matches_numpy(oracle_mod):
+    rng = np.random.default_rng(11)
+    # magnitudes across the subnormal, normal and overflow ranges, both signs
+    mags = np.ldexp(rng.uniform(1.0, 2.0, 20000), rng.integers(-30, 18, 20000))
+    x = mags * rng.choice([-1.0, 1.0], 20000)
+    # exact ties at every spacing: (2q + 1) / 2 units of 2^-24 .. 2^5
+    q = rng.integers(0, 2048, 4000)
+    sp = rng.integers(-24, 6, 4000)
+    ties = np.ldexp(2.0 * q + 1.0, sp - 1)
+    allx = np.concatenate([x, ties, -ties])
+    got = oracle_mod.f64_to_f16_bits(allx)
+    want = _np_f16_bits_from_f64(allx)
+    bad = np.nonzero(~_same_f16(got, want))[0]
+    assert bad.size == 0, [(float(allx[i]), hex(got[i]), hex(want[i])) for i in bad[:5]]
+
+
+@pytest.mark.parametrize("f16", [False, True])
+def test_gemm_f16out_integer_inputs(oracle_mod, f16):
+    # integer operands: the float64 sum is exact, and results between 2048 and 65504 land on
+    # the f16 grid's even-spaced integers, so the rounding of exact values is what is checked
+    rng = np.random.default_rng(3)
+    M, N, K = 24, 40, 300
+    A = rng.integers(-3, 4, (M, K)).astype(np.float32)
+    B = rng.integers(-3, 4, (K, N)).astype(np.float32)
+    C = rng.integers(-50, 51, (M, N)).astype(np.float32)
+    reached = False
+    for alpha, beta in ((1.0, 0.0), (48.0, 0.5), (-24.5, 2.0), (0.0, 1.5)):
+        D16, _ = oracle_mod.gemm_f16out(A, B, C, alpha, beta, f16_inputs=f16)
+        exact = alpha * (A.astype(np.int64) @ B.astype(np.int64)).astype(np.float64) + beta * C.astype(np.float64)
+        assert np.array_equal(D16, _np_f16_bits_from_f64(exact)), (alpha, beta)
+        reached |= bool(((np.abs(exact) > 2048) & (np.abs(exact) < 65504)).any())
+    assert reached   # the test reaches the spaced-out integers
+
+
+def test_gemm_f16out_brute_force_exact_rationals(oracle_mod):
+    rnd = random.Random(17)
+    for trial in range(60):
+        M, N, K = rnd.randint(1, 4), rnd.randint(1, 4), rnd.randint(1, 6)
+        # f16 operands with full 11-bit significands at mixed scales
+        A = (synth.matrix(M, K, seed=300 + trial, tensor=0) * 4).astype(np.float16).astype(np.float32)
+        B = (synth.matrix(K, N, seed=300 + trial, tensor=1) * 64).astype(np.float16).astype(np.float32)
+        C = synth.matrix(M, N, seed=300 + trial, tensor=2).astype(np.float16).astype(np.float32)
+        alpha = rnd.choice([1.0, -0.5, 3.0, 0.375])
+        beta = rnd.choice([0.0, 1.0, -2.0, 0.25])
+        D16, _ = oracle_mod.gemm_f16out(A, B, C, alpha, beta)
+        for i in range(M):
+            for j in range(N):
+                s = sum(Fraction(float(A[i, k])) * Fraction(float(B[k, j])) for k in range(K))
+                exact = Fraction(alpha) * s + Fraction(beta) * Fraction(float(C[i, j]))
+                # the exact value needs at most 53 significant bits here, so float() is exact
+                assert Fraction(float(exact)) == exact
+                want = int(_np_f16_bits_from_f64(np.array([float(exact)]))[0])
+                assert int(D16[i, j]) == want, (trial, i, j, float(exact))
+
+
+def test_gemm_f16out_agrees_with_gemm_where_f32_is_exact(oracle_mod):
+    # on f16-grid data whose results are exact in f32, rounding the f32 result to f16 and
+    # rounding straight from float64 agree
+    A = synth.matrix(17, 23, seed=5, tensor=0, dist="int3")
+    B = synth.matrix(23, 9, seed=5, tensor=1, dist="int3")
+    C = synth.matrix(17, 9, seed=5, tensor=2, dist="int3")
+    D32, _ = oracle_mod.gemm(A, B, C, 0.5, -1.0)
+    D16, _ = oracle_mod.gemm_f16out(A, B, C, 0.5, -1.0)
+    assert np.array_equal(D16, _np_f16_bits(D32))
