@@ -11,7 +11,9 @@ Prints one JSON line.  `value` is the whole job's GEMM throughput, sum of 2MNK o
 GEMMs of all steps on all ranks divided by the slowest rank's summed device time of its
 steps (CUDA events on the launching stream; L2 flushed between steps, outside the events).
 `e2e` is the same metric through the public C ABI with host buffers: the pinned-host copies
-of the step's inputs in, the GEMMs, and the results back out, all inside the timed region.
+of each step's inputs in, the GEMMs, and the results back out, all inside the timed region,
+with the copies of neighbouring steps overlapping the GEMMs (two buffer sets, three streams);
+`e2e.serial` runs the same steps one after another on one stream.
 `roofline` places the dominant kernel (the f32 SIMT GEMM) against the FP32 issue rate of
 the SMs; `roofline_tc_gemm` and `roofline_cast` place the tensor-core GEMM kernel and the
 cast pass against the measured tensor and HBM peaks.  `cpu_baseline` times the CPU oracle
@@ -309,37 +311,77 @@ def gpu_arm(args):
     if st != phx.PHX_OK:
         raise RuntimeError(f"device status after the timed steps: {phx.status_string(st)}")
 
-    # end to end through the public C ABI with host buffers: copies inside the timed region
+    # End to end through the public C ABI with host buffers: every step copies its inputs in
+    # from pinned host memory and its two results back out, inside the timed region.  The
+    # steps run the way a serving loop runs them: two buffer sets and three streams, so the
+    # copies in of step i+1 and out of step i-1 overlap the GEMMs of step i.  The same steps
+    # one after another on one stream are reported beside it ("serial").
     pA, pB = torch.from_numpy(hA).pin_memory(), torch.from_numpy(hB).pin_memory()
     pC = torch.from_numpy(hC).pin_memory()
-    out32 = torch.empty_like(pC).pin_memory()
-    out16 = torch.empty_like(pC).pin_memory()
-    dA, dB = torch.empty_like(A), torch.empty_like(B)
-    dC32, dC16 = torch.empty_like(C32), torch.empty_like(C32)
-
-    def e2e_step():
-        dA.copy_(pA, non_blocking=True)
-        dB.copy_(pB, non_blocking=True)
-        dC32.copy_(pC, non_blocking=True)
-        dC16.copy_(pC, non_blocking=True)
-        phx.check(phx.phx_sgemm(M, N, K, ALPHA, dA.data_ptr(), dB.data_ptr(), BETA, dC32.data_ptr(), sh))
-        phx.check(phx.phx_gemm_f16tc_f32acc(M, N, K, ALPHA, dA.data_ptr(), dB.data_ptr(), BETA,
-                                            dC16.data_ptr(), sh))
-        out32.copy_(dC32, non_blocking=True)
-        out16.copy_(dC16, non_blocking=True)
-
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    bufs = []
     for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    e2e_steps = max(3, min(args.steps, 10))
+        bufs.append({"A": torch.empty_like(A), "B": torch.empty_like(B), "C32": torch.empty_like(C32),
+                     "C16": torch.empty_like(C32), "o32": torch.empty_like(pC).pin_memory(),
+                     "o16": torch.empty_like(pC).pin_memory(), "in": torch.cuda.Event(),
+                     "comp": torch.cuda.Event(), "out": torch.cuda.Event()})
+
+    def gemms(b):
+        phx.check(phx.phx_sgemm(M, N, K, ALPHA, b["A"].data_ptr(), b["B"].data_ptr(), BETA, b["C32"].data_ptr(), sh))
+        phx.check(phx.phx_gemm_f16tc_f32acc(M, N, K, ALPHA, b["A"].data_ptr(), b["B"].data_ptr(), BETA,
+                                            b["C16"].data_ptr(), sh))
+
+    def copy_in(b):
+        b["A"].copy_(pA, non_blocking=True)
+        b["B"].copy_(pB, non_blocking=True)
+        b["C32"].copy_(pC, non_blocking=True)
+        b["C16"].copy_(pC, non_blocking=True)
+
+    def copy_out(b):
+        b["o32"].copy_(b["C32"], non_blocking=True)
+        b["o16"].copy_(b["C16"], non_blocking=True)
+
+    def e2e_pipelined(nsteps):
+        for i in range(nsteps):
+            b = bufs[i % 2]
+            with torch.cuda.stream(s_in):
+                s_in.wait_event(b["comp"])   # the buffer's last GEMMs are done with it
+                s_in.wait_event(b["out"])    # and its last results are out
+                copy_in(b)
+                b["in"].record(s_in)
+            stream.wait_event(b["in"])
+            gemms(b)
+            b["comp"].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(b["comp"])
+                copy_out(b)
+                b["out"].record(s_out)
+
+    def e2e_serial(nsteps):
+        b = bufs[0]
+        for _ in range(nsteps):
+            copy_in(b)
+            gemms(b)
+            copy_out(b)
+
+    e2e_steps = max(4, min(args.steps, 10))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
+    e2e_pipelined(2)
+    torch.cuda.synchronize()
+    e0.record(s_in)
+    e2e_pipelined(e2e_steps)
+    e1.record(s_out)
     torch.cuda.synchronize()
     e2e_s = e0.elapsed_time(e1) / 1e3
     e2e_max_s = reduce_max(e2e_s, ws, dev)
+    with torch.cuda.stream(stream):
+        e2e_serial(2)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        e2e_serial(e2e_steps)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    serial_max_s = reduce_max(e0.elapsed_time(e1) / 1e3, ws, dev)
     h2d = M * K * 4 + K * N * 4 + 2 * M * N * 4
     d2h = 2 * M * N * 4
 
@@ -410,7 +452,10 @@ def gpu_arm(args):
         "cpu_baseline": cpu,
         "e2e": {"value": whole_job_tflops(ws, e2e_steps, GEMMS_PER_STEP * FLOPS_PER_GEMM, e2e_max_s),
                 "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": e2e_steps},
+                "steps": e2e_steps,
+                "schedule": "copies in of step i+1 and out of step i-1 overlap the GEMMs of step i "
+                            "(two buffer sets, three streams)",
+                "serial": whole_job_tflops(ws, e2e_steps, GEMMS_PER_STEP * FLOPS_PER_GEMM, serial_max_s)},
         "clocks": clocks,
         "gpu_launches": launches,
         "kernel_launches_per_step": {k: v[0] / prof_steps for k, v in prof.items()},

@@ -64,16 +64,35 @@ __host__ __device__ constexpr int64_t round_up(int64_t x, int64_t m) { return (x
 constexpr int kTT = 64;
 
 struct CastJob {
-    const float* src;
+    const void* src;  // f32, or f16 when src_f16
     __half* dst;
-    int64_t rows;   // rows of the K-major result
-    int trans;      // source stored K x rows
-    int vec;        // 16-byte source loads allowed
-    int blocks;     // blocks of the launch this job takes
-    int tiles_r;    // trans: 64-row tiles along rows
+    int64_t rows;     // rows of the K-major result
+    int trans;        // source stored K x rows
+    int src_f16;      // the source is already f16: the job only copies (and transposes)
+    int vec;          // 16-byte source loads allowed
+    int blocks;       // blocks of the launch this job takes (0: no job)
+    int tiles_r;      // trans: 64-row tiles along rows
 };
 
 __device__ __forceinline__ int tt_swizzle(int k) { return ((k >> 3) & 7) << 2; }
+
+// Four consecutive f16 values (8 bytes, 8-byte aligned) as floats, and back, rounded to
+// nearest even.
+__device__ __forceinline__ float4 load4_h(const __half* p) {
+    const uint2 raw = *reinterpret_cast<const uint2*>(p);
+    const __half2 lo = *reinterpret_cast<const __half2*>(&raw.x);
+    const __half2 hi = *reinterpret_cast<const __half2*>(&raw.y);
+    return make_float4(__low2float(lo), __high2float(lo), __low2float(hi), __high2float(hi));
+}
+
+__device__ __forceinline__ void store4_h(__half* p, float4 v) {
+    const __half2 lo = __floats2half2_rn(v.x, v.y);
+    const __half2 hi = __floats2half2_rn(v.z, v.w);
+    uint2 raw;
+    raw.x = *reinterpret_cast<const uint32_t*>(&lo);
+    raw.y = *reinterpret_cast<const uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(p) = raw;
+}
 
 __device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
     uint4 out;
@@ -99,7 +118,21 @@ __global__ void __launch_bounds__(256) cast_kernel(CastJob j0, CastJob j1, int64
         for (int64_t idx = static_cast<int64_t>(b) * 256 + tid; idx < total; idx += stride) {
             const int64_t r = idx / chunks;
             const int64_t c = (idx - r * chunks) * 8;
-            const float* src = j.src + r * K + c;
+            if (j.src_f16) {
+                const __half* hs = static_cast<const __half*>(j.src) + r * K + c;
+                uint4 raw;
+                if (j.vec && c + 8 <= K) {
+                    raw = __ldcs(reinterpret_cast<const uint4*>(hs));
+                } else {
+                    __half h[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) h[q] = (c + q < K) ? hs[q] : __float2half_rn(0.f);
+                    raw = *reinterpret_cast<const uint4*>(h);
+                }
+                *reinterpret_cast<uint4*>(j.dst + r * Kp + c) = raw;
+                continue;
+            }
+            const float* src = static_cast<const float*>(j.src) + r * K + c;
             float v[8];
             if (j.vec && c + 8 <= K) {
                 const float4 x = __ldcs(reinterpret_cast<const float4*>(src));
@@ -118,24 +151,56 @@ __global__ void __launch_bounds__(256) cast_kernel(CastJob j0, CastJob j1, int64
     const int64_t R = j.rows;
     const int64_t r0 = static_cast<int64_t>(b % j.tiles_r) * kTT;
     const int64_t k0 = static_cast<int64_t>(b / j.tiles_r) * kTT;
+    if (j.src_f16) {
+        // f16 source: 8 halves (16 bytes) per load, 8 lanes per 128-byte row segment; the
+        // values widen to f32 exactly and pack8 below rounds them back unchanged
 #pragma unroll
-    for (int i = 0; i < kTT * kTT / 4 / 256; ++i) {
-        const int e = tid + i * 256;
-        const int k = e / (kTT / 4);
-        const int r4 = (e % (kTT / 4)) * 4;
-        const int64_t gk = k0 + k;
-        const int64_t gr = r0 + r4;
-        float4 v;
-        if (j.vec && gk < K && gr + 3 < R) {
-            v = __ldcs(reinterpret_cast<const float4*>(j.src + gk * R + gr));
-        } else {
+        for (int i = 0; i < kTT * kTT / 8 / 256; ++i) {
+            const int e = tid + i * 256;
+            const int k = e / (kTT / 8);
+            const int r8 = (e % (kTT / 8)) * 8;
+            const int64_t gk = k0 + k;
+            const int64_t gr = r0 + r8;
             const bool rk = gk < K;
-            v.x = (rk && gr + 0 < R) ? j.src[gk * R + gr + 0] : 0.f;
-            v.y = (rk && gr + 1 < R) ? j.src[gk * R + gr + 1] : 0.f;
-            v.z = (rk && gr + 2 < R) ? j.src[gk * R + gr + 2] : 0.f;
-            v.w = (rk && gr + 3 < R) ? j.src[gk * R + gr + 3] : 0.f;
+            const __half* hs = static_cast<const __half*>(j.src) + gk * R + gr;
+            float v[8];
+            if (j.vec && rk && gr + 7 < R) {
+                const uint4 raw = __ldcs(reinterpret_cast<const uint4*>(hs));
+                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const __half2 h2 = *reinterpret_cast<const __half2*>(&w[q]);
+                    v[2 * q] = __low2float(h2);
+                    v[2 * q + 1] = __high2float(h2);
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) v[q] = (rk && gr + q < R) ? __half2float(hs[q]) : 0.f;
+            }
+            *reinterpret_cast<float4*>(&tile[k][r8 ^ tt_swizzle(k)]) = make_float4(v[0], v[1], v[2], v[3]);
+            *reinterpret_cast<float4*>(&tile[k][(r8 + 4) ^ tt_swizzle(k)]) = make_float4(v[4], v[5], v[6], v[7]);
         }
-        *reinterpret_cast<float4*>(&tile[k][r4 ^ tt_swizzle(k)]) = v;
+    } else {
+#pragma unroll
+        for (int i = 0; i < kTT * kTT / 4 / 256; ++i) {
+            const int e = tid + i * 256;
+            const int k = e / (kTT / 4);
+            const int r4 = (e % (kTT / 4)) * 4;
+            const int64_t gk = k0 + k;
+            const int64_t gr = r0 + r4;
+            const bool rk = gk < K;
+            const float* fs = static_cast<const float*>(j.src) + gk * R + gr;
+            float4 v;
+            if (j.vec && rk && gr + 3 < R) {
+                v = __ldcs(reinterpret_cast<const float4*>(fs));
+            } else {
+                v.x = (rk && gr + 0 < R) ? fs[0] : 0.f;
+                v.y = (rk && gr + 1 < R) ? fs[1] : 0.f;
+                v.z = (rk && gr + 2 < R) ? fs[2] : 0.f;
+                v.w = (rk && gr + 3 < R) ? fs[3] : 0.f;
+            }
+            *reinterpret_cast<float4*>(&tile[k][r4 ^ tt_swizzle(k)]) = v;
+        }
     }
     __syncthreads();
 #pragma unroll
@@ -207,13 +272,13 @@ struct TcLayout {
     static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "swizzle atoms stay 1024-aligned");
 };
 
-template <int BN, int STAGES, int PAIR>
+template <int BN, int STAGES, int PAIR, bool OUT_H>
 __global__ void __launch_bounds__(kThreadsTc, 1)
 gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const __grid_constant__ CUtensorMap tmB_half, const __grid_constant__ CUtensorMap tmB_quarter,
                   float* __restrict__ C, int M, int N, int num_kb, float alpha, float beta, int tiles_m,
                   int tiles_n, unsigned int* status, int full_tiles, int tail_split, int ksplit,
-                  int kb_per_slice, float* __restrict__ partial) {
+                  int kb_per_slice, float* __restrict__ partial, __half* __restrict__ Ch) {
     using L = TcLayout<BN, STAGES, PAIR>;
     constexpr bool kPair = PAIR != 0;
     constexpr bool kTwoSm = PAIR == 2;
@@ -415,6 +480,8 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         uint32_t acc = 0, acc_phase = 0;
         const bool vec = (N % 4 == 0) && ((reinterpret_cast<uintptr_t>(C) & 15u) == 0) &&
                          (partial == nullptr || (reinterpret_cast<uintptr_t>(partial) & 15u) == 0);
+        // an f16 result (Ch) moves 4 halves = 8 bytes per lane on the vector path
+        const bool vec_h = (N % 4 == 0) && ((reinterpret_cast<uintptr_t>(Ch) & 7u) == 0);
         for (int w = first_item; w < num_items; w += item_stride) {
             const Item it = decode(w);
             // a k slice writes its plane of partial products; a whole tile writes C
@@ -422,6 +489,9 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             const float a_out = it.slice >= 0 ? 1.f : alpha;
             const float b_out = it.slice >= 0 ? 0.f : beta;
             const bool read_c = b_out != 0.f;
+            // a whole tile of a half-precision result rounds alpha * acc + beta * c_old to f16
+            // once (a k slice still writes f32 partial products)
+            const bool out_h = OUT_H && it.slice < 0;
             // warp-uniform outcome: the tcgen05.ld below is .sync.aligned
             if (!__all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), acc_phase, abort_flag, status))) break;
             tc_fence_after();
@@ -443,7 +513,8 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                                     __uint_as_float(r[q * 4 + 2]), __uint_as_float(r[q * 4 + 3]));
                 __syncwarp();
                 const int col0 = it.n0 + c * 32;
-                if (vec) {
+                // one code path for both result types: only the loads and stores of C differ
+                if (out_h ? vec_h : vec) {
                     const int cc = (lane % 8) * 4;
                     const int col = col0 + cc;
                     float4 cv[8];
@@ -451,9 +522,9 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 #pragma unroll
                         for (int q = 0; q < 8; ++q) {
                             const int row = row0 + q * 4 + lane / 8;
-                            cv[q] = (row < M && col < N)
-                                        ? *reinterpret_cast<const float4*>(Cout + static_cast<int64_t>(row) * N + col)
-                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+                            const int64_t off = static_cast<int64_t>(row) * N + col;
+                            cv[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            if (row < M && col < N) cv[q] = out_h ? load4_h(Ch + off) : *reinterpret_cast<const float4*>(Cout + off);
                         }
                     }
 #pragma unroll
@@ -473,7 +544,11 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                                 o.z = fmaf(b_out, cv[q].z, o.z);
                                 o.w = fmaf(b_out, cv[q].w, o.w);
                             }
-                            *reinterpret_cast<float4*>(Cout + static_cast<int64_t>(row) * N + col) = o;
+                            const int64_t off = static_cast<int64_t>(row) * N + col;
+                            if (out_h)
+                                store4_h(Ch + off, o);
+                            else
+                                *reinterpret_cast<float4*>(Cout + off) = o;
                         }
                     }
                 } else {
@@ -484,7 +559,9 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 #pragma unroll
                         for (int rr = 0; rr < 32; ++rr) {
                             const int row = row0 + rr;
-                            cs[rr] = (row < M && col < N) ? Cout[static_cast<int64_t>(row) * N + col] : 0.f;
+                            const int64_t off = static_cast<int64_t>(row) * N + col;
+                            cs[rr] = 0.f;
+                            if (row < M && col < N) cs[rr] = out_h ? __half2float(Ch[off]) : Cout[off];
                         }
                     }
 #pragma unroll
@@ -493,7 +570,11 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         if (row < M && col < N) {
                             float o = a_out * epi[rr * L::kEpiStride + lane];
                             if (read_c) o = fmaf(b_out, cs[rr], o);
-                            Cout[static_cast<int64_t>(row) * N + col] = o;
+                            const int64_t off = static_cast<int64_t>(row) * N + col;
+                            if (out_h)
+                                Ch[off] = __float2half_rn(o);
+                            else
+                                Cout[off] = o;
                         }
                     }
                 }
@@ -551,11 +632,12 @@ EncodeTiledFn encode_fn() {
 
 // Tensor map of a row-major f16 matrix (rows x Kp) read in boxes of 64 halves x box_rows,
 // 128-byte swizzle, zero fill outside the matrix.
-bool make_map(CUtensorMap* map, const __half* ptr, int64_t rows, int64_t Kp, int box_rows) {
+// A K-major f16 operand: `rows` rows of `Kp` halves (a multiple of 8), `ld` halves apart.
+bool make_map(CUtensorMap* map, const __half* ptr, int64_t rows, int64_t Kp, int box_rows, int64_t ld) {
     EncodeTiledFn enc = encode_fn();
     if (enc == nullptr) return false;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(Kp), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(Kp) * 2};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t estr[2] = {1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(ptr), dims, strides,
@@ -564,11 +646,12 @@ bool make_map(CUtensorMap* map, const __half* ptr, int64_t rows, int64_t Kp, int
 }
 
 using TcKernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, float*, int, int, int,
-                            float, float, int, int, unsigned int*, int, int, int, int, float*);
+                            float, float, int, int, unsigned int*, int, int, int, int, float*, __half*);
 
 struct TcEntry {
     F16Config cfg;
-    TcKernelFn fn;
+    TcKernelFn fn;    // f32 result
+    TcKernelFn fn_h;  // f16 result
     uint32_t smem;
 };
 
@@ -577,7 +660,8 @@ struct TcEntry {
 template <int BN, int STAGES, int PAIR>
 TcEntry make_tc_entry() {
     return TcEntry{F16Config{PAIR == 2 ? 2 * kBM : kBM, BN, kBK, STAGES, PAIR == 0 ? 1 : 2},
-                   &gemm_f16tc_kernel<BN, STAGES, PAIR>, TcLayout<BN, STAGES, PAIR>::kDynSmem};
+                   &gemm_f16tc_kernel<BN, STAGES, PAIR, false>, &gemm_f16tc_kernel<BN, STAGES, PAIR, true>,
+                   TcLayout<BN, STAGES, PAIR>::kDynSmem};
 }
 
 const TcEntry kTcEntries[] = {
@@ -599,25 +683,29 @@ size_t f16tc_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     return static_cast<size_t>(round_up(M * Kp * 2, 256) + round_up(N * Kp * 2, 256));
 }
 
-cudaError_t f16tc_cast_launch_ex(int trans_a, int trans_b, int64_t M, int64_t N, int64_t K,
-                                 const float* A, const float* B, void* workspace, int num_sms,
+cudaError_t f16tc_prepare_launch(int in_f16, int trans_a, int trans_b, int64_t M, int64_t N, int64_t K,
+                                 const void* A, const void* B, __half* Ah, __half* Bt, int num_sms,
                                  cudaStream_t stream) {
     const int64_t Kp = round_up(K, 8);
-    __half* Ah = static_cast<__half*>(workspace);
-    __half* Bt = reinterpret_cast<__half*>(static_cast<char*>(workspace) + round_up(M * Kp * 2, 256));
-    auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    auto aligned = [](const void* p, uintptr_t mask) { return (reinterpret_cast<uintptr_t>(p) & mask) == 0; };
     // K-major A is A itself unless A is given transposed; K-major B is the transpose of B
     // unless B is given transposed.
-    auto make_job = [&](const float* src, __half* dst, int64_t rows, int trans) {
+    auto make_job = [&](const void* src, __half* dst, int64_t rows, int trans) {
         CastJob j;
         j.src = src;
         j.dst = dst;
         j.rows = rows;
         j.trans = trans;
-        j.vec = (trans ? rows % 4 == 0 : K % 4 == 0) && al16(src);
+        j.src_f16 = in_f16 ? 1 : 0;
+        if (trans)
+            j.vec = rows % (in_f16 ? 8 : 4) == 0 && aligned(src, 15u);
+        else
+            j.vec = (in_f16 ? K % 8 == 0 : K % 4 == 0) && aligned(src, 15u);
         j.tiles_r = static_cast<int>((rows + kTT - 1) / kTT);
-        int64_t blocks;
-        if (trans) {
+        int64_t blocks = 0;
+        if (dst == nullptr) {
+            blocks = 0;
+        } else if (trans) {
             blocks = static_cast<int64_t>(j.tiles_r) * ((Kp + kTT - 1) / kTT);
         } else {
             blocks = (rows * (Kp / 8) + 255) / 256;
@@ -630,9 +718,19 @@ cudaError_t f16tc_cast_launch_ex(int trans_a, int trans_b, int64_t M, int64_t N,
     const CastJob ja = make_job(A, Ah, M, trans_a ? 1 : 0);
     const CastJob jb = make_job(B, Bt, N, trans_b ? 0 : 1);
     const int64_t blocks = static_cast<int64_t>(ja.blocks) + jb.blocks;
-    if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    if (blocks > 0x7FFFFFFF || ja.blocks == 0x3FFFFFFF || jb.blocks == 0x3FFFFFFF) return cudaErrorInvalidValue;
+    if (blocks == 0) return cudaSuccess;
     cast_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(ja, jb, K, Kp);
     return cudaGetLastError();
+}
+
+cudaError_t f16tc_cast_launch_ex(int trans_a, int trans_b, int64_t M, int64_t N, int64_t K,
+                                 const float* A, const float* B, void* workspace, int num_sms,
+                                 cudaStream_t stream) {
+    const int64_t Kp = round_up(K, 8);
+    __half* Ah = static_cast<__half*>(workspace);
+    __half* Bt = reinterpret_cast<__half*>(static_cast<char*>(workspace) + round_up(M * Kp * 2, 256));
+    return f16tc_prepare_launch(0, trans_a, trans_b, M, N, K, A, B, Ah, Bt, num_sms, stream);
 }
 
 cudaError_t f16tc_cast_launch(int64_t M, int64_t N, int64_t K, const float* A, const float* B,
@@ -672,17 +770,27 @@ size_t f16tc_split_bytes(int index, int64_t M, int64_t N, int64_t K, int num_sms
 cudaError_t f16tc_gemm_launch(int index, int64_t M, int64_t N, int64_t K, float alpha, float beta,
                               float* C, const void* workspace, void* split_ws, unsigned int* status,
                               int num_sms, cudaStream_t stream) {
-    const TcEntry& e = kTcEntries[index];
     const int64_t Kp = round_up(K, 8);
     const __half* Ah = static_cast<const __half*>(workspace);
     const __half* Bt = reinterpret_cast<const __half*>(static_cast<const char*>(workspace) +
                                                        round_up(M * Kp * 2, 256));
+    return f16tc_gemm_launch_ops(index, M, N, K, alpha, beta, C, nullptr, Ah, Kp, Bt, Kp, split_ws, status,
+                                 num_sms, stream);
+}
+
+cudaError_t f16tc_gemm_launch_ops(int index, int64_t M, int64_t N, int64_t K, float alpha, float beta,
+                                  float* C, __half* Ch, const __half* Ah, int64_t lda, const __half* Bt,
+                                  int64_t ldb, void* split_ws, unsigned int* status, int num_sms,
+                                  cudaStream_t stream) {
+    const TcEntry& e = kTcEntries[index];
+    const int64_t Kp = round_up(K, 8);
     CUtensorMap mapA, mapB, mapB_half, mapB_quarter;
-    if (!make_map(&mapA, Ah, M, Kp, kBM) || !make_map(&mapB, Bt, N, Kp, e.cfg.tile_n) ||
-        !make_map(&mapB_half, Bt, N, Kp, e.cfg.tile_n / 2) ||
-        !make_map(&mapB_quarter, Bt, N, Kp, e.cfg.tile_n / 4))
+    if (!make_map(&mapA, Ah, M, Kp, kBM, lda) || !make_map(&mapB, Bt, N, Kp, e.cfg.tile_n, ldb) ||
+        !make_map(&mapB_half, Bt, N, Kp, e.cfg.tile_n / 2, ldb) ||
+        !make_map(&mapB_quarter, Bt, N, Kp, e.cfg.tile_n / 4, ldb))
         return cudaErrorInvalidValue;
-    cudaError_t err = cudaFuncSetAttribute(reinterpret_cast<const void*>(e.fn),
+    const TcKernelFn fn = Ch != nullptr ? e.fn_h : e.fn;
+    cudaError_t err = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(e.smem));
     if (err != cudaSuccess) return err;
@@ -725,17 +833,18 @@ cudaError_t f16tc_gemm_launch(int index, int64_t M, int64_t N, int64_t K, float 
     lc.numAttrs = 2;
     const int m32 = static_cast<int>(M), n32 = static_cast<int>(N), full32 = static_cast<int>(full);
     float* partial = ksplit > 1 ? static_cast<float*>(split_ws) : nullptr;
-    err = cudaLaunchKernelEx(&lc, e.fn, mapA, mapB, mapB_half, mapB_quarter, C, m32, n32, num_kb, alpha,
-                             beta, tiles_m, tiles_n, status, full32, tail_split, ksplit, kb_per, partial);
+    err = cudaLaunchKernelEx(&lc, fn, mapA, mapB, mapB_half, mapB_quarter, C, m32, n32, num_kb, alpha,
+                             beta, tiles_m, tiles_n, status, full32, tail_split, ksplit, kb_per, partial, Ch);
     if (err != cudaSuccess) {
         // a stream that does not take programmatic launches: launch normally
         cudaGetLastError();
         lc.numAttrs = 1;
-        err = cudaLaunchKernelEx(&lc, e.fn, mapA, mapB, mapB_half, mapB_quarter, C, m32, n32, num_kb,
+        err = cudaLaunchKernelEx(&lc, fn, mapA, mapB, mapB_half, mapB_quarter, C, m32, n32, num_kb,
                                  alpha, beta, tiles_m, tiles_n, status, full32, tail_split, ksplit, kb_per,
-                                 partial);
+                                 partial, Ch);
     }
     if (err != cudaSuccess || ksplit == 1) return err;
+    if (Ch != nullptr) return splitk_reduce_launch_h(partial, ksplit, M, N, alpha, beta, Ch, num_sms, stream);
     return splitk_reduce_launch(partial, ksplit, M, N, alpha, beta, C, num_sms, stream);
 }
 

@@ -288,12 +288,12 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Per device and kernel: the dynamic shared memory attribute is set once and the number
 // of resident CTAs per SM measured once.
-int prepared_occupancy(SkinnyFn fn, size_t smem) {
+int prepared_occupancy(const void* fn, size_t smem) {
     static std::mutex mu;
     static std::map<std::pair<int, const void*>, int> occ;
     int dev = 0;
     cudaGetDevice(&dev);
-    const auto key = std::make_pair(dev, reinterpret_cast<const void*>(fn));
+    const auto key = std::make_pair(dev, fn);
     std::lock_guard<std::mutex> lock(mu);
     auto it = occ.find(key);
     if (it != occ.end()) return it->second;
@@ -307,6 +307,27 @@ int prepared_occupancy(SkinnyFn fn, size_t smem) {
     if (blocks < 1) blocks = 1;
     occ.emplace(key, blocks);
     return blocks;
+}
+
+// Slices of K for `tiles` output tiles on `slots` resident CTAs: one wave, each slice at
+// least `min_rows` long and a multiple of `align`, at most one cluster of 8 slices per tile
+// once that gives every SM a CTA; beyond that the clusters of a tile write partial planes.
+bool plan_slices(int64_t tiles, int64_t slots, int64_t K, int64_t min_rows, int64_t align, int num_sms, int* cs_out,
+                 int* planes_out, int* k_cta_out) {
+    int64_t slices = tiles >= slots ? 1 : slots / tiles;
+    const int64_t by_k = cdiv(K, min_rows);
+    if (slices > by_k) slices = by_k;
+    if (slices > kSkMaxCluster && tiles * kSkMaxCluster >= num_sms) slices = kSkMaxCluster;
+    if (slices < 1) slices = 1;
+    const int64_t planes = cdiv(slices, kSkMaxCluster);
+    const int64_t cs = cdiv(slices, planes);
+    slices = cs * planes;
+    const int64_t k_cta = cdiv(cdiv(K, slices), align) * align;
+    if (k_cta > 0x7FFFFFFF || planes > 65535) return false;
+    *cs_out = static_cast<int>(cs);
+    *planes_out = static_cast<int>(planes);
+    *k_cta_out = static_cast<int>(k_cta);
+    return true;
 }
 
 struct SkinnyPlan {
@@ -327,26 +348,227 @@ bool skinny_plan(int f16, int64_t M, int64_t N, int64_t K, const float* B, int n
     const bool vec = N % 4 == 0 && (reinterpret_cast<uintptr_t>(B) & 15u) == 0;
     p->fn = f16 ? pick<true>(p->mt, vec) : pick<false>(p->mt, vec);
     p->smem = smem_for(p->mt);
-    const int occ = prepared_occupancy(p->fn, p->smem);
+    const int occ = prepared_occupancy(reinterpret_cast<const void*>(p->fn), p->smem);
     if (occ < 0) return false;
-    const int64_t slots = static_cast<int64_t>(num_sms) * occ;
-    const int64_t tiles = p->strips * p->mchunks;
-    const int64_t min_rows = static_cast<int64_t>(kSkWarps) * kSkU;
-    int64_t slices = tiles >= slots ? 1 : slots / tiles;
-    const int64_t by_k = cdiv(K, min_rows);
-    if (slices > by_k) slices = by_k;
-    // one cluster per tile already gives every SM a CTA: no partial planes
-    if (slices > kSkMaxCluster && tiles * kSkMaxCluster >= num_sms) slices = kSkMaxCluster;
-    if (slices < 1) slices = 1;
-    const int64_t planes = cdiv(slices, kSkMaxCluster);
-    const int64_t cs = cdiv(slices, planes);
-    slices = cs * planes;
-    const int64_t k_cta = cdiv(cdiv(K, slices), 8) * 8;
-    if (k_cta > 0x7FFFFFFF) return false;
-    p->cs = static_cast<int>(cs);
-    p->planes = static_cast<int>(planes);
-    p->k_cta = static_cast<int>(k_cta);
-    return true;
+    return plan_slices(p->strips * p->mchunks, static_cast<int64_t>(num_sms) * occ, K,
+                       static_cast<int64_t>(kSkWarps) * kSkU, 8, num_sms, &p->cs, &p->planes, &p->k_cta);
+}
+
+// ---------------------------------------------------------------------------------------
+// B stored transposed (N x K, each output column one contiguous row of B): the layout of a
+// weight matrix W in x @ W^T.  Every column is a dot product of one row of A with one row of
+// W, both contiguous along k, so the CTA streams rows of W and reads A alongside:
+//   - A CTA owns 32 columns (rows of W), up to 16 rows of A (MT) and a slice of K, which it
+//     walks in chunks of 128.  A chunk of W (32 x 128) and of A (MT x 128) is one stage of
+//     a CTA-wide cp.async ring (kNtStages deep, copies past an edge write zeros), and one
+//     barrier per chunk makes it visible and frees the oldest slot.
+//   - Warp w takes rows 4w .. 4w+3 of W; lane l takes k = 4l .. 4l+3 of every chunk (one
+//     16-byte read per row), so each lane sums its own k's for the 4 x MT outputs, and the
+//     32 lanes are added at the end with a butterfly of shuffles (a fixed order).
+//   - The f16 variant rounds each element of W where it is used (every element is used by
+//     one lane) and the A values in place once they land (all warps use them).
+//   - The K slices of a tile are added through distributed shared memory in rank order, as
+//     in the kernel above, or, past 8 slices, through partial planes.
+// ---------------------------------------------------------------------------------------
+constexpr int kNtRows = 32;    // rows of W (output columns) per CTA
+constexpr int kNtKc = 128;     // k per chunk
+constexpr int kNtStages = 4;   // chunks in the ring
+
+__host__ __device__ constexpr int nt_stage_floats(int mt) { return (kNtRows + mt) * kNtKc; }
+
+__host__ __device__ constexpr size_t nt_smem(int mt) {
+    return static_cast<size_t>(kNtStages) * nt_stage_floats(mt) * 4 + static_cast<size_t>(mt) * kNtRows * 4;
+}
+
+template <int MT, bool F16, bool VEC>
+__global__ void __launch_bounds__(kSkThreads, 2) skinny_nt_kernel(
+    const float* __restrict__ A, const float* __restrict__ W, float* __restrict__ C, float* __restrict__ partial,
+    int M, int N, int K, int k_cta, int cs, int mchunks, int strips, int a_trans, float alpha, float beta) {
+    constexpr int S = kNtStages;
+    constexpr int SF = nt_stage_floats(MT);
+    constexpr int E = MT * kNtRows;
+    extern __shared__ float4 nt_smem4[];
+    float* ring = reinterpret_cast<float*>(nt_smem4);  // [S][32 + MT][64]: rows of W, then of A
+    float* tile = ring + S * SF;                        // [MT][32] sums of this CTA
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int rank = cs > 1 ? static_cast<int>(ptx::cluster_ctarank()) : 0;
+    const int t = static_cast<int>(blockIdx.x) / cs;
+    const int mc = t % mchunks;
+    const int strip = t / mchunks;
+    const int m0 = mc * MT;
+    const int n0 = strip * kNtRows;
+    const int slice = static_cast<int>(blockIdx.y) * cs + rank;
+    const int64_t k0 = static_cast<int64_t>(slice) * k_cta;
+    const int kn = k0 >= K ? 0 : static_cast<int>(K - k0 < k_cta ? K - k0 : k_cta);
+    const int chunks = (kn + kNtKc - 1) / kNtKc;
+
+    // Enqueue chunk c into slot c % S: 16-byte copies of W rows (4-byte ones when W's rows are
+    // not 16-byte aligned), 4-byte copies of A.  An empty commit group past the last chunk
+    // keeps the group count.  (A thread's copies of A are the ones it rounds in place.)
+    auto issue = [&](int c) {
+        if (c < chunks) {
+            float* st = ring + (c % S) * SF;
+            const int kb = c * kNtKc;
+            for (int e = tid; e < kNtRows * (kNtKc / 4); e += kSkThreads) {
+                const int r = e / (kNtKc / 4), k4 = (e % (kNtKc / 4)) * 4;
+                const int n = n0 + r;
+                const float* src = W + static_cast<int64_t>(n) * K + k0 + kb + k4;
+                const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(st + r * kNtKc + k4));
+                if (VEC) {
+                    const bool ok = n < N && kb + k4 < kn;  // kn and the k offsets are multiples of 4
+                    cp_async_16(dst, ok ? src : W, ok);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const bool ok = n < N && kb + k4 + q < kn;
+                        cp_async_4(dst + 4 * q, ok ? src + q : W, ok);
+                    }
+                }
+            }
+            float* as = st + kNtRows * kNtKc;
+            for (int e = tid; e < MT * kNtKc; e += kSkThreads) {
+                const int m = e / kNtKc, k = e % kNtKc;
+                const bool ok = m0 + m < M && kb + k < kn;
+                const int64_t gk = k0 + kb + k;
+                const float* src = !ok ? A : a_trans ? A + gk * M + m0 + m : A + static_cast<int64_t>(m0 + m) * K + gk;
+                cp_async_4(static_cast<uint32_t>(__cvta_generic_to_shared(as + e)), src, ok);
+            }
+        }
+        asm volatile("cp.async.commit_group;\n" ::: "memory");
+    };
+
+    float acc[4][MT];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int m = 0; m < MT; ++m) acc[r][m] = 0.f;
+
+#pragma unroll
+    for (int c = 0; c < S - 1; ++c) issue(c);
+    for (int c = 0; c < chunks; ++c) {
+        asm volatile("cp.async.wait_group %0;\n" ::"n"(S - 2) : "memory");
+        if (F16) {
+            // round, in place, the A values this thread copied (the same index set as issue)
+            float* as = ring + (c % S) * SF + kNtRows * kNtKc;
+            for (int e = tid; e < MT * kNtKc; e += kSkThreads) as[e] = round_f16(as[e]);
+        }
+        __syncthreads();  // chunk c visible to all; chunk c-1's slot is free
+        issue(c + S - 1);
+        const float* st = ring + (c % S) * SF;
+        float4 w4[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            w4[r] = reinterpret_cast<const float4*>(st + (4 * warp + r) * kNtKc)[lane];
+            if (F16) {
+                w4[r].x = round_f16(w4[r].x);
+                w4[r].y = round_f16(w4[r].y);
+                w4[r].z = round_f16(w4[r].z);
+                w4[r].w = round_f16(w4[r].w);
+            }
+        }
+        const float* as = st + kNtRows * kNtKc;
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            const float4 a4 = reinterpret_cast<const float4*>(as + m * kNtKc)[lane];
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                acc[r][m] = fmaf(a4.w, w4[r].w, fmaf(a4.z, w4[r].z, fmaf(a4.y, w4[r].y, fmaf(a4.x, w4[r].x, acc[r][m]))));
+        }
+    }
+    asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+
+    // the 32 lanes' sums: a butterfly, so every lane ends with every total
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            float v = acc[r][m];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            acc[r][m] = v;
+        }
+    if (lane == 0) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int m = 0; m < MT; ++m) tile[m * kNtRows + 4 * warp + r] = acc[r][m];
+    }
+
+    int e_begin = 0, e_end = E;
+    if (cs > 1) {
+        ptx::cluster_sync();
+        e_begin = rank * E / cs;
+        e_end = (rank + 1) * E / cs;
+    } else {
+        __syncthreads();
+    }
+    const uint32_t tile_addr = static_cast<uint32_t>(__cvta_generic_to_shared(tile));
+    for (int e = e_begin + tid; e < e_end; e += kSkThreads) {
+        float v;
+        if (cs > 1) {
+            v = ld_shared_cluster(ptx::map_to_rank(tile_addr + 4u * e, 0));
+            for (int q = 1; q < cs; ++q) v += ld_shared_cluster(ptx::map_to_rank(tile_addr + 4u * e, q));
+        } else {
+            v = tile[e];
+        }
+        const int m = e / kNtRows, cidx = e % kNtRows;
+        const int mm = m0 + m, n = n0 + cidx;
+        if (mm >= M || n >= N) continue;
+        const int64_t idx = static_cast<int64_t>(mm) * N + n;
+        if (partial != nullptr)
+            partial[static_cast<int64_t>(blockIdx.y) * M * N + idx] = v;
+        else
+            C[idx] = beta == 0.f ? alpha * v : fmaf(alpha, v, beta * C[idx]);
+    }
+    if (cs > 1) ptx::cluster_sync();
+}
+
+using SkinnyNtFn = void (*)(const float*, const float*, float*, float*, int, int, int, int, int, int, int, int,
+                            float, float);
+
+template <int MT, bool F16>
+SkinnyNtFn pick_nt_vec(bool vec) {
+    return vec ? skinny_nt_kernel<MT, F16, true> : skinny_nt_kernel<MT, F16, false>;
+}
+
+template <bool F16>
+SkinnyNtFn pick_nt(int mt, bool vec) {
+    switch (mt) {
+        case 1: return pick_nt_vec<1, F16>(vec);
+        case 2: return pick_nt_vec<2, F16>(vec);
+        case 4: return pick_nt_vec<4, F16>(vec);
+        case 8: return pick_nt_vec<8, F16>(vec);
+        default: return pick_nt_vec<16, F16>(vec);
+    }
+}
+
+struct SkinnyNtPlan {
+    int mt = 1, mchunks = 1, cs = 1, planes = 1, k_cta = 1, strips = 1;
+    size_t smem = 0;
+    SkinnyNtFn fn = nullptr;
+};
+
+bool skinny_nt_plan(int f16, int64_t M, int64_t N, int64_t K, const float* W, int num_sms, SkinnyNtPlan* p) {
+    if (M > 0x7FFFFFFF || N > 0x7FFFFFFF || K > 0x7FFFFFFF) return false;
+    p->mt = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16;
+    p->mchunks = static_cast<int>(cdiv(M, p->mt));
+    const int64_t strips = cdiv(N, kNtRows);
+    if (strips * p->mchunks > 0x7FFFFFFF / kSkMaxCluster) return false;
+    p->strips = static_cast<int>(strips);
+    const bool vec = K % 4 == 0 && (reinterpret_cast<uintptr_t>(W) & 15u) == 0;
+    p->fn = f16 ? pick_nt<true>(p->mt, vec) : pick_nt<false>(p->mt, vec);
+    switch (p->mt) {
+        case 1: p->smem = nt_smem(1); break;
+        case 2: p->smem = nt_smem(2); break;
+        case 4: p->smem = nt_smem(4); break;
+        case 8: p->smem = nt_smem(8); break;
+        default: p->smem = nt_smem(16); break;
+    }
+    const int occ = prepared_occupancy(reinterpret_cast<const void*>(p->fn), p->smem);
+    if (occ < 0) return false;
+    return plan_slices(strips * p->mchunks, static_cast<int64_t>(num_sms) * occ, K, 2 * kNtKc, kNtKc, num_sms,
+                       &p->cs, &p->planes, &p->k_cta);
 }
 
 }  // namespace
@@ -381,6 +603,38 @@ cudaError_t skinny_launch(int f16, int a_trans, int64_t M, int64_t N, int64_t K,
     cfg.numAttrs = 1;
     cudaError_t err = cudaLaunchKernelEx(&cfg, p.fn, A, B, C, partial, static_cast<int>(M), N, static_cast<int>(K),
                                          p.k_cta, p.cs, p.mchunks, p.strips, a_trans ? 1 : 0, alpha, beta);
+    if (err != cudaSuccess || p.planes == 1) return err;
+    return splitk_reduce_launch(partial, p.planes, M, N, alpha, beta, C, num_sms, stream);
+}
+
+size_t skinny_nt_workspace_bytes(int f16, int64_t M, int64_t N, int64_t K, const float* W, int num_sms) {
+    SkinnyNtPlan p;
+    if (!skinny_nt_plan(f16, M, N, K, W, num_sms, &p)) return 0;
+    return p.planes > 1 ? static_cast<size_t>(p.planes) * static_cast<size_t>(M * N) * 4 : 0;
+}
+
+cudaError_t skinny_nt_launch(int f16, int a_trans, int64_t M, int64_t N, int64_t K, float alpha,
+                             const float* A, const float* W, float beta, float* C, void* workspace,
+                             int num_sms, cudaStream_t stream) {
+    SkinnyNtPlan p;
+    if (!skinny_nt_plan(f16, M, N, K, W, num_sms, &p)) return cudaErrorInvalidValue;
+    if (p.planes > 1 && workspace == nullptr) return cudaErrorInvalidValue;
+    float* partial = p.planes > 1 ? static_cast<float*>(workspace) : nullptr;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.strips) * p.mchunks * p.cs, static_cast<unsigned>(p.planes), 1);
+    cfg.blockDim = dim3(kSkThreads, 1, 1);
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(p.cs);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t err = cudaLaunchKernelEx(&cfg, p.fn, A, W, C, partial, static_cast<int>(M), static_cast<int>(N),
+                                         static_cast<int>(K), p.k_cta, p.cs, p.mchunks, p.strips, a_trans ? 1 : 0,
+                                         alpha, beta);
     if (err != cudaSuccess || p.planes == 1) return err;
     return splitk_reduce_launch(partial, p.planes, M, N, alpha, beta, C, num_sms, stream);
 }

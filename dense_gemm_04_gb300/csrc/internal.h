@@ -5,6 +5,7 @@
 // gemm_f16tc.cu and probes.cu.
 #pragma once
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
@@ -50,6 +51,13 @@ cudaError_t sgemm_launch(int index, int64_t M, int64_t N, int64_t K, float alpha
 cudaError_t splitk_reduce_launch(const float* partial, int slices, int64_t M, int64_t N, float alpha,
                                  float beta, float* C, int num_sms, cudaStream_t stream);
 
+// The same reduction into an f16 C: C <- round_f16(alpha * sum + beta * C).
+cudaError_t splitk_reduce_launch_h(const float* partial, int slices, int64_t M, int64_t N, float alpha,
+                                   float beta, __half* C, int num_sms, cudaStream_t stream);
+
+// C <- beta * C for an f16 C (beta == 0: zeros without reading C), rounded to nearest even.
+cudaError_t scale_c_h_launch(int64_t M, int64_t N, float beta, __half* C, cudaStream_t stream);
+
 // dst (cols x rows) <- the transpose of src (rows x cols), both row-major f32.
 cudaError_t transpose_f32_launch(const float* src, float* dst, int64_t rows, int64_t cols,
                                  cudaStream_t stream);
@@ -68,6 +76,12 @@ size_t skinny_workspace_bytes(int f16, int64_t M, int64_t N, int64_t K, const fl
 cudaError_t skinny_launch(int f16, int a_trans, int64_t M, int64_t N, int64_t K, float alpha,
                           const float* A, const float* B, float beta, float* C, void* workspace,
                           int num_sms, cudaStream_t stream);
+
+// The same with B stored transposed as W (N x K): C <- alpha * op(A) @ W^T + beta * C.
+size_t skinny_nt_workspace_bytes(int f16, int64_t M, int64_t N, int64_t K, const float* W, int num_sms);
+cudaError_t skinny_nt_launch(int f16, int a_trans, int64_t M, int64_t N, int64_t K, float alpha,
+                             const float* A, const float* W, float beta, float* C, void* workspace,
+                             int num_sms, cudaStream_t stream);
 
 // C <- beta * C (beta == 0: C <- 0 without reading C).  Used for K == 0 or alpha == 0.
 cudaError_t scale_c_launch(int64_t M, int64_t N, float beta, float* C, cudaStream_t stream);
@@ -92,6 +106,14 @@ size_t f16tc_workspace_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t f16tc_cast_launch(int64_t M, int64_t N, int64_t K, const float* A, const float* B,
                               void* workspace, int num_sms, cudaStream_t stream);
 
+// The general preparation pass: the K-major f16 operands Ah (M x Kp) and Bt (N x Kp) from A
+// and B, which are f32 (rounded to nearest even) or, with in_f16, already f16 (copied).
+// With trans_a, A is stored K x M; with trans_b, B is stored N x K.  A null Ah or Bt skips
+// that operand (one the GEMM reads in place).
+cudaError_t f16tc_prepare_launch(int in_f16, int trans_a, int trans_b, int64_t M, int64_t N, int64_t K,
+                                 const void* A, const void* B, __half* Ah, __half* Bt, int num_sms,
+                                 cudaStream_t stream);
+
 // The same for operands given transposed: with trans_a, A is stored K x M; with trans_b, B
 // is stored N x K.  The result in `workspace` is the same K-major pair.
 cudaError_t f16tc_cast_launch_ex(int trans_a, int trans_b, int64_t M, int64_t N, int64_t K,
@@ -109,6 +131,14 @@ size_t f16tc_split_bytes(int index, int64_t M, int64_t N, int64_t K, int num_sms
 cudaError_t f16tc_gemm_launch(int index, int64_t M, int64_t N, int64_t K, float alpha, float beta,
                               float* C, const void* workspace, void* split_ws, unsigned int* status,
                               int num_sms, cudaStream_t stream);
+
+// The GEMM on explicit K-major f16 operands: Ah (M rows, lda halves apart) and Bt (N rows,
+// ldb apart), lda and ldb multiples of 8 and both 16-byte aligned.  The result goes to C
+// (f32) or, when Ch is not null, to Ch (f16, alpha * acc + beta * c_old rounded once).
+cudaError_t f16tc_gemm_launch_ops(int index, int64_t M, int64_t N, int64_t K, float alpha, float beta,
+                                  float* C, __half* Ch, const __half* Ah, int64_t lda, const __half* Bt,
+                                  int64_t ldb, void* split_ws, unsigned int* status, int num_sms,
+                                  cudaStream_t stream);
 
 // The configuration index a call of `variant` with this shape would use now (pinned, tuned
 // or default), as phx_get_config reports it (phx_api.cu).

@@ -119,17 +119,26 @@ phx_status validate_sizes(int64_t M, int64_t N, int64_t K) {
     return PHX_OK;
 }
 
-phx_status validate(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C) {
+// Sizes, null and alignment checks and the C overlap rule for operands of `ab` bytes per
+// element (A, B) and `cb` bytes per element (C); pointers must be aligned to their element.
+phx_status validate_elems(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C,
+                          int64_t ab, int64_t cb) {
     if (validate_sizes(M, N, K) != PHX_OK) return PHX_ERR_INVALID;
     if (M == 0 || N == 0) return PHX_OK;
-    auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) != 0; };
-    if (C == nullptr || misaligned(C)) return PHX_ERR_INVALID;
+    auto misaligned = [](const void* p, int64_t bytes) {
+        return (reinterpret_cast<uintptr_t>(p) & static_cast<uintptr_t>(bytes - 1)) != 0;
+    };
+    if (C == nullptr || misaligned(C, cb)) return PHX_ERR_INVALID;
     if (K > 0) {
-        if (A == nullptr || B == nullptr || misaligned(A) || misaligned(B)) return PHX_ERR_INVALID;
-        if (overlaps(A, M * K * 4, C, M * N * 4) || overlaps(B, K * N * 4, C, M * N * 4))
+        if (A == nullptr || B == nullptr || misaligned(A, ab) || misaligned(B, ab)) return PHX_ERR_INVALID;
+        if (overlaps(A, M * K * ab, C, M * N * cb) || overlaps(B, K * N * ab, C, M * N * cb))
             return PHX_ERR_INVALID;
     }
     return PHX_OK;
+}
+
+phx_status validate(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C) {
+    return validate_elems(M, N, K, A, B, C, 4, 4);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -239,8 +248,14 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // Defaults when nothing is pinned or tuned: the largest tile that still gives every SM
 // work (the trade-off "gemm, f32" section "Tuning" describes: larger tiles reuse more,
 // but leave fewer CTAs to spread over the card).
+int default_tile_config(int variant, int64_t M, int64_t N, int sms);
+
 int default_config(int variant, int64_t M, int64_t N, int sms) {
     if (M <= skinny_default_max_m(variant)) return skinny_index(variant);
+    return default_tile_config(variant, M, N, sms);
+}
+
+int default_tile_config(int variant, int64_t M, int64_t N, int sms) {
     if (variant == PHX_VARIANT_SGEMM) {
         const int64_t slots = 2 * static_cast<int64_t>(sms);  // two CTAs per SM
         // 128 x 128 tiles whenever they exist: a grid too small for the GPU is then split
@@ -400,43 +415,25 @@ phx_status launch_sgemm_transposed(int cfg, int trans_a, int trans_b, int64_t M,
                                    float alpha, const float* A, const float* B, float beta, float* C,
                                    DevState* d, cudaStream_t stream);
 
-// The skinny kernel reads A in either storage order; B stored transposed is copied into its
-// plain layout first (pooled scratch).
+// The skinny kernels read A in either storage order; B stored transposed (N x K) has a
+// kernel of its own, which streams B's rows.
 phx_status launch_skinny(int variant, int trans_a, int trans_b, int64_t M, int64_t N, int64_t K,
                          float alpha, const float* A, const float* B, float beta, float* C,
                          DevState* d, cudaStream_t stream) {
     const int f16 = variant == PHX_VARIANT_F16TC ? 1 : 0;
-    void* bt = nullptr;
-    if (trans_b) {
-        if (cudaMallocFromPoolAsync(&bt, static_cast<size_t>(K * N * 4), d->pool, stream) != cudaSuccess) {
-            cudaGetLastError();
-            return PHX_ERR_NOMEM;
-        }
-        const cudaError_t err = timed(kKindTranspose, stream, [&] {
-            return phx::transpose_f32_launch(B, static_cast<float*>(bt), N, K, stream);
-        });
-        if (err != cudaSuccess) {
-            cudaFreeAsync(bt, stream);
-            return PHX_ERR_LAUNCH;
-        }
-        B = static_cast<const float*>(bt);
-    }
-    const size_t bytes = phx::skinny_workspace_bytes(f16, M, N, K, B, d->sm_count);
+    const size_t bytes = trans_b ? phx::skinny_nt_workspace_bytes(f16, M, N, K, B, d->sm_count)
+                                 : phx::skinny_workspace_bytes(f16, M, N, K, B, d->sm_count);
     void* ws = nullptr;
-    phx_status st = PHX_OK;
     if (bytes > 0 && cudaMallocFromPoolAsync(&ws, bytes, d->pool, stream) != cudaSuccess) {
         cudaGetLastError();
-        st = PHX_ERR_NOMEM;
+        return PHX_ERR_NOMEM;
     }
-    if (st == PHX_OK) {
-        const cudaError_t err = timed(kKindSkinny, stream, [&] {
-            return phx::skinny_launch(f16, trans_a, M, N, K, alpha, A, B, beta, C, ws, d->sm_count, stream);
-        });
-        if (err != cudaSuccess) st = PHX_ERR_LAUNCH;
-    }
+    const cudaError_t err = timed(kKindSkinny, stream, [&] {
+        return trans_b ? phx::skinny_nt_launch(f16, trans_a, M, N, K, alpha, A, B, beta, C, ws, d->sm_count, stream)
+                       : phx::skinny_launch(f16, trans_a, M, N, K, alpha, A, B, beta, C, ws, d->sm_count, stream);
+    });
     if (ws != nullptr) cudaFreeAsync(ws, stream);
-    if (bt != nullptr) cudaFreeAsync(bt, stream);
-    return st;
+    return err == cudaSuccess ? PHX_OK : PHX_ERR_LAUNCH;
 }
 
 phx_status launch_variant(int variant, int cfg, int64_t M, int64_t N, int64_t K, float alpha,
@@ -531,6 +528,57 @@ phx_status gemm_entry(int variant, int64_t M, int64_t N, int64_t K, float alpha,
     return launch_variant(variant, cfg, M, N, K, alpha, A, B, beta, C, d, stream, trans_a, trans_b);
 }
 
+// Half-precision operands (phx_gemm_f16in_*): no rounding pass, only the copy into the
+// K-major layout the tensor cores read, which A skips when it can be read in place (stored
+// M x K with K a multiple of 8 and 16-byte aligned).  The tile configuration is the f16
+// variant's; where that would be the skinny kernel, which reads f32, the default tile.
+phx_status f16in_entry(int trans_a, int trans_b, int64_t M, int64_t N, int64_t K, float alpha, const void* A,
+                       const void* B, float beta, float* C, __half* Ch, cudaStream_t stream) {
+    phx_status st = validate_elems(M, N, K, A, B, C != nullptr ? static_cast<const void*>(C) : Ch, 2,
+                                   C != nullptr ? 4 : 2);
+    if (st != PHX_OK) return st;
+    if (M == 0 || N == 0) return PHX_OK;
+    DevState* d = nullptr;
+    st = device_state(&d);
+    if (st != PHX_OK) return st;
+    if (K == 0 || alpha == 0.f) {
+        if (beta == 1.f) return PHX_OK;
+        const cudaError_t err = timed(kKindScale, stream, [&] {
+            return C != nullptr ? phx::scale_c_launch(M, N, beta, C, stream) : phx::scale_c_h_launch(M, N, beta, Ch, stream);
+        });
+        return err == cudaSuccess ? PHX_OK : PHX_ERR_LAUNCH;
+    }
+    int cfg = choose_config(PHX_VARIANT_F16TC, M, N, K, d->sm_count);
+    if (cfg == skinny_index(PHX_VARIANT_F16TC)) cfg = default_tile_config(PHX_VARIANT_F16TC, M, N, d->sm_count);
+    if (cfg < 0) return PHX_ERR_INTERNAL;
+    const int64_t Kp = (K + 7) / 8 * 8;
+    const bool a_direct = !trans_a && K % 8 == 0 && (reinterpret_cast<uintptr_t>(A) & 15u) == 0;
+    auto r256 = [](int64_t b) { return (b + 255) / 256 * 256; };
+    const int64_t a_bytes = a_direct ? 0 : r256(M * Kp * 2);
+    const int64_t b_bytes = r256(N * Kp * 2);
+    const size_t split_bytes = phx::f16tc_split_bytes(cfg, M, N, K, d->sm_count);
+    void* ws = nullptr;
+    if (cudaMallocFromPoolAsync(&ws, static_cast<size_t>(a_bytes + b_bytes) + split_bytes, d->pool, stream) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return PHX_ERR_NOMEM;
+    }
+    __half* Ah = a_direct ? nullptr : static_cast<__half*>(ws);
+    __half* Bt = reinterpret_cast<__half*>(static_cast<char*>(ws) + a_bytes);
+    void* split_ws = split_bytes > 0 ? static_cast<char*>(ws) + a_bytes + b_bytes : nullptr;
+    cudaError_t err = timed(kKindCast, stream, [&] {
+        return phx::f16tc_prepare_launch(1, trans_a, trans_b, M, N, K, A, B, Ah, Bt, d->sm_count, stream);
+    });
+    if (err == cudaSuccess)
+        err = timed(kKindTcGemm, stream, [&] {
+            const __half* a_ops = a_direct ? static_cast<const __half*>(A) : Ah;
+            return phx::f16tc_gemm_launch_ops(cfg, M, N, K, alpha, beta, C, Ch, a_ops, a_direct ? K : Kp, Bt, Kp,
+                                              split_ws, d->status, d->sm_count, stream);
+        });
+    cudaFreeAsync(ws, stream);
+    return err == cudaSuccess ? PHX_OK : PHX_ERR_LAUNCH;
+}
+
 bool valid_op(phx_op op) {
     const int v = static_cast<int>(op);
     return v == PHX_OP_N || v == PHX_OP_T;
@@ -601,6 +649,21 @@ phx_status phx_gemm_f16tc_f32acc_ex(phx_op op_a, phx_op op_b, int64_t M, int64_t
     if (!valid_op(op_a) || !valid_op(op_b)) return PHX_ERR_INVALID;
     return gemm_entry(PHX_VARIANT_F16TC, M, N, K, alpha, A, B, beta, C, stream, op_a == PHX_OP_T,
                       op_b == PHX_OP_T);
+}
+
+phx_status phx_gemm_f16in_f32acc(phx_op op_a, phx_op op_b, int64_t M, int64_t N, int64_t K, float alpha,
+                                 const phx_f16* A, const phx_f16* B, float beta, float* C,
+                                 phx_stream_t stream) {
+    if (!valid_op(op_a) || !valid_op(op_b)) return PHX_ERR_INVALID;
+    return f16in_entry(op_a == PHX_OP_T, op_b == PHX_OP_T, M, N, K, alpha, A, B, beta, C, nullptr, stream);
+}
+
+phx_status phx_gemm_f16in_f16out(phx_op op_a, phx_op op_b, int64_t M, int64_t N, int64_t K, float alpha,
+                                 const phx_f16* A, const phx_f16* B, float beta, phx_f16* C,
+                                 phx_stream_t stream) {
+    if (!valid_op(op_a) || !valid_op(op_b)) return PHX_ERR_INVALID;
+    return f16in_entry(op_a == PHX_OP_T, op_b == PHX_OP_T, M, N, K, alpha, A, B, beta, nullptr,
+                       reinterpret_cast<__half*>(C), stream);
 }
 
 phx_status phx_f16tc_workspace_bytes(int64_t M, int64_t N, int64_t K, size_t* bytes) {

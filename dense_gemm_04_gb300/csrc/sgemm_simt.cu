@@ -349,6 +349,26 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ P, int S, int64_t
     }
 }
 
+// The split-K reduction into a half-precision C: the slices added in order in f32, then
+// alpha * sum + beta * c_old rounded to f16 once.
+__global__ void splitk_reduce_h_kernel(const float* __restrict__ P, int S, int64_t plane, float alpha, float beta,
+                                       __half* __restrict__ C) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < plane; i += stride) {
+        float acc = P[i];
+        for (int s = 1; s < S; ++s) acc += P[s * plane + i];
+        float o = alpha * acc;
+        if (beta != 0.f) o = fmaf(beta, __half2float(C[i]), o);
+        C[i] = __float2half_rn(o);
+    }
+}
+
+__global__ void scale_c_h_kernel(__half* __restrict__ C, int64_t n, float beta) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
+        C[i] = __float2half_rn(beta == 0.f ? 0.f : beta * __half2float(C[i]));
+}
+
 // dst (cols x rows) <- src (rows x cols) transposed, through 32 x 32 tiles of shared
 // memory padded by one column (conflict-free in both directions).
 __global__ void __launch_bounds__(256) transpose_f32_kernel(const float* __restrict__ src, float* __restrict__ dst,
@@ -514,6 +534,25 @@ cudaError_t splitk_reduce_launch(const float* partial, int slices, int64_t M, in
     if (blocks < 1) blocks = 1;
     splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(partial, slices, plane, alpha,
                                                                              beta, C, vec);
+    return cudaGetLastError();
+}
+
+cudaError_t splitk_reduce_launch_h(const float* partial, int slices, int64_t M, int64_t N, float alpha,
+                                   float beta, __half* C, int num_sms, cudaStream_t stream) {
+    const int64_t plane = M * N;
+    int64_t blocks = (plane + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    if (blocks > cap) blocks = cap;
+    splitk_reduce_h_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(partial, slices, plane, alpha,
+                                                                               beta, C);
+    return cudaGetLastError();
+}
+
+cudaError_t scale_c_h_launch(int64_t M, int64_t N, float beta, __half* C, cudaStream_t stream) {
+    const int64_t n = M * N;
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    scale_c_h_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(C, n, beta);
     return cudaGetLastError();
 }
 

@@ -37,6 +37,8 @@ _SIGNATURES = {
     "phx_gemm_f16tc_f32acc_noalloc": (_i32, [_i64, _i64, _i64, _f32, _vp, _vp, _f32, _vp, _vp]),
     "phx_sgemm_ex": (_i32, [_i32, _i32, _i64, _i64, _i64, _f32, _vp, _vp, _f32, _vp, _vp]),
     "phx_gemm_f16tc_f32acc_ex": (_i32, [_i32, _i32, _i64, _i64, _i64, _f32, _vp, _vp, _f32, _vp, _vp]),
+    "phx_gemm_f16in_f32acc": (_i32, [_i32, _i32, _i64, _i64, _i64, _f32, _vp, _vp, _f32, _vp, _vp]),
+    "phx_gemm_f16in_f16out": (_i32, [_i32, _i32, _i64, _i64, _i64, _f32, _vp, _vp, _f32, _vp, _vp]),
     "phx_f16tc_workspace_bytes": (_i32, [_i64, _i64, _i64, ctypes.POINTER(_sz)]),
     "phx_status_string": (_cp, [_i32]),
     "phx_check_device_status": (_i32, [_vp]),
@@ -147,6 +149,32 @@ def sgemm(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
     else:
         check(phx_sgemm_ex(op_a, op_b, M, N, K, alpha, A.data_ptr(), B.data_ptr(), beta, C.data_ptr(),
                            _stream_handle(stream)), "phx_sgemm_ex")
+    return C
+
+
+def gemm_f16(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
+    """C <- alpha * A @ B + beta * C for half-precision A and B (torch.float16, contiguous or
+    transpose views), summed in f32 on the tensor cores; C is float32 (phx_gemm_f16in_f32acc)
+    or float16 (phx_gemm_f16in_f16out: rounded to f16 once).  In place; returns C."""
+    import torch
+    for name, t in (("A", A), ("B", B)):
+        if t.dtype != torch.float16:
+            raise TypeError(f"{name} must be float16, got {t.dtype}")
+        if not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA tensor")
+    if C.dtype not in (torch.float32, torch.float16) or not C.is_cuda:
+        raise TypeError(f"C must be a float32 or float16 CUDA tensor, got {C.dtype}")
+    op_a, op_b = _operand_op(A, "A"), _operand_op(B, "B")
+    if C.dim() != 2 or not C.is_contiguous():
+        raise ValueError("C must be a contiguous 2-D tensor")
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K or tuple(C.shape) != (M, N):
+        raise ValueError(f"shapes do not match: A {tuple(A.shape)}, B {tuple(B.shape)}, C {tuple(C.shape)}")
+    fn, name = ((phx_gemm_f16in_f32acc, "phx_gemm_f16in_f32acc") if C.dtype == torch.float32
+                else (phx_gemm_f16in_f16out, "phx_gemm_f16in_f16out"))
+    check(fn(op_a, op_b, M, N, K, alpha, A.data_ptr(), B.data_ptr(), beta, C.data_ptr(), _stream_handle(stream)),
+          name)
     return C
 
 

@@ -1,7 +1,7 @@
 """Shape and arithmetic-intensity sweep of both GEMM precisions, placed on the roofline.
 
-    python -m dense_gemm_04_gb300.sweep [--out results.json] [--quick] [--layouts] [--skinny]
-    python -m dense_gemm_04_gb300.sweep --one M,N,K [--variant sgemm|f16tc] [--calls 5]
+    python -m dense_gemm_04_gb300.sweep [--out results.json] [--quick] [--layouts] [--skinny] [--f16in]
+    python -m dense_gemm_04_gb300.sweep --one M,N,K [--variant sgemm|f16tc|f16in|f16out] [--calls 5]
 
 For every shape of the workload sweep ((8192, 8192, 1024), (1024, 1024, 16384),
 (16384, 128, 4096), (4095, 4097, 4093) with alpha = 2, beta = -1; squares 512 .. 16384 with
@@ -209,7 +209,7 @@ def run_layouts(n=4096, rounds=3, seed=0, seconds=0.5):
     return rows
 
 
-def run_skinny(rounds=3, seed=0, seconds=0.3, queue=50):
+def run_skinny(rounds=3, seed=0, seconds=0.3, queue=50, b_transposed=False):
     """The lab's skinny-matrix sweep (Part 5): (M x 4096) @ (4096 x 4096) for M = 1 .. 2048,
     both precisions, alpha = 1, beta = 0, with the default configuration (the skinny kernel
     for small M).  Times are the median over shuffled rounds of `queue` back-to-back calls
@@ -220,6 +220,9 @@ def run_skinny(rounds=3, seed=0, seconds=0.3, queue=50):
     K = N = 4096
     Ms = [1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024, 2048]
     B = torch.rand(K, N, device="cuda") * 2 - 1
+    if b_transposed:   # B stored N x K, the layout of a weight matrix in x @ W^T
+        B = B.t().contiguous()
+    op_b = phx.OP_T if b_transposed else phx.OP_N
     X = {M: (torch.rand(M, K, device="cuda") * 2 - 1, torch.zeros(M, N, device="cuda")) for M in Ms}
     cases = [(v, M) for v in ("sgemm", "f16tc") for M in Ms]
     times = {c: [] for c in cases}
@@ -229,8 +232,8 @@ def run_skinny(rounds=3, seed=0, seconds=0.3, queue=50):
         for ci in rng.permutation(len(cases)):
             v, M = cases[ci]
             A, C = X[M]
-            fn = phx.phx_sgemm if v == "sgemm" else phx.phx_gemm_f16tc_f32acc
-            call = lambda: phx.check(fn(M, N, K, 1.0, A.data_ptr(), B.data_ptr(), 0.0, C.data_ptr(), st))
+            fn = phx.phx_sgemm_ex if v == "sgemm" else phx.phx_gemm_f16tc_f32acc_ex
+            call = lambda: phx.check(fn(phx.OP_N, op_b, M, N, K, 1.0, A.data_ptr(), B.data_ptr(), 0.0, C.data_ptr(), st))
             t0 = time.perf_counter()
             while time.perf_counter() - t0 < seconds / 2:
                 call()
@@ -251,16 +254,61 @@ def run_skinny(rounds=3, seed=0, seconds=0.3, queue=50):
     return rows
 
 
+def run_f16in(rounds=3, seed=0, seconds=0.5):
+    """Half-precision operands against the f32-operand tensor-core path (the lab's Part 4
+    precision study: cuBLAS f16 GEMM), squares 2048 .. 8192 with alpha = 1, beta = 0.5:
+    phx_gemm_f16tc_f32acc (f32 in, rounded in the op), phx_gemm_f16in_f32acc (f16 in, f32
+    out) and phx_gemm_f16in_f16out (f16 in and out).  Median seconds of steady timing over
+    shuffled rounds."""
+    import torch
+    st = torch.cuda.current_stream().cuda_stream
+    sizes = (2048, 4096, 8192)
+    kinds = ("f32in_f32out", "f16in_f32out", "f16in_f16out")
+    cases = [(n, k) for n in sizes for k in kinds]
+    times = {c: [] for c in cases}
+    rng = np.random.default_rng(seed)
+    for _ in range(rounds):
+        for ci in rng.permutation(len(cases)):
+            n, kind = cases[ci]
+            A = torch.rand(n, n, device="cuda") * 2 - 1
+            B = torch.rand(n, n, device="cuda") * 2 - 1
+            C = torch.rand(n, n, device="cuda") * 2 - 1
+            if kind == "f32in_f32out":
+                call = lambda: phx.check(phx.phx_gemm_f16tc_f32acc(n, n, n, 1.0, A.data_ptr(), B.data_ptr(), 0.5,
+                                                                   C.data_ptr(), st))
+            else:
+                A, B = A.half(), B.half()
+                if kind == "f16in_f16out":
+                    C = C.half()
+                fn = phx.phx_gemm_f16in_f32acc if kind == "f16in_f32out" else phx.phx_gemm_f16in_f16out
+                call = lambda: phx.check(fn(0, 0, n, n, n, 1.0, A.data_ptr(), B.data_ptr(), 0.5, C.data_ptr(), st))
+            times[cases[ci]].append(steady(call, seconds=seconds))
+            del A, B, C
+            torch.cuda.empty_cache()
+    return [{"n": n, "kind": kind, "seconds": float(np.median(times[(n, kind)])),
+             "tflops": 2.0 * n ** 3 / float(np.median(times[(n, kind)])) / 1e12} for n, kind in cases]
+
+
 def run_one(M, N, K, variant, calls=5, alpha=1.0, beta=0.0):
-    """A handful of calls of one shape with the default configuration, for profilers."""
+    """A handful of calls of one shape with the default configuration, for profilers.
+    variant: sgemm, f16tc (f32 operands), f16in (f16 operands, f32 C) or f16out (f16
+    operands and C)."""
     import torch
     st = torch.cuda.current_stream().cuda_stream
     A = torch.rand(M, K, device="cuda") * 2 - 1
     B = torch.rand(K, N, device="cuda") * 2 - 1
     C = torch.zeros(M, N, device="cuda")
-    fn = phx.phx_sgemm if variant == "sgemm" else phx.phx_gemm_f16tc_f32acc
+    if variant in ("f16in", "f16out"):
+        A, B = A.half(), B.half()
+        if variant == "f16out":
+            C = C.half()
+        fn = phx.phx_gemm_f16in_f32acc if variant == "f16in" else phx.phx_gemm_f16in_f16out
+        call = lambda: fn(0, 0, M, N, K, alpha, A.data_ptr(), B.data_ptr(), beta, C.data_ptr(), st)
+    else:
+        fn = phx.phx_sgemm if variant == "sgemm" else phx.phx_gemm_f16tc_f32acc
+        call = lambda: fn(M, N, K, alpha, A.data_ptr(), B.data_ptr(), beta, C.data_ptr(), st)
     for _ in range(calls):
-        phx.check(fn(M, N, K, alpha, A.data_ptr(), B.data_ptr(), beta, C.data_ptr(), st))
+        phx.check(call())
     torch.cuda.synchronize()
     return phx.get_config(0 if variant == "sgemm" else 1, M, N, K)
 
@@ -271,16 +319,26 @@ def main():
     ap.add_argument("--quick", action="store_true", help="skip shapes above 2^40 MNK and shorten timings")
     ap.add_argument("--layouts", action="store_true", help="time the four storage orders at 4096^3 only")
     ap.add_argument("--skinny", action="store_true", help="time M = 1 .. 2048 rows against K = N = 4096 only")
+    ap.add_argument("--b-transposed", action="store_true", help="with --skinny: B stored N x K")
+    ap.add_argument("--f16in", action="store_true", help="time half-precision operands against f32 ones only")
     ap.add_argument("--one", default=None, metavar="M,N,K", help="only run a few calls of this shape (for profilers)")
-    ap.add_argument("--variant", default="sgemm", choices=("sgemm", "f16tc"), help="with --one")
+    ap.add_argument("--variant", default="sgemm", choices=("sgemm", "f16tc", "f16in", "f16out"), help="with --one")
     ap.add_argument("--calls", type=int, default=5, help="with --one")
     args = ap.parse_args()
+    if args.f16in:
+        rows = run_f16in()
+        for row in rows:
+            print(f"{row['n']:6d}^3 {row['kind']:14s} {row['seconds'] * 1e6:9.1f} us {row['tflops']:8.1f} TFLOP/s")
+        if args.out:
+            with open(args.out, "w") as f:
+                json.dump({"f16in": rows}, f, indent=1)
+        return 0
     if args.one:
         M, N, K = (int(x) for x in args.one.split(","))
         print(f"{args.variant} {(M, N, K)} x{args.calls}: {run_one(M, N, K, args.variant, args.calls)}")
         return 0
     if args.skinny:
-        rows = run_skinny()
+        rows = run_skinny(b_transposed=args.b_transposed)
         for row in rows:
             print(f"{row['variant']:6s} M={row['M']:5d} {row['seconds'] * 1e6:9.1f} us {row['tflops']:8.2f} TFLOP/s "
                   f"{row['gbs']:7.0f} GB/s  I={row['intensity']:7.1f}  [{row['config']}]")

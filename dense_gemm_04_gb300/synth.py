@@ -18,6 +18,8 @@ Distributions (row-major linear index i):
     "uniform"   x = (h >> 40) * 2^-23 - 1     uniform on [-1, 1), a 2^-23 grid exact in f32
     "unit"      x = (h >> 40) * 2^-24         uniform on [0, 1), exact in f32
     "int3"      x = ((h >> 32) mod 7) - 3     integers in {-3, ..., 3}
+    "f16grid"   x = (h >> 53) * 2^-10 - 1     uniform on [-1, 1), a 2^-10 grid exact in f16
+                                              (inputs for the half-precision entry points)
 
 The pages' workloads are i.i.d. dense random matrices (uniform [0,1) in the lab's ladder,
 uniform [-0.5, 0.5) in its precision study, normal in its cuBLAS sweeps); the workloads
@@ -28,7 +30,7 @@ from __future__ import annotations
 import numpy as np
 
 TENSOR_A, TENSOR_B, TENSOR_C = 0, 1, 2
-DISTRIBUTIONS = ("uniform", "unit", "int3")
+DISTRIBUTIONS = ("uniform", "unit", "int3", "f16grid")
 
 _G = np.uint64(0x9E3779B97F4A7C15)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)
@@ -72,6 +74,8 @@ def _values(h: np.ndarray, dist: str) -> np.ndarray:
         return ((h >> np.uint64(40)).astype(np.float64) * 2.0 ** -24).astype(np.float32)
     if dist == "int3":
         return (((h >> np.uint64(32)) % np.uint64(7)).astype(np.int64) - 3).astype(np.float32)
+    if dist == "f16grid":
+        return ((h >> np.uint64(53)).astype(np.float64) * 2.0 ** -10 - 1.0).astype(np.float32)
     raise ValueError(f"unknown distribution {dist!r}; expected one of {DISTRIBUTIONS}")
 
 

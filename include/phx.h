@@ -143,6 +143,31 @@ phx_status phx_gemm_f16tc_f32acc_ex(phx_op op_a, phx_op op_b, int64_t M, int64_t
                                     int64_t K, float alpha, const float* A, const float* B,
                                     float beta, float* C, phx_stream_t stream);
 
+/* An IEEE 754 binary16 value, as its bit pattern (the layout of __half and torch.float16). */
+typedef uint16_t phx_f16;
+
+/* Half-precision operands, after the matrix-multiplication lab's cuBLAS f16 GEMM (Part 4,
+ * "precision", and Part 5): A and B are f16 already, so there is no rounding pass; the
+ * f16 x f16 products are summed in f32 by tcgen05.mma exactly as in
+ * phx_gemm_f16tc_f32acc, and the epilogue computes alpha * acc + beta * c_old in f32.
+ *   phx_gemm_f16in_f32acc   C is f32 (M x N floats), as phx_gemm_f16tc_f32acc.
+ *   phx_gemm_f16in_f16out   C is f16: c_old is read as f16 and alpha * acc + beta * c_old
+ *                           is rounded to the nearest f16 (ties to even) once.  A grid split
+ *                           along K adds its f32 partial sums first and rounds once too.
+ * op_a / op_b give the storage order as for the _ex calls.  A, B (and an f16 C) must be
+ * 2-byte aligned, an f32 C 4-byte aligned.  A stored M x K with K % 8 == 0 and 16-byte
+ * alignment is read in place; otherwise it is copied into the K-major layout the tensor
+ * cores read, and B always is (N x K halves, padded to a multiple of 8), in scratch taken in
+ * stream order from the library's pooled device memory (PHX_ERR_NOMEM if that fails).  The
+ * tile configuration is the f16 variant's (pins and tuning apply); where that is "SKINNY",
+ * which reads f32 operands, the default tile configuration is used instead. */
+phx_status phx_gemm_f16in_f32acc(phx_op op_a, phx_op op_b, int64_t M, int64_t N, int64_t K,
+                                 float alpha, const phx_f16* A, const phx_f16* B, float beta,
+                                 float* C, phx_stream_t stream);
+phx_status phx_gemm_f16in_f16out(phx_op op_a, phx_op op_b, int64_t M, int64_t N, int64_t K,
+                                 float alpha, const phx_f16* A, const phx_f16* B, float beta,
+                                 phx_f16* C, phx_stream_t stream);
+
 /* Workspace bytes phx_gemm_f16tc_f32acc takes for this shape: the rounded A (M rows) and
  * the rounded, transposed B (N rows), each row padded with zeros to a multiple of 8
  * halves. */

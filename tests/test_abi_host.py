@@ -215,3 +215,20 @@ def test_binding_storage_order():
         phx._operand_op(torch.zeros(6, 6)[::2, ::2], "A")
     with pytest.raises(ValueError):
         phx._operand_op(torch.zeros(2, 3, 4), "A")
+
+
+def test_f16_inputs_argument_checks():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    for fn in (phx.phx_gemm_f16in_f32acc, phx.phx_gemm_f16in_f16out):
+        assert fn(3, 0, 8, 8, 8, 1.0, 0x1000, 0x2000, 0.0, 0x4000, None) == phx.PHX_ERR_INVALID  # bad op
+        assert fn(0, 0, 8, 8, 8, 1.0, 0x1001, 0x2000, 0.0, 0x4000, None) == phx.PHX_ERR_INVALID  # odd address
+        assert fn(0, 0, 8, 8, 8, 1.0, 0x1000, 0x2000, 0.0, 0x4000, None) == phx.PHX_ERR_ARCH
+        assert fn(0, 0, 0, 8, 8, 1.0, None, None, 0.0, None, None) == phx.PHX_OK
+    # A (8 x 8 halves = 128 bytes) ends right where an f16 C starts: no overlap; one byte
+    # earlier it overlaps
+    assert phx.phx_gemm_f16in_f16out(0, 0, 8, 8, 8, 1.0, 0x1000, 0x3000, 0.0, 0x1080, None) == phx.PHX_ERR_ARCH
+    assert phx.phx_gemm_f16in_f16out(0, 0, 8, 8, 8, 1.0, 0x1000, 0x3000, 0.0, 0x107E, None) == phx.PHX_ERR_INVALID
+    # an f32 C must be 4-byte aligned
+    assert phx.phx_gemm_f16in_f32acc(0, 0, 8, 8, 8, 1.0, 0x1000, 0x3000, 0.0, 0x4002, None) == phx.PHX_ERR_INVALID

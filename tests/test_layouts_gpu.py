@@ -4,9 +4,10 @@ phx_gemm_f16tc_f32acc_ex on a GB300.
 
 Each case is checked twice: against the oracle on op(A), op(B) (bit for bit on integer
 inputs, within 8 * sqrt(K) * 2^-24 * (|alpha| sum|a||b| + |beta||C|) otherwise), and bit for bit
-against the plain-layout call on contiguous copies of op(A), op(B), since a transposed
-operand only changes how the operands are read, not which products are summed in which
-order.
+against the plain-layout call on contiguous copies of op(A), op(B): on the tile paths a
+transposed operand only changes how the operands are read, not which products are summed in
+which order.  (The skinny path's kernel for B stored transposed sums in its own order and
+is checked against the oracle only.)
 """
 import itertools
 
@@ -92,7 +93,11 @@ def test_layout_parity(vname, op_a, op_b, shape):
             assert_bits_equal(got, want, what)
         else:
             assert_within_bound(got, want, mag, C, K, alpha, beta, what)
-        assert_bits_equal(got, _run_plain(variant, A, B, C, alpha, beta), what + " vs plain layout")
+        # the tile paths copy (or round) a transposed operand into the plain layout and run the
+        # same kernels; the skinny path has a kernel of its own for B stored transposed, which
+        # sums in another order (the oracle check above covers it)
+        if not (op_b == phx.OP_T and phx.get_config(variant, M, N, K) == "SKINNY"):
+            assert_bits_equal(got, _run_plain(variant, A, B, C, alpha, beta), what + " vs plain layout")
 
 
 @pytest.mark.parametrize("vname", list(VARIANTS))

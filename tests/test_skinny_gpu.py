@@ -4,8 +4,9 @@ Part 5), both precisions, through the C ABI on a GB300, against the oracle.
 It is the default for small M and can be pinned ("SKINNY") for any M.  Covered here: M from
 1 to 64 at the sweep's K = N = 4096 in both precisions; ragged N (scalar loads, partial
 column strips), K shorter than one slice and K split into many slices; A stored transposed
-(read in place) and B stored transposed (copied first); a B pointer only 4-byte aligned;
-M beyond one block of 16 rows; the degenerate cases; run-to-run determinism.
+(read in place); B stored transposed (N x K, the layout of W in x @ W^T: the kernel that
+streams B's rows), from 1 to 64 rows, ragged and long K, aligned or not; a B pointer only
+4-byte aligned; M beyond one block of 16 rows; the degenerate cases; run-to-run determinism.
 """
 import numpy as np
 import pytest
@@ -84,6 +85,54 @@ def test_skinny_transposed_operands(vname):
                 torch.cuda.synchronize()
                 assert st == phx.PHX_OK
                 assert_bits_equal(dC.cpu().numpy(), want, f"{vname} ops ({op_a},{op_b}) {(M, N, K)}")
+
+
+def _run_ex(variant, op_a, op_b, A, B, C, alpha, beta, offset=0):
+    import torch
+    M, K = A.shape
+    N = B.shape[1]
+
+    def dev(x):
+        flat = torch.zeros(x.size + offset, dtype=torch.float32)
+        flat[offset:] = torch.from_numpy(np.ascontiguousarray(x).reshape(-1))
+        return flat.cuda()
+
+    a = A.T if op_a == phx.OP_T else A
+    b = B.T if op_b == phx.OP_T else B
+    dA, dB = dev(a), dev(b)
+    dC = torch.from_numpy(C.copy()).cuda()
+    fn = phx.phx_sgemm_ex if variant == phx.VARIANT_SGEMM else phx.phx_gemm_f16tc_f32acc_ex
+    st = fn(op_a, op_b, M, N, K, alpha, dA.data_ptr() + 4 * offset, dB.data_ptr() + 4 * offset, beta,
+            dC.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    return st, dC.cpu().numpy()
+
+
+@pytest.mark.parametrize("vname", list(VARIANTS))
+@pytest.mark.parametrize("shape", [(1, 4096, 4096), (2, 4096, 4096), (4, 4096, 4096), (8, 4096, 4096),
+                                   (16, 4096, 4096), (33, 4096, 4096), (3, 333, 777), (16, 33, 130),
+                                   (2, 100, 65536), (5, 1, 64), (1, 1, 1), (64, 64, 4100)])
+def test_skinny_b_stored_transposed(vname, shape):
+    # B stored N x K (x @ W^T): the kernel that streams B's rows
+    variant, f16 = VARIANTS[vname]
+    M, N, K = shape
+    for dist, seed in (("int3", 21), ("uniform", 22)):
+        A, B, C = synth.problem(M, N, K, seed=seed, dist=dist)
+        want, mag = oracle.gemm(A, B, C, 2.0, -1.0, f16_inputs=f16)
+        for op_a in (phx.OP_N, phx.OP_T):
+            st, got = _run_ex(variant, op_a, phx.OP_T, A, B, C, 2.0, -1.0)
+            assert st == phx.PHX_OK, phx.status_string(st)
+            what = f"skinny {vname} B^T {shape} {dist} op_a={op_a}"
+            if dist == "int3":
+                assert_bits_equal(got, want, what)
+            else:
+                assert_within_bound(got, want, mag, C, K, 2.0, -1.0, what)
+    # W only 4-byte aligned: 4-byte copies
+    A, B, C = synth.problem(M, N, K, seed=23, dist="int3")
+    want, _ = oracle.gemm(A, B, C, 1.0, 0.5, f16_inputs=f16)
+    st, got = _run_ex(variant, phx.OP_N, phx.OP_T, A, B, C, 1.0, 0.5, offset=1)
+    assert st == phx.PHX_OK
+    assert_bits_equal(got, want, f"skinny {vname} B^T {shape} unaligned")
 
 
 @pytest.mark.parametrize("vname", list(VARIANTS))

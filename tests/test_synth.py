@@ -41,6 +41,12 @@ def test_distributions():
     assert w.min() >= 0.0 and w.max() < 1.0
     i3 = synth.matrix(256, 257, seed=0, dist="int3")
     assert set(np.unique(i3).tolist()) == {-3.0, -2.0, -1.0, 0.0, 1.0, 2.0, 3.0}
+    g = synth.matrix(256, 257, seed=0, dist="f16grid")
+    assert g.min() >= -1.0 and g.max() < 1.0
+    # a 2^-10 grid, and every value is exactly an f16 value
+    assert np.array_equal(g.astype(np.float64) * 2 ** 10, np.round(g.astype(np.float64) * 2 ** 10))
+    assert np.array_equal(g.astype(np.float16).astype(np.float32), g)
+    assert len(np.unique(g)) > 1500
 
 
 def test_fill_is_index_addressable_and_chunk_independent():
