@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <chrono>
 #include <cmath>
 #include <cstdint>
@@ -282,6 +283,9 @@ int choose_config(int variant, int64_t M, int64_t N, int64_t K, int sms) {
     return default_config(variant, M, N, sms);
 }
 
+// The configuration the last GEMM call of each variant launched (-1: none yet), for reports.
+std::atomic<int> g_last_cfg[2] = {{-1}, {-1}};
+
 // ---------------------------------------------------------------------------------------
 // The tuner's selection logic, shared by phx_autotune and phx_selftest_tuner.
 // measure(i) returns the seconds one launch of candidate i took, or a negative value if
@@ -522,6 +526,7 @@ phx_status gemm_entry(int variant, int64_t M, int64_t N, int64_t K, float alpha,
     }
     const int cfg = choose_config(variant, M, N, K, d->sm_count);
     if (cfg < 0) return PHX_ERR_INTERNAL;
+    g_last_cfg[variant].store(cfg);
     if (log_level() >= 2)
         std::fprintf(stderr, "[phx] variant %d (%lld,%lld,%lld): %s\n", variant, (long long)M,
                      (long long)N, (long long)K, config_name(variant, cfg).c_str());
@@ -551,6 +556,7 @@ phx_status f16in_entry(int trans_a, int trans_b, int64_t M, int64_t N, int64_t K
     int cfg = choose_config(PHX_VARIANT_F16TC, M, N, K, d->sm_count);
     if (cfg == skinny_index(PHX_VARIANT_F16TC)) cfg = default_tile_config(PHX_VARIANT_F16TC, M, N, d->sm_count);
     if (cfg < 0) return PHX_ERR_INTERNAL;
+    g_last_cfg[PHX_VARIANT_F16TC].store(cfg);
     const int64_t Kp = (K + 7) / 8 * 8;
     const bool a_direct = !trans_a && K % 8 == 0 && (reinterpret_cast<uintptr_t>(A) & 15u) == 0;
     auto r256 = [](int64_t b) { return (b + 255) / 256 * 256; };
@@ -756,6 +762,12 @@ phx_status phx_get_config(int variant, int64_t M, int64_t N, int64_t K, char* bu
     const int cfg = choose_config(variant, M, N, K, sms);
     if (cfg < 0) return PHX_ERR_INTERNAL;
     return copy_name(config_name(variant, cfg), buf, buflen);
+}
+
+phx_status phx_last_config(int variant, char* buf, size_t buflen) {
+    if (num_configs(variant) < 0) return PHX_ERR_INVALID;
+    const int cfg = g_last_cfg[variant].load();
+    return copy_name(cfg < 0 ? std::string("NONE") : config_name(variant, cfg), buf, buflen);
 }
 
 phx_status phx_autotune(int variant, int64_t M, int64_t N, int64_t K, int finalists, int rounds,

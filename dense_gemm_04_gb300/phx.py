@@ -46,6 +46,7 @@ _SIGNATURES = {
     "phx_config_name": (_i32, [_i32, _i32, _cp, _sz]),
     "phx_set_config": (_i32, [_i32, _cp]),
     "phx_get_config": (_i32, [_i32, _i64, _i64, _i64, _cp, _sz]),
+    "phx_last_config": (_i32, [_i32, _cp, _sz]),
     "phx_autotune": (_i32, [_i32, _i64, _i64, _i64, _i32, _i32, _i32, _vp]),
     "phx_tune_cache_save": (_i32, [_cp]),
     "phx_tune_cache_load": (_i32, [_cp]),
@@ -223,6 +224,13 @@ def set_config(variant: int, spec) -> None:
 def get_config(variant: int, M: int, N: int, K: int) -> str:
     buf = ctypes.create_string_buffer(160)
     check(phx_get_config(variant, M, N, K, buf, len(buf)), "phx_get_config")
+    return buf.value.decode()
+
+
+def last_config(variant: int) -> str:
+    """The configuration the last GEMM call of `variant` launched ("NONE" before the first)."""
+    buf = ctypes.create_string_buffer(256)
+    check(phx_last_config(variant, buf, 256), "phx_last_config")
     return buf.value.decode()
 
 

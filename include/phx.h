@@ -233,6 +233,12 @@ phx_status phx_set_config(int variant, const char* spec);
 phx_status phx_get_config(int variant, int64_t M, int64_t N, int64_t K, char* buf,
                           size_t buflen);
 
+/* Name of the configuration the last GEMM call of `variant` launched ("NONE" before the
+ * first), for reports: phx_sgemm and phx_sgemm_ex for the f32 variant; phx_gemm_f16tc_f32acc,
+ * its _ex form and the half-precision entry points for the f16 variant.  Degenerate calls
+ * that launch no GEMM do not count. */
+phx_status phx_last_config(int variant, char* buf, size_t buflen);
+
 /* Tune `variant` for the shape (M, N, K), following "gemm, f32" section "Tuning":
  * stage 1 times every configuration briefly on scratch inputs and skips any that fails;
  * stage 2 runs the fastest `finalists` for `settle_ms` milliseconds to settle the clocks,

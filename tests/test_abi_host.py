@@ -232,3 +232,13 @@ def test_f16_inputs_argument_checks():
     assert phx.phx_gemm_f16in_f16out(0, 0, 8, 8, 8, 1.0, 0x1000, 0x3000, 0.0, 0x107E, None) == phx.PHX_ERR_INVALID
     # an f32 C must be 4-byte aligned
     assert phx.phx_gemm_f16in_f32acc(0, 0, 8, 8, 8, 1.0, 0x1000, 0x3000, 0.0, 0x4002, None) == phx.PHX_ERR_INVALID
+
+
+def test_last_config_before_any_gemm():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert phx.last_config(phx.VARIANT_SGEMM) == "NONE"
+    assert phx.last_config(phx.VARIANT_F16TC) == "NONE"
+    with pytest.raises(phx.PhxError):
+        phx.last_config(5)

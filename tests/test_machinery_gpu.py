@@ -88,3 +88,17 @@ def test_concurrent_streams_share_the_workspace_pool():
     for i in range(len(shapes)):
         for c in outs[i]:
             assert_bits_equal(c.cpu().numpy(), wants[i])
+
+
+@pytest.mark.gpu
+def test_last_config_reports_what_ran():
+    import torch
+    from dense_gemm_04_gb300 import phx
+    A = torch.rand(512, 512, device="cuda")
+    C = torch.zeros(512, 512, device="cuda")
+    for variant, fn in ((phx.VARIANT_SGEMM, phx.sgemm), (phx.VARIANT_F16TC, phx.gemm_f16tc_f32acc)):
+        phx.set_config(variant, None)
+        fn(A, A, C)
+        assert phx.last_config(variant) == phx.get_config(variant, 512, 512, 512)
+        fn(A[:8].contiguous(), A, C[:8].contiguous())   # few rows: the skinny kernel
+        assert phx.last_config(variant) == "SKINNY"
