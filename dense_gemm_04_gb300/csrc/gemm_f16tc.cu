@@ -29,6 +29,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstring>
 #include <mutex>
 
 #include "internal.h"
@@ -258,12 +259,17 @@ struct TcLayout {
     // offsets from the 1024-byte aligned base
     static constexpr uint32_t kA = 0;
     static constexpr uint32_t kB = STAGES * kABytes;
-    // per epilogue warp, a 32 x 32 f32 chunk with rows padded to 36 floats
+    // per epilogue warp: a 32 x 32 f32 chunk with rows padded to 36 floats (staging), or,
+    // for the TMA epilogue, two 32 x 32 chunks in the 128-byte swizzled layout of a TMA box
+    // (1024-byte aligned)
     static constexpr uint32_t kEpiStride = 36;
+    static constexpr uint32_t kEpiWarpFloats = 2 * 32 * 32;
+    static_assert(32 * kEpiStride <= kEpiWarpFloats, "the staging chunk fits the warp's region");
     static constexpr uint32_t kEpi = STAGES * kStageBytes;
-    static constexpr uint32_t kEpiBytes = kEpiWarps * 32 * kEpiStride * 4;
+    static constexpr uint32_t kEpiBytes = kEpiWarps * kEpiWarpFloats * 4;
     static constexpr uint32_t kBars = kEpi + kEpiBytes;               // 8-byte aligned
-    static constexpr uint32_t kNumBars = 2 * STAGES + 4 + 1;          // full, empty, tfull, tempty, done
+    // full, empty, tfull, tempty, done, and two c_old barriers per epilogue warp
+    static constexpr uint32_t kNumBars = 2 * STAGES + 4 + 1 + 2 * kEpiWarps;
     static constexpr uint32_t kTmemSlot = kBars + 8 * kNumBars;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     static constexpr uint32_t kEnd = kAbort + 4;
@@ -272,13 +278,14 @@ struct TcLayout {
     static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "swizzle atoms stay 1024-aligned");
 };
 
-template <int BN, int STAGES, int PAIR, bool OUT_H>
+template <int BN, int STAGES, int PAIR, bool OUT_H, bool EPI_TMA>
 __global__ void __launch_bounds__(kThreadsTc, 1)
 gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const __grid_constant__ CUtensorMap tmB_half, const __grid_constant__ CUtensorMap tmB_quarter,
                   float* __restrict__ C, int M, int N, int num_kb, float alpha, float beta, int tiles_m,
                   int tiles_n, unsigned int* status, int full_tiles, int tail_split, int ksplit,
-                  int kb_per_slice, float* __restrict__ partial, __half* __restrict__ Ch) {
+                  int kb_per_slice, float* __restrict__ partial, __half* __restrict__ Ch,
+                  const __grid_constant__ CUtensorMap tmC, int epi_tma) {
     using L = TcLayout<BN, STAGES, PAIR>;
     constexpr bool kPair = PAIR != 0;
     constexpr bool kTwoSm = PAIR == 2;
@@ -295,6 +302,7 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     auto tfull_bar = [&](int a) { return bars + 8u * (2 * STAGES + a); };
     auto tempty_bar = [&](int a) { return bars + 8u * (2 * STAGES + 2 + a); };
     const uint32_t done_bar = bars + 8u * (2 * STAGES + 4);
+    auto cold_bar = [&](int w, int b) { return bars + 8u * (2 * STAGES + 5 + 2 * w + b); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + L::kTmemSlot);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + L::kAbort);
 
@@ -342,6 +350,8 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         return it;
     };
 
+    auto row0_of = [&](const Item& it) { return it.pm * kBM + warp * 32; };
+
     if (warp == kProducerWarp && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
@@ -356,6 +366,11 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             mbar_init(tempty_bar(a), kTwoSm ? 2 * kEpiWarps : kEpiWarps);
         }
         mbar_init(done_bar, 1);
+        for (int w = 0; w < kEpiWarps; ++w) {
+            mbar_init(cold_bar(w, 0), 1);
+            mbar_init(cold_bar(w, 1), 1);
+        }
+        if (epi_tma) tma_prefetch_desc(&tmC);
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -476,12 +491,35 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             mbar_wait_drain(done_bar, 0);
         }
     } else if (warp < kEpiWarps) {
-        float* epi = reinterpret_cast<float*>(base_ptr + L::kEpi) + warp * 32 * L::kEpiStride;
+        float* epi = reinterpret_cast<float*>(base_ptr + L::kEpi) + warp * L::kEpiWarpFloats;
         uint32_t acc = 0, acc_phase = 0;
         const bool vec = (N % 4 == 0) && ((reinterpret_cast<uintptr_t>(C) & 15u) == 0) &&
                          (partial == nullptr || (reinterpret_cast<uintptr_t>(partial) & 15u) == 0);
         // an f16 result (Ch) moves 4 halves = 8 bytes per lane on the vector path
         const bool vec_h = (N % 4 == 0) && ((reinterpret_cast<uintptr_t>(Ch) & 7u) == 0);
+        // The TMA epilogue (f32 C, whole tiles, N % 4 == 0, C 16-byte aligned): each 32 x 32
+        // chunk's c_old arrives by TMA in one of the warp's two swizzled buffers (the next
+        // chunk's while this one is finished), lane = row finishes the row in place from the
+        // accumulator, and the chunk leaves by TMA store.
+        const bool tma_c = EPI_TMA && !OUT_H && epi_tma != 0 && ksplit == 1;
+        const bool load_c = tma_c && beta != 0.f;
+        const uint32_t ebuf = smem_u32(epi);
+        auto swz = [](int r, int u) { return r * 32 + ((u ^ (r & 7)) << 2); };
+        uint32_t cph = 0;          // phase bit of each buffer's c_old barrier
+        uint32_t cpend = 0;        // buffers with a c_old load in flight
+        // a chunk with no element inside C is neither loaded nor stored
+        auto live = [&](const Item& x, int c) { return x.pm * kBM + warp * 32 < M && x.n0 + c * 32 < N; };
+        auto load_cold = [&](int w_req, int c_req, int b) {  // lane 0
+            if (w_req >= num_items) return;
+            const Item nx = decode(w_req);
+            if (!live(nx, c_req)) return;
+            mbar_arrive_expect_tx(cold_bar(warp, b), 32 * 32 * 4);
+            tma_load_2d(ebuf + b * 4096, &tmC, nx.n0 + c_req * 32, nx.pm * kBM + warp * 32, cold_bar(warp, b));
+            cpend |= 1u << b;
+        };
+        int cc = 0;  // chunks finished by this warp, across items: buffer cc & 1
+        bool prev_stored = false;  // chunk cc - 1 left by TMA store
+        if (load_c && lane == 0) load_cold(first_item, 0, 0);
         for (int w = first_item; w < num_items; w += item_stride) {
             const Item it = decode(w);
             // a k slice writes its plane of partial products; a whole tile writes C
@@ -495,14 +533,79 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             // warp-uniform outcome: the tcgen05.ld below is .sync.aligned
             if (!__all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), acc_phase, abort_flag, status))) break;
             tc_fence_after();
+            bool ok = true;
+            const int nch = it.width / 32;
+            const uint32_t t_base = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + acc * BN;
+#pragma unroll 1
+            for (int c = 0; tma_c && c < nch; ++c, ++cc) {
+                const int b = cc & 1;
+                if (lane == 0) {
+                    if (load_c) {
+                        // the other buffer's last store has read it: take the next chunk's c_old
+                        bulk_wait_read<0>();
+                        if (c + 1 < nch)
+                            load_cold(w, c + 1, b ^ 1);
+                        else
+                            load_cold(w + item_stride, 0, b ^ 1);
+                    } else if (prev_stored) {
+                        bulk_wait_read<1>();  // this buffer's store (two chunks back) has read it
+                    } else {
+                        bulk_wait_read<0>();  // the last store may have come from this buffer
+                    }
+                }
+                const bool chunk_live = live(it, c);
+                __syncwarp();
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(t_base + c * 32, r);
+                tmem_ld_wait();
+                if (load_c && chunk_live) {
+                    if (!__all_sync(0xffffffffu, mbar_wait(cold_bar(warp, b), (cph >> b) & 1u, abort_flag, status))) {
+                        ok = false;
+                        break;
+                    }
+                    cph ^= 1u << b;
+                    if (lane == 0) cpend &= ~(1u << b);
+                }
+                __syncwarp();
+                if (!chunk_live) {
+                    prev_stored = false;
+                    continue;
+                }
+                float* buf = epi + b * 32 * 32;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    float4* p4 = reinterpret_cast<float4*>(buf + swz(lane, u));
+                    float4 o;
+                    o.x = alpha * __uint_as_float(r[u * 4 + 0]);
+                    o.y = alpha * __uint_as_float(r[u * 4 + 1]);
+                    o.z = alpha * __uint_as_float(r[u * 4 + 2]);
+                    o.w = alpha * __uint_as_float(r[u * 4 + 3]);
+                    if (load_c) {
+                        const float4 co = *p4;
+                        o.x = fmaf(beta, co.x, o.x);
+                        o.y = fmaf(beta, co.y, o.y);
+                        o.z = fmaf(beta, co.z, o.z);
+                        o.w = fmaf(beta, co.w, o.w);
+                    }
+                    *p4 = o;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&tmC, ebuf + b * 4096, it.n0 + c * 32, row0_of(it));
+                    bulk_commit();
+                }
+                prev_stored = true;
+            }
+            if (!ok) break;
             // Each chunk of 32 rows x 32 columns goes from TMEM (lane = row) through this
             // warp's shared-memory buffer, so that C is read and written along rows: four
             // rows of 128 bytes per float4 instruction, or one row of 128 bytes per scalar
             // instruction when N is not a multiple of 4.
             const int row0 = it.pm * kBM + warp * 32;
-            const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + acc * BN;
+            const uint32_t t_addr = t_base;
 #pragma unroll 1
-            for (int c = 0; c < it.width / 32; ++c) {
+            for (int c = 0; !tma_c && c < nch; ++c) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(t_addr + c * 32, r);
                 tmem_ld_wait();
@@ -593,6 +696,14 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
         }
+        if (tma_c && lane == 0) {
+            bulk_wait<0>();  // every store of C has completed
+            // a c_old load still in flight (one requested before an abandoned wait) lands
+            // before the CTA's shared memory goes away
+            for (int b = 0; b < 2; ++b)
+                if (cpend & (1u << b)) mbar_wait_drain(cold_bar(warp, b), (cph >> b) & 1u);
+        }
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -646,12 +757,28 @@ bool make_map(CUtensorMap* map, const __half* ptr, int64_t rows, int64_t Kp, int
 }
 
 using TcKernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, float*, int, int, int,
-                            float, float, int, int, unsigned int*, int, int, int, int, float*, __half*);
+                            float, float, int, int, unsigned int*, int, int, int, int, float*, __half*,
+                            CUtensorMap, int);
+
+// C (M x N f32, rows N floats apart) as 32 x 32 boxes in the 128-byte swizzled layout, for
+// the TMA epilogue.  Needs N % 4 == 0 and a 16-byte aligned C.
+bool make_map_c(CUtensorMap* map, float* C, int64_t M, int64_t N) {
+    EncodeTiledFn enc = encode_fn();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * 4};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, C, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 struct TcEntry {
     F16Config cfg;
-    TcKernelFn fn;    // f32 result
-    TcKernelFn fn_h;  // f16 result
+    TcKernelFn fn;      // f32 result
+    TcKernelFn fn_tma;  // f32 result through the TMA epilogue
+    TcKernelFn fn_h;    // f16 result
     uint32_t smem;
 };
 
@@ -660,8 +787,8 @@ struct TcEntry {
 template <int BN, int STAGES, int PAIR>
 TcEntry make_tc_entry() {
     return TcEntry{F16Config{PAIR == 2 ? 2 * kBM : kBM, BN, kBK, STAGES, PAIR == 0 ? 1 : 2},
-                   &gemm_f16tc_kernel<BN, STAGES, PAIR, false>, &gemm_f16tc_kernel<BN, STAGES, PAIR, true>,
-                   TcLayout<BN, STAGES, PAIR>::kDynSmem};
+                   &gemm_f16tc_kernel<BN, STAGES, PAIR, false, false>, &gemm_f16tc_kernel<BN, STAGES, PAIR, false, true>,
+                   &gemm_f16tc_kernel<BN, STAGES, PAIR, true, false>, TcLayout<BN, STAGES, PAIR>::kDynSmem};
 }
 
 const TcEntry kTcEntries[] = {
@@ -789,11 +916,14 @@ cudaError_t f16tc_gemm_launch_ops(int index, int64_t M, int64_t N, int64_t K, fl
         !make_map(&mapB_half, Bt, N, Kp, e.cfg.tile_n / 2, ldb) ||
         !make_map(&mapB_quarter, Bt, N, Kp, e.cfg.tile_n / 4, ldb))
         return cudaErrorInvalidValue;
-    const TcKernelFn fn = Ch != nullptr ? e.fn_h : e.fn;
-    cudaError_t err = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(e.smem));
-    if (err != cudaSuccess) return err;
+    // the TMA epilogue for an f32 C whose rows are 16-byte aligned (whole tiles: decided
+    // below, once the split is known)
+    CUtensorMap mapC;
+    std::memset(&mapC, 0, sizeof mapC);
+    const bool c_tma_ok = Ch == nullptr && N % 4 == 0 && (reinterpret_cast<uintptr_t>(C) & 15u) == 0 &&
+                          make_map_c(&mapC, C, M, N);
+    TcKernelFn fn = Ch != nullptr ? e.fn_h : e.fn;
+    cudaError_t err = cudaSuccess;
     const int tiles_m = static_cast<int>((M + kBM - 1) / kBM);  // 128-row tiles (one per CTA)
     const int tiles_n = static_cast<int>((N + e.cfg.tile_n - 1) / e.cfg.tile_n);
     // With clusters of two, work is counted in pairs of tiles and in CTA pairs.
@@ -833,15 +963,21 @@ cudaError_t f16tc_gemm_launch_ops(int index, int64_t M, int64_t N, int64_t K, fl
     lc.numAttrs = 2;
     const int m32 = static_cast<int>(M), n32 = static_cast<int>(N), full32 = static_cast<int>(full);
     float* partial = ksplit > 1 ? static_cast<float*>(split_ws) : nullptr;
+    const int epi_tma = (c_tma_ok && ksplit == 1) ? 1 : 0;
+    if (epi_tma) fn = e.fn_tma;
+    err = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(e.smem));
+    if (err != cudaSuccess) return err;
     err = cudaLaunchKernelEx(&lc, fn, mapA, mapB, mapB_half, mapB_quarter, C, m32, n32, num_kb, alpha,
-                             beta, tiles_m, tiles_n, status, full32, tail_split, ksplit, kb_per, partial, Ch);
+                             beta, tiles_m, tiles_n, status, full32, tail_split, ksplit, kb_per, partial, Ch,
+                             mapC, epi_tma);
     if (err != cudaSuccess) {
         // a stream that does not take programmatic launches: launch normally
         cudaGetLastError();
         lc.numAttrs = 1;
         err = cudaLaunchKernelEx(&lc, fn, mapA, mapB, mapB_half, mapB_quarter, C, m32, n32, num_kb,
                                  alpha, beta, tiles_m, tiles_n, status, full32, tail_split, ksplit, kb_per,
-                                 partial, Ch);
+                                 partial, Ch, mapC, epi_tma);
     }
     if (err != cudaSuccess || ksplit == 1) return err;
     if (Ch != nullptr) return splitk_reduce_launch_h(partial, ksplit, M, N, alpha, beta, Ch, num_sms, stream);

@@ -2,6 +2,7 @@
 
     python -m dense_gemm_04_gb300.sweep [--out results.json] [--quick] [--layouts] [--skinny] [--f16in]
     python -m dense_gemm_04_gb300.sweep --one M,N,K [--variant sgemm|f16tc|f16in|f16out] [--calls 5]
+        [--alpha 1] [--beta 0]
 
 For every shape of the workload sweep ((8192, 8192, 1024), (1024, 1024, 16384),
 (16384, 128, 4096), (4095, 4097, 4093) with alpha = 2, beta = -1; squares 512 .. 16384 with
@@ -324,6 +325,8 @@ def main():
     ap.add_argument("--one", default=None, metavar="M,N,K", help="only run a few calls of this shape (for profilers)")
     ap.add_argument("--variant", default="sgemm", choices=("sgemm", "f16tc", "f16in", "f16out"), help="with --one")
     ap.add_argument("--calls", type=int, default=5, help="with --one")
+    ap.add_argument("--alpha", type=float, default=1.0, help="with --one")
+    ap.add_argument("--beta", type=float, default=0.0, help="with --one")
     args = ap.parse_args()
     if args.f16in:
         rows = run_f16in()
@@ -335,7 +338,8 @@ def main():
         return 0
     if args.one:
         M, N, K = (int(x) for x in args.one.split(","))
-        print(f"{args.variant} {(M, N, K)} x{args.calls}: {run_one(M, N, K, args.variant, args.calls)}")
+        print(f"{args.variant} {(M, N, K)} x{args.calls}: "
+              f"{run_one(M, N, K, args.variant, args.calls, args.alpha, args.beta)}")
         return 0
     if args.skinny:
         rows = run_skinny(b_transposed=args.b_transposed)
