@@ -282,3 +282,36 @@ def test_tiling_does_not_change_values():
             else:
                 assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), (vname, cfg)
         phx.set_config(variant, None)
+
+
+# ----------------------------------------------------------------------------------------
+# The tensor-core kernel's TMA epilogue (f32 C with rows 16 bytes apart): ragged M with
+# whole warps of a tile past the edge, half-width tail tiles, beta = 0 and != 0, and a C
+# pointer that is only 4-byte aligned (the register-path epilogue instead)
+# ----------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("shape", [(4000, 4096, 512),    # the last tile row: warps 1..3 past M
+                                   (1000, 2048, 320),    # 8 x 8 pair tiles: a half-width tail round
+                                   (300, 132, 100),      # N % 32 != 0 (a chunk past the edge)
+                                   (2304, 2304, 1024)])  # 9 x 9 pair tiles
+def test_tc_tma_epilogue(shape):
+    M, N, K = shape
+    _check("f16tc", M, N, K, 1.5, 0.5, "int3", seed=41)
+    _check("f16tc", M, N, K, 2.0, -1.0, "uniform", seed=42)
+    _check("f16tc", M, N, K, 1.0, 0.0, "int3", seed=43)
+
+
+def test_tc_epilogue_unaligned_c():
+    import torch
+    M, N, K = 512, 256, 128
+    A, B, C = synth.problem(M, N, K, seed=44, dist="int3")
+    want, _ = oracle.gemm(A, B, C, 1.5, 0.5, f16_inputs=True)
+    flat = torch.zeros(M * N + 1)
+    flat[1:] = torch.from_numpy(C.reshape(-1))
+    dC = flat.cuda()
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    st = phx.phx_gemm_f16tc_f32acc(M, N, K, 1.5, dA.data_ptr(), dB.data_ptr(), 0.5, dC.data_ptr() + 4,
+                                   torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert st == phx.PHX_OK
+    assert_bits_equal(dC.cpu().numpy()[1:].reshape(M, N), want, "C 4-byte aligned")
