@@ -364,24 +364,31 @@ def gpu_arm(args):
             gemms(b)
             copy_out(b)
 
+    # three timed runs of e2e_steps steps each; the median run is reported (the host's
+    # memory system is shared with other work on the machine)
     e2e_steps = max(4, min(args.steps, 10))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_pipelined(2)
     torch.cuda.synchronize()
-    e0.record(s_in)
-    e2e_pipelined(e2e_steps)
-    e1.record(s_out)
-    torch.cuda.synchronize()
-    e2e_s = e0.elapsed_time(e1) / 1e3
-    e2e_max_s = reduce_max(e2e_s, ws, dev)
+    runs = []
+    for _ in range(3):
+        e0.record(s_in)
+        e2e_pipelined(e2e_steps)
+        e1.record(s_out)
+        torch.cuda.synchronize()
+        runs.append(e0.elapsed_time(e1) / 1e3)
+    e2e_max_s = reduce_max(statistics.median(runs), ws, dev)
+    serial_runs = []
     with torch.cuda.stream(stream):
         e2e_serial(2)
         torch.cuda.synchronize()
-        e0.record(stream)
-        e2e_serial(e2e_steps)
-        e1.record(stream)
-        torch.cuda.synchronize()
-    serial_max_s = reduce_max(e0.elapsed_time(e1) / 1e3, ws, dev)
+        for _ in range(3):
+            e0.record(stream)
+            e2e_serial(e2e_steps)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            serial_runs.append(e0.elapsed_time(e1) / 1e3)
+    serial_max_s = reduce_max(statistics.median(serial_runs), ws, dev)
     h2d = M * K * 4 + K * N * 4 + 2 * M * N * 4
     d2h = 2 * M * N * 4
 
@@ -452,7 +459,7 @@ def gpu_arm(args):
         "cpu_baseline": cpu,
         "e2e": {"value": whole_job_tflops(ws, e2e_steps, GEMMS_PER_STEP * FLOPS_PER_GEMM, e2e_max_s),
                 "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": e2e_steps,
+                "steps": e2e_steps, "runs": 3, "run_ms": [1e3 * r for r in runs],
                 "schedule": "copies in of step i+1 and out of step i-1 overlap the GEMMs of step i "
                             "(two buffer sets, three streams)",
                 "serial": whole_job_tflops(ws, e2e_steps, GEMMS_PER_STEP * FLOPS_PER_GEMM, serial_max_s)},
