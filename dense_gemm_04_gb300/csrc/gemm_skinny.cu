@@ -385,6 +385,9 @@ __global__ void __launch_bounds__(kSkThreads, 2) skinny_nt_kernel(
     const float* __restrict__ A, const float* __restrict__ W, float* __restrict__ C, float* __restrict__ partial,
     int M, int N, int K, int k_cta, int cs, int mchunks, int strips, int a_trans, float alpha, float beta) {
     constexpr int S = kNtStages;
+    // A stored M x K with rows on 16-byte boundaries (the host passes a_trans = 2 for that)
+    const bool a_vec = a_trans == 2;
+    if (a_vec) a_trans = 0;
     constexpr int SF = nt_stage_floats(MT);
     constexpr int E = MT * kNtRows;
     extern __shared__ float4 nt_smem4[];
@@ -427,12 +430,22 @@ __global__ void __launch_bounds__(kSkThreads, 2) skinny_nt_kernel(
                 }
             }
             float* as = st + kNtRows * kNtKc;
-            for (int e = tid; e < MT * kNtKc; e += kSkThreads) {
-                const int m = e / kNtKc, k = e % kNtKc;
-                const bool ok = m0 + m < M && kb + k < kn;
-                const int64_t gk = k0 + kb + k;
-                const float* src = !ok ? A : a_trans ? A + gk * M + m0 + m : A + static_cast<int64_t>(m0 + m) * K + gk;
-                cp_async_4(static_cast<uint32_t>(__cvta_generic_to_shared(as + e)), src, ok);
+            if (a_vec) {
+                // A stored M x K with 16-byte rows: 16-byte copies (kn is a multiple of 4 then)
+                for (int e = tid; e < MT * (kNtKc / 4); e += kSkThreads) {
+                    const int m = e / (kNtKc / 4), k4 = (e % (kNtKc / 4)) * 4;
+                    const bool ok = m0 + m < M && kb + k4 < kn;
+                    const float* src = ok ? A + static_cast<int64_t>(m0 + m) * K + k0 + kb + k4 : A;
+                    cp_async_16(static_cast<uint32_t>(__cvta_generic_to_shared(as + m * kNtKc + k4)), src, ok);
+                }
+            } else {
+                for (int e = tid; e < MT * kNtKc; e += kSkThreads) {
+                    const int m = e / kNtKc, k = e % kNtKc;
+                    const bool ok = m0 + m < M && kb + k < kn;
+                    const int64_t gk = k0 + kb + k;
+                    const float* src = !ok ? A : a_trans ? A + gk * M + m0 + m : A + static_cast<int64_t>(m0 + m) * K + gk;
+                    cp_async_4(static_cast<uint32_t>(__cvta_generic_to_shared(as + e)), src, ok);
+                }
             }
         }
         asm volatile("cp.async.commit_group;\n" ::: "memory");
@@ -449,9 +462,22 @@ __global__ void __launch_bounds__(kSkThreads, 2) skinny_nt_kernel(
     for (int c = 0; c < chunks; ++c) {
         asm volatile("cp.async.wait_group %0;\n" ::"n"(S - 2) : "memory");
         if (F16) {
-            // round, in place, the A values this thread copied (the same index set as issue)
+            // round, in place, the A values this thread copied (the same index sets as issue:
+            // only a thread's own copies are known to have landed before the barrier)
             float* as = ring + (c % S) * SF + kNtRows * kNtKc;
-            for (int e = tid; e < MT * kNtKc; e += kSkThreads) as[e] = round_f16(as[e]);
+            if (a_vec) {
+                for (int e = tid; e < MT * (kNtKc / 4); e += kSkThreads) {
+                    float4* p4 = reinterpret_cast<float4*>(as + (e / (kNtKc / 4)) * kNtKc + (e % (kNtKc / 4)) * 4);
+                    float4 v = *p4;
+                    v.x = round_f16(v.x);
+                    v.y = round_f16(v.y);
+                    v.z = round_f16(v.z);
+                    v.w = round_f16(v.w);
+                    *p4 = v;
+                }
+            } else {
+                for (int e = tid; e < MT * kNtKc; e += kSkThreads) as[e] = round_f16(as[e]);
+            }
         }
         __syncthreads();  // chunk c visible to all; chunk c-1's slot is free
         issue(c + S - 1);
@@ -632,9 +658,11 @@ cudaError_t skinny_nt_launch(int f16, int a_trans, int64_t M, int64_t N, int64_t
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    // a_trans = 2: A stored M x K with 16-byte aligned rows, copied 16 bytes at a time
+    const int a_mode = a_trans ? 1 : (K % 4 == 0 && (reinterpret_cast<uintptr_t>(A) & 15u) == 0) ? 2 : 0;
     cudaError_t err = cudaLaunchKernelEx(&cfg, p.fn, A, W, C, partial, static_cast<int>(M), static_cast<int>(N),
-                                         static_cast<int>(K), p.k_cta, p.cs, p.mchunks, p.strips, a_trans ? 1 : 0,
-                                         alpha, beta);
+                                         static_cast<int>(K), p.k_cta, p.cs, p.mchunks, p.strips, a_mode, alpha,
+                                         beta);
     if (err != cudaSuccess || p.planes == 1) return err;
     return splitk_reduce_launch(partial, p.planes, M, N, alpha, beta, C, num_sms, stream);
 }

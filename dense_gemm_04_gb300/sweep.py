@@ -2,7 +2,7 @@
 
     python -m dense_gemm_04_gb300.sweep [--out results.json] [--quick] [--layouts] [--skinny] [--f16in]
     python -m dense_gemm_04_gb300.sweep --one M,N,K [--variant sgemm|f16tc|f16in|f16out] [--calls 5]
-        [--alpha 1] [--beta 0]
+        [--alpha 1] [--beta 0] [--b-transposed]
 
 For every shape of the workload sweep ((8192, 8192, 1024), (1024, 1024, 16384),
 (16384, 128, 4096), (4095, 4097, 4093) with alpha = 2, beta = -1; squares 512 .. 16384 with
@@ -290,24 +290,27 @@ def run_f16in(rounds=3, seed=0, seconds=0.5):
              "tflops": 2.0 * n ** 3 / float(np.median(times[(n, kind)])) / 1e12} for n, kind in cases]
 
 
-def run_one(M, N, K, variant, calls=5, alpha=1.0, beta=0.0):
+def run_one(M, N, K, variant, calls=5, alpha=1.0, beta=0.0, b_transposed=False):
     """A handful of calls of one shape with the default configuration, for profilers.
     variant: sgemm, f16tc (f32 operands), f16in (f16 operands, f32 C) or f16out (f16
-    operands and C)."""
+    operands and C); b_transposed: B stored N x K."""
     import torch
     st = torch.cuda.current_stream().cuda_stream
     A = torch.rand(M, K, device="cuda") * 2 - 1
     B = torch.rand(K, N, device="cuda") * 2 - 1
+    if b_transposed:
+        B = B.t().contiguous()
+    op_b = phx.OP_T if b_transposed else phx.OP_N
     C = torch.zeros(M, N, device="cuda")
     if variant in ("f16in", "f16out"):
         A, B = A.half(), B.half()
         if variant == "f16out":
             C = C.half()
         fn = phx.phx_gemm_f16in_f32acc if variant == "f16in" else phx.phx_gemm_f16in_f16out
-        call = lambda: fn(0, 0, M, N, K, alpha, A.data_ptr(), B.data_ptr(), beta, C.data_ptr(), st)
+        call = lambda: fn(0, op_b, M, N, K, alpha, A.data_ptr(), B.data_ptr(), beta, C.data_ptr(), st)
     else:
-        fn = phx.phx_sgemm if variant == "sgemm" else phx.phx_gemm_f16tc_f32acc
-        call = lambda: fn(M, N, K, alpha, A.data_ptr(), B.data_ptr(), beta, C.data_ptr(), st)
+        fn = phx.phx_sgemm_ex if variant == "sgemm" else phx.phx_gemm_f16tc_f32acc_ex
+        call = lambda: fn(0, op_b, M, N, K, alpha, A.data_ptr(), B.data_ptr(), beta, C.data_ptr(), st)
     for _ in range(calls):
         phx.check(call())
     torch.cuda.synchronize()
@@ -320,7 +323,7 @@ def main():
     ap.add_argument("--quick", action="store_true", help="skip shapes above 2^40 MNK and shorten timings")
     ap.add_argument("--layouts", action="store_true", help="time the four storage orders at 4096^3 only")
     ap.add_argument("--skinny", action="store_true", help="time M = 1 .. 2048 rows against K = N = 4096 only")
-    ap.add_argument("--b-transposed", action="store_true", help="with --skinny: B stored N x K")
+    ap.add_argument("--b-transposed", action="store_true", help="with --skinny or --one: B stored N x K")
     ap.add_argument("--f16in", action="store_true", help="time half-precision operands against f32 ones only")
     ap.add_argument("--one", default=None, metavar="M,N,K", help="only run a few calls of this shape (for profilers)")
     ap.add_argument("--variant", default="sgemm", choices=("sgemm", "f16tc", "f16in", "f16out"), help="with --one")
@@ -339,7 +342,7 @@ def main():
     if args.one:
         M, N, K = (int(x) for x in args.one.split(","))
         print(f"{args.variant} {(M, N, K)} x{args.calls}: "
-              f"{run_one(M, N, K, args.variant, args.calls, args.alpha, args.beta)}")
+              f"{run_one(M, N, K, args.variant, args.calls, args.alpha, args.beta, args.b_transposed)}")
         return 0
     if args.skinny:
         rows = run_skinny(b_transposed=args.b_transposed)
