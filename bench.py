@@ -404,8 +404,9 @@ def gpu_arm(args):
     sm_max = clocks.get("sm_max_mhz") or peaks["sm_max_mhz"]
 
     def per_launch_ms(kind):
+        # one call of each kind per step (a call may launch several kernels of its kind)
         n, ms = prof[kind]
-        return ms / n if n else None
+        return ms / prof_steps if n else None
 
     sg_ms = per_launch_ms("sgemm")
     tc_ms = per_launch_ms("tc_gemm")

@@ -848,7 +848,7 @@ cudaError_t f16tc_prepare_launch(int in_f16, int trans_a, int trans_b, int64_t M
     if (blocks > 0x7FFFFFFF || ja.blocks == 0x3FFFFFFF || jb.blocks == 0x3FFFFFFF) return cudaErrorInvalidValue;
     if (blocks == 0) return cudaSuccess;
     cast_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(ja, jb, K, Kp);
-    return cudaGetLastError();
+    return launched(cudaGetLastError());
 }
 
 cudaError_t f16tc_cast_launch_ex(int trans_a, int trans_b, int64_t M, int64_t N, int64_t K,
@@ -979,6 +979,7 @@ cudaError_t f16tc_gemm_launch_ops(int index, int64_t M, int64_t N, int64_t K, fl
                                  alpha, beta, tiles_m, tiles_n, status, full32, tail_split, ksplit, kb_per,
                                  partial, Ch, mapC, epi_tma);
     }
+    err = launched(err);
     if (err != cudaSuccess || ksplit == 1) return err;
     if (Ch != nullptr) return splitk_reduce_launch_h(partial, ksplit, M, N, alpha, beta, Ch, num_sms, stream);
     return splitk_reduce_launch(partial, ksplit, M, N, alpha, beta, C, num_sms, stream);

@@ -629,6 +629,7 @@ cudaError_t skinny_launch(int f16, int a_trans, int64_t M, int64_t N, int64_t K,
     cfg.numAttrs = 1;
     cudaError_t err = cudaLaunchKernelEx(&cfg, p.fn, A, B, C, partial, static_cast<int>(M), N, static_cast<int>(K),
                                          p.k_cta, p.cs, p.mchunks, p.strips, a_trans ? 1 : 0, alpha, beta);
+    err = launched(err);
     if (err != cudaSuccess || p.planes == 1) return err;
     return splitk_reduce_launch(partial, p.planes, M, N, alpha, beta, C, num_sms, stream);
 }
@@ -663,6 +664,7 @@ cudaError_t skinny_nt_launch(int f16, int a_trans, int64_t M, int64_t N, int64_t
     cudaError_t err = cudaLaunchKernelEx(&cfg, p.fn, A, W, C, partial, static_cast<int>(M), static_cast<int>(N),
                                          static_cast<int>(K), p.k_cta, p.cs, p.mchunks, p.strips, a_mode, alpha,
                                          beta);
+    err = launched(err);
     if (err != cudaSuccess || p.planes == 1) return err;
     return splitk_reduce_launch(partial, p.planes, M, N, alpha, beta, C, num_sms, stream);
 }

@@ -12,6 +12,17 @@
 
 namespace phx {
 
+// Kernels this thread has enqueued through the library so far: every launch site adds its
+// successful launches, and the event profile counts kernels per call from the difference.
+void note_launches(int n);
+int64_t noted_launches();
+
+// `err` of a kernel launch, noted as one launch when it succeeded.
+inline cudaError_t launched(cudaError_t err) {
+    if (err == cudaSuccess) note_launches(1);
+    return err;
+}
+
 // Status codes written into the per-device status word by kernels (0 = nothing to report).
 enum DeviceStatus : unsigned int {
     kDevOk = 0,

@@ -377,9 +377,11 @@ __global__ void tune_fill_kernel(float* p, int64_t n, uint32_t salt) {
 enum KernelKind { kKindSgemm = 0, kKindCast = 1, kKindTcGemm = 2, kKindScale = 3, kKindTranspose = 4,
                   kKindSkinny = 5, kNumKinds = 6 };
 
+thread_local int64_t t_launches = 0;
+
 struct Profile {
     bool on = false;
-    std::vector<std::tuple<int, cudaEvent_t, cudaEvent_t>> marks;  // kind, begin, end
+    std::vector<std::tuple<int, cudaEvent_t, cudaEvent_t, int64_t>> marks;  // kind, begin, end, kernels
     std::vector<cudaEvent_t> spare;
 };
 std::mutex g_prof_mu;
@@ -406,9 +408,10 @@ cudaError_t timed(int kind, cudaStream_t stream, F&& launch) {
     }
     cudaEvent_t b = prof_event(), e = prof_event();
     cudaEventRecord(b, stream);
+    const int64_t n0 = t_launches;
     const cudaError_t err = launch();
     cudaEventRecord(e, stream);
-    g_prof.marks.emplace_back(kind, b, e);
+    g_prof.marks.emplace_back(kind, b, e, t_launches - n0);
     return err;
 }
 
@@ -724,7 +727,7 @@ phx_status phx_profile_stop(int64_t* launches, double* ms) {
             cudaGetLastError();
             st = PHX_ERR_LAUNCH;
         }
-        launches[kind] += 1;
+        launches[kind] += std::get<3>(m);
         ms[kind] += t;
         g_prof.spare.push_back(std::get<1>(m));
         g_prof.spare.push_back(std::get<2>(m));
@@ -934,3 +937,11 @@ phx_status phx_selftest_tuner(int n, const double* base_s, const int* fail, doub
 }
 
 }  // extern "C"
+
+namespace phx {
+
+void note_launches(int n) { t_launches += n; }
+
+int64_t noted_launches() { return t_launches; }
+
+}  // namespace phx

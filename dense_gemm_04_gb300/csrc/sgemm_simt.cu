@@ -93,10 +93,36 @@ __host__ __device__ constexpr int sgemm_smem_floats(int bm, int bn, int bk, int 
     return stages * bm * bk + 2 * bk * at_row_stride(bm) + stages * bk * bn;
 }
 
-template <int BM, int BN, int BK, int STAGES, int TM, int TN, bool MASKED, bool FMA2, int MINB>
-__global__ void __launch_bounds__(kThreads, MINB)
-sgemm_kernel(const float* __restrict__ A, const float* __restrict__ B, float* __restrict__ C,
-             int M, int N, int K, float alpha, float beta, int k_slice, float* __restrict__ partial) {
+// Stream-K tail.  A grid of more than one wave whose last wave would leave SMs idle runs
+// its whole waves as tiles (sgemm_kernel over tiles [0, dp_tiles)) and spreads the k tiles
+// of the remaining (tail) tiles evenly over `blocks` blocks of sgemm_streamk_kernel, one
+// per CTA slot of the GPU, launched first so that they fill the GPU together: block s takes
+// k tiles [s * work / blocks, (s + 1) * work / blocks) of the tail's k tiles laid end to end
+// (tile after tile).  streamk_fixup_kernel then adds each tail tile's partial tiles in k
+// order and applies alpha and beta.  The tail thus takes the same time on every slot,
+// instead of leaving SMs idle for a fraction of a wave.
+struct StreamK {
+    int dp_tiles;   // tiles [0, dp_tiles) are whole tiles; the rest are the tail
+    int blocks;     // stream-K blocks (0: none)
+    int64_t work;   // tail tiles x k tiles per tile
+    float* slots;   // 2 * blocks tiles of BM x BN partial sums
+};
+
+// First k tile (of the tail's, end to end) of stream-K block s.
+__host__ __device__ __forceinline__ int64_t streamk_begin(int64_t s, int64_t work, int64_t blocks) {
+    return s * work / blocks;
+}
+
+// One output tile, or the k range [0, K) of one: the CTA's whole computation, shared by the
+// tile kernel and the stream-K kernel below.  A and B point at the range's first k column
+// and row, A's rows lda floats apart; element (row, col) of the result goes to
+// out[(row - r_off) * ldo + col - c_off] (C itself, a plane of split-K partial products,
+// or a stream-K block's tile of partial sums).
+template <int BM, int BN, int BK, int STAGES, int TM, int TN, bool MASKED, bool FMA2>
+__device__ __forceinline__ void sgemm_tile(const float* __restrict__ A, const float* __restrict__ B, int lda,
+                                           int M, int N, int K, int m0, int n0, float alpha, float beta,
+                                           float* __restrict__ out, int ldo, int r_off, int c_off,
+                                           float* smem) {
     constexpr int WTM = kLanesM * TM;  // warp tile
     constexpr int WTN = kLanesN * TN;
     constexpr int WARPS_M = BM / WTM;
@@ -109,7 +135,6 @@ sgemm_kernel(const float* __restrict__ A, const float* __restrict__ B, float* __
     constexpr int AT_BUF = BK * LDT;
     constexpr int B_STAGE = BK * BN;        // [k][n]
 
-    extern __shared__ __align__(16) float smem[];
     float* As = smem;                        // STAGES x A_STAGE
     float* At = As + STAGES * A_STAGE;       // 2 x AT_BUF
     float* Bs = At + 2 * AT_BUF;             // STAGES x B_STAGE
@@ -122,26 +147,6 @@ sgemm_kernel(const float* __restrict__ A, const float* __restrict__ B, float* __
     const int lm = lane / kLanesN;
     const int ln = lane % kLanesN;
 
-    // Split K (gridDim.y slices): slice y multiplies the k range [y * k_slice, ...) and
-    // writes its partial product, alpha = 1 and beta = 0, to its own M x N plane of
-    // `partial`; a separate pass adds the planes in slice order and applies alpha and beta.
-    const int lda = K;  // row stride of A
-    if (gridDim.y > 1) {
-        const int k0s = static_cast<int>(blockIdx.y) * k_slice;
-        A += k0s;
-        B += static_cast<int64_t>(k0s) * N;
-        K = min(K - k0s, k_slice);
-        C = partial + static_cast<int64_t>(blockIdx.y) * M * N;
-        alpha = 1.f;
-        beta = 0.f;
-    }
-
-    const int tiles_m = (M + BM - 1) / BM;
-    const int tiles_n = (N + BN - 1) / BN;
-    int pm, pn;
-    tile_coords(blockIdx.x, tiles_m, tiles_n, pm, pn);
-    const int m0 = pm * BM;
-    const int n0 = pn * BN;
     const int num_k_tiles = (K + BK - 1) / BK;
 
     // Copy k tile `kt` of A (TILE_M x TILE_K) and B (TILE_K x TILE_N) into ring slot `stage`.
@@ -283,12 +288,12 @@ sgemm_kernel(const float* __restrict__ A, const float* __restrict__ B, float* __
     for (int i = 0; i < TM; ++i) {
         const int row = m0 + wm * WTM + (i / 4) * (kLanesM * 4) + lm * 4 + (i % 4);
         if (MASKED && row >= M) continue;
-        float* crow = C + static_cast<int64_t>(row) * N;
+        float* crow = out + static_cast<int64_t>(row - r_off) * ldo;
 #pragma unroll
         for (int h = 0; h < TN / 4; ++h) {
             const int col = n0 + wn * WTN + h * (kLanesN * 4) + ln * 4;
             if constexpr (!MASKED) {
-                float4* p = reinterpret_cast<float4*>(crow + col);
+                float4* p = reinterpret_cast<float4*>(crow + (col - c_off));
                 float4 o;
                 o.x = alpha * acc[i][h * 4 + 0];
                 o.y = alpha * acc[i][h * 4 + 1];
@@ -307,11 +312,126 @@ sgemm_kernel(const float* __restrict__ A, const float* __restrict__ B, float* __
                 for (int c = 0; c < 4; ++c) {
                     if (col + c < N) {
                         float o = alpha * acc[i][h * 4 + c];
-                        if (read_c) o = fmaf(beta, crow[col + c], o);
-                        crow[col + c] = o;
+                        if (read_c) o = fmaf(beta, crow[col - c_off + c], o);
+                        crow[col - c_off + c] = o;
                     }
                 }
             }
+        }
+    }
+}
+
+template <int BM, int BN, int BK, int STAGES, int TM, int TN, bool MASKED, bool FMA2, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB)
+sgemm_kernel(const float* __restrict__ A, const float* __restrict__ B, float* __restrict__ C,
+             int M, int N, int K, float alpha, float beta, int k_slice, float* __restrict__ partial) {
+    extern __shared__ __align__(16) float smem[];
+    // Split K (gridDim.y slices): slice y multiplies the k range [y * k_slice, ...) and
+    // writes its partial product, alpha = 1 and beta = 0, to its own M x N plane of
+    // `partial`; a separate pass adds the planes in slice order and applies alpha and beta.
+    const int lda = K;  // row stride of A
+    if (gridDim.y > 1) {
+        const int k0s = static_cast<int>(blockIdx.y) * k_slice;
+        A += k0s;
+        B += static_cast<int64_t>(k0s) * N;
+        K = min(K - k0s, k_slice);
+        C = partial + static_cast<int64_t>(blockIdx.y) * M * N;
+        alpha = 1.f;
+        beta = 0.f;
+    }
+    int pm, pn;
+    tile_coords(blockIdx.x, (M + BM - 1) / BM, (N + BN - 1) / BN, pm, pn);
+    sgemm_tile<BM, BN, BK, STAGES, TM, TN, MASKED, FMA2>(A, B, lda, M, N, K, pm * BM, pn * BN, alpha, beta, C, N, 0,
+                                                         0, smem);
+}
+
+// Stream-K block s: k tiles [streamk_begin(s), streamk_begin(s + 1)) of the tail tiles'
+// k tiles laid end to end, as at most two segments (the end of one tile, the start of the
+// next), each written as a BM x BN tile of partial sums to slot 2s + segment.
+template <int BM, int BN, int BK, int STAGES, int TM, int TN, bool MASKED, bool FMA2, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB)
+sgemm_streamk_kernel(const float* __restrict__ A, const float* __restrict__ B, int M, int N, int K,
+                     const StreamK sk) {
+    extern __shared__ __align__(16) float smem[];
+    const int k_tiles = (K + BK - 1) / BK;
+    const int64_t s = blockIdx.x;
+    int64_t it = streamk_begin(s, sk.work, sk.blocks);
+    const int64_t end = streamk_begin(s + 1, sk.work, sk.blocks);
+    int seg = 0;
+#pragma unroll 1
+    while (it < end) {
+        const int t = static_cast<int>(it / k_tiles);
+        const int kt0 = static_cast<int>(it - static_cast<int64_t>(t) * k_tiles);
+        const int kt1 = static_cast<int>(min(static_cast<int64_t>(k_tiles), kt0 + (end - it)));
+        int pm, pn;
+        tile_coords(sk.dp_tiles + t, (M + BM - 1) / BM, (N + BN - 1) / BN, pm, pn);
+        if (seg > 0) __syncthreads();  // the first segment is done with the shared buffers
+        sgemm_tile<BM, BN, BK, STAGES, TM, TN, MASKED, FMA2>(
+            A + kt0 * BK, B + static_cast<int64_t>(kt0) * BK * N, K, M, N, min(K - kt0 * BK, (kt1 - kt0) * BK),
+            pm * BM, pn * BN, 1.f, 0.f, sk.slots + (2 * s + seg) * (BM * BN), BN, pm * BM, pn * BN, smem);
+        it += kt1 - kt0;
+        ++seg;
+    }
+}
+
+// Finish the tail tiles of a stream-K launch: block t takes tail tile t (tile dp_tiles + t
+// of the tile order), adds the partial tiles of the stream-K blocks whose k ranges meet it
+// in k order (a block that began in the tile before holds its part in its second slot),
+// and writes C <- alpha * sum + beta * C (beta == 0: C not read).  Every block's range is
+// at most one tile long, so it meets at most two tiles.
+__global__ void __launch_bounds__(256) streamk_fixup_kernel(StreamK sk, int k_tiles, int bm, int bn, int M, int N,
+                                                            float alpha, float beta, float* __restrict__ C,
+                                                            int vec) {
+    const int t = static_cast<int>(blockIdx.x);
+    const int64_t lo = static_cast<int64_t>(t) * k_tiles;
+    const int64_t hi = lo + k_tiles;
+    // the first stream-K block whose range contains k tile lo
+    int64_t b0 = lo * sk.blocks / sk.work;
+    while (b0 > 0 && streamk_begin(b0, sk.work, sk.blocks) > lo) --b0;
+    while (b0 + 1 < sk.blocks && streamk_begin(b0 + 1, sk.work, sk.blocks) <= lo) ++b0;
+    int pm, pn;
+    tile_coords(sk.dp_tiles + t, (M + bm - 1) / bm, (N + bn - 1) / bn, pm, pn);
+    const int m0 = pm * bm, n0 = pn * bn;
+    const int64_t tile_elems = static_cast<int64_t>(bm) * bn;
+    const int step = vec ? 4 : 1;
+    for (int e = threadIdx.x * step; e < bm * bn; e += blockDim.x * step) {
+        const int row = m0 + e / bn;
+        const int col = n0 + e % bn;
+        if (row >= M || col >= N) continue;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        bool first = true;
+        for (int64_t b = b0; b < sk.blocks; ++b) {
+            const int64_t s0 = streamk_begin(b, sk.work, sk.blocks);
+            const int64_t s1 = streamk_begin(b + 1, sk.work, sk.blocks);
+            if (s0 >= hi) break;
+            if (s1 <= s0) continue;  // an empty range wrote nothing
+            const float* src = sk.slots + (2 * b + (s0 < lo ? 1 : 0)) * tile_elems + e;
+            float4 v;
+            if (vec) {
+                v = __ldcs(reinterpret_cast<const float4*>(src));
+            } else {
+                v = make_float4(__ldcs(src), 0.f, 0.f, 0.f);
+            }
+            if (first) {
+                acc = v;
+                first = false;
+            } else {
+                acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+            }
+        }
+        float* c = C + static_cast<int64_t>(row) * N + col;
+        if (vec) {
+            float4 o = make_float4(alpha * acc.x, alpha * acc.y, alpha * acc.z, alpha * acc.w);
+            if (beta != 0.f) {
+                const float4 co = *reinterpret_cast<const float4*>(c);
+                o.x = fmaf(beta, co.x, o.x); o.y = fmaf(beta, co.y, o.y);
+                o.z = fmaf(beta, co.z, o.z); o.w = fmaf(beta, co.w, o.w);
+            }
+            *reinterpret_cast<float4*>(c) = o;
+        } else {
+            float o = alpha * acc.x;
+            if (beta != 0.f) o = fmaf(beta, *c, o);
+            *c = o;
         }
     }
 }
@@ -404,11 +524,14 @@ __global__ void scale_c_kernel(float* __restrict__ C, int64_t n, float beta) {
 // 4x4..8x16 register micro-tiles covers, times STAGES in {3, 4} and the FMA2 switch.
 // ---------------------------------------------------------------------------------------
 using KernelFn = void (*)(const float*, const float*, float*, int, int, int, float, float, int, float*);
+using StreamKFn = void (*)(const float*, const float*, int, int, int, StreamK);
 
 struct Entry {
     SgemmConfig cfg;
     KernelFn aligned;
     KernelFn masked;
+    StreamKFn sk_aligned;  // the stream-K blocks of the same tile shape
+    StreamKFn sk_masked;
     int smem_bytes;
 };
 
@@ -421,6 +544,8 @@ constexpr Entry make_entry() {
     return Entry{SgemmConfig{BM, BN, BK, STAGES, FMA2},
                  &sgemm_kernel<BM, BN, BK, STAGES, TM, TN, false, FMA2 != 0, MINB>,
                  &sgemm_kernel<BM, BN, BK, STAGES, TM, TN, true, FMA2 != 0, MINB>,
+                 &sgemm_streamk_kernel<BM, BN, BK, STAGES, TM, TN, false, FMA2 != 0, MINB>,
+                 &sgemm_streamk_kernel<BM, BN, BK, STAGES, TM, TN, true, FMA2 != 0, MINB>,
                  sgemm_smem_floats(BM, BN, BK, STAGES) * 4};
 }
 
@@ -490,14 +615,46 @@ int64_t k_per_slice(const Entry& e, bool aligned, int64_t M, int64_t N, int64_t 
     return (k_tiles + split - 1) / split * e.cfg.tile_k;
 }
 
+// Stream-K tail of a grid of more than one wave (see StreamK): the whole waves as tiles,
+// the k tiles of the tail tiles over one block per CTA slot.  Used when it shortens the
+// tail by at least kStreamKMinGain of a wave: a last wave of T tiles now takes
+// ceil(T / SMs) / (CTAs per SM) of a wave (a CTA alone on its SM runs that many times
+// faster: the kernel is bound by the SM's FMA rate), and T / slots once spread evenly.
+// K must give every block at least kStreamKMinKTiles k tiles.
+constexpr double kStreamKMinGain = 0.05;
+constexpr int64_t kStreamKMinKTiles = 8;
+
+StreamK streamk_plan(const Entry& e, bool aligned, int64_t M, int64_t N, int64_t K, int num_sms) {
+    StreamK sk{0, 0, 0, nullptr};
+    const int64_t tiles = ((M + e.cfg.tile_m - 1) / e.cfg.tile_m) * ((N + e.cfg.tile_n - 1) / e.cfg.tile_n);
+    const int64_t per_sm = ctas_per_sm(aligned ? e.aligned : e.masked, e.smem_bytes);
+    const int64_t slots = per_sm * num_sms;
+    const int64_t k_tiles = (K + e.cfg.tile_k - 1) / e.cfg.tile_k;
+    if (num_sms <= 0 || tiles <= slots) return sk;
+    const int64_t tail = tiles % slots;
+    if (tail == 0) return sk;
+    const double now = static_cast<double>((tail + num_sms - 1) / num_sms) / static_cast<double>(per_sm);
+    const double spread = static_cast<double>(tail) / static_cast<double>(slots);
+    if (now - spread < kStreamKMinGain) return sk;
+    const int64_t work = tail * k_tiles;
+    int64_t blocks = slots;
+    if (work / blocks < kStreamKMinKTiles) return sk;
+    sk.dp_tiles = static_cast<int>(tiles - tail);
+    sk.blocks = static_cast<int>(blocks);
+    sk.work = work;
+    return sk;
+}
+
 }  // namespace
 
 size_t sgemm_workspace_bytes(int index, int64_t M, int64_t N, int64_t K, const float* A,
                              const float* B, const float* C, int num_sms) {
     const Entry& e = kEntries[index];
-    const int64_t ks = k_per_slice(e, sgemm_is_aligned(index, M, N, K, A, B, C), M, N, K, num_sms);
-    if (ks >= K) return 0;
-    return static_cast<size_t>((K + ks - 1) / ks) * static_cast<size_t>(M * N) * 4;
+    const bool aligned = sgemm_is_aligned(index, M, N, K, A, B, C);
+    const int64_t ks = k_per_slice(e, aligned, M, N, K, num_sms);
+    if (ks < K) return static_cast<size_t>((K + ks - 1) / ks) * static_cast<size_t>(M * N) * 4;
+    const StreamK sk = streamk_plan(e, aligned, M, N, K, num_sms);
+    return static_cast<size_t>(2 * sk.blocks) * e.cfg.tile_m * e.cfg.tile_n * 4;
 }
 
 cudaError_t sgemm_launch(int index, int64_t M, int64_t N, int64_t K, float alpha,
@@ -516,11 +673,34 @@ cudaError_t sgemm_launch(int index, int64_t M, int64_t N, int64_t K, float alpha
     if (workspace == nullptr) ks = K;
     const int64_t slices = (K + ks - 1) / ks;
     float* partial = slices > 1 ? static_cast<float*>(workspace) : nullptr;
-    fn<<<dim3(static_cast<unsigned>(tiles), static_cast<unsigned>(slices)), kThreads, e.smem_bytes, stream>>>(
+    StreamK sk{0, 0, 0, nullptr};
+    if (slices == 1 && workspace != nullptr) sk = streamk_plan(e, aligned, M, N, K, num_sms);
+    if (sk.blocks > 0) {
+        // the stream-K blocks first, one per CTA slot: they fill the GPU on their own
+        StreamKFn skf = aligned ? e.sk_aligned : e.sk_masked;
+        err = cudaFuncSetAttribute(reinterpret_cast<const void*>(skf), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   e.smem_bytes);
+        if (err != cudaSuccess) return err;
+        sk.slots = static_cast<float*>(workspace);
+        skf<<<static_cast<unsigned>(sk.blocks), kThreads, e.smem_bytes, stream>>>(
+            A, B, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), sk);
+        err = launched(cudaGetLastError());
+        if (err != cudaSuccess) return err;
+    }
+    const int64_t grid = sk.blocks > 0 ? sk.dp_tiles : tiles;
+    fn<<<dim3(static_cast<unsigned>(grid), static_cast<unsigned>(slices)), kThreads, e.smem_bytes, stream>>>(
         A, B, C, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), alpha, beta,
         static_cast<int>(ks), partial);
-    err = cudaGetLastError();
-    if (err != cudaSuccess || slices == 1) return err;
+    err = launched(cudaGetLastError());
+    if (err != cudaSuccess) return err;
+    if (sk.blocks > 0) {
+        const int vec = (N % 4 == 0) && ((reinterpret_cast<uintptr_t>(C) & 15u) == 0);
+        streamk_fixup_kernel<<<static_cast<unsigned>(tiles - sk.dp_tiles), 256, 0, stream>>>(
+            sk, static_cast<int>((K + e.cfg.tile_k - 1) / e.cfg.tile_k), e.cfg.tile_m, e.cfg.tile_n,
+            static_cast<int>(M), static_cast<int>(N), alpha, beta, C, vec);
+        return launched(cudaGetLastError());
+    }
+    if (slices == 1) return err;
     return splitk_reduce_launch(partial, static_cast<int>(slices), M, N, alpha, beta, C, num_sms, stream);
 }
 
@@ -534,7 +714,7 @@ cudaError_t splitk_reduce_launch(const float* partial, int slices, int64_t M, in
     if (blocks < 1) blocks = 1;
     splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(partial, slices, plane, alpha,
                                                                              beta, C, vec);
-    return cudaGetLastError();
+    return launched(cudaGetLastError());
 }
 
 cudaError_t splitk_reduce_launch_h(const float* partial, int slices, int64_t M, int64_t N, float alpha,
@@ -545,7 +725,7 @@ cudaError_t splitk_reduce_launch_h(const float* partial, int slices, int64_t M, 
     if (blocks > cap) blocks = cap;
     splitk_reduce_h_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(partial, slices, plane, alpha,
                                                                                beta, C);
-    return cudaGetLastError();
+    return launched(cudaGetLastError());
 }
 
 cudaError_t scale_c_h_launch(int64_t M, int64_t N, float beta, __half* C, cudaStream_t stream) {
@@ -553,7 +733,7 @@ cudaError_t scale_c_h_launch(int64_t M, int64_t N, float beta, __half* C, cudaSt
     int64_t blocks = (n + 255) / 256;
     if (blocks > 4096) blocks = 4096;
     scale_c_h_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(C, n, beta);
-    return cudaGetLastError();
+    return launched(cudaGetLastError());
 }
 
 cudaError_t transpose_f32_launch(const float* src, float* dst, int64_t rows, int64_t cols,
@@ -561,7 +741,7 @@ cudaError_t transpose_f32_launch(const float* src, float* dst, int64_t rows, int
     const int64_t gx = (cols + 31) / 32, gy = (rows + 31) / 32;
     if (gx * gy > 0x7FFFFFFF) return cudaErrorInvalidValue;
     transpose_f32_kernel<<<static_cast<unsigned>(gx * gy), 256, 0, stream>>>(src, dst, rows, cols, gx);
-    return cudaGetLastError();
+    return launched(cudaGetLastError());
 }
 
 cudaError_t scale_c_launch(int64_t M, int64_t N, float beta, float* C, cudaStream_t stream) {
@@ -569,7 +749,7 @@ cudaError_t scale_c_launch(int64_t M, int64_t N, float beta, float* C, cudaStrea
     int64_t blocks = (n + 255) / 256;
     if (blocks > 4096) blocks = 4096;
     scale_c_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(C, n, beta);
-    return cudaGetLastError();
+    return launched(cudaGetLastError());
 }
 
 }  // namespace phx

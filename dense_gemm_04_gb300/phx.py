@@ -270,7 +270,7 @@ def profile_start() -> None:
 
 
 def profile_stop():
-    """Stop the profile; returns {kind name: (launches, total device ms)}."""
+    """Stop the profile; returns {kind name: (kernels launched, total device ms)}."""
     kinds = len(KIND_NAMES)
     n = (_i64 * kinds)()
     ms = (ctypes.c_double * kinds)()

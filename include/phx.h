@@ -200,8 +200,11 @@ enum { PHX_KIND_SGEMM = 0, PHX_KIND_F16_CAST = 1, PHX_KIND_TC_GEMM = 2, PHX_KIND
 phx_status phx_profile_start(void);
 
 /* Stop the profile: synchronise the recorded events and write, for each kind k in
- * [0, PHX_NUM_KINDS), the number of launches[k] and their summed device time ms[k] in
- * milliseconds.  Both arrays are caller-owned host arrays of PHX_NUM_KINDS elements. */
+ * [0, PHX_NUM_KINDS), the number of kernels launched[k] and their summed device time ms[k]
+ * in milliseconds (one call may launch several kernels of its kind: a long f32 GEMM whose
+ * last wave is spread as stream-K blocks launches those, the tiles and a fix-up; a grid
+ * split along K adds its reduction).  Both arrays are caller-owned host arrays of
+ * PHX_NUM_KINDS elements. */
 phx_status phx_profile_stop(int64_t* launches, double* ms);
 
 /* ---------------------------------------------------------------------------------------
