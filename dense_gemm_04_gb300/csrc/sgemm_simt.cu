@@ -99,8 +99,9 @@ __host__ __device__ constexpr int sgemm_smem_floats(int bm, int bn, int bk, int 
 // per CTA slot of the GPU, launched first so that they fill the GPU together: block s takes
 // k tiles [s * work / blocks, (s + 1) * work / blocks) of the tail's k tiles laid end to end
 // (tile after tile).  streamk_fixup_kernel then adds each tail tile's partial tiles in k
-// order and applies alpha and beta.  The tail thus takes the same time on every slot,
-// instead of leaving SMs idle for a fraction of a wave.
+// order and applies alpha and beta, before the whole tiles run (while the partial tiles
+// are still in L2).  The tail thus takes the same time on every slot, instead of leaving
+// SMs idle for a fraction of a wave.
 struct StreamK {
     int dp_tiles;   // tiles [0, dp_tiles) are whole tiles; the rest are the tail
     int blocks;     // stream-K blocks (0: none)
@@ -378,50 +379,56 @@ sgemm_streamk_kernel(const float* __restrict__ A, const float* __restrict__ B, i
 // of the tile order), adds the partial tiles of the stream-K blocks whose k ranges meet it
 // in k order (a block that began in the tile before holds its part in its second slot),
 // and writes C <- alpha * sum + beta * C (beta == 0: C not read).  Every block's range is
-// at most one tile long, so it meets at most two tiles.
-__global__ void __launch_bounds__(256) streamk_fixup_kernel(StreamK sk, int k_tiles, int bm, int bn, int M, int N,
+// at most one tile long, so it meets at most two tiles.  The block has bm * bn / 64
+// threads, each owning 16 float4s of the tile (thread x, float4 x + i * blockDim.x), so a
+// partial tile is read with 16 independent 16-byte loads per thread; the segment bounds
+// are the same for the whole block and computed once per segment.
+constexpr int kFixupVec = 16;
+
+__global__ void __launch_bounds__(512) streamk_fixup_kernel(StreamK sk, int k_tiles, int bm, int bn, int M, int N,
                                                             float alpha, float beta, float* __restrict__ C,
                                                             int vec) {
     const int t = static_cast<int>(blockIdx.x);
     const int64_t lo = static_cast<int64_t>(t) * k_tiles;
     const int64_t hi = lo + k_tiles;
     // the first stream-K block whose range contains k tile lo
-    int64_t b0 = lo * sk.blocks / sk.work;
-    while (b0 > 0 && streamk_begin(b0, sk.work, sk.blocks) > lo) --b0;
-    while (b0 + 1 < sk.blocks && streamk_begin(b0 + 1, sk.work, sk.blocks) <= lo) ++b0;
+    int64_t b = lo * sk.blocks / sk.work;
+    while (b > 0 && streamk_begin(b, sk.work, sk.blocks) > lo) --b;
+    while (b + 1 < sk.blocks && streamk_begin(b + 1, sk.work, sk.blocks) <= lo) ++b;
     int pm, pn;
     tile_coords(sk.dp_tiles + t, (M + bm - 1) / bm, (N + bn - 1) / bn, pm, pn);
     const int m0 = pm * bm, n0 = pn * bn;
     const int64_t tile_elems = static_cast<int64_t>(bm) * bn;
-    const int step = vec ? 4 : 1;
-    for (int e = threadIdx.x * step; e < bm * bn; e += blockDim.x * step) {
+    float4 acc[kFixupVec];
+    bool first = true;
+    int64_t s0 = streamk_begin(b, sk.work, sk.blocks);
+    for (; b < sk.blocks && s0 < hi; ++b) {
+        const int64_t s1 = streamk_begin(b + 1, sk.work, sk.blocks);
+        if (s1 > s0) {  // an empty range wrote nothing
+            const float4* src = reinterpret_cast<const float4*>(sk.slots + (2 * b + (s0 < lo ? 1 : 0)) * tile_elems);
+#pragma unroll
+            for (int i = 0; i < kFixupVec; ++i) {
+                const float4 v = __ldcs(src + threadIdx.x + i * blockDim.x);
+                if (first) {
+                    acc[i] = v;
+                } else {
+                    acc[i].x += v.x; acc[i].y += v.y; acc[i].z += v.z; acc[i].w += v.w;
+                }
+            }
+            first = false;
+        }
+        s0 = s1;
+    }
+#pragma unroll
+    for (int i = 0; i < kFixupVec; ++i) {
+        const int e = 4 * (threadIdx.x + i * blockDim.x);
         const int row = m0 + e / bn;
         const int col = n0 + e % bn;
         if (row >= M || col >= N) continue;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        bool first = true;
-        for (int64_t b = b0; b < sk.blocks; ++b) {
-            const int64_t s0 = streamk_begin(b, sk.work, sk.blocks);
-            const int64_t s1 = streamk_begin(b + 1, sk.work, sk.blocks);
-            if (s0 >= hi) break;
-            if (s1 <= s0) continue;  // an empty range wrote nothing
-            const float* src = sk.slots + (2 * b + (s0 < lo ? 1 : 0)) * tile_elems + e;
-            float4 v;
-            if (vec) {
-                v = __ldcs(reinterpret_cast<const float4*>(src));
-            } else {
-                v = make_float4(__ldcs(src), 0.f, 0.f, 0.f);
-            }
-            if (first) {
-                acc = v;
-                first = false;
-            } else {
-                acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-            }
-        }
         float* c = C + static_cast<int64_t>(row) * N + col;
+        const float a[4] = {acc[i].x, acc[i].y, acc[i].z, acc[i].w};
         if (vec) {
-            float4 o = make_float4(alpha * acc.x, alpha * acc.y, alpha * acc.z, alpha * acc.w);
+            float4 o = make_float4(alpha * a[0], alpha * a[1], alpha * a[2], alpha * a[3]);
             if (beta != 0.f) {
                 const float4 co = *reinterpret_cast<const float4*>(c);
                 o.x = fmaf(beta, co.x, o.x); o.y = fmaf(beta, co.y, o.y);
@@ -429,9 +436,13 @@ __global__ void __launch_bounds__(256) streamk_fixup_kernel(StreamK sk, int k_ti
             }
             *reinterpret_cast<float4*>(c) = o;
         } else {
-            float o = alpha * acc.x;
-            if (beta != 0.f) o = fmaf(beta, *c, o);
-            *c = o;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (col + q >= N) break;
+                float o = alpha * a[q];
+                if (beta != 0.f) o = fmaf(beta, c[q], o);
+                c[q] = o;
+            }
         }
     }
 }
@@ -686,21 +697,22 @@ cudaError_t sgemm_launch(int index, int64_t M, int64_t N, int64_t K, float alpha
             A, B, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), sk);
         err = launched(cudaGetLastError());
         if (err != cudaSuccess) return err;
+        // then the tail tiles of C, while the partial tiles are still in L2 (the whole tiles
+        // below write other elements of C)
+        const int vec = (N % 4 == 0) && ((reinterpret_cast<uintptr_t>(C) & 15u) == 0);
+        streamk_fixup_kernel<<<static_cast<unsigned>(tiles - sk.dp_tiles), e.cfg.tile_m * e.cfg.tile_n / (4 * kFixupVec),
+                               0, stream>>>(
+            sk, static_cast<int>((K + e.cfg.tile_k - 1) / e.cfg.tile_k), e.cfg.tile_m, e.cfg.tile_n,
+            static_cast<int>(M), static_cast<int>(N), alpha, beta, C, vec);
+        err = launched(cudaGetLastError());
+        if (err != cudaSuccess) return err;
     }
     const int64_t grid = sk.blocks > 0 ? sk.dp_tiles : tiles;
     fn<<<dim3(static_cast<unsigned>(grid), static_cast<unsigned>(slices)), kThreads, e.smem_bytes, stream>>>(
         A, B, C, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), alpha, beta,
         static_cast<int>(ks), partial);
     err = launched(cudaGetLastError());
-    if (err != cudaSuccess) return err;
-    if (sk.blocks > 0) {
-        const int vec = (N % 4 == 0) && ((reinterpret_cast<uintptr_t>(C) & 15u) == 0);
-        streamk_fixup_kernel<<<static_cast<unsigned>(tiles - sk.dp_tiles), 256, 0, stream>>>(
-            sk, static_cast<int>((K + e.cfg.tile_k - 1) / e.cfg.tile_k), e.cfg.tile_m, e.cfg.tile_n,
-            static_cast<int>(M), static_cast<int>(N), alpha, beta, C, vec);
-        return launched(cudaGetLastError());
-    }
-    if (slices == 1) return err;
+    if (err != cudaSuccess || slices == 1) return err;
     return splitk_reduce_launch(partial, static_cast<int>(slices), M, N, alpha, beta, C, num_sms, stream);
 }
 
