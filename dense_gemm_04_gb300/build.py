@@ -36,7 +36,7 @@ def sources():
 
 
 def _headers_mtime() -> float:
-    hs = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh", ".map"))]
+    hs = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh", ".inc", ".map"))]
     hs.append(os.path.join(ROOT, "include", "phx.h"))
     return max(os.path.getmtime(h) for h in hs)
 

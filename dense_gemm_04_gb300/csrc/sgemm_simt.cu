@@ -29,6 +29,9 @@
 //     ordinary IEEE f32 fused multiply-add, so the values are the same.
 //   * Epilogue: C is read once (not at all when beta == 0) and written once, with 16-byte
 //     accesses on the aligned path.
+//   * A grid of more than one wave whose last wave would leave SMs idle spreads that wave's
+//     k tiles evenly over one stream-K block per CTA slot (StreamK below).
+// The tile body is in sgemm_tile_body.inc.
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 
@@ -114,236 +117,31 @@ __host__ __device__ __forceinline__ int64_t streamk_begin(int64_t s, int64_t wor
     return s * work / blocks;
 }
 
-// One output tile, or the k range [0, K) of one: the CTA's whole computation, shared by the
-// tile kernel and the stream-K kernel below.  A and B point at the range's first k column
-// and row, A's rows lda floats apart; element (row, col) of the result goes to
-// out[(row - r_off) * ldo + col - c_off] (C itself, a plane of split-K partial products,
-// or a stream-K block's tile of partial sums).
-template <int BM, int BN, int BK, int STAGES, int TM, int TN, bool MASKED, bool FMA2>
-__device__ __forceinline__ void sgemm_tile(const float* __restrict__ A, const float* __restrict__ B, int lda,
-                                           int M, int N, int K, int m0, int n0, float alpha, float beta,
-                                           float* __restrict__ out, int ldo, int r_off, int c_off,
-                                           float* smem) {
-    constexpr int WTM = kLanesM * TM;  // warp tile
-    constexpr int WTN = kLanesN * TN;
-    constexpr int WARPS_M = BM / WTM;
-    constexpr int WARPS_N = BN / WTN;
-    static_assert(WARPS_M * WARPS_N * 32 == kThreads, "8 warps must tile the CTA tile");
-    static_assert(TM % 4 == 0 && TN % 4 == 0 && BK % 4 == 0, "float4 fragments");
-    static_assert(STAGES >= 3, "the ring keeps one panel ahead of the transposed one");
-    constexpr int A_STAGE = BM * BK;        // staging, [m][k] as copied from A
-    constexpr int LDT = at_row_stride(BM);  // k-major copy, [k][m]
-    constexpr int AT_BUF = BK * LDT;
-    constexpr int B_STAGE = BK * BN;        // [k][n]
-
-    float* As = smem;                        // STAGES x A_STAGE
-    float* At = As + STAGES * A_STAGE;       // 2 x AT_BUF
-    float* Bs = At + 2 * AT_BUF;             // STAGES x B_STAGE
-
-    const int tid = threadIdx.x;
-    const int lane = tid & 31;
-    const int warp = tid >> 5;
-    const int wm = warp / WARPS_N;
-    const int wn = warp % WARPS_N;
-    const int lm = lane / kLanesN;
-    const int ln = lane % kLanesN;
-
-    const int num_k_tiles = (K + BK - 1) / BK;
-
-    // Copy k tile `kt` of A (TILE_M x TILE_K) and B (TILE_K x TILE_N) into ring slot `stage`.
-    auto load_tile = [&](int kt, int stage) {
-        const int k0 = kt * BK;
-        float* as = As + stage * A_STAGE;
-        float* bs = Bs + stage * B_STAGE;
-        if constexpr (!MASKED) {
-#pragma unroll
-            for (int e = tid; e < BM * BK / 4; e += kThreads) {
-                const int m = e / (BK / 4);
-                const int k4 = e % (BK / 4);
-                cp_async_16(smem_addr(as + m * BK + k4 * 4),
-                            A + static_cast<int64_t>(m0 + m) * lda + k0 + k4 * 4);
-            }
-#pragma unroll
-            for (int e = tid; e < BK * BN / 4; e += kThreads) {
-                const int k = e / (BN / 4);
-                const int n4 = e % (BN / 4);
-                cp_async_16(smem_addr(bs + k * BN + n4 * 4),
-                            B + static_cast<int64_t>(k0 + k) * N + n0 + n4 * 4);
-            }
-        } else {
-#pragma unroll
-            for (int e = tid; e < BM * BK; e += kThreads) {
-                const int m = e / BK;
-                const int k = e % BK;
-                const bool ok = (m0 + m < M) && (k0 + k < K);
-                const float* src = ok ? A + static_cast<int64_t>(m0 + m) * lda + k0 + k : A;
-                cp_async_4(smem_addr(as + m * BK + k), src, ok);
-            }
-#pragma unroll
-            for (int e = tid; e < BK * BN; e += kThreads) {
-                const int k = e / BN;
-                const int n = e % BN;
-                const bool ok = (k0 + k < K) && (n0 + n < N);
-                const float* src = ok ? B + static_cast<int64_t>(k0 + k) * N + n0 + n : B;
-                cp_async_4(smem_addr(bs + k * BN + n), src, ok);
-            }
-        }
-    };
-
-    // Rewrite ring slot `stage` of A, [m][k], as the k-major buffer `buf`, [k][m].
-    auto transpose_a = [&](int stage, int buf) {
-        const float* as = As + stage * A_STAGE;
-        float* at = At + buf * AT_BUF;
-#pragma unroll
-        for (int e = tid; e < BM * BK / 4; e += kThreads) {
-            const int m = e / (BK / 4);
-            const int k4 = e % (BK / 4);
-            const float4 v = *reinterpret_cast<const float4*>(as + m * BK + k4 * 4);
-            at[(k4 * 4 + 0) * LDT + m] = v.x;
-            at[(k4 * 4 + 1) * LDT + m] = v.y;
-            at[(k4 * 4 + 2) * LDT + m] = v.z;
-            at[(k4 * 4 + 3) * LDT + m] = v.w;
-        }
-    };
-
-    // Accumulators: rows  wm*WTM + g*16 + lm*4 + r   (g < TM/4, r < 4)
-    //               cols  wn*WTN + h*32 + ln*4 + c   (h < TN/4, c < 4)
-    float acc[TM][TN];
-#pragma unroll
-    for (int i = 0; i < TM; ++i)
-#pragma unroll
-        for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
-
-    // Prologue: panels 0 .. STAGES-2 in flight, panel 0 transposed.
-#pragma unroll
-    for (int s = 0; s < STAGES - 1; ++s) {
-        if (s < num_k_tiles) load_tile(s, s);
-        cp_async_commit();
-    }
-    cp_async_wait<STAGES - 2>();
-    __syncthreads();
-    transpose_a(0, 0);
-
-    for (int kt = 0; kt < num_k_tiles; ++kt) {
-        // Panels up to kt+1 have landed; after the barrier they and the transposed panel kt
-        // are visible to every thread, and everyone has finished reading the buffers of
-        // iteration kt-1 (ring slot (kt-1) % STAGES and k-major buffer (kt+1) % 2), which
-        // this iteration refills.
-        cp_async_wait<STAGES - 3>();
-        __syncthreads();
-        const float* at = At + (kt & 1) * AT_BUF + wm * WTM + lm * 4;
-        const float* bs = Bs + (kt % STAGES) * B_STAGE + wn * WTN + ln * 4;
-#pragma unroll
-        for (int kk = 0; kk < BK; ++kk) {
-            // The copies of panel kt+STAGES-1 are issued a quarter of the way through this
-            // panel's k steps and the next A panel is rewritten k-major at five eighths:
-            // both then overlap the multiply-adds instead of sitting between the barrier
-            // and the first multiply-add (measured: +11 % at 4096^3 over issuing both
-            // right after the barrier).
-            if (kk == BK / 4) {
-                const int nk = kt + STAGES - 1;
-                if (nk < num_k_tiles) load_tile(nk, nk % STAGES);
-                cp_async_commit();
-            }
-            if (kk == (BK * 5) / 8 && kt + 1 < num_k_tiles) transpose_a((kt + 1) % STAGES, (kt + 1) & 1);
-            float a[TM], b[TN];
-#pragma unroll
-            for (int g = 0; g < TM / 4; ++g) {
-                const float4 v = *reinterpret_cast<const float4*>(at + kk * LDT + g * (kLanesM * 4));
-                a[g * 4 + 0] = v.x;
-                a[g * 4 + 1] = v.y;
-                a[g * 4 + 2] = v.z;
-                a[g * 4 + 3] = v.w;
-            }
-#pragma unroll
-            for (int h = 0; h < TN / 4; ++h) {
-                const float4 v = *reinterpret_cast<const float4*>(bs + kk * BN + h * (kLanesN * 4));
-                b[h * 4 + 0] = v.x;
-                b[h * 4 + 1] = v.y;
-                b[h * 4 + 2] = v.z;
-                b[h * 4 + 3] = v.w;
-            }
-#pragma unroll
-            for (int i = 0; i < TM; ++i) {
-                if constexpr (FMA2) {
-                    const float2 aa = make_float2(a[i], a[i]);
-#pragma unroll
-                    for (int j = 0; j < TN; j += 2) {
-                        float2 c2 = make_float2(acc[i][j], acc[i][j + 1]);
-                        c2 = __ffma2_rn(aa, make_float2(b[j], b[j + 1]), c2);
-                        acc[i][j] = c2.x;
-                        acc[i][j + 1] = c2.y;
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-                }
-            }
-        }
-    }
-    cp_async_wait<0>();
-
-    // Epilogue: C <- alpha * acc + beta * C_old, C read only when beta != 0.
-    const bool read_c = beta != 0.f;
-#pragma unroll
-    for (int i = 0; i < TM; ++i) {
-        const int row = m0 + wm * WTM + (i / 4) * (kLanesM * 4) + lm * 4 + (i % 4);
-        if (MASKED && row >= M) continue;
-        float* crow = out + static_cast<int64_t>(row - r_off) * ldo;
-#pragma unroll
-        for (int h = 0; h < TN / 4; ++h) {
-            const int col = n0 + wn * WTN + h * (kLanesN * 4) + ln * 4;
-            if constexpr (!MASKED) {
-                float4* p = reinterpret_cast<float4*>(crow + (col - c_off));
-                float4 o;
-                o.x = alpha * acc[i][h * 4 + 0];
-                o.y = alpha * acc[i][h * 4 + 1];
-                o.z = alpha * acc[i][h * 4 + 2];
-                o.w = alpha * acc[i][h * 4 + 3];
-                if (read_c) {
-                    const float4 c = *p;
-                    o.x = fmaf(beta, c.x, o.x);
-                    o.y = fmaf(beta, c.y, o.y);
-                    o.z = fmaf(beta, c.z, o.z);
-                    o.w = fmaf(beta, c.w, o.w);
-                }
-                *p = o;
-            } else {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    if (col + c < N) {
-                        float o = alpha * acc[i][h * 4 + c];
-                        if (read_c) o = fmaf(beta, crow[col - c_off + c], o);
-                        crow[col - c_off + c] = o;
-                    }
-                }
-            }
-        }
-    }
+// One output tile, or a k range of one: the CTA's whole computation, shared by the tile
+// kernel and the stream-K kernel below.  Without LOCAL: tile blockIdx.x, whole K (or the
+// k slice of a split grid), into C (or the slice's plane of `partial`).  With LOCAL: k
+// tiles [kt0, kt1) of `tile`, alpha = 1 and beta = 0, into the BM x BN tile of partial sums
+// at C (element (row, col) at C[(row - m0) * BN + col - n0]).
+template <int BM, int BN, int BK, int STAGES, int TM, int TN, bool MASKED, bool FMA2, bool LOCAL>
+__device__ __forceinline__ void sgemm_tile(const float* __restrict__ A, const float* __restrict__ B,
+                                           float* __restrict__ C, int M, int N, int K, float alpha, float beta,
+                                           int k_slice, float* __restrict__ partial, int tile, int kt0, int kt1) {
+#include "sgemm_tile_body.inc"
 }
 
 template <int BM, int BN, int BK, int STAGES, int TM, int TN, bool MASKED, bool FMA2, int MINB>
 __global__ void __launch_bounds__(kThreads, MINB)
 sgemm_kernel(const float* __restrict__ A, const float* __restrict__ B, float* __restrict__ C,
              int M, int N, int K, float alpha, float beta, int k_slice, float* __restrict__ partial) {
-    extern __shared__ __align__(16) float smem[];
-    // Split K (gridDim.y slices): slice y multiplies the k range [y * k_slice, ...) and
-    // writes its partial product, alpha = 1 and beta = 0, to its own M x N plane of
-    // `partial`; a separate pass adds the planes in slice order and applies alpha and beta.
-    const int lda = K;  // row stride of A
-    if (gridDim.y > 1) {
-        const int k0s = static_cast<int>(blockIdx.y) * k_slice;
-        A += k0s;
-        B += static_cast<int64_t>(k0s) * N;
-        K = min(K - k0s, k_slice);
-        C = partial + static_cast<int64_t>(blockIdx.y) * M * N;
-        alpha = 1.f;
-        beta = 0.f;
+    if constexpr (!MASKED) {
+        sgemm_tile<BM, BN, BK, STAGES, TM, TN, false, FMA2, false>(A, B, C, M, N, K, alpha, beta, k_slice, partial, 0,
+                                                                   0, 0);
+    } else {
+        constexpr bool LOCAL = false;
+        int tile = 0;
+        const int kt0 = 0, kt1 = 0;
+#include "sgemm_tile_body.inc"
     }
-    int pm, pn;
-    tile_coords(blockIdx.x, (M + BM - 1) / BM, (N + BN - 1) / BN, pm, pn);
-    sgemm_tile<BM, BN, BK, STAGES, TM, TN, MASKED, FMA2>(A, B, lda, M, N, K, pm * BM, pn * BN, alpha, beta, C, N, 0,
-                                                         0, smem);
 }
 
 // Stream-K block s: k tiles [streamk_begin(s), streamk_begin(s + 1)) of the tail tiles'
@@ -353,7 +151,6 @@ template <int BM, int BN, int BK, int STAGES, int TM, int TN, bool MASKED, bool 
 __global__ void __launch_bounds__(kThreads, MINB)
 sgemm_streamk_kernel(const float* __restrict__ A, const float* __restrict__ B, int M, int N, int K,
                      const StreamK sk) {
-    extern __shared__ __align__(16) float smem[];
     const int k_tiles = (K + BK - 1) / BK;
     const int64_t s = blockIdx.x;
     int64_t it = streamk_begin(s, sk.work, sk.blocks);
@@ -364,12 +161,9 @@ sgemm_streamk_kernel(const float* __restrict__ A, const float* __restrict__ B, i
         const int t = static_cast<int>(it / k_tiles);
         const int kt0 = static_cast<int>(it - static_cast<int64_t>(t) * k_tiles);
         const int kt1 = static_cast<int>(min(static_cast<int64_t>(k_tiles), kt0 + (end - it)));
-        int pm, pn;
-        tile_coords(sk.dp_tiles + t, (M + BM - 1) / BM, (N + BN - 1) / BN, pm, pn);
         if (seg > 0) __syncthreads();  // the first segment is done with the shared buffers
-        sgemm_tile<BM, BN, BK, STAGES, TM, TN, MASKED, FMA2>(
-            A + kt0 * BK, B + static_cast<int64_t>(kt0) * BK * N, K, M, N, min(K - kt0 * BK, (kt1 - kt0) * BK),
-            pm * BM, pn * BN, 1.f, 0.f, sk.slots + (2 * s + seg) * (BM * BN), BN, pm * BM, pn * BN, smem);
+        sgemm_tile<BM, BN, BK, STAGES, TM, TN, MASKED, FMA2, true>(A, B, sk.slots + (2 * s + seg) * (BM * BN), M, N, K,
+                                                                   1.f, 0.f, 0, nullptr, sk.dp_tiles + t, kt0, kt1);
         it += kt1 - kt0;
         ++seg;
     }
