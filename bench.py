@@ -219,8 +219,9 @@ def reference_arm(args):
 
 
 def _traffic_from_profiles(kernel: str):
-    """DRAM bytes per launch recorded from an ncu capture, if the kernel's source is
-    unchanged since (profiles/dram_traffic.txt: kernel, bytes per launch, source hash)."""
+    """DRAM bytes per call recorded from ncu captures, if the kernel's source is unchanged
+    since (profiles/dram_traffic.txt: kernel, bytes per call, source hash; a call of the f32
+    GEMM at 4096^3 is three kernels, summed there)."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
