@@ -169,20 +169,24 @@ sgemm_streamk_kernel(const float* __restrict__ A, const float* __restrict__ B, i
     }
 }
 
-// Finish the tail tiles of a stream-K launch: block t takes tail tile t (tile dp_tiles + t
-// of the tile order), adds the partial tiles of the stream-K blocks whose k ranges meet it
-// in k order (a block that began in the tile before holds its part in its second slot),
-// and writes C <- alpha * sum + beta * C (beta == 0: C not read).  Every block's range is
-// at most one tile long, so it meets at most two tiles.  The block has bm * bn / 64
-// threads, each owning 16 float4s of the tile (thread x, float4 x + i * blockDim.x), so a
-// partial tile is read with 16 independent 16-byte loads per thread; the segment bounds
-// are the same for the whole block and computed once per segment.
-constexpr int kFixupVec = 16;
+// Finish the tail tiles of a stream-K launch: C <- alpha * sum + beta * C (beta == 0: C not
+// read), where the sum adds, in k order, the partial tiles of the stream-K blocks whose k
+// ranges meet the tile (a block that began in the tile before holds its part in its second
+// slot; every block's range is at most one tile long, so it meets at most two tiles).
+// bm * bn / 4096 blocks of 256 threads share a tile, each thread owning 4 float4s
+// (thread x of part q: float4 q * 1024 + x + 256 i).  The partial tiles are read four at a
+// time, all their loads in flight together, and added in k order; the segment bounds are
+// the same for the whole block.
+constexpr int kFixupVec = 4;      // float4s per thread and partial tile
+constexpr int kFixupBatch = 4;    // partial tiles whose loads are in flight together
+constexpr int kFixupThreads = 256;
 
-__global__ void __launch_bounds__(512) streamk_fixup_kernel(StreamK sk, int k_tiles, int bm, int bn, int M, int N,
-                                                            float alpha, float beta, float* __restrict__ C,
-                                                            int vec) {
-    const int t = static_cast<int>(blockIdx.x);
+__global__ void __launch_bounds__(kFixupThreads) streamk_fixup_kernel(StreamK sk, int k_tiles, int bm, int bn, int M,
+                                                                      int N, float alpha, float beta,
+                                                                      float* __restrict__ C, int vec) {
+    const int parts = bm * bn / (4 * kFixupVec * kFixupThreads);
+    const int t = static_cast<int>(blockIdx.x) / parts;
+    const int part = static_cast<int>(blockIdx.x) - t * parts;
     const int64_t lo = static_cast<int64_t>(t) * k_tiles;
     const int64_t hi = lo + k_tiles;
     // the first stream-K block whose range contains k tile lo
@@ -193,29 +197,47 @@ __global__ void __launch_bounds__(512) streamk_fixup_kernel(StreamK sk, int k_ti
     tile_coords(sk.dp_tiles + t, (M + bm - 1) / bm, (N + bn - 1) / bn, pm, pn);
     const int m0 = pm * bm, n0 = pn * bn;
     const int64_t tile_elems = static_cast<int64_t>(bm) * bn;
+    const int first4 = part * (kFixupVec * kFixupThreads) + static_cast<int>(threadIdx.x);  // float4 index
     float4 acc[kFixupVec];
     bool first = true;
     int64_t s0 = streamk_begin(b, sk.work, sk.blocks);
-    for (; b < sk.blocks && s0 < hi; ++b) {
-        const int64_t s1 = streamk_begin(b + 1, sk.work, sk.blocks);
-        if (s1 > s0) {  // an empty range wrote nothing
-            const float4* src = reinterpret_cast<const float4*>(sk.slots + (2 * b + (s0 < lo ? 1 : 0)) * tile_elems);
-#pragma unroll
-            for (int i = 0; i < kFixupVec; ++i) {
-                const float4 v = __ldcs(src + threadIdx.x + i * blockDim.x);
-                if (first) {
-                    acc[i] = v;
-                } else {
-                    acc[i].x += v.x; acc[i].y += v.y; acc[i].z += v.z; acc[i].w += v.w;
-                }
-            }
-            first = false;
+    while (b < sk.blocks && s0 < hi) {
+        // up to kFixupBatch non-empty partial tiles of this tile, in k order
+        const float4* src[kFixupBatch];
+        int n = 0;
+        while (n < kFixupBatch && b < sk.blocks && s0 < hi) {
+            const int64_t s1 = streamk_begin(b + 1, sk.work, sk.blocks);
+            if (s1 > s0)  // an empty range wrote nothing
+                src[n++] = reinterpret_cast<const float4*>(sk.slots + (2 * b + (s0 < lo ? 1 : 0)) * tile_elems);
+            s0 = s1;
+            ++b;
         }
-        s0 = s1;
+        float4 v[kFixupBatch][kFixupVec];
+#pragma unroll
+        for (int q = 0; q < kFixupBatch; ++q) {
+            if (q < n) {
+#pragma unroll
+                for (int i = 0; i < kFixupVec; ++i) v[q][i] = __ldcs(src[q] + first4 + i * kFixupThreads);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < kFixupBatch; ++q) {
+            if (q < n) {
+#pragma unroll
+                for (int i = 0; i < kFixupVec; ++i) {
+                    if (first) {
+                        acc[i] = v[q][i];
+                    } else {
+                        acc[i].x += v[q][i].x; acc[i].y += v[q][i].y; acc[i].z += v[q][i].z; acc[i].w += v[q][i].w;
+                    }
+                }
+                first = false;
+            }
+        }
     }
 #pragma unroll
     for (int i = 0; i < kFixupVec; ++i) {
-        const int e = 4 * (threadIdx.x + i * blockDim.x);
+        const int e = 4 * (first4 + i * kFixupThreads);
         const int row = m0 + e / bn;
         const int col = n0 + e % bn;
         if (row >= M || col >= N) continue;
@@ -420,14 +442,29 @@ int64_t k_per_slice(const Entry& e, bool aligned, int64_t M, int64_t N, int64_t 
     return (k_tiles + split - 1) / split * e.cfg.tile_k;
 }
 
-// Stream-K tail of a grid of more than one wave (see StreamK): the whole waves as tiles,
-// the k tiles of the tail tiles over one block per CTA slot.  Used when it shortens the
-// tail by at least kStreamKMinGain of a wave: a last wave of T tiles now takes
-// ceil(T / SMs) / (CTAs per SM) of a wave (a CTA alone on its SM runs that many times
-// faster: the kernel is bound by the SM's FMA rate), and T / slots once spread evenly.
-// K must give every block at least kStreamKMinKTiles k tiles.
+// Stream-K plan (see StreamK).  The last, partial wave of the tile grid -- or the whole
+// grid when it is less than one wave -- has T tiles of I k tiles each; its T * I k tiles go
+// to P blocks, P = min(slots, T * I / kStreamKMinKTiles, kStreamKMaxSegments * T) and at
+// least T (so that every block's range is at most one tile long and each block gets
+// kStreamKMinKTiles or more; a tile is then split into at most about kStreamKMaxSegments
+// partial tiles, which bounds the fix-up).
+//   * Time in units of one tile computed by a CTA alone on its SM (the kernel is bound by
+//     the SM's FMA rate, so CTAs sharing an SM share that rate): the T tiles as tiles take
+//     ceil(T / SMs), the P blocks ceil(P / SMs) * T / P.  The plan is used when that saves
+//     at least kStreamKMinGain of a wave (CTAs per SM tile times).
+//   * Each segment costs a pipeline fill and a tile of partial sums, and the fix-up adds a
+//     pass.  So blocks of fewer than kStreamKLongKTiles k tiles are used only where they
+//     beat the alternative (the T tiles, or a grid split along K into slices) by a margin.
+//     In k tiles of a lone CTA: n CTAs of k k-tiles each take ceil(n / SMs) * k.  The
+//     blocks must take at most half of the alternative's time, or kStreamKOverheadKTiles
+//     less.  Measured (f32, 128 x 128 tile, 152 SMs): 256^3 and 512^3 gain from blocks of
+//     8 k tiles, 1024^3 and (300, 500, 3000) run faster split along K, and (2048, 2048,
+//     256) as tiles.
 constexpr double kStreamKMinGain = 0.05;
 constexpr int64_t kStreamKMinKTiles = 8;
+constexpr int64_t kStreamKLongKTiles = 64;
+constexpr int64_t kStreamKMaxSegments = 8;
+constexpr double kStreamKOverheadKTiles = 12.0;
 
 StreamK streamk_plan(const Entry& e, bool aligned, int64_t M, int64_t N, int64_t K, int num_sms) {
     StreamK sk{0, 0, 0, nullptr};
@@ -435,15 +472,30 @@ StreamK streamk_plan(const Entry& e, bool aligned, int64_t M, int64_t N, int64_t
     const int64_t per_sm = ctas_per_sm(aligned ? e.aligned : e.masked, e.smem_bytes);
     const int64_t slots = per_sm * num_sms;
     const int64_t k_tiles = (K + e.cfg.tile_k - 1) / e.cfg.tile_k;
-    if (num_sms <= 0 || tiles <= slots) return sk;
-    const int64_t tail = tiles % slots;
+    if (num_sms <= 0 || tiles <= 0) return sk;
+    const int64_t tail = tiles > slots ? tiles % slots : tiles;
     if (tail == 0) return sk;
-    const double now = static_cast<double>((tail + num_sms - 1) / num_sms) / static_cast<double>(per_sm);
-    const double spread = static_cast<double>(tail) / static_cast<double>(slots);
-    if (now - spread < kStreamKMinGain) return sk;
     const int64_t work = tail * k_tiles;
     int64_t blocks = slots;
-    if (work / blocks < kStreamKMinKTiles) return sk;
+    if (blocks > work / kStreamKMinKTiles) blocks = work / kStreamKMinKTiles;
+    if (blocks > kStreamKMaxSegments * tail) blocks = kStreamKMaxSegments * tail;
+    if (blocks < tail) return sk;
+    const double as_tiles = static_cast<double>((tail + num_sms - 1) / num_sms);
+    const double spread = static_cast<double>((blocks + num_sms - 1) / num_sms) * static_cast<double>(tail) /
+                          static_cast<double>(blocks);
+    if ((as_tiles - spread) / static_cast<double>(per_sm) < kStreamKMinGain) return sk;
+    if (work / blocks < kStreamKLongKTiles) {
+        int64_t alt_ctas = tail, alt_k = k_tiles;  // the alternative: CTAs, k tiles each
+        if (tiles <= slots) {
+            const int64_t ks = k_per_slice(e, aligned, M, N, K, num_sms);
+            alt_ctas = tiles * ((K + ks - 1) / ks);
+            alt_k = (ks + e.cfg.tile_k - 1) / e.cfg.tile_k;
+        }
+        const double alt_t = static_cast<double>((alt_ctas + num_sms - 1) / num_sms) * static_cast<double>(alt_k);
+        const double sk_t = static_cast<double>((blocks + num_sms - 1) / num_sms) * static_cast<double>(work) /
+                            static_cast<double>(blocks);
+        if (sk_t > 0.5 * alt_t && sk_t + kStreamKOverheadKTiles > alt_t) return sk;
+    }
     sk.dp_tiles = static_cast<int>(tiles - tail);
     sk.blocks = static_cast<int>(blocks);
     sk.work = work;
@@ -456,10 +508,11 @@ size_t sgemm_workspace_bytes(int index, int64_t M, int64_t N, int64_t K, const f
                              const float* B, const float* C, int num_sms) {
     const Entry& e = kEntries[index];
     const bool aligned = sgemm_is_aligned(index, M, N, K, A, B, C);
+    const StreamK sk = streamk_plan(e, aligned, M, N, K, num_sms);
+    if (sk.blocks > 0) return static_cast<size_t>(2 * sk.blocks) * e.cfg.tile_m * e.cfg.tile_n * 4;
     const int64_t ks = k_per_slice(e, aligned, M, N, K, num_sms);
     if (ks < K) return static_cast<size_t>((K + ks - 1) / ks) * static_cast<size_t>(M * N) * 4;
-    const StreamK sk = streamk_plan(e, aligned, M, N, K, num_sms);
-    return static_cast<size_t>(2 * sk.blocks) * e.cfg.tile_m * e.cfg.tile_n * 4;
+    return 0;
 }
 
 cudaError_t sgemm_launch(int index, int64_t M, int64_t N, int64_t K, float alpha,
@@ -474,12 +527,14 @@ cudaError_t sgemm_launch(int index, int64_t M, int64_t N, int64_t K, float alpha
     if (err != cudaSuccess) return err;
     const int64_t tiles = ((M + e.cfg.tile_m - 1) / e.cfg.tile_m) * ((N + e.cfg.tile_n - 1) / e.cfg.tile_n);
     if (tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
-    int64_t ks = k_per_slice(e, aligned, M, N, K, num_sms);
+    // a stream-K spread of the last wave (or of the whole grid) first; else a grid too small
+    // for the GPU split along K; else tiles only (no scratch: tiles only)
+    StreamK sk{0, 0, 0, nullptr};
+    if (workspace != nullptr) sk = streamk_plan(e, aligned, M, N, K, num_sms);
+    int64_t ks = sk.blocks > 0 ? K : k_per_slice(e, aligned, M, N, K, num_sms);
     if (workspace == nullptr) ks = K;
     const int64_t slices = (K + ks - 1) / ks;
     float* partial = slices > 1 ? static_cast<float*>(workspace) : nullptr;
-    StreamK sk{0, 0, 0, nullptr};
-    if (slices == 1 && workspace != nullptr) sk = streamk_plan(e, aligned, M, N, K, num_sms);
     if (sk.blocks > 0) {
         // the stream-K blocks first, one per CTA slot: they fill the GPU on their own
         StreamKFn skf = aligned ? e.sk_aligned : e.sk_masked;
@@ -494,14 +549,15 @@ cudaError_t sgemm_launch(int index, int64_t M, int64_t N, int64_t K, float alpha
         // then the tail tiles of C, while the partial tiles are still in L2 (the whole tiles
         // below write other elements of C)
         const int vec = (N % 4 == 0) && ((reinterpret_cast<uintptr_t>(C) & 15u) == 0);
-        streamk_fixup_kernel<<<static_cast<unsigned>(tiles - sk.dp_tiles), e.cfg.tile_m * e.cfg.tile_n / (4 * kFixupVec),
-                               0, stream>>>(
+        const int parts = e.cfg.tile_m * e.cfg.tile_n / (4 * kFixupVec * kFixupThreads);
+        streamk_fixup_kernel<<<static_cast<unsigned>((tiles - sk.dp_tiles) * parts), kFixupThreads, 0, stream>>>(
             sk, static_cast<int>((K + e.cfg.tile_k - 1) / e.cfg.tile_k), e.cfg.tile_m, e.cfg.tile_n,
             static_cast<int>(M), static_cast<int>(N), alpha, beta, C, vec);
         err = launched(cudaGetLastError());
         if (err != cudaSuccess) return err;
     }
     const int64_t grid = sk.blocks > 0 ? sk.dp_tiles : tiles;
+    if (grid == 0) return cudaSuccess;  // the whole grid went to the stream-K blocks
     fn<<<dim3(static_cast<unsigned>(grid), static_cast<unsigned>(slices)), kThreads, e.smem_bytes, stream>>>(
         A, B, C, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), alpha, beta,
         static_cast<int>(ks), partial);

@@ -1,14 +1,13 @@
-"""The stream-K tail of the f32 GEMM on a GB300, through phx_sgemm, against the oracle.
+"""Stream-K schedules of the f32 GEMM on a GB300, through phx_sgemm, against the oracle.
 
-A grid of more than one wave whose last wave would leave SMs idle runs its whole waves as
-tiles and spreads the k tiles of the remaining tiles evenly over one block per CTA slot;
-each tail tile is then the sum, in k order, of up to a few partial tiles ("gemm, f32",
-sections "One output tile per CTA" and "Tuning": the same products, only split along k).
-The shapes below give the 128 x 128 tile (two CTAs per SM, 304 slots on 152 SMs) grids of
-324, 342 and 1088 tiles: tails of 20, 38 and 176 tiles, aligned and masked, with K long
-enough for at least 8 k tiles per block.  Integer inputs must match the oracle bit for bit
-(every partial sum is exact), uniform ones within 8 * sqrt(K) * 2^-24 * (|alpha| sum|a||b| +
-|beta||C|).
+A grid whose last wave would leave SMs idle -- or a grid of less than one wave -- spreads the
+k tiles of that wave's tiles evenly over stream-K blocks; each such tile is then the sum, in
+k order, of a few partial tiles ("gemm, f32", sections "One output tile per CTA" and
+"Tuning": the same products, only split along k).  With the 128 x 128 tile (two CTAs per
+SM, 304 slots on 152 SMs) the shapes below give: tails of 20, 38 and 176 tiles after whole
+waves, aligned and masked; and whole grids of 4, 16, 64 (masked) and 128 tiles spread over
+8 to 304 blocks.  Integer inputs must match the oracle bit for bit (every partial sum is
+exact), uniform ones within 8 * sqrt(K) * 2^-24 * (|alpha| sum|a||b| + |beta||C|).
 """
 import numpy as np
 import pytest
@@ -41,8 +40,9 @@ def _check(M, N, K, alpha, beta, dist, seed):
     return got
 
 
-@pytest.mark.parametrize("shape", [(2304, 2304, 2048), (2300, 2310, 2000), (4096, 4352, 512)])
-def test_streamk_tail_parity(shape):
+@pytest.mark.parametrize("shape", [(2304, 2304, 2048), (2300, 2310, 2000), (4096, 4352, 512),
+                                   (256, 256, 256), (512, 512, 512), (1000, 1000, 8000), (16384, 128, 4096)])
+def test_streamk_parity(shape):
     M, N, K = shape
     _check(M, N, K, 1.5, 0.5, "int3", seed=31)
     _check(M, N, K, 2.0, -1.0, "uniform", seed=32)
@@ -68,13 +68,15 @@ def test_streamk_special_values_and_determinism():
 
 
 def test_profile_counts_the_kernels_of_each_schedule():
-    # on 152 SMs with the 128 x 128 tile: a tail spread as stream-K blocks launches three
-    # kernels (stream-K blocks, whole tiles, fix-up), one wave of tiles one, and a grid too
-    # small for the GPU split along K two (the slices and their reduction)
+    # on 152 SMs with the 128 x 128 tile: whole waves plus a tail spread as stream-K blocks
+    # launch three kernels (stream-K blocks, fix-up, whole tiles); one wave of tiles, one; a
+    # grid split along K, two (the slices and their reduction); a grid spread whole as
+    # stream-K blocks, two (the blocks and the fix-up)
     import torch
     if torch.cuda.get_device_properties(0).multi_processor_count != 152:
         pytest.skip("the schedules below are those of a 152-SM GPU")
-    for shape, kernels in (((2304, 2304, 2048), 3), ((2048, 2048, 256), 1), ((128, 128, 16384), 2)):
+    for shape, kernels in (((2304, 2304, 2048), 3), ((2048, 2048, 256), 1), ((1024, 1024, 1024), 2),
+                           ((128, 128, 16384), 2)):
         M, N, K = shape
         A, B, C = synth.problem(M, N, K, seed=36, dist="int3")
         phx.profile_start()
