@@ -49,9 +49,12 @@ bool sgemm_is_aligned(int index, int64_t M, int64_t N, int64_t K, const float* A
 size_t sgemm_workspace_bytes(int index, int64_t M, int64_t N, int64_t K, const float* A,
                              const float* B, const float* C, int num_sms);
 
-// Enqueue config `index` (aligned or masked kernel as decided by sgemm_is_aligned), split
-// along K when sgemm_workspace_bytes says so and `workspace` holds that many bytes (with
-// workspace == nullptr it never splits), followed by the reduction of the slices.
+// Enqueue config `index` (the aligned kernel when sgemm_is_aligned; else the kernel with
+// 16-byte edge copies when K % 4 == N % 4 == 0 and A, B, C are 16-byte aligned; else the one
+// with 4-byte edge copies).  When sgemm_workspace_bytes is not 0 and `workspace` holds that
+// many bytes, the last partial wave (or a grid of less than one wave) is spread as stream-K
+// blocks and then fixed up, or a small grid is split along K and then reduced; with
+// workspace == nullptr the grid runs as tiles only.
 // Requires M, N > 0, K > 0 and alpha != 0 (the caller handles the degenerate cases).
 cudaError_t sgemm_launch(int index, int64_t M, int64_t N, int64_t K, float alpha,
                          const float* A, const float* B, float beta, float* C, void* workspace,

@@ -11,9 +11,11 @@
 //     with cp.async, so the copies of the next STAGES-1 panels overlap the math on the
 //     current one (the @pipeline double buffering, generalised to STAGES >= 2).
 //   * Aligned path: both panels move as 16-byte cp.async.cg copies (the @aligned promise:
-//     no masks, 16-byte vector loads).  Masked path: 4-byte cp.async.ca copies whose
-//     source size is 0 past an edge, which writes zeros ("extra 128-byte lines, masked
-//     elements"); stores past an edge are skipped.  Both paths compute the same values.
+//     no masks, 16-byte vector loads).  Masked paths: when rows are still 16 bytes apart
+//     (K % 4 == N % 4 == 0, aligned bases), 16-byte copies whose source size is 0 past an
+//     edge; otherwise 4-byte cp.async.ca copies of that kind ("extra 128-byte lines, masked
+//     elements").  Either writes zeros past an edge, and stores past an edge are skipped.
+//     All paths compute the same values.
 //   * The output tile is split over 8 warps (4 x 2) and each warp's tile over its 32 lanes
 //     (4 x 8); every thread owns a TM x TN register micro-tile of accumulators, as the
 //     lab's register-tiling rung does (Part 2, "register tiling"; Part 2, "The register
@@ -63,6 +65,21 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const float* src, bool 
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const float* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
 }
+
+// 16-byte asynchronous copy that, with pred false, reads nothing and writes 16 zero bytes.
+__device__ __forceinline__ void cp_async_16_zfill(uint32_t dst, const float* src, bool pred) {
+    const int bytes = pred ? 16 : 0;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(bytes)
+                 : "memory");
+}
+
+// How a kernel treats the edges of the matrices: every dimension a whole number of tiles and
+// 16-byte rows (none); rows 16 bytes apart (K % 4 == N % 4 == 0, 16-byte aligned bases) and
+// tiles past M, N or K (vec: 16-byte copies and stores, pieces past an edge zero or
+// skipped); anything else (scalar: 4-byte copies and stores).
+constexpr int kEdgeNone = 0;
+constexpr int kEdgeScalar = 1;
+constexpr int kEdgeVec = 2;
 
 __device__ __forceinline__ void cp_async_commit() {
     asm volatile("cp.async.commit_group;\n" ::: "memory");
@@ -122,20 +139,20 @@ __host__ __device__ __forceinline__ int64_t streamk_begin(int64_t s, int64_t wor
 // k slice of a split grid), into C (or the slice's plane of `partial`).  With LOCAL: k
 // tiles [kt0, kt1) of `tile`, alpha = 1 and beta = 0, into the BM x BN tile of partial sums
 // at C (element (row, col) at C[(row - m0) * BN + col - n0]).
-template <int BM, int BN, int BK, int STAGES, int TM, int TN, bool MASKED, bool FMA2, bool LOCAL>
+template <int BM, int BN, int BK, int STAGES, int TM, int TN, int EDGE, bool FMA2, bool LOCAL>
 __device__ __forceinline__ void sgemm_tile(const float* __restrict__ A, const float* __restrict__ B,
                                            float* __restrict__ C, int M, int N, int K, float alpha, float beta,
                                            int k_slice, float* __restrict__ partial, int tile, int kt0, int kt1) {
 #include "sgemm_tile_body.inc"
 }
 
-template <int BM, int BN, int BK, int STAGES, int TM, int TN, bool MASKED, bool FMA2, int MINB>
+template <int BM, int BN, int BK, int STAGES, int TM, int TN, int EDGE, bool FMA2, int MINB>
 __global__ void __launch_bounds__(kThreads, MINB)
 sgemm_kernel(const float* __restrict__ A, const float* __restrict__ B, float* __restrict__ C,
              int M, int N, int K, float alpha, float beta, int k_slice, float* __restrict__ partial) {
-    if constexpr (!MASKED) {
-        sgemm_tile<BM, BN, BK, STAGES, TM, TN, false, FMA2, false>(A, B, C, M, N, K, alpha, beta, k_slice, partial, 0,
-                                                                   0, 0);
+    if constexpr (EDGE != kEdgeScalar) {
+        sgemm_tile<BM, BN, BK, STAGES, TM, TN, EDGE, FMA2, false>(A, B, C, M, N, K, alpha, beta, k_slice, partial, 0,
+                                                                  0, 0);
     } else {
         constexpr bool LOCAL = false;
         int tile = 0;
@@ -147,7 +164,7 @@ sgemm_kernel(const float* __restrict__ A, const float* __restrict__ B, float* __
 // Stream-K block s: k tiles [streamk_begin(s), streamk_begin(s + 1)) of the tail tiles'
 // k tiles laid end to end, as at most two segments (the end of one tile, the start of the
 // next), each written as a BM x BN tile of partial sums to slot 2s + segment.
-template <int BM, int BN, int BK, int STAGES, int TM, int TN, bool MASKED, bool FMA2, int MINB>
+template <int BM, int BN, int BK, int STAGES, int TM, int TN, int EDGE, bool FMA2, int MINB>
 __global__ void __launch_bounds__(kThreads, MINB)
 sgemm_streamk_kernel(const float* __restrict__ A, const float* __restrict__ B, int M, int N, int K,
                      const StreamK sk) {
@@ -162,7 +179,7 @@ sgemm_streamk_kernel(const float* __restrict__ A, const float* __restrict__ B, i
         const int kt0 = static_cast<int>(it - static_cast<int64_t>(t) * k_tiles);
         const int kt1 = static_cast<int>(min(static_cast<int64_t>(k_tiles), kt0 + (end - it)));
         if (seg > 0) __syncthreads();  // the first segment is done with the shared buffers
-        sgemm_tile<BM, BN, BK, STAGES, TM, TN, MASKED, FMA2, true>(A, B, sk.slots + (2 * s + seg) * (BM * BN), M, N, K,
+        sgemm_tile<BM, BN, BK, STAGES, TM, TN, EDGE, FMA2, true>(A, B, sk.slots + (2 * s + seg) * (BM * BN), M, N, K,
                                                                    1.f, 0.f, 0, nullptr, sk.dp_tiles + t, kt0, kt1);
         it += kt1 - kt0;
         ++seg;
@@ -355,10 +372,8 @@ using StreamKFn = void (*)(const float*, const float*, int, int, int, StreamK);
 
 struct Entry {
     SgemmConfig cfg;
-    KernelFn aligned;
-    KernelFn masked;
-    StreamKFn sk_aligned;  // the stream-K blocks of the same tile shape
-    StreamKFn sk_masked;
+    KernelFn fn[3];   // tile kernel by edge mode (kEdgeNone, kEdgeScalar, kEdgeVec)
+    StreamKFn sk[3];  // the stream-K blocks of the same tile shape
     int smem_bytes;
 };
 
@@ -369,10 +384,12 @@ constexpr Entry make_entry() {
     // up to 64 accumulators a thread: two CTAs per SM (128 registers); 128: one CTA
     constexpr int MINB = TM * TN > 64 ? 1 : 2;
     return Entry{SgemmConfig{BM, BN, BK, STAGES, FMA2},
-                 &sgemm_kernel<BM, BN, BK, STAGES, TM, TN, false, FMA2 != 0, MINB>,
-                 &sgemm_kernel<BM, BN, BK, STAGES, TM, TN, true, FMA2 != 0, MINB>,
-                 &sgemm_streamk_kernel<BM, BN, BK, STAGES, TM, TN, false, FMA2 != 0, MINB>,
-                 &sgemm_streamk_kernel<BM, BN, BK, STAGES, TM, TN, true, FMA2 != 0, MINB>,
+                 {&sgemm_kernel<BM, BN, BK, STAGES, TM, TN, kEdgeNone, FMA2 != 0, MINB>,
+                  &sgemm_kernel<BM, BN, BK, STAGES, TM, TN, kEdgeScalar, FMA2 != 0, MINB>,
+                  &sgemm_kernel<BM, BN, BK, STAGES, TM, TN, kEdgeVec, FMA2 != 0, MINB>},
+                 {&sgemm_streamk_kernel<BM, BN, BK, STAGES, TM, TN, kEdgeNone, FMA2 != 0, MINB>,
+                  &sgemm_streamk_kernel<BM, BN, BK, STAGES, TM, TN, kEdgeScalar, FMA2 != 0, MINB>,
+                  &sgemm_streamk_kernel<BM, BN, BK, STAGES, TM, TN, kEdgeVec, FMA2 != 0, MINB>},
                  sgemm_smem_floats(BM, BN, BK, STAGES) * 4};
 }
 
@@ -406,6 +423,17 @@ bool sgemm_is_aligned(int index, int64_t M, int64_t N, int64_t K, const float* A
 
 namespace {
 
+// The edge mode of config `index` for this problem (see kEdgeNone).
+int sgemm_edge(int index, int64_t M, int64_t N, int64_t K, const float* A, const float* B, const float* C) {
+    if (sgemm_is_aligned(index, M, N, K, A, B, C)) return kEdgeNone;
+    auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    return (K % 4 == 0 && N % 4 == 0 && al16(A) && al16(B) && al16(C)) ? kEdgeVec : kEdgeScalar;
+}
+
+}  // namespace
+
+namespace {
+
 // CTAs of `fn` that fit on one SM at once (cached per kernel).
 int ctas_per_sm(KernelFn fn, int smem) {
     static std::mutex mu;
@@ -430,9 +458,9 @@ constexpr int kMinKTilesPerSlice = 16;
 
 // Elements of K per slice when a grid too small for the GPU is split along K (the grid
 // gets one row of CTAs per slice); K itself when it is not split.
-int64_t k_per_slice(const Entry& e, bool aligned, int64_t M, int64_t N, int64_t K, int num_sms) {
+int64_t k_per_slice(const Entry& e, int edge, int64_t M, int64_t N, int64_t K, int num_sms) {
     const int64_t tiles = ((M + e.cfg.tile_m - 1) / e.cfg.tile_m) * ((N + e.cfg.tile_n - 1) / e.cfg.tile_n);
-    const int64_t slots = static_cast<int64_t>(ctas_per_sm(aligned ? e.aligned : e.masked, e.smem_bytes)) * num_sms;
+    const int64_t slots = static_cast<int64_t>(ctas_per_sm(e.fn[edge], e.smem_bytes)) * num_sms;
     const int64_t k_tiles = (K + e.cfg.tile_k - 1) / e.cfg.tile_k;
     if (num_sms <= 0 || 2 * tiles > slots) return K;
     int64_t split = slots / tiles;
@@ -466,10 +494,10 @@ constexpr int64_t kStreamKLongKTiles = 64;
 constexpr int64_t kStreamKMaxSegments = 8;
 constexpr double kStreamKOverheadKTiles = 12.0;
 
-StreamK streamk_plan(const Entry& e, bool aligned, int64_t M, int64_t N, int64_t K, int num_sms) {
+StreamK streamk_plan(const Entry& e, int edge, int64_t M, int64_t N, int64_t K, int num_sms) {
     StreamK sk{0, 0, 0, nullptr};
     const int64_t tiles = ((M + e.cfg.tile_m - 1) / e.cfg.tile_m) * ((N + e.cfg.tile_n - 1) / e.cfg.tile_n);
-    const int64_t per_sm = ctas_per_sm(aligned ? e.aligned : e.masked, e.smem_bytes);
+    const int64_t per_sm = ctas_per_sm(e.fn[edge], e.smem_bytes);
     const int64_t slots = per_sm * num_sms;
     const int64_t k_tiles = (K + e.cfg.tile_k - 1) / e.cfg.tile_k;
     if (num_sms <= 0 || tiles <= 0) return sk;
@@ -487,7 +515,7 @@ StreamK streamk_plan(const Entry& e, bool aligned, int64_t M, int64_t N, int64_t
     if (work / blocks < kStreamKLongKTiles) {
         int64_t alt_ctas = tail, alt_k = k_tiles;  // the alternative: CTAs, k tiles each
         if (tiles <= slots) {
-            const int64_t ks = k_per_slice(e, aligned, M, N, K, num_sms);
+            const int64_t ks = k_per_slice(e, edge, M, N, K, num_sms);
             alt_ctas = tiles * ((K + ks - 1) / ks);
             alt_k = (ks + e.cfg.tile_k - 1) / e.cfg.tile_k;
         }
@@ -507,10 +535,10 @@ StreamK streamk_plan(const Entry& e, bool aligned, int64_t M, int64_t N, int64_t
 size_t sgemm_workspace_bytes(int index, int64_t M, int64_t N, int64_t K, const float* A,
                              const float* B, const float* C, int num_sms) {
     const Entry& e = kEntries[index];
-    const bool aligned = sgemm_is_aligned(index, M, N, K, A, B, C);
-    const StreamK sk = streamk_plan(e, aligned, M, N, K, num_sms);
+    const int edge = sgemm_edge(index, M, N, K, A, B, C);
+    const StreamK sk = streamk_plan(e, edge, M, N, K, num_sms);
     if (sk.blocks > 0) return static_cast<size_t>(2 * sk.blocks) * e.cfg.tile_m * e.cfg.tile_n * 4;
-    const int64_t ks = k_per_slice(e, aligned, M, N, K, num_sms);
+    const int64_t ks = k_per_slice(e, edge, M, N, K, num_sms);
     if (ks < K) return static_cast<size_t>((K + ks - 1) / ks) * static_cast<size_t>(M * N) * 4;
     return 0;
 }
@@ -519,8 +547,8 @@ cudaError_t sgemm_launch(int index, int64_t M, int64_t N, int64_t K, float alpha
                          const float* A, const float* B, float beta, float* C, void* workspace,
                          int num_sms, cudaStream_t stream) {
     const Entry& e = kEntries[index];
-    const bool aligned = sgemm_is_aligned(index, M, N, K, A, B, C);
-    KernelFn fn = aligned ? e.aligned : e.masked;
+    const int edge = sgemm_edge(index, M, N, K, A, B, C);
+    KernelFn fn = e.fn[edge];
     cudaError_t err = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            e.smem_bytes);
@@ -530,14 +558,14 @@ cudaError_t sgemm_launch(int index, int64_t M, int64_t N, int64_t K, float alpha
     // a stream-K spread of the last wave (or of the whole grid) first; else a grid too small
     // for the GPU split along K; else tiles only (no scratch: tiles only)
     StreamK sk{0, 0, 0, nullptr};
-    if (workspace != nullptr) sk = streamk_plan(e, aligned, M, N, K, num_sms);
-    int64_t ks = sk.blocks > 0 ? K : k_per_slice(e, aligned, M, N, K, num_sms);
+    if (workspace != nullptr) sk = streamk_plan(e, edge, M, N, K, num_sms);
+    int64_t ks = sk.blocks > 0 ? K : k_per_slice(e, edge, M, N, K, num_sms);
     if (workspace == nullptr) ks = K;
     const int64_t slices = (K + ks - 1) / ks;
     float* partial = slices > 1 ? static_cast<float*>(workspace) : nullptr;
     if (sk.blocks > 0) {
         // the stream-K blocks first, one per CTA slot: they fill the GPU on their own
-        StreamKFn skf = aligned ? e.sk_aligned : e.sk_masked;
+        StreamKFn skf = e.sk[edge];
         err = cudaFuncSetAttribute(reinterpret_cast<const void*>(skf), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    e.smem_bytes);
         if (err != cudaSuccess) return err;

@@ -321,3 +321,38 @@ def test_tc_epilogue_unaligned_c():
     torch.cuda.synchronize()
     assert st == phx.PHX_OK
     assert_bits_equal(dC.cpu().numpy()[1:].reshape(M, N), want, "C 4-byte aligned")
+
+
+# ----------------------------------------------------------------------------------------
+# The f32 kernel's vector edge path: M or N (or K) not a whole number of tiles, but rows 16
+# bytes apart (K % 4 == N % 4 == 0, 16-byte aligned bases), so the copies stay 16 bytes wide
+# and zero-fill past the edges.  Both it and the scalar edge path, which the same operands
+# take when they start 4 bytes past a 16-byte boundary, against the oracle (the two kernels
+# may differ in occupancy, and so in how a small grid's k sums are grouped).
+# ----------------------------------------------------------------------------------------
+@pytest.mark.parametrize("shape", [(301, 260, 200), (129, 132, 20), (2000, 2048, 512), (1000, 1000, 8000),
+                                   (60, 4096, 1024), (49, 4, 4), (250, 4, 1000)])
+def test_sgemm_vector_edge_path(shape):
+    import torch
+    M, N, K = shape
+    for dist, seed in (("int3", 41), ("uniform", 42)):
+        A, B, C = synth.problem(M, N, K, seed=seed, dist=dist)
+        want, mag = oracle.gemm(A, B, C, 1.5, -0.5, f16_inputs=False)
+        out = {}
+        for offset in (0, 1):
+            def dev(x):
+                flat = torch.zeros(x.size + 4, dtype=torch.float32)
+                flat[offset:offset + x.size] = torch.from_numpy(np.ascontiguousarray(x).reshape(-1))
+                return flat.cuda()
+            dA, dB, dC = dev(A), dev(B), dev(C)
+            st = phx.phx_sgemm(M, N, K, 1.5, dA.data_ptr() + 4 * offset, dB.data_ptr() + 4 * offset, -0.5,
+                               dC.data_ptr() + 4 * offset, torch.cuda.current_stream().cuda_stream)
+            torch.cuda.synchronize()
+            assert st == phx.PHX_OK, phx.status_string(st)
+            out[offset] = dC.cpu().numpy()[offset:offset + M * N].reshape(M, N)
+        for offset, path in ((0, "vector"), (1, "scalar")):
+            what = f"sgemm edges {shape} {dist} ({path})"
+            if dist == "int3":
+                assert_bits_equal(out[offset], want, what)
+            else:
+                assert_within_bound(out[offset], want, mag, C, K, 1.5, -0.5, what)
