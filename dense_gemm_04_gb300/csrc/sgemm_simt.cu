@@ -113,15 +113,16 @@ __host__ __device__ constexpr int sgemm_smem_floats(int bm, int bn, int bk, int 
     return stages * bm * bk + 2 * bk * at_row_stride(bm) + stages * bk * bn;
 }
 
-// Stream-K tail.  A grid of more than one wave whose last wave would leave SMs idle runs
-// its whole waves as tiles (sgemm_kernel over tiles [0, dp_tiles)) and spreads the k tiles
-// of the remaining (tail) tiles evenly over `blocks` blocks of sgemm_streamk_kernel, one
-// per CTA slot of the GPU, launched first so that they fill the GPU together: block s takes
-// k tiles [s * work / blocks, (s + 1) * work / blocks) of the tail's k tiles laid end to end
-// (tile after tile).  streamk_fixup_kernel then adds each tail tile's partial tiles in k
-// order and applies alpha and beta, before the whole tiles run (while the partial tiles
-// are still in L2).  The tail thus takes the same time on every slot, instead of leaving
-// SMs idle for a fraction of a wave.
+// Stream-K.  A grid whose last, partial wave would leave SMs idle -- or a grid of less than
+// one wave -- runs its whole waves as tiles (sgemm_kernel over tiles [0, dp_tiles)) and
+// spreads the k tiles of the remaining (tail) tiles evenly over `blocks` blocks of
+// sgemm_streamk_kernel, at most one per CTA slot of the GPU, launched first so that they
+// fill the GPU together: block s takes k tiles [s * work / blocks, (s + 1) * work / blocks)
+// of the tail's k tiles laid end to end (tile after tile).  streamk_fixup_kernel then adds
+// each tail tile's partial tiles in k order and applies alpha and beta, before the whole
+// tiles run (while the partial tiles are still in L2).  The tail thus takes the same time
+// on every block, instead of leaving SMs idle for a fraction of a wave.  (streamk_plan
+// decides when, and how many blocks.)
 struct StreamK {
     int dp_tiles;   // tiles [0, dp_tiles) are whole tiles; the rest are the tail
     int blocks;     // stream-K blocks (0: none)
