@@ -60,6 +60,15 @@ cudaError_t sgemm_launch(int index, int64_t M, int64_t N, int64_t K, float alpha
                          const float* A, const float* B, float beta, float* C, void* workspace,
                          int num_sms, cudaStream_t stream);
 
+// Host check of the f32 GEMM's schedule for config `index` with `per_sm` CTAs per SM on
+// `num_sms` SMs (no device involved): out[0] tiles that run whole (all of them without a
+// stream-K part; each split into out[3] slices when the grid is split along K), out[1]
+// stream-K blocks, out[2] their k tiles, out[3] K slices of a grid split along K (1: none),
+// out[4] the most tile segments one stream-K block writes, out[5] 1 if, for every spread
+// tile, the slots the fix-up reads are, in k order, exactly the segments the blocks write
+// for it and those cover its k tiles once, else 0.
+void sgemm_schedule_selftest(int index, int64_t M, int64_t N, int64_t K, int per_sm, int num_sms, int64_t out[6]);
+
 // C <- alpha * (P[0] + ... + P[slices-1]) + beta * C, where P[s] is the s-th M x N plane of
 // `partial`, added in that order (beta == 0: C not read).  Finishes a GEMM split along K.
 cudaError_t splitk_reduce_launch(const float* partial, int slices, int64_t M, int64_t N, float alpha,

@@ -909,6 +909,15 @@ phx_status phx_selftest_bounded_wait(uint64_t limit_ns, phx_stream_t stream) {
     return phx::selftest_wait_launch(limit_ns, d->status, stream) == cudaSuccess ? PHX_OK : PHX_ERR_LAUNCH;
 }
 
+phx_status phx_selftest_sgemm_schedule(int config, int64_t M, int64_t N, int64_t K, int ctas_per_sm, int num_sms,
+                                       int64_t* out) {
+    if (out == nullptr || config < 0 || config >= phx::sgemm_num_configs() || ctas_per_sm <= 0 || ctas_per_sm > 32 ||
+        num_sms <= 0 || num_sms > 4096 || M <= 0 || N <= 0 || K <= 0 || validate_sizes(M, N, K) != PHX_OK)
+        return PHX_ERR_INVALID;
+    phx::sgemm_schedule_selftest(config, M, N, K, ctas_per_sm, num_sms, out);
+    return PHX_OK;
+}
+
 phx_status phx_selftest_tuner(int n, const double* base_s, const int* fail, double noise,
                               double drift, int finalists, int rounds, uint64_t seed, int* picked,
                               int64_t* launches) {

@@ -37,9 +37,12 @@
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
+#include <array>
 #include <cstdint>
 #include <map>
 #include <mutex>
+#include <vector>
 
 #include "internal.h"
 
@@ -135,6 +138,14 @@ __host__ __device__ __forceinline__ int64_t streamk_begin(int64_t s, int64_t wor
     return s * work / blocks;
 }
 
+// The stream-K block whose range contains k tile `lo` (of the tail's, end to end).
+__host__ __device__ __forceinline__ int64_t streamk_first_block(int64_t lo, int64_t work, int64_t blocks) {
+    int64_t b = lo * blocks / work;
+    while (b > 0 && streamk_begin(b, work, blocks) > lo) --b;
+    while (b + 1 < blocks && streamk_begin(b + 1, work, blocks) <= lo) ++b;
+    return b;
+}
+
 // One output tile, or a k range of one: the CTA's whole computation, shared by the tile
 // kernel and the stream-K kernel below.  Without LOCAL: tile blockIdx.x, whole K (or the
 // k slice of a split grid), into C (or the slice's plane of `partial`).  With LOCAL: k
@@ -207,10 +218,7 @@ __global__ void __launch_bounds__(kFixupThreads) streamk_fixup_kernel(StreamK sk
     const int part = static_cast<int>(blockIdx.x) - t * parts;
     const int64_t lo = static_cast<int64_t>(t) * k_tiles;
     const int64_t hi = lo + k_tiles;
-    // the first stream-K block whose range contains k tile lo
-    int64_t b = lo * sk.blocks / sk.work;
-    while (b > 0 && streamk_begin(b, sk.work, sk.blocks) > lo) --b;
-    while (b + 1 < sk.blocks && streamk_begin(b + 1, sk.work, sk.blocks) <= lo) ++b;
+    int64_t b = streamk_first_block(lo, sk.work, sk.blocks);
     int pm, pn;
     tile_coords(sk.dp_tiles + t, (M + bm - 1) / bm, (N + bn - 1) / bn, pm, pn);
     const int m0 = pm * bm, n0 = pn * bn;
@@ -459,16 +467,22 @@ constexpr int kMinKTilesPerSlice = 16;
 
 // Elements of K per slice when a grid too small for the GPU is split along K (the grid
 // gets one row of CTAs per slice); K itself when it is not split.
-int64_t k_per_slice(const Entry& e, int edge, int64_t M, int64_t N, int64_t K, int num_sms) {
-    const int64_t tiles = ((M + e.cfg.tile_m - 1) / e.cfg.tile_m) * ((N + e.cfg.tile_n - 1) / e.cfg.tile_n);
-    const int64_t slots = static_cast<int64_t>(ctas_per_sm(e.fn[edge], e.smem_bytes)) * num_sms;
-    const int64_t k_tiles = (K + e.cfg.tile_k - 1) / e.cfg.tile_k;
-    if (num_sms <= 0 || 2 * tiles > slots) return K;
+// The split for `tiles` tiles of `k_tiles` k tiles on `slots` CTA slots, in elements of K
+// per slice (K itself: no split).
+int64_t k_per_slice_core(int64_t tiles, int64_t k_tiles, int64_t slots, int tile_k, int64_t K) {
+    if (slots <= 0 || 2 * tiles > slots) return K;
     int64_t split = slots / tiles;
     if (split > kMaxSplit) split = kMaxSplit;
     if (split > k_tiles / kMinKTilesPerSlice) split = k_tiles / kMinKTilesPerSlice;
     if (split < 2) return K;
-    return (k_tiles + split - 1) / split * e.cfg.tile_k;
+    return (k_tiles + split - 1) / split * tile_k;
+}
+
+int64_t k_per_slice(const Entry& e, int edge, int64_t M, int64_t N, int64_t K, int num_sms) {
+    const int64_t tiles = ((M + e.cfg.tile_m - 1) / e.cfg.tile_m) * ((N + e.cfg.tile_n - 1) / e.cfg.tile_n);
+    const int64_t slots = static_cast<int64_t>(ctas_per_sm(e.fn[edge], e.smem_bytes)) * num_sms;
+    const int64_t k_tiles = (K + e.cfg.tile_k - 1) / e.cfg.tile_k;
+    return k_per_slice_core(tiles, k_tiles, slots, e.cfg.tile_k, K);
 }
 
 // Stream-K plan (see StreamK).  The last, partial wave of the tile grid -- or the whole
@@ -495,13 +509,12 @@ constexpr int64_t kStreamKLongKTiles = 64;
 constexpr int64_t kStreamKMaxSegments = 8;
 constexpr double kStreamKOverheadKTiles = 12.0;
 
-StreamK streamk_plan(const Entry& e, int edge, int64_t M, int64_t N, int64_t K, int num_sms) {
+// The plan for `tiles` tiles of `k_tiles` k tiles (of tile_k values of K) with `per_sm` CTAs
+// per SM on `num_sms` SMs; no device queries, so it can be checked on the host.
+StreamK streamk_plan_core(int64_t tiles, int64_t k_tiles, int64_t per_sm, int64_t num_sms, int tile_k, int64_t K) {
     StreamK sk{0, 0, 0, nullptr};
-    const int64_t tiles = ((M + e.cfg.tile_m - 1) / e.cfg.tile_m) * ((N + e.cfg.tile_n - 1) / e.cfg.tile_n);
-    const int64_t per_sm = ctas_per_sm(e.fn[edge], e.smem_bytes);
     const int64_t slots = per_sm * num_sms;
-    const int64_t k_tiles = (K + e.cfg.tile_k - 1) / e.cfg.tile_k;
-    if (num_sms <= 0 || tiles <= 0) return sk;
+    if (num_sms <= 0 || per_sm <= 0 || tiles <= 0 || k_tiles <= 0) return sk;
     const int64_t tail = tiles > slots ? tiles % slots : tiles;
     if (tail == 0) return sk;
     const int64_t work = tail * k_tiles;
@@ -516,9 +529,9 @@ StreamK streamk_plan(const Entry& e, int edge, int64_t M, int64_t N, int64_t K, 
     if (work / blocks < kStreamKLongKTiles) {
         int64_t alt_ctas = tail, alt_k = k_tiles;  // the alternative: CTAs, k tiles each
         if (tiles <= slots) {
-            const int64_t ks = k_per_slice(e, edge, M, N, K, num_sms);
+            const int64_t ks = k_per_slice_core(tiles, k_tiles, slots, tile_k, K);
             alt_ctas = tiles * ((K + ks - 1) / ks);
-            alt_k = (ks + e.cfg.tile_k - 1) / e.cfg.tile_k;
+            alt_k = (ks + tile_k - 1) / tile_k;
         }
         const double alt_t = static_cast<double>((alt_ctas + num_sms - 1) / num_sms) * static_cast<double>(alt_k);
         const double sk_t = static_cast<double>((blocks + num_sms - 1) / num_sms) * static_cast<double>(work) /
@@ -531,7 +544,66 @@ StreamK streamk_plan(const Entry& e, int edge, int64_t M, int64_t N, int64_t K, 
     return sk;
 }
 
+StreamK streamk_plan(const Entry& e, int edge, int64_t M, int64_t N, int64_t K, int num_sms) {
+    const int64_t tiles = ((M + e.cfg.tile_m - 1) / e.cfg.tile_m) * ((N + e.cfg.tile_n - 1) / e.cfg.tile_n);
+    const int64_t k_tiles = (K + e.cfg.tile_k - 1) / e.cfg.tile_k;
+    return streamk_plan_core(tiles, k_tiles, ctas_per_sm(e.fn[edge], e.smem_bytes), num_sms, e.cfg.tile_k, K);
+}
+
 }  // namespace
+
+void sgemm_schedule_selftest(int index, int64_t M, int64_t N, int64_t K, int per_sm, int num_sms, int64_t out[6]) {
+    const Entry& e = kEntries[index];
+    const int64_t tiles = ((M + e.cfg.tile_m - 1) / e.cfg.tile_m) * ((N + e.cfg.tile_n - 1) / e.cfg.tile_n);
+    const int64_t k_tiles = (K + e.cfg.tile_k - 1) / e.cfg.tile_k;
+    const StreamK sk = streamk_plan_core(tiles, k_tiles, per_sm, num_sms, e.cfg.tile_k, K);
+    const int64_t ks = sk.blocks > 0 ? K
+                                     : k_per_slice_core(tiles, k_tiles, static_cast<int64_t>(per_sm) * num_sms,
+                                                        e.cfg.tile_k, K);
+    out[0] = sk.blocks > 0 ? sk.dp_tiles : tiles;
+    out[1] = sk.blocks;
+    out[2] = sk.work;
+    out[3] = (K + ks - 1) / ks;
+    out[4] = 0;
+    out[5] = 1;
+    if (sk.blocks == 0) return;
+    // the segments the stream-K blocks write, walked as sgemm_streamk_kernel walks them:
+    // (first k tile, end k tile, slot) per tail tile
+    const int64_t tail = tiles - sk.dp_tiles;
+    std::vector<std::vector<std::array<int64_t, 3>>> written(static_cast<size_t>(tail));
+    for (int64_t b = 0; b < sk.blocks; ++b) {
+        int64_t it = streamk_begin(b, sk.work, sk.blocks);
+        const int64_t end = streamk_begin(b + 1, sk.work, sk.blocks);
+        int64_t seg = 0;
+        while (it < end) {
+            const int64_t t = it / k_tiles;
+            const int64_t kt0 = it - t * k_tiles;
+            const int64_t kt1 = std::min(k_tiles, kt0 + (end - it));
+            written[static_cast<size_t>(t)].push_back({kt0, kt1, 2 * b + seg});
+            it += kt1 - kt0;
+            ++seg;
+        }
+        out[4] = std::max(out[4], seg);
+    }
+    // the slots the fix-up reads, walked as streamk_fixup_kernel walks them
+    for (int64_t t = 0; t < tail; ++t) {
+        const int64_t lo = t * k_tiles, hi = lo + k_tiles;
+        int64_t b = streamk_first_block(lo, sk.work, sk.blocks);
+        int64_t s0 = streamk_begin(b, sk.work, sk.blocks);
+        std::vector<int64_t> reads;
+        for (; b < sk.blocks && s0 < hi; ++b) {
+            const int64_t s1 = streamk_begin(b + 1, sk.work, sk.blocks);
+            if (s1 > s0) reads.push_back(2 * b + (s0 < lo ? 1 : 0));
+            s0 = s1;
+        }
+        const auto& w = written[static_cast<size_t>(t)];
+        bool ok = reads.size() == w.size() && !w.empty() && w.front()[0] == 0 && w.back()[1] == k_tiles;
+        for (size_t q = 0; ok && q < w.size(); ++q) {
+            ok = reads[q] == w[q][2] && (q == 0 || w[q - 1][1] == w[q][0]);
+        }
+        if (!ok) out[5] = 0;
+    }
+}
 
 size_t sgemm_workspace_bytes(int index, int64_t M, int64_t N, int64_t K, const float* A,
                              const float* B, const float* C, int num_sms) {

@@ -57,6 +57,7 @@ _SIGNATURES = {
     "phx_selftest_tuner": (_i32, [_i32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_i32),
                                   ctypes.c_double, ctypes.c_double, _i32, _i32, _u64,
                                   ctypes.POINTER(_i32), ctypes.POINTER(_i64)]),
+    "phx_selftest_sgemm_schedule": (_i32, [_i32, _i64, _i64, _i64, _i32, _i32, ctypes.POINTER(_i64)]),
     "phx_validate_args": (_i32, [_i64, _i64, _i64, _vp, _vp, _vp]),
     "phx_version": (_cp, []),
     "phx_profile_start": (_i32, []),
@@ -276,6 +277,16 @@ def profile_stop():
     ms = (ctypes.c_double * kinds)()
     check(phx_profile_stop(n, ms), "phx_profile_stop")
     return {KIND_NAMES[k]: (int(n[k]), float(ms[k])) for k in range(kinds)}
+
+
+def sgemm_schedule(config: str, M: int, N: int, K: int, ctas_per_sm: int = 2, num_sms: int = 152) -> dict:
+    """The f32 GEMM's schedule for `config` on a GPU of `num_sms` SMs, worked out on the host
+    (phx_selftest_sgemm_schedule)."""
+    out = (_i64 * 6)()
+    check(phx_selftest_sgemm_schedule(config_names(VARIANT_SGEMM).index(config), M, N, K, ctas_per_sm, num_sms, out),
+          "phx_selftest_sgemm_schedule")
+    keys = ("whole_tiles", "streamk_blocks", "streamk_k_tiles", "k_slices", "max_segments", "bookkeeping_ok")
+    return dict(zip(keys, (int(v) for v in out)))
 
 
 def validate_args(M, N, K, A, B, C) -> int:

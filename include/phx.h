@@ -300,6 +300,23 @@ phx_status phx_selftest_tuner(int n, const double* base_s, const int* fail, doub
                               double drift, int finalists, int rounds, uint64_t seed,
                               int* picked, int64_t* launches);
 
+/* The f32 GEMM's schedule for configuration `config` (an index of phx_config_name for
+ * PHX_VARIANT_SGEMM, not the skinny one) and shape (M, N, K), as it would be on a GPU with
+ * `num_sms` SMs and `ctas_per_sm` CTAs of that configuration per SM, worked out on the host
+ * without any GPU.  Writes six values to the caller's array out[6]:
+ *   out[0]  tiles that run whole: all of them without a stream-K part (each split into
+ *           out[3] K slices when the grid is split along K), else those before it;
+ *   out[1]  stream-K blocks (0: no stream-K part);
+ *   out[2]  the k tiles (TILE_K values of K each) those blocks share;
+ *   out[3]  K slices of a grid split along K (1: not split);
+ *   out[4]  the most tile segments one stream-K block writes (at most 2 by design);
+ *   out[5]  1 if, for every spread tile, the partial tiles the fix-up adds are, in k order,
+ *           exactly the ones the stream-K blocks write for it and cover its k tiles once;
+ *           else 0.
+ * PHX_ERR_INVALID for a bad configuration, shape or machine size. */
+phx_status phx_selftest_sgemm_schedule(int config, int64_t M, int64_t N, int64_t K, int ctas_per_sm,
+                                       int num_sms, int64_t* out);
+
 /* Argument validation as the GEMM calls perform it, without launching anything and
  * without touching the device: PHX_OK if (M, N, K, A, B, C) would be accepted. */
 phx_status phx_validate_args(int64_t M, int64_t N, int64_t K, const void* A, const void* B,
