@@ -77,10 +77,17 @@ enum { PHX_VARIANT_SGEMM = 0, PHX_VARIANT_F16TC = 1 };
  * multiply-add; the epilogue computes alpha * acc + beta * c_old in f32.  Tile-aligned
  * shapes with 16-byte aligned pointers take the aligned fast path, all others a masked
  * path (loads past an edge read zero, stores past an edge are skipped) that gives the
- * same result.  A grid too small to fill the GPU is split along K: each slice of K writes
- * its partial products to scratch taken, in stream order, from the library's pooled device
- * memory (PHX_ERR_NOMEM if that fails), and one more kernel sums the slices in slice order
- * and applies the epilogue, so results do not depend on timing.  Other shapes allocate
+ * same result; the masked path keeps 16-byte copies when K % 4 == N % 4 == 0 and the
+ * pointers are 16-byte aligned.
+ * Two schedules use scratch taken, in stream order, from the library's pooled device
+ * memory (PHX_ERR_NOMEM if that fails):
+ *   - stream-K: the k steps of a last, partial wave of tiles -- or of a whole grid of less
+ *     than one wave -- are shared evenly by one block per CTA slot, each writing partial
+ *     tiles, which one more kernel adds in k order before applying the epilogue;
+ *   - split-K: a grid too small to fill the GPU is split along K, each slice writing its
+ *     partial products, which one more kernel adds in slice order.
+ * The library picks between them and plain tiles by shape.  Either way the order of every
+ * sum is fixed by the shape, so results do not depend on timing.  Other shapes allocate
  * nothing. */
 phx_status phx_sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float* A,
                      const float* B, float beta, float* C, phx_stream_t stream);
