@@ -259,8 +259,8 @@ int default_config(int variant, int64_t M, int64_t N, int sms) {
 int default_tile_config(int variant, int64_t M, int64_t N, int sms) {
     if (variant == PHX_VARIANT_SGEMM) {
         const int64_t slots = 2 * static_cast<int64_t>(sms);  // two CTAs per SM
-        // 128 x 128 tiles whenever they exist: a grid too small for the GPU is then split
-        // along K, which keeps the larger, more efficient tile
+        // 128 x 128 tiles whenever they exist: a grid too small for the GPU is then spread as
+        // stream-K blocks or split along K, which keeps the larger, more efficient tile
         if (M >= 128 && N >= 128) return parse_config(variant, "TILE_M=128 TILE_N=128 TILE_K=16 STAGES=4 FMA2=1");
         if (ceil_div(M, 128) * ceil_div(N, 128) >= slots) return parse_config(variant, "TILE_M=128 TILE_N=128 TILE_K=16 STAGES=4 FMA2=1");
         if (ceil_div(M, 128) * ceil_div(N, 64) >= slots) return parse_config(variant, "TILE_M=128 TILE_N=64 TILE_K=8 STAGES=4");
@@ -451,7 +451,7 @@ phx_status launch_variant(int variant, int cfg, int64_t M, int64_t N, int64_t K,
     if (variant == PHX_VARIANT_SGEMM && (trans_a || trans_b))
         return launch_sgemm_transposed(cfg, trans_a, trans_b, M, N, K, alpha, A, B, beta, C, d, stream);
     if (variant == PHX_VARIANT_SGEMM) {
-        // pooled scratch only when a small grid is split along K
+        // pooled scratch only for a stream-K spread or a grid split along K
         const size_t bytes = phx::sgemm_workspace_bytes(cfg, M, N, K, A, B, C, d->sm_count);
         void* ws = nullptr;
         if (bytes > 0 && cudaMallocFromPoolAsync(&ws, bytes, d->pool, stream) != cudaSuccess) {

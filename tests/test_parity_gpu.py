@@ -232,8 +232,9 @@ def test_lab_error_levels():
 
 
 # ----------------------------------------------------------------------------------------
-# Small grids split along K (the slices' partial products added in slice order) and tiles
-# of a last, partial round dealt out as half-width items (tensor cores)
+# Small grids split along K (the slices' partial products added in slice order) or spread
+# as stream-K blocks (f32), and tiles of a last, partial round dealt out as half-width items
+# (tensor cores)
 # ----------------------------------------------------------------------------------------
 
 TAIL_SHAPES = [(640, 512, 2048), (650, 500, 2000), (5000, 300, 700), (4224, 4096, 256), (129, 257, 4100)]
