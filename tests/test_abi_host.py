@@ -242,3 +242,15 @@ def test_last_config_before_any_gemm():
     assert phx.last_config(phx.VARIANT_F16TC) == "NONE"
     with pytest.raises(phx.PhxError):
         phx.last_config(5)
+
+
+def test_profile_kinds_match_the_header():
+    # one name per PHX_KIND_* of include/phx.h, in order
+    import re
+    with open(phx.HEADER_PATH) as f:
+        text = f.read()
+    kinds = {m.group(1): int(m.group(2)) for m in re.finditer(r"PHX_KIND_([A-Z0-9_]+)\s*=\s*(\d+)", text)}
+    num = int(re.search(r"PHX_NUM_KINDS\s*=\s*(\d+)", text).group(1))
+    assert len(phx.KIND_NAMES) == num == len(kinds)
+    for name, idx in kinds.items():
+        assert phx.KIND_NAMES[idx] == name.lower(), (name, idx)
