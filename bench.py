@@ -23,7 +23,9 @@ on a bounded sample of the same workload.
 implementation: the pages describe their kernels but ship no library).
 
 The path does not shard in this build, so with N GPUs each rank runs its own replica of
-the step (no collective on the data path) and `scaling` is "weak".
+the step (no collective on the data path) and `scaling` is "weak".  `--gpus N` with N > 1,
+run as a plain script, starts N ranks itself (torch.distributed.run, one process per GPU,
+rank r on GPU r); under an outside torchrun launch WORLD_SIZE must equal N.
 """
 from __future__ import annotations
 
@@ -71,6 +73,17 @@ def reduce_max(x: float, ws: int, device=None) -> float:
     return float(t.item())
 
 
+def reduce_sum(x: float, ws: int, device=None) -> float:
+    """The sum of x over all ranks; x itself on one rank."""
+    if ws == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
 def whole_job_tflops(ws: int, steps: int, flops_per_step: float, max_seconds: float) -> float:
     """Throughput of the whole job: the work of every rank over the slowest rank's time.
     Each rank runs its own replica of the step (the path is not sharded), so the work grows
@@ -89,6 +102,38 @@ def _peaks():
     except (OSError, KeyError, ValueError):
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
                 "sm_max_mhz": 2070.0, "source": "fallback"}
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def f16_peak(peaks: dict, clocks: dict) -> tuple[float, str]:
+    """Denominator of the tensor-core fractions: the measured burst bf16 rate (dense f16 runs
+    at the bf16 rate), which applies to a kernel timed alone or in a short step at the
+    maximum clock; scaled by the run's median SM clock when that was below the maximum or a
+    throttle reason was active."""
+    burst = peaks["bf16_tflops"]
+    mhz, mx = clocks.get("sm_mhz"), clocks.get("sm_max_mhz") or peaks["sm_max_mhz"]
+    if mhz and (clocks.get("reasons") or mhz < 0.98 * mx):
+        return burst * mhz / mx, f"{peaks['source']} bf16 burst x run clock {mhz:.0f}/{mx:.0f} MHz"
+    return burst, f"{peaks['source']} bf16 burst (run at {mhz or mx:.0f} MHz, no throttle reason)"
 
 
 class ClockSampler:
@@ -237,21 +282,17 @@ def _traffic_from_profiles(kernel: str):
     return None
 
 
-def gpu_arm(args):
+def measure_replica(args, local: int, ws: int) -> dict:
+    """Time this rank's replica of the step on GPU `local`; returns its raw measurements."""
     import torch
     import torch.distributed as dist
     from dense_gemm_04_gb300 import phx, synth
 
-    ws, rank, local = _dist_env()
-    if ws > 1:
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
     props = torch.cuda.get_device_properties(local)
-    sms = props.multi_processor_count
-    peaks = _peaks()
 
     # inputs resident in HBM before any timing
     hA = synth.matrix(M, K, seed=0, tensor=synth.TENSOR_A)
@@ -263,22 +304,26 @@ def gpu_arm(args):
     C16 = C32.clone()
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)   # > 129 MB L2
 
-    def step():
+    def sgemm():
         phx.check(phx.phx_sgemm(M, N, K, ALPHA, A.data_ptr(), B.data_ptr(), BETA, C32.data_ptr(), sh))
+
+    def f16():
         phx.check(phx.phx_gemm_f16tc_f32acc(M, N, K, ALPHA, A.data_ptr(), B.data_ptr(), BETA,
                                             C16.data_ptr(), sh))
 
     # settle the clocks under the same work, then the W warm-up steps (all untimed)
     t0 = time.perf_counter()
     while time.perf_counter() - t0 < args.settle_s:
-        step()
+        sgemm()
+        f16()
         torch.cuda.synchronize()
     for _ in range(args.warmup):
-        step()
+        sgemm()
+        f16()
     torch.cuda.synchronize()
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+    # three events per step: start, between the two GEMM calls, end
+    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(args.steps)]
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -287,27 +332,29 @@ def gpu_arm(args):
         for i in range(args.steps):
             flush.fill_(i & 0xFF)                   # evict L2 (outside the step's events)
             ev[i][0].record(stream)
-            step()
+            sgemm()
             ev[i][1].record(stream)
+            f16()
+            ev[i][2].record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
     if ws > 1:
         dist.barrier()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
+    step_ms = [a.elapsed_time(c) for a, _, c in ev]
+    sgemm_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    f16_ms = [b.elapsed_time(c) for _, b, c in ev]
 
-    # Per-kernel device times, from a separate pass with the library's event profile on:
-    # events between the cast and the tensor-core GEMM would stop the GEMM's prologue from
-    # overlapping the cast, so they stay out of the timed steps above.
+    # Per-kernel device times, from a separate pass with the library's event profile on.
+    # Events between the cast and the tensor-core GEMM serialise the two, so this pass times
+    # each kernel alone; the timed steps above run them as the call does.
     prof_steps = max(10, min(args.steps, 50))
     phx.profile_start()
     for i in range(prof_steps):
         flush.fill_(i & 0xFF)
-        step()
+        sgemm()
+        f16()
     torch.cuda.synchronize()
     prof = phx.profile_stop()
-    launches_per_step = sum(n for n, _ in prof.values()) / prof_steps
-    max_s = reduce_max(sum(step_ms) / 1e3, ws, dev)
-    launches = int(round(launches_per_step * args.steps))
     st = phx.check_device_status()
     if st != phx.PHX_OK:
         raise RuntimeError(f"device status after the timed steps: {phx.status_string(st)}")
@@ -380,7 +427,6 @@ def gpu_arm(args):
         e1.record(s_out)
         torch.cuda.synchronize()
         runs.append(e0.elapsed_time(e1) / 1e3)
-    e2e_max_s = reduce_max(statistics.median(runs), ws, dev)
     serial_runs = []
     with torch.cuda.stream(stream):
         e2e_serial(2)
@@ -391,27 +437,60 @@ def gpu_arm(args):
             e1.record(stream)
             torch.cuda.synchronize()
             serial_runs.append(e0.elapsed_time(e1) / 1e3)
-    serial_max_s = reduce_max(statistics.median(serial_runs), ws, dev)
-    h2d = M * K * 4 + K * N * 4 + 2 * M * N * 4
-    d2h = 2 * M * N * 4
+    return {
+        "sms": props.multi_processor_count, "step_ms": step_ms, "sgemm_ms": sgemm_ms, "f16_ms": f16_ms,
+        "prof": prof, "prof_steps": prof_steps, "clocks": clk.summary(), "wall": wall,
+        "e2e_steps": e2e_steps, "e2e_runs": runs, "e2e_serial_runs": serial_runs,
+        "h2d": M * K * 4 + K * N * 4 + 2 * M * N * 4, "d2h": 2 * M * N * 4,
+        "configs": {"sgemm": phx.get_config(0, M, N, K), "f16tc_f32acc": phx.get_config(1, M, N, K)},
+    }
 
+
+def gpu_arm(args, replica=None, backend=None):
+    """One rank of the bench: time this rank's replica (measure_replica, or `replica` with the
+    same signature), take the slowest rank's times, and print the JSON line on rank 0.  The
+    process group is NCCL on GPUs (gloo without one, or as `backend` says); it carries only
+    the barriers and the reductions of the timings."""
+    import torch
+    import torch.distributed as dist
+
+    ws, rank, local = _dist_env()
+    if ws != args.gpus:
+        raise SystemExit(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={ws}: one rank per GPU is required")
+    backend = backend or ("nccl" if torch.cuda.is_available() else "gloo")
+    if ws > 1:
+        dist.init_process_group(backend)
+    dev = torch.device("cuda", local) if backend == "nccl" else None
+    peaks = _peaks()
+    r = (replica or measure_replica)(args, local, ws)
+    max_s = reduce_max(sum(r["step_ms"]) / 1e3, ws, dev)
+    e2e_max_s = reduce_max(statistics.median(r["e2e_runs"]), ws, dev)
+    serial_max_s = reduce_max(statistics.median(r["e2e_serial_runs"]), ws, dev)
+    # every rank counts itself in: the line's n_gpus is the number of replicas that ran
+    n_ranks = int(round(reduce_sum(1.0, ws, dev)))
+    if n_ranks != args.gpus:
+        raise SystemExit(f"bench.py: {n_ranks} ranks reported for --gpus {args.gpus}")
     if rank != 0:
         if ws > 1:
             dist.destroy_process_group()
         return 0
 
     value = whole_job_tflops(ws, args.steps, GEMMS_PER_STEP * FLOPS_PER_GEMM, max_s)
-    clocks = clk.summary()
+    clocks = r["clocks"]
+    sms = r["sms"]
     sm_max = clocks.get("sm_max_mhz") or peaks["sm_max_mhz"]
+    prof, prof_steps = r["prof"], r["prof_steps"]
+    launches_per_step = sum(n for n, _ in prof.values()) / prof_steps
+    launches = int(round(launches_per_step * args.steps))
 
-    def per_launch_ms(kind):
+    def per_call_ms(kind):
         # one call of each kind per step (a call may launch several kernels of its kind)
         n, ms = prof[kind]
         return ms / prof_steps if n else None
 
-    sg_ms = per_launch_ms("sgemm")
-    tc_ms = per_launch_ms("tc_gemm")
-    cast_ms = per_launch_ms("f16_cast")
+    sg_ms = per_call_ms("sgemm")
+    tc_ms = per_call_ms("tc_gemm")
+    cast_ms = per_call_ms("f16_cast")
     fp32_peak = sms * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
     run_mhz = clocks.get("sm_mhz")
     sg_tflops = FLOPS_PER_GEMM / (sg_ms / 1e3) / 1e12
@@ -422,34 +501,40 @@ def gpu_arm(args):
                 "algorithmic_bytes": 4.0 * (M * K + K * N + 2 * M * N)}
     if run_mhz:
         roofline["frac_at_run_clock"] = sg_tflops / (sms * FP32_LANES_PER_SM * 2 * run_mhz * 1e6 / 1e12)
+    # the f16 call as it runs inside the timed steps (cast and GEMM as the call launches them)
+    f16_call_ms = statistics.median(r["f16_ms"])
+    f16_call_tflops = FLOPS_PER_GEMM / (f16_call_ms / 1e3) / 1e12
     tc_tflops = FLOPS_PER_GEMM / (tc_ms / 1e3) / 1e12
-    tc_peak = peaks["bf16_tflops_sustained"]
-    roofline_tc = {"bound": "tensor", "kernel": "tcgen05 f16 GEMM (f32 accumulate)", "achieved": tc_tflops,
-                   "peak": tc_peak, "unit": "TFLOP/s", "frac": tc_tflops / tc_peak,
-                   "traffic": _traffic_from_profiles("tc_gemm"),
-                   "peak_source": f"{peaks['source']} bf16 sustained (dense f16 = bf16 rate)",
-                   "algorithmic_bytes": 2.0 * (M * K + K * N) + 4.0 * 2 * M * N}
+    tc_peak, tc_peak_src = f16_peak(peaks, clocks)
+    roofline_tc = {"bound": "tensor", "kernel": "tcgen05 f16 GEMM (f32 accumulate), timed alone",
+                   "achieved": tc_tflops, "peak": tc_peak, "unit": "TFLOP/s", "frac": tc_tflops / tc_peak,
+                   "traffic": _traffic_from_profiles("tc_gemm"), "peak_source": tc_peak_src,
+                   "algorithmic_bytes": 2.0 * (M * K + K * N) + 4.0 * 2 * M * N,
+                   "call_tflops": f16_call_tflops, "call_frac": f16_call_tflops / tc_peak,
+                   "call": "the whole phx_gemm_f16tc_f32acc call (cast + GEMM) in the timed steps"}
     cast_bytes = 6.0 * (M * K + K * N)
     cast_gbs = cast_bytes / (cast_ms / 1e3) / 1e9
-    roofline_cast = {"bound": "hbm", "kernel": "f32->f16 cast pass (A and B, one launch)", "achieved": cast_gbs,
-                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": cast_gbs / peaks["hbm_gbs"],
-                     "traffic": _traffic_from_profiles("f16_cast"), "algorithmic_bytes": cast_bytes}
-    f16_ms = tc_ms + cast_ms
+    roofline_cast = {"bound": "hbm", "kernel": "f32->f16 cast pass (A and B, one launch), timed alone",
+                     "achieved": cast_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": cast_gbs / peaks["hbm_gbs"], "traffic": _traffic_from_profiles("f16_cast"),
+                     "algorithmic_bytes": cast_bytes}
+    sg_call_ms = statistics.median(r["sgemm_ms"])
     variants = {
-        "sgemm": {"tflops": sg_tflops, "ms": sg_ms, "config": phx.get_config(0, M, N, K)},
-        "f16tc_f32acc": {"tflops": FLOPS_PER_GEMM / (f16_ms / 1e3) / 1e12, "ms": f16_ms,
-                         "gemm_kernel_ms": tc_ms, "cast_ms": cast_ms,
-                         "frac_of_tensor_peak": FLOPS_PER_GEMM / (f16_ms / 1e3) / 1e12 / tc_peak,
-                         "config": phx.get_config(1, M, N, K)},
+        "sgemm": {"tflops": FLOPS_PER_GEMM / (sg_call_ms / 1e3) / 1e12, "ms": sg_call_ms,
+                  "kernels_alone_ms": sg_ms, "config": r["configs"]["sgemm"]},
+        "f16tc_f32acc": {"tflops": f16_call_tflops, "ms": f16_call_ms, "gemm_kernel_alone_ms": tc_ms,
+                         "cast_alone_ms": cast_ms, "frac_of_tensor_peak": f16_call_tflops / tc_peak,
+                         "config": r["configs"]["f16tc_f32acc"]},
     }
     cpu = None
     if ws == 1 and not args.no_cpu_baseline:
         v, rows, t, cores = _oracle_sample(args.cpu_seconds)
-        cpu = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": cores, "cpu_model": cpu_model(), "kind": "oracle",
                "sample": f"the oracle on the first {rows} of {M} rows of both GEMMs of the workload "
                          f"({rows}x{N}x{K} each, f32 and f16-rounded inputs), {t:.1f} s"}
+    e2e_steps = r["e2e_steps"]
     out = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": n_ranks, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * max_s / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32 (SIMT) + f16xf16->f32 (tensor cores)",
         "data": DATA,
@@ -462,8 +547,8 @@ def gpu_arm(args):
         "roofline_cast": roofline_cast,
         "cpu_baseline": cpu,
         "e2e": {"value": whole_job_tflops(ws, e2e_steps, GEMMS_PER_STEP * FLOPS_PER_GEMM, e2e_max_s),
-                "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": e2e_steps, "runs": 3, "run_ms": [1e3 * r for r in runs],
+                "unit": "TFLOP/s", "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
+                "steps": e2e_steps, "runs": len(r["e2e_runs"]), "run_ms": [1e3 * x for x in r["e2e_runs"]],
                 "schedule": "copies in of step i+1 and out of step i-1 overlap the GEMMs of step i "
                             "(two buffer sets, three streams)",
                 "serial": whole_job_tflops(ws, e2e_steps, GEMMS_PER_STEP * FLOPS_PER_GEMM, serial_max_s)},
@@ -471,7 +556,7 @@ def gpu_arm(args):
         "gpu_launches": launches,
         "kernel_launches_per_step": {k: v[0] / prof_steps for k, v in prof.items()},
         "kernel_times_from": f"a separate pass of {prof_steps} steps with per-kernel events",
-        "wall_s_timed_region": wall,
+        "wall_s_timed_region": r["wall"],
         "peaks": peaks,
     }
     print(json.dumps(out), flush=True)
@@ -480,7 +565,23 @@ def gpu_arm(args):
     return 0
 
 
-def main():
+def launch_ranks(n: int, argv: list[str]) -> int:
+    """Start n ranks of this script on this node (torch.distributed.run, one process per
+    GPU, rendezvous on 127.0.0.1) and return the launcher's exit status."""
+    import socket
+    sock = socket.socket()
+    sock.bind(("127.0.0.1", 0))
+    port = sock.getsockname()[1]
+    sock.close()
+    script = os.path.abspath(sys.argv[0]) if sys.argv and sys.argv[0].endswith(".py") else os.path.abspath(__file__)
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), script, *argv]
+    return subprocess.call(cmd)
+
+
+def main(argv=None, replica=None, backend=None):
+    """Parse the command line and run one arm; with --gpus N > 1 outside a torchrun launch,
+    start N ranks of the running script first.  `replica` and `backend` go to gpu_arm."""
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=500)
@@ -491,10 +592,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--reference-rows", type=int, default=64,
                     help="rows of the workload the reference arm's oracle evaluates per step")
-    args = ap.parse_args()
+    args = ap.parse_args(argv)
+    if args.gpus < 1:
+        ap.error("--gpus must be at least 1")
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        return launch_ranks(args.gpus, sys.argv[1:] if argv is None else list(argv))
     if args.impl == "reference":
         return reference_arm(args)
-    return gpu_arm(args)
+    return gpu_arm(args, replica=replica, backend=backend)
 
 
 if __name__ == "__main__":

@@ -240,9 +240,6 @@ __device__ __forceinline__ void tc_tile_coords(int t, int tiles_m, int tiles_n, 
 
 // PAIR selects how CTAs cooperate:
 //   0  one CTA per tile;
-//   1  clusters of two CTAs take vertically adjacent tiles with the same B tile; each loads
-//      one half of that B tile and multicasts it to both (each SM pulls half of B's bytes
-//      from L2), and each MMA thread frees a ring slot in both CTAs (multicast commit);
 //   2  clusters of two CTAs run the 2-SM MMA (tcgen05.mma.cta_group::2, M = 256): each CTA
 //      stages its own 128 rows of A and its own half of the B tile, and the even CTA's MMA
 //      thread multiplies the pair's 256 x TILE_N tile, each CTA receiving its 128 rows of
@@ -359,7 +356,7 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         tma_prefetch_desc(&tmB_quarter);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), PAIR == 1 ? 2 : 1);
+            mbar_init(empty_bar(s), 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
@@ -417,13 +414,7 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     } else {
                         mbar_arrive_expect_tx(full_bar(stage), L::kABytes + (full ? L::kBBytes : L::kBBytes / 2));
                         tma_load_2d(a_dst, &tmA, kb * kBK, it.pm * kBM, full_bar(stage));
-                        if (PAIR == 1 && full) {
-                            // this CTA's half of the shared B tile, to both CTAs of the pair
-                            tma_load_2d_multicast(b_dst + rank * (L::kBBytes / 2), &tmB_half, kb * kBK,
-                                                  it.n0 + static_cast<int>(rank) * BN_HALF, full_bar(stage), 0x3);
-                        } else {
-                            tma_load_2d(b_dst, full ? &tmB : &tmB_half, kb * kBK, it.n0, full_bar(stage));
-                        }
+                        tma_load_2d(b_dst, full ? &tmB : &tmB_half, kb * kBK, it.n0, full_bar(stage));
                     }
                     issued_mask |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -469,8 +460,6 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     // the slot is free again (in both CTAs of a pair)
                     if constexpr (kTwoSm)
                         mma_commit_2sm_multicast(empty_bar(stage), 0x3);
-                    else if constexpr (PAIR == 1)
-                        mma_commit_multicast(empty_bar(stage), 0x3);
                     else
                         mma_commit(empty_bar(stage));
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -782,10 +771,11 @@ struct TcEntry {
     uint32_t smem;
 };
 
-// PAIR 0 and 1 run in the configuration names as CLUSTER=1 / CLUSTER=2 (TILE_M = 128 per CTA);
-// PAIR 2 as TILE_M=256 (the pair's 2-SM tile).
+// PAIR 0 runs in the configuration names as TILE_M=128 (one CTA per tile), PAIR 2 as
+// TILE_M=256 (the pair's 2-SM tile).
 template <int BN, int STAGES, int PAIR>
 TcEntry make_tc_entry() {
+    static_assert(PAIR == 0 || PAIR == 2, "one CTA per tile, or the 2-SM pair");
     return TcEntry{F16Config{PAIR == 2 ? 2 * kBM : kBM, BN, kBK, STAGES, PAIR == 0 ? 1 : 2},
                    &gemm_f16tc_kernel<BN, STAGES, PAIR, false, false>, &gemm_f16tc_kernel<BN, STAGES, PAIR, false, true>,
                    &gemm_f16tc_kernel<BN, STAGES, PAIR, true, false>, TcLayout<BN, STAGES, PAIR>::kDynSmem};
@@ -793,9 +783,8 @@ TcEntry make_tc_entry() {
 
 const TcEntry kTcEntries[] = {
     make_tc_entry<256, 4, 0>(), make_tc_entry<256, 3, 0>(), make_tc_entry<128, 6, 0>(),
-    make_tc_entry<128, 4, 0>(), make_tc_entry<64, 8, 0>(),  make_tc_entry<256, 4, 1>(),
-    make_tc_entry<128, 6, 1>(), make_tc_entry<256, 6, 2>(), make_tc_entry<256, 5, 2>(),
-    make_tc_entry<128, 8, 2>(),
+    make_tc_entry<128, 4, 0>(), make_tc_entry<64, 8, 0>(),  make_tc_entry<256, 6, 2>(),
+    make_tc_entry<256, 5, 2>(), make_tc_entry<128, 8, 2>(),
 };
 constexpr int kNumTc = sizeof(kTcEntries) / sizeof(kTcEntries[0]);
 
@@ -927,7 +916,7 @@ cudaError_t f16tc_gemm_launch_ops(int index, int64_t M, int64_t N, int64_t K, fl
     const int tiles_m = static_cast<int>((M + kBM - 1) / kBM);  // 128-row tiles (one per CTA)
     const int tiles_n = static_cast<int>((N + e.cfg.tile_n - 1) / e.cfg.tile_n);
     // With clusters of two, work is counted in pairs of tiles and in CTA pairs.
-    const bool mc = e.cfg.cluster == 2;  // CTA pairs (multicast, or the 2-SM MMA)
+    const bool mc = e.cfg.cluster == 2;  // CTA pairs running the 2-SM MMA
     const int64_t workers = mc ? num_sms / 2 : num_sms;
     const int64_t tiles = static_cast<int64_t>(mc ? (tiles_m + 1) / 2 : tiles_m) * tiles_n;
     // Whole tiles for the full rounds of the persistent grid; the tiles of a last, partial

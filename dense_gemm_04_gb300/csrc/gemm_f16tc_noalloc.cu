@@ -11,12 +11,14 @@
 // array below, which the CUDA runtime sets up with this library's device code, so the call
 // itself allocates nothing.
 //
-// The array is 64 MiB (kNoAllocScratchBytes): the f16 copies of a 4096 x 4096 x 4096
-// problem fit exactly.  Every GPU that loads this part of the library holds those 64 MiB
-// until the process exits.  All calls share the one array, on every stream, so calls whose
-// work overlaps on the GPU race with each other: order them on one stream, or synchronise.
-// The cast pass rewrites every byte of scratch a call reads (the zero padding included),
-// so nothing has to be cleared between calls.
+// The array is 64 MiB (kNoAllocScratchBytes): the scratch of a 4096 x 4096 x 4096 problem,
+// the f16 copies of A and B, fits exactly.  Every GPU that loads this part of the library
+// holds those 64 MiB until the process exits.  All calls share the one array, on every
+// stream, so calls whose work overlaps on the GPU race with each other: order them on one
+// stream, or synchronise.  Each call rewrites every byte of scratch it reads (the cast pass
+// writes the zero padding too; split-K slices write whole planes), so nothing has to be
+// cleared between calls.  The array also holds the status word of the kernels' bounded
+// waits, which phx_check_device_status reads and clears.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -84,13 +86,32 @@ phx_status noalloc_setup(const NoAllocDevice** out) {
 
 }  // namespace
 
+namespace phx {
+
+cudaError_t noalloc_take_status(unsigned int* word) {
+    *word = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorNoDevice;
+    unsigned char* base = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_noalloc_mu);
+        auto it = g_noalloc_dev.find(dev);
+        if (it == g_noalloc_dev.end() || it->second.status != PHX_OK) return cudaSuccess;
+        base = it->second.base;
+    }
+    cudaError_t err = cudaMemcpy(word, base, sizeof *word, cudaMemcpyDeviceToHost);
+    if (err == cudaSuccess) err = cudaMemset(base, 0, sizeof *word);
+    return err;
+}
+
+}  // namespace phx
+
 extern "C" phx_status phx_gemm_f16tc_f32acc_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
                                                     const float* A, const float* B, float beta,
                                                     float* C, phx_stream_t stream) {
     phx_status st = phx_validate_args(M, N, K, A, B, C);
     if (st != PHX_OK) return st;
     if (M == 0 || N == 0) return PHX_OK;
-    if (phx::f16tc_workspace_bytes(M, N, K) > kNoAllocScratchBytes) return PHX_ERR_NOMEM;
     const NoAllocDevice* d = nullptr;
     st = noalloc_setup(&d);
     if (st != PHX_OK) return st;
@@ -99,7 +120,7 @@ extern "C" phx_status phx_gemm_f16tc_f32acc_noalloc(int64_t M, int64_t N, int64_
         return phx::scale_c_launch(M, N, beta, C, stream) == cudaSuccess ? PHX_OK : PHX_ERR_LAUNCH;
     }
     const int cfg = phx::choose_config_for(PHX_VARIANT_F16TC, M, N, K, d->sm_count);
-    if (cfg < 0) return PHX_ERR_INTERNAL;
+    if (cfg < 0) return cfg == phx::kBadConfigPin ? PHX_ERR_CONFIG : PHX_ERR_INTERNAL;
     unsigned int* status_word = reinterpret_cast<unsigned int*>(d->base);
     void* workspace = d->base + kStatusBytes;
     if (phx::is_skinny_config(PHX_VARIANT_F16TC, cfg)) {
@@ -109,9 +130,20 @@ extern "C" phx_status phx_gemm_f16tc_f32acc_noalloc(int64_t M, int64_t N, int64_
                        cudaSuccess
                    ? PHX_OK : PHX_ERR_LAUNCH;
     }
-    cudaError_t err = phx::f16tc_cast_launch(M, N, K, A, B, workspace, d->sm_count, stream);
-    if (err == cudaSuccess)
-        err = phx::f16tc_gemm_launch(cfg, M, N, K, alpha, beta, C, workspace, nullptr, status_word,
-                                     d->sm_count, stream);
-    return err == cudaSuccess ? PHX_OK : PHX_ERR_LAUNCH;
+    // the same scratch layout and kernels as the pooled entry point (split-K planes included),
+    // so the results are the same bit for bit
+    if (phx::f16tc_run_bytes(cfg, M, N, K, d->sm_count) > kNoAllocScratchBytes) return PHX_ERR_NOMEM;
+    return phx::f16tc_run(cfg, 0, 0, M, N, K, alpha, A, B, beta, C, workspace, status_word, d->sm_count,
+                          stream) == cudaSuccess
+               ? PHX_OK : PHX_ERR_LAUNCH;
+}
+
+extern "C" phx_status phx_selftest_bounded_wait_noalloc(uint64_t limit_ns, phx_stream_t stream) {
+    const NoAllocDevice* d = nullptr;
+    const phx_status st = noalloc_setup(&d);
+    if (st != PHX_OK) return st;
+    if (limit_ns < 1000) limit_ns = 1000;
+    if (limit_ns > 1000000000ull) limit_ns = 1000000000ull;
+    return phx::selftest_wait_launch(limit_ns, reinterpret_cast<unsigned int*>(d->base), stream) == cudaSuccess
+               ? PHX_OK : PHX_ERR_LAUNCH;
 }

@@ -114,7 +114,7 @@ cudaError_t scale_c_launch(int64_t M, int64_t N, float beta, float* C, cudaStrea
 // ---------------------------------------------------------------------------------------
 struct F16Config {
     int tile_m, tile_n, tile_k, stages;
-    int cluster;  // 1, or 2: CTA pairs share their B tile through TMA multicast
+    int cluster;  // 1: one CTA per 128-row tile; 2: CTA pairs running the 2-SM MMA (TILE_M = 256)
 };
 
 int f16tc_num_configs();
@@ -163,8 +163,23 @@ cudaError_t f16tc_gemm_launch_ops(int index, int64_t M, int64_t N, int64_t K, fl
                                   int64_t ldb, void* split_ws, unsigned int* status, int num_sms,
                                   cudaStream_t stream);
 
+// One whole call of the f16 variant with configuration `cfg` (not the skinny kernel):
+// the cast pass into `ws` and the tcgen05 GEMM (split along K into `ws` when the grid is too
+// small for the GPU), both on `stream`; `ws` holds f16tc_run_bytes(...) bytes, 256-byte
+// aligned.  The pooled and the allocation-free entry points both run this (phx_api.cu).
+size_t f16tc_run_bytes(int cfg, int64_t M, int64_t N, int64_t K, int num_sms);
+cudaError_t f16tc_run(int cfg, int trans_a, int trans_b, int64_t M, int64_t N, int64_t K, float alpha,
+                      const float* A, const float* B, float beta, float* C, void* ws, unsigned int* status,
+                      int num_sms, cudaStream_t stream);
+
+// The allocation-free entry point's status word on the current device (gemm_f16tc_noalloc.cu):
+// copied to *word and cleared when that entry point has set up this device, else *word = 0.
+cudaError_t noalloc_take_status(unsigned int* word);
+
 // The configuration index a call of `variant` with this shape would use now (pinned, tuned
-// or default), as phx_get_config reports it (phx_api.cu).
+// or default), as phx_get_config reports it (phx_api.cu); kBadConfigPin when the variant's
+// PHX_CONFIG_* environment pin does not parse (the call then returns PHX_ERR_CONFIG).
+constexpr int kBadConfigPin = -2;
 int choose_config_for(int variant, int64_t M, int64_t N, int64_t K, int sms);
 
 // True if configuration `cfg` of `variant` is the skinny kernel rather than a GEMM tile.
@@ -175,7 +190,7 @@ bool is_skinny_config(int variant, int cfg);
 // ---------------------------------------------------------------------------------------
 cudaError_t probe_ffma_launch(int packed, int64_t blocks, int iters, float* out,
                               cudaStream_t stream);
-cudaError_t probe_stream_read_launch(const float* x, int64_t n, float* sink, int64_t blocks,
+cudaError_t probe_stream_read_launch(const float* x, int64_t n, uint32_t* fold, int64_t blocks,
                                      cudaStream_t stream);
 cudaError_t probe_mma_f16_launch(int64_t ctas, int iters, int n, float* sink,
                                  unsigned int* status, cudaStream_t stream);

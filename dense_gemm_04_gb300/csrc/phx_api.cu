@@ -10,6 +10,7 @@
 // section "Tuning" (two stages, finalists timed over rounds under the same clocks) and the
 // lab's stopwatches (settle the clock before timing; shuffle the order every round).
 #include <cuda_runtime.h>
+#include <dlfcn.h>
 
 #include <algorithm>
 #include <atomic>
@@ -104,6 +105,73 @@ phx_status device_state(DevState** out) {
     return d.init_status;
 }
 
+// The tuning cache's name for the current device: its name with spaces as underscores, a
+// colon and its SM count ("NVIDIA_GB300:152"); "none" without a usable device.  A tuned
+// configuration is only ever applied on a device with the tag it was tuned on.
+std::string device_tag() {
+    static std::mutex mu;
+    static std::map<int, std::string> tags;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return "none";
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = tags.find(dev);
+    if (it != tags.end()) return it->second;
+    cudaDeviceProp prop;
+    std::string tag = "none";
+    if (cudaGetDeviceProperties(&prop, dev) == cudaSuccess) {
+        tag = prop.name;
+        for (char& c : tag)
+            if (c == ' ' || c == '\t') c = '_';
+        tag += ":" + std::to_string(prop.multiProcessorCount);
+    } else {
+        cudaGetLastError();
+    }
+    tags[dev] = tag;
+    return tag;
+}
+
+// The current SM clock of a device in MHz, read through NVML (query calls only; nothing is
+// set), or -1 when NVML is not available.  Used to record the clock beside every timing of
+// the tuner's second stage.
+struct NvmlApi {
+    bool ok = false;
+    int (*get_handle_by_pci)(const char*, void**) = nullptr;
+    int (*get_clock)(void*, int, unsigned int*) = nullptr;
+};
+
+const NvmlApi& nvml() {
+    static NvmlApi api;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* h = dlopen("libnvidia-ml.so.1", RTLD_NOW | RTLD_LOCAL);
+        if (h == nullptr) return;
+        auto init = reinterpret_cast<int (*)()>(dlsym(h, "nvmlInit_v2"));
+        api.get_handle_by_pci = reinterpret_cast<int (*)(const char*, void**)>(
+            dlsym(h, "nvmlDeviceGetHandleByPciBusId_v2"));
+        api.get_clock = reinterpret_cast<int (*)(void*, int, unsigned int*)>(dlsym(h, "nvmlDeviceGetClockInfo"));
+        api.ok = init != nullptr && api.get_handle_by_pci != nullptr && api.get_clock != nullptr && init() == 0;
+    });
+    return api;
+}
+
+double sm_clock_mhz(int dev) {
+    const NvmlApi& api = nvml();
+    if (!api.ok) return -1.0;
+    char bus[64];
+    if (cudaDeviceGetPCIBusId(bus, sizeof bus, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return -1.0;
+    }
+    void* handle = nullptr;
+    unsigned int mhz = 0;
+    constexpr int kNvmlClockSm = 1;  // nvmlClockType_t: graphics 0, SM 1, memory 2
+    if (api.get_handle_by_pci(bus, &handle) != 0 || api.get_clock(handle, kNvmlClockSm, &mhz) != 0) return -1.0;
+    return static_cast<double>(mhz);
+}
+
 // ---------------------------------------------------------------------------------------
 // Argument checks
 // ---------------------------------------------------------------------------------------
@@ -174,17 +242,16 @@ std::string config_name(int variant, int i) {
                       c.tile_n, c.tile_k, c.stages, c.fma2);
     } else {
         const F16Config& c = phx::f16tc_config(i);
-        // CLUSTER=2 is written out for CTA pairs of 128-row tiles; a 256-row tile is always
-        // a 2-SM pair
-        std::snprintf(buf, sizeof buf, "TILE_M=%d TILE_N=%d TILE_K=%d STAGES=%d%s", c.tile_m, c.tile_n,
-                      c.tile_k, c.stages, (c.cluster == 2 && c.tile_m == 128) ? " CLUSTER=2" : "");
+        // a 256-row tile is a 2-SM pair; a 128-row tile one CTA
+        std::snprintf(buf, sizeof buf, "TILE_M=%d TILE_N=%d TILE_K=%d STAGES=%d", c.tile_m, c.tile_n,
+                      c.tile_k, c.stages);
     }
     return buf;
 }
 
 // Parse "KEY=value KEY=value ..." and return the first compiled config that matches every
-// given key (TILE_M, TILE_N, TILE_K required; STAGES optional; FMA2 for the f32 variant and
-// CLUSTER for the f16 variant optional, default 0 and 1), or -1.
+// given key (TILE_M, TILE_N, TILE_K required; STAGES optional; FMA2 for the f32 variant
+// optional, default 0), or -1.
 int parse_config(int variant, const char* spec) {
     if (spec == nullptr || num_configs(variant) < 0) return -1;
     std::map<std::string, int> kv;
@@ -203,45 +270,68 @@ int parse_config(int variant, const char* spec) {
         char* end = nullptr;
         const long v = std::strtol(val.c_str(), &end, 10);
         if (end == nullptr || *end != '\0') return -1;
-        if (key != "TILE_M" && key != "TILE_N" && key != "TILE_K" && key != "STAGES" && key != "FMA2" &&
-            key != "CLUSTER")
+        if (key != "TILE_M" && key != "TILE_N" && key != "TILE_K" && key != "STAGES" && key != "FMA2")
             return -1;
         if (variant == PHX_VARIANT_F16TC && key == "FMA2") return -1;
-        if (variant == PHX_VARIANT_SGEMM && key == "CLUSTER") return -1;
         kv[key] = static_cast<int>(v);
     }
     if (!kv.count("TILE_M") || !kv.count("TILE_N") || !kv.count("TILE_K")) return -1;
     const int n = tile_configs(variant);
     for (int i = 0; i < n; ++i) {
-        int tm, tn, tk, st, f2 = 0, cl = 1;
+        int tm, tn, tk, st, f2 = 0;
         if (variant == PHX_VARIANT_SGEMM) {
             const SgemmConfig& c = phx::sgemm_config(i);
             tm = c.tile_m; tn = c.tile_n; tk = c.tile_k; st = c.stages; f2 = c.fma2;
         } else {
             const F16Config& c = phx::f16tc_config(i);
-            tm = c.tile_m; tn = c.tile_n; tk = c.tile_k; st = c.stages; cl = c.cluster;
+            tm = c.tile_m; tn = c.tile_n; tk = c.tile_k; st = c.stages;
         }
         if (kv["TILE_M"] != tm || kv["TILE_N"] != tn || kv["TILE_K"] != tk) continue;
         if (kv.count("STAGES") && kv["STAGES"] != st) continue;
         if (kv.count("FMA2") && kv["FMA2"] != f2) continue;
         if (!kv.count("FMA2") && variant == PHX_VARIANT_SGEMM && f2 != 0) continue;
-        const int cl_default = (variant == PHX_VARIANT_F16TC && tm == 256) ? 2 : 1;
-        if ((kv.count("CLUSTER") ? kv["CLUSTER"] : cl_default) != cl) continue;
         return i;
     }
     return -1;
 }
 
-using ShapeKey = std::tuple<int, int64_t, int64_t, int64_t>;
+// Tuned configurations by (device tag, variant, M, N, K).
+using ShapeKey = std::tuple<std::string, int, int64_t, int64_t, int64_t>;
 std::map<ShapeKey, int> g_tuned;  // guarded by g_mu
+// Pinned configuration per variant: -1 none, kBadPin for an unparsable PHX_CONFIG_* (every
+// call of that variant then returns PHX_ERR_CONFIG until phx_set_config replaces the pin).
+constexpr int kBadPin = phx::kBadConfigPin;
 int g_pin[2] = {-1, -1};          // guarded by g_mu
 bool g_env_done = false;
+
+phx_status tune_cache_read(const char* path, std::map<ShapeKey, int>* out);
 
 void load_env_once_locked() {
     if (g_env_done) return;
     g_env_done = true;
-    if (const char* s = std::getenv("PHX_CONFIG_SGEMM")) g_pin[0] = parse_config(PHX_VARIANT_SGEMM, s);
-    if (const char* s = std::getenv("PHX_CONFIG_F16TC")) g_pin[1] = parse_config(PHX_VARIANT_F16TC, s);
+    const char* names[2] = {"PHX_CONFIG_SGEMM", "PHX_CONFIG_F16TC"};
+    for (int v = 0; v < 2; ++v) {
+        const char* s = std::getenv(names[v]);
+        if (s == nullptr) continue;
+        g_pin[v] = parse_config(v, s);
+        if (g_pin[v] < 0) {
+            g_pin[v] = kBadPin;
+            std::fprintf(stderr, "[phx] %s=\"%s\" names no compiled configuration; calls of this variant "
+                                 "return PHX_ERR_CONFIG until phx_set_config replaces the pin\n", names[v], s);
+        }
+    }
+    // PHX_TUNE_CACHE: a tuning cache file read at the first call (and written by phx_autotune)
+    if (const char* path = std::getenv("PHX_TUNE_CACHE")) {
+        std::map<ShapeKey, int> loaded;
+        std::ifstream probe(path);
+        if (probe) {
+            probe.close();
+            if (tune_cache_read(path, &loaded) == PHX_OK)
+                for (const auto& kv : loaded) g_tuned[kv.first] = kv.second;
+            else
+                std::fprintf(stderr, "[phx] PHX_TUNE_CACHE=%s does not parse; it is ignored\n", path);
+        }
+    }
 }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -274,13 +364,58 @@ int default_tile_config(int variant, int64_t M, int64_t N, int sms) {
     return parse_config(variant, "TILE_M=128 TILE_N=64 TILE_K=64 STAGES=8");
 }
 
+// The configuration for a call: the pin, else the tuned one for this device and shape, else
+// the default; kBadPin when the variant's PHX_CONFIG_* pin does not parse.
 int choose_config(int variant, int64_t M, int64_t N, int64_t K, int sms) {
+    const std::string tag = device_tag();
     std::lock_guard<std::mutex> lock(g_mu);
     load_env_once_locked();
-    if (g_pin[variant] >= 0) return g_pin[variant];
-    auto it = g_tuned.find(ShapeKey(variant, M, N, K));
+    if (g_pin[variant] >= 0 || g_pin[variant] == kBadPin) return g_pin[variant];
+    auto it = g_tuned.find(ShapeKey(tag, variant, M, N, K));
     if (it != g_tuned.end()) return it->second;
     return default_config(variant, M, N, sms);
+}
+
+phx_status config_error(int cfg) { return cfg == kBadPin ? PHX_ERR_CONFIG : PHX_ERR_INTERNAL; }
+
+// The last tuning run's report per variant (phx_autotune_report); guarded by g_mu.
+std::string g_tune_report[2];
+
+// Tuning cache file: "# ..." comments, then one line per entry:
+//   <device tag> <variant> <M> <N> <K> <configuration name>
+// Entries of every device are kept; a call only uses those of its own device's tag.
+phx_status tune_cache_write_locked(const char* path) {
+    std::ofstream f(path);
+    if (!f) return PHX_ERR_INVALID;
+    f << "# phx tuning cache: device variant M N K config\n";
+    for (const auto& kv : g_tuned) {
+        f << std::get<0>(kv.first) << ' ' << std::get<1>(kv.first) << ' ' << std::get<2>(kv.first) << ' '
+          << std::get<3>(kv.first) << ' ' << std::get<4>(kv.first) << ' '
+          << config_name(std::get<1>(kv.first), kv.second) << '\n';
+    }
+    return f ? PHX_OK : PHX_ERR_INVALID;
+}
+
+phx_status tune_cache_read(const char* path, std::map<ShapeKey, int>* out) {
+    std::ifstream f(path);
+    if (!f) return PHX_ERR_INVALID;
+    std::string line;
+    while (std::getline(f, line)) {
+        if (line.empty() || line[0] == '#') continue;
+        std::istringstream in(line);
+        std::string tag;
+        int variant;
+        long long M, N, K;
+        if (!(in >> tag >> variant >> M >> N >> K)) return PHX_ERR_CONFIG;
+        if (tag.find(':') == std::string::npos && tag != "none") return PHX_ERR_CONFIG;
+        std::string rest;
+        std::getline(in, rest);
+        if (num_configs(variant) < 0) return PHX_ERR_CONFIG;
+        const int idx = parse_config(variant, rest.c_str());
+        if (idx < 0) return PHX_ERR_CONFIG;
+        (*out)[ShapeKey(tag, variant, M, N, K)] = idx;
+    }
+    return PHX_OK;
 }
 
 // The configuration the last GEMM call of each variant launched (-1: none yet), for reports.
@@ -304,7 +439,8 @@ double median(std::vector<double> v) {
 
 TuneOutcome tune_select(int n, const std::function<double(int)>& measure,
                         const std::function<double()>& elapsed, int finalists, int rounds,
-                        double settle_s, uint64_t seed) {
+                        double settle_s, uint64_t seed,
+                        const std::function<void(int, double)>& stage2_timed = nullptr) {
     TuneOutcome out;
     auto run = [&](int i) {
         ++out.launches;
@@ -342,8 +478,12 @@ TuneOutcome tune_select(int n, const std::function<double(int)>& measure,
         for (int i : order) {
             if (dropped[i]) continue;
             const double s = run(i);
-            if (s < 0) dropped[i] = true;
-            else times[i].push_back(s);
+            if (s < 0) {
+                dropped[i] = true;
+            } else {
+                times[i].push_back(s);
+                if (stage2_timed) stage2_timed(i, s);
+            }
         }
     }
     double best = 0.0;
@@ -464,24 +604,15 @@ phx_status launch_variant(int variant, int cfg, int64_t M, int64_t N, int64_t K,
         if (ws != nullptr) cudaFreeAsync(ws, stream);
         return err == cudaSuccess ? PHX_OK : PHX_ERR_LAUNCH;
     }
-    // one pooled block: the f16 operand copies, then (for a grid split along K) the partial
-    // products of the slices
-    const size_t cast_bytes = phx::f16tc_workspace_bytes(M, N, K);
-    const size_t split_bytes = phx::f16tc_split_bytes(cfg, M, N, K, d->sm_count);
+    // one pooled block holds the call's scratch (phx::f16tc_run_bytes)
     void* ws = nullptr;
-    if (cudaMallocFromPoolAsync(&ws, cast_bytes + split_bytes, d->pool, stream) != cudaSuccess) {
+    if (cudaMallocFromPoolAsync(&ws, phx::f16tc_run_bytes(cfg, M, N, K, d->sm_count), d->pool, stream) !=
+        cudaSuccess) {
         cudaGetLastError();
         return PHX_ERR_NOMEM;
     }
-    void* split_ws = split_bytes > 0 ? static_cast<char*>(ws) + cast_bytes : nullptr;
-    cudaError_t err = timed(kKindCast, stream, [&] {
-        return phx::f16tc_cast_launch_ex(trans_a, trans_b, M, N, K, A, B, ws, d->sm_count, stream);
-    });
-    if (err == cudaSuccess)
-        err = timed(kKindTcGemm, stream, [&] {
-            return phx::f16tc_gemm_launch(cfg, M, N, K, alpha, beta, C, ws, split_ws, d->status,
-                                          d->sm_count, stream);
-        });
+    const cudaError_t err = phx::f16tc_run(cfg, trans_a, trans_b, M, N, K, alpha, A, B, beta, C, ws, d->status,
+                                           d->sm_count, stream);
     cudaFreeAsync(ws, stream);
     return err == cudaSuccess ? PHX_OK : PHX_ERR_LAUNCH;
 }
@@ -528,7 +659,7 @@ phx_status gemm_entry(int variant, int64_t M, int64_t N, int64_t K, float alpha,
                    ? PHX_OK : PHX_ERR_LAUNCH;
     }
     const int cfg = choose_config(variant, M, N, K, d->sm_count);
-    if (cfg < 0) return PHX_ERR_INTERNAL;
+    if (cfg < 0) return config_error(cfg);
     g_last_cfg[variant].store(cfg);
     if (log_level() >= 2)
         std::fprintf(stderr, "[phx] variant %d (%lld,%lld,%lld): %s\n", variant, (long long)M,
@@ -558,7 +689,7 @@ phx_status f16in_entry(int trans_a, int trans_b, int64_t M, int64_t N, int64_t K
     }
     int cfg = choose_config(PHX_VARIANT_F16TC, M, N, K, d->sm_count);
     if (cfg == skinny_index(PHX_VARIANT_F16TC)) cfg = default_tile_config(PHX_VARIANT_F16TC, M, N, d->sm_count);
-    if (cfg < 0) return PHX_ERR_INTERNAL;
+    if (cfg < 0) return config_error(cfg);
     g_last_cfg[PHX_VARIANT_F16TC].store(cfg);
     const int64_t Kp = (K + 7) / 8 * 8;
     const bool a_direct = !trans_a && K % 8 == 0 && (reinterpret_cast<uintptr_t>(A) & 15u) == 0;
@@ -603,6 +734,28 @@ phx_status copy_name(const std::string& s, char* buf, size_t buflen) {
 }  // namespace
 
 namespace phx {
+size_t f16tc_run_bytes(int cfg, int64_t M, int64_t N, int64_t K, int num_sms) {
+    // the f16 operand copies, then (for a grid split along K) the partial products of the
+    // slices
+    return f16tc_workspace_bytes(M, N, K) + f16tc_split_bytes(cfg, M, N, K, num_sms);
+}
+
+cudaError_t f16tc_run(int cfg, int trans_a, int trans_b, int64_t M, int64_t N, int64_t K, float alpha,
+                      const float* A, const float* B, float beta, float* C, void* ws, unsigned int* status,
+                      int num_sms, cudaStream_t stream) {
+    const size_t cast_bytes = f16tc_workspace_bytes(M, N, K);
+    const size_t split_bytes = f16tc_split_bytes(cfg, M, N, K, num_sms);
+    void* split_ws = split_bytes > 0 ? static_cast<char*>(ws) + cast_bytes : nullptr;
+    cudaError_t err = timed(kKindCast, stream, [&] {
+        return f16tc_cast_launch_ex(trans_a, trans_b, M, N, K, A, B, ws, num_sms, stream);
+    });
+    if (err == cudaSuccess)
+        err = timed(kKindTcGemm, stream, [&] {
+            return f16tc_gemm_launch(cfg, M, N, K, alpha, beta, C, ws, split_ws, status, num_sms, stream);
+        });
+    return err;
+}
+
 // The configuration a call of `variant` with this shape would use (pin, tuned, default),
 // for entry points outside this file.
 int choose_config_for(int variant, int64_t M, int64_t N, int64_t K, int sms) {
@@ -683,20 +836,40 @@ phx_status phx_f16tc_workspace_bytes(int64_t M, int64_t N, int64_t K, size_t* by
 }
 
 phx_status phx_check_device_status(phx_stream_t stream) {
-    DevState* d = nullptr;
-    phx_status st = device_state(&d);
-    if (st != PHX_OK) return st;
+    // Reads and clears both status words of the current device: the one of the pooled entry
+    // points (if any of them ran here) and the one inside the allocation-free entry point's
+    // static scratch (if that ran here).  Allocates nothing.
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return PHX_ERR_ARCH;
+    }
+    unsigned int* pooled_word = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        auto it = g_dev.find(dev);
+        if (it != g_dev.end() && it->second.ready) {
+            if (it->second.init_status != PHX_OK) return it->second.init_status;
+            pooled_word = it->second.status;
+        }
+    }
     if (cudaStreamSynchronize(stream) != cudaSuccess) {
         cudaGetLastError();
         return PHX_ERR_LAUNCH;
     }
     unsigned int word = 0;
-    if (cudaMemcpy(&word, d->status, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess ||
-        cudaMemset(d->status, 0, sizeof word) != cudaSuccess) {
+    if (pooled_word != nullptr &&
+        (cudaMemcpy(&word, pooled_word, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess ||
+         cudaMemset(pooled_word, 0, sizeof word) != cudaSuccess)) {
         cudaGetLastError();
         return PHX_ERR_LAUNCH;
     }
-    return (word & phx::kDevTimeout) ? PHX_ERR_TIMEOUT : PHX_OK;
+    unsigned int noalloc_word = 0;
+    if (phx::noalloc_take_status(&noalloc_word) != cudaSuccess) {
+        cudaGetLastError();
+        return PHX_ERR_LAUNCH;
+    }
+    return ((word | noalloc_word) & phx::kDevTimeout) ? PHX_ERR_TIMEOUT : PHX_OK;
 }
 
 phx_status phx_profile_start(void) {
@@ -763,7 +936,7 @@ phx_status phx_get_config(int variant, int64_t M, int64_t N, int64_t K, char* bu
     DevState* d = nullptr;
     if (device_state(&d) == PHX_OK) sms = d->sm_count;
     const int cfg = choose_config(variant, M, N, K, sms);
-    if (cfg < 0) return PHX_ERR_INTERNAL;
+    if (cfg < 0) return config_error(cfg);
     return copy_name(config_name(variant, cfg), buf, buflen);
 }
 
@@ -781,6 +954,9 @@ phx_status phx_autotune(int variant, int64_t M, int64_t N, int64_t K, int finali
     DevState* d = nullptr;
     phx_status st = device_state(&d);
     if (st != PHX_OK) return st;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const std::string tag = device_tag();
     float *A = nullptr, *B = nullptr, *C = nullptr;
     if (cudaMalloc(&A, 4 * M * K) != cudaSuccess || cudaMalloc(&B, 4 * K * N) != cudaSuccess ||
         cudaMalloc(&C, 4 * M * N) != cudaSuccess) {
@@ -812,9 +988,12 @@ phx_status phx_autotune(int variant, int64_t M, int64_t N, int64_t K, int finali
     auto elapsed = [&]() {
         return std::chrono::duration<double>(std::chrono::steady_clock::now() - start).count();
     };
+    // every second-stage timing with the SM clock read right after it (NVML, -1 if absent)
+    std::map<int, std::vector<std::pair<double, double>>> stage2;
+    auto stage2_timed = [&](int i, double sec) { stage2[i].emplace_back(sec, sm_clock_mhz(dev)); };
     const TuneOutcome res = tune_select(n, measure, elapsed, finalists > 0 ? finalists : 4,
                                         rounds > 0 ? rounds : 9, settle_ms > 0 ? settle_ms * 1e-3 : 0.25,
-                                        0x5eedull ^ static_cast<uint64_t>(M * 31 + N * 17 + K));
+                                        0x5eedull ^ static_cast<uint64_t>(M * 31 + N * 17 + K), stage2_timed);
     cudaEventDestroy(e0);
     cudaEventDestroy(e1);
     cudaStreamSynchronize(stream);
@@ -825,48 +1004,53 @@ phx_status phx_autotune(int variant, int64_t M, int64_t N, int64_t K, int finali
     st = phx_check_device_status(stream);
     if (st != PHX_OK) return st;
     if (res.picked < 0) return PHX_ERR_LAUNCH;
-    if (log_level() >= 1)
-        std::fprintf(stderr, "[phx] tuned variant %d (%lld,%lld,%lld): %s (%lld launches)\n", variant,
-                     (long long)M, (long long)N, (long long)K, config_name(variant, res.picked).c_str(),
-                     (long long)res.launches);
+    // The report of this run: one line per finalist with its median time and the median SM
+    // clock of its timings.
+    std::ostringstream rep;
+    rep << "device " << tag << " variant " << variant << " shape " << M << ' ' << N << ' ' << K
+        << " picked " << config_name(variant, res.picked) << " launches " << res.launches << '\n';
+    for (const auto& kv : stage2) {
+        std::vector<double> t, c;
+        for (const auto& x : kv.second) {
+            t.push_back(x.first);
+            if (x.second > 0) c.push_back(x.second);
+        }
+        char line[256];
+        std::snprintf(line, sizeof line, "  %-48s median_ms %.4f sm_mhz %.0f timings %zu\n",
+                      config_name(variant, kv.first).c_str(), 1e3 * median(t), c.empty() ? -1.0 : median(c),
+                      t.size());
+        rep << line;
+    }
+    if (log_level() >= 1) std::fprintf(stderr, "[phx] tuned: %s", rep.str().c_str());
     std::lock_guard<std::mutex> lock(g_mu);
-    g_tuned[ShapeKey(variant, M, N, K)] = res.picked;
+    g_tune_report[variant] = rep.str();
+    g_tuned[ShapeKey(tag, variant, M, N, K)] = res.picked;
+    if (const char* path = std::getenv("PHX_TUNE_CACHE")) {
+        if (tune_cache_write_locked(path) != PHX_OK)
+            std::fprintf(stderr, "[phx] PHX_TUNE_CACHE=%s could not be written\n", path);
+    }
     return PHX_OK;
 }
 
+phx_status phx_autotune_report(int variant, char* buf, size_t buflen) {
+    if (num_configs(variant) < 0) return PHX_ERR_INVALID;
+    std::lock_guard<std::mutex> lock(g_mu);
+    return copy_name(g_tune_report[variant].empty() ? std::string("NONE\n") : g_tune_report[variant], buf, buflen);
+}
+
+phx_status phx_device_tag(char* buf, size_t buflen) { return copy_name(device_tag(), buf, buflen); }
+
 phx_status phx_tune_cache_save(const char* path) {
     if (path == nullptr) return PHX_ERR_INVALID;
-    std::ofstream f(path);
-    if (!f) return PHX_ERR_INVALID;
     std::lock_guard<std::mutex> lock(g_mu);
-    f << "# phx tuning cache: variant M N K config\n";
-    for (const auto& kv : g_tuned) {
-        f << std::get<0>(kv.first) << ' ' << std::get<1>(kv.first) << ' ' << std::get<2>(kv.first)
-          << ' ' << std::get<3>(kv.first) << ' ' << config_name(std::get<0>(kv.first), kv.second)
-          << '\n';
-    }
-    return f ? PHX_OK : PHX_ERR_INVALID;
+    return tune_cache_write_locked(path);
 }
 
 phx_status phx_tune_cache_load(const char* path) {
     if (path == nullptr) return PHX_ERR_INVALID;
-    std::ifstream f(path);
-    if (!f) return PHX_ERR_INVALID;
     std::map<ShapeKey, int> loaded;
-    std::string line;
-    while (std::getline(f, line)) {
-        if (line.empty() || line[0] == '#') continue;
-        std::istringstream in(line);
-        int variant;
-        long long M, N, K;
-        if (!(in >> variant >> M >> N >> K)) return PHX_ERR_CONFIG;
-        std::string rest;
-        std::getline(in, rest);
-        if (num_configs(variant) < 0) return PHX_ERR_CONFIG;
-        const int idx = parse_config(variant, rest.c_str());
-        if (idx < 0) return PHX_ERR_CONFIG;
-        loaded[ShapeKey(variant, M, N, K)] = idx;
-    }
+    const phx_status st = tune_cache_read(path, &loaded);
+    if (st != PHX_OK) return st;
     std::lock_guard<std::mutex> lock(g_mu);
     for (const auto& kv : loaded) g_tuned[kv.first] = kv.second;
     return PHX_OK;
@@ -880,15 +1064,15 @@ phx_status phx_probe_ffma(int packed, int64_t blocks, int iters, float* out, phx
     return phx::probe_ffma_launch(packed, blocks, iters, out, stream) == cudaSuccess ? PHX_OK : PHX_ERR_LAUNCH;
 }
 
-phx_status phx_probe_stream_read(const float* x, int64_t n, float* sink, int64_t blocks,
+phx_status phx_probe_stream_read(const float* x, int64_t n, uint32_t* fold, int64_t blocks,
                                  phx_stream_t stream) {
-    if (x == nullptr || sink == nullptr || n <= 0 || n % 4 != 0 || blocks <= 0 || blocks > 0x7FFFFFFF ||
+    if (x == nullptr || fold == nullptr || n <= 0 || n % 4 != 0 || blocks <= 0 || blocks > 0x7FFFFFFF ||
         (reinterpret_cast<uintptr_t>(x) & 15u) != 0)
         return PHX_ERR_INVALID;
     DevState* d = nullptr;
     phx_status st = device_state(&d);
     if (st != PHX_OK) return st;
-    return phx::probe_stream_read_launch(x, n, sink, blocks, stream) == cudaSuccess ? PHX_OK : PHX_ERR_LAUNCH;
+    return phx::probe_stream_read_launch(x, n, fold, blocks, stream) == cudaSuccess ? PHX_OK : PHX_ERR_LAUNCH;
 }
 
 phx_status phx_probe_mma_f16(int64_t ctas, int iters, int n, float* sink, phx_stream_t stream) {

@@ -1,10 +1,11 @@
 // probes.cu -- roof probes and device self-tests for sm_103a.
 //
-// The probes follow the matrix-multiplication lab's Part 1 ("the two roofs, again"): the
-// FP32 roof is measured with a kernel of nothing but independent multiply-adds held in
-// registers, the memory roof with a streaming read.  A third probe measures the dense
-// f16 tensor-core roof with tcgen05.mma on shared-memory operands and no global traffic.
-// They exist to measure roofline denominators; they compute nothing anyone needs.
+// The matrix-multiplication lab's Part 1 ("the two roofs, again") measures the FP32 roof
+// with a kernel of nothing but register-resident multiply-adds and the memory roof with a
+// kernel that only reads.  The two probes here measure the same two quantities on sm_103a
+// with kernels designed for it; a third measures the dense f16 tensor-core roof with
+// tcgen05.mma on shared-memory operands and no global traffic.  They exist to measure
+// roofline denominators; they compute nothing anyone needs.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -18,53 +19,90 @@ namespace {
 
 using namespace ptx;
 
-// Eight independent multiply-add chains per thread (scalar) or eight chains of f32x2 pairs
-// (packed): 16 (or 32) floating-point operations per thread per iteration.
-template <bool PACKED>
-__global__ void __launch_bounds__(256) ffma_probe_kernel(float* out, int iters) {
-    const float seed = 1e-6f * static_cast<float>(threadIdx.x);
-    const float b = 0.99999f;
-    const float c = 1e-5f;
-    if constexpr (!PACKED) {
-        float a0 = seed, a1 = seed + 0.1f, a2 = seed + 0.2f, a3 = seed + 0.3f;
-        float a4 = seed + 0.4f, a5 = seed + 0.5f, a6 = seed + 0.6f, a7 = seed + 0.7f;
-#pragma unroll 8
-        for (int k = 0; k < iters; ++k) {
-            a0 = fmaf(a0, b, c); a1 = fmaf(a1, b, c); a2 = fmaf(a2, b, c); a3 = fmaf(a3, b, c);
-            a4 = fmaf(a4, b, c); a5 = fmaf(a5, b, c); a6 = fmaf(a6, b, c); a7 = fmaf(a7, b, c);
-        }
-        out[blockIdx.x * blockDim.x + threadIdx.x] = a0 + a1 + a2 + a3 + a4 + a5 + a6 + a7;
-    } else {
-        const float2 b2 = make_float2(b, b);
-        const float2 c2 = make_float2(c, c);
-        float2 a0 = make_float2(seed, seed + 0.05f), a1 = make_float2(seed + 0.1f, seed + 0.15f);
-        float2 a2 = make_float2(seed + 0.2f, seed + 0.25f), a3 = make_float2(seed + 0.3f, seed + 0.35f);
-        float2 a4 = make_float2(seed + 0.4f, seed + 0.45f), a5 = make_float2(seed + 0.5f, seed + 0.55f);
-        float2 a6 = make_float2(seed + 0.6f, seed + 0.65f), a7 = make_float2(seed + 0.7f, seed + 0.75f);
-#pragma unroll 8
-        for (int k = 0; k < iters; ++k) {
-            a0 = __ffma2_rn(a0, b2, c2); a1 = __ffma2_rn(a1, b2, c2);
-            a2 = __ffma2_rn(a2, b2, c2); a3 = __ffma2_rn(a3, b2, c2);
-            a4 = __ffma2_rn(a4, b2, c2); a5 = __ffma2_rn(a5, b2, c2);
-            a6 = __ffma2_rn(a6, b2, c2); a7 = __ffma2_rn(a7, b2, c2);
-        }
-        out[blockIdx.x * blockDim.x + threadIdx.x] = a0.x + a0.y + a1.x + a1.y + a2.x + a2.y +
-                                                     a3.x + a3.y + a4.x + a4.y + a5.x + a5.y +
-                                                     a6.x + a6.y + a7.x + a7.y;
-    }
+// FP32 issue-rate probe.  Each SM of sm_103a has 4 sub-partitions of 32 FP32 lanes; a
+// dependent multiply-add waits a few cycles for its predecessor, so each thread keeps
+// kProbeLanes independent recurrences x <- x * rho + tau in registers, and the grid puts
+// many warps on every SM.  rho and tau arrive as arguments, so the compiler can neither
+// fold nor shorten the recurrences; with rho = 1 - 2^-12 and tau = 2^-13 every value stays
+// in [0.5, 1) (the fixed point is 0.5).  PACKED runs the same recurrences two lanes per
+// f32x2 instruction.  Both forms do 2 * kProbeLanes FLOPs per thread and iteration.  The
+// lanes are folded by a pairwise tree and each thread stores its fold, so no recurrence is
+// dead code.
+constexpr int kProbeLanes = 12;
+
+__device__ __forceinline__ float probe_seed(uint32_t g, int i) {
+    uint32_t h = g * 0x85EBCA6Bu + static_cast<uint32_t>(i) * 0xC2B2AE35u;
+    h ^= h >> 16;
+    return __uint_as_float(0x3F000000u | (h & 0x007FFFFFu));  // [0.5, 1)
 }
 
-// Grid-stride float4 read of n floats (n % 4 == 0, x 16-byte aligned).
-__global__ void __launch_bounds__(256) stream_read_kernel(const float4* __restrict__ x, int64_t n4,
-                                                          float* sink) {
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    float acc = 0.f;
+template <bool PACKED>
+__global__ void __launch_bounds__(256) fp32_issue_probe_kernel(float* out, int iters, float rho, float tau) {
+    const uint32_t g = blockIdx.x * blockDim.x + threadIdx.x;
+    float v[kProbeLanes];
+#pragma unroll
+    for (int i = 0; i < kProbeLanes; ++i) v[i] = probe_seed(g, i);
+    if constexpr (PACKED) {
+        float2 w[kProbeLanes / 2];
+#pragma unroll
+        for (int i = 0; i < kProbeLanes / 2; ++i) w[i] = make_float2(v[2 * i], v[2 * i + 1]);
+        const float2 r2 = make_float2(rho, rho), t2 = make_float2(tau, tau);
 #pragma unroll 4
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
-        const float4 v = __ldcs(x + i);
-        acc += v.x + v.y + v.z + v.w;
+        for (int it = 0; it < iters; ++it) {
+#pragma unroll
+            for (int i = 0; i < kProbeLanes / 2; ++i) w[i] = __ffma2_rn(w[i], r2, t2);
+        }
+#pragma unroll
+        for (int i = 0; i < kProbeLanes / 2; ++i) {
+            v[2 * i] = w[i].x;
+            v[2 * i + 1] = w[i].y;
+        }
+    } else {
+#pragma unroll 4
+        for (int it = 0; it < iters; ++it) {
+#pragma unroll
+            for (int i = 0; i < kProbeLanes; ++i) v[i] = fmaf(v[i], rho, tau);
+        }
     }
-    if (acc == 1234.5f) sink[0] = acc;
+#pragma unroll
+    for (int step = 1; step < kProbeLanes; step *= 2) {
+#pragma unroll
+        for (int i = 0; i + step < kProbeLanes; i += 2 * step) v[i] += v[i + step];
+    }
+    out[g] = v[0];
+}
+
+// HBM read probe.  Block b reads its own contiguous slice of the buffer (16-byte words),
+// each thread four words 4 KiB apart per step, so every warp keeps four 512-byte requests
+// in flight and each block walks its slice front to back.  The words are folded with XOR
+// (integer work, far below the load rate) and each block stores its fold in fold[b]: the
+// XOR of all folds equals the XOR of every 32-bit word of the buffer, which the caller can
+// check, so no load can be dropped.
+__global__ void __launch_bounds__(256) hbm_read_probe_kernel(const uint4* __restrict__ x, int64_t words,
+                                                             uint32_t* fold) {
+    const int64_t per = (words + gridDim.x - 1) / gridDim.x;
+    const int64_t begin = static_cast<int64_t>(blockIdx.x) * per;
+    const int64_t end = begin + per < words ? begin + per : words;
+    uint32_t f = 0;
+    int64_t i = begin + threadIdx.x;
+    for (; i + 3 * 256 < end; i += 4 * 256) {
+        const uint4 a = __ldcs(x + i), b = __ldcs(x + i + 256);
+        const uint4 c = __ldcs(x + i + 512), d = __ldcs(x + i + 768);
+        f ^= (a.x ^ a.y ^ a.z ^ a.w) ^ (b.x ^ b.y ^ b.z ^ b.w) ^ (c.x ^ c.y ^ c.z ^ c.w) ^ (d.x ^ d.y ^ d.z ^ d.w);
+    }
+    for (; i < end; i += 256) {
+        const uint4 a = __ldcs(x + i);
+        f ^= a.x ^ a.y ^ a.z ^ a.w;
+    }
+    f = __reduce_xor_sync(0xffffffffu, f);
+    __shared__ uint32_t warp_fold[8];
+    if (threadIdx.x % 32 == 0) warp_fold[threadIdx.x / 32] = f;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t t = 0;
+        for (int w = 0; w < 8; ++w) t ^= warp_fold[w];
+        fold[blockIdx.x] = t;
+    }
 }
 
 // Tensor-core probe: one thread per CTA issues `iters` rounds of four M=128 x N x K=16
@@ -138,17 +176,18 @@ __global__ void wait_selftest_kernel(uint64_t limit_ns, unsigned int* status) {
 }  // namespace
 
 cudaError_t probe_ffma_launch(int packed, int64_t blocks, int iters, float* out, cudaStream_t stream) {
+    const float rho = 1.0f - 1.0f / 4096.0f, tau = 1.0f / 8192.0f;
     if (packed)
-        ffma_probe_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(out, iters);
+        fp32_issue_probe_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(out, iters, rho, tau);
     else
-        ffma_probe_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(out, iters);
+        fp32_issue_probe_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(out, iters, rho, tau);
     return cudaGetLastError();
 }
 
-cudaError_t probe_stream_read_launch(const float* x, int64_t n, float* sink, int64_t blocks,
+cudaError_t probe_stream_read_launch(const float* x, int64_t n, uint32_t* fold, int64_t blocks,
                                      cudaStream_t stream) {
-    stream_read_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        reinterpret_cast<const float4*>(x), n / 4, sink);
+    hbm_read_probe_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(reinterpret_cast<const uint4*>(x),
+                                                                             n / 4, fold);
     return cudaGetLastError();
 }
 

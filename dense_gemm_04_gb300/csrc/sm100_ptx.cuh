@@ -138,18 +138,6 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// The same load delivered to every CTA of the cluster named in `mask` (bit i = rank i), at
-// offset `dst` of each CTA's shared memory, with completion signalled on the barrier at
-// offset `bar` of each of those CTAs.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap* map, int32_t x,
-                                                      int32_t y, uint32_t bar, uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(mask)
-        : "memory");
-}
-
 // 2-SM form: the load lands in this CTA's shared memory at `dst`, and its bytes are counted
 // on the barrier at shared::cluster address `bar_cluster`, which may be in the peer CTA.
 __device__ __forceinline__ void tma_load_2d_2sm(uint32_t dst, const CUtensorMap* map, int32_t x,
@@ -304,15 +292,6 @@ __device__ __forceinline__ void mma_commit_2sm(uint32_t bar) {
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-        : "memory");
-}
-
-// As mma_commit, arriving once on the barrier at offset `bar` of every CTA in `mask`.
-__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(bar),
-        "h"(mask)
         : "memory");
 }
 

@@ -50,10 +50,13 @@ _SIGNATURES = {
     "phx_autotune": (_i32, [_i32, _i64, _i64, _i64, _i32, _i32, _i32, _vp]),
     "phx_tune_cache_save": (_i32, [_cp]),
     "phx_tune_cache_load": (_i32, [_cp]),
+    "phx_device_tag": (_i32, [_cp, _sz]),
+    "phx_autotune_report": (_i32, [_i32, _cp, _sz]),
     "phx_probe_ffma": (_i32, [_i32, _i64, _i32, _vp, _vp]),
     "phx_probe_stream_read": (_i32, [_vp, _i64, _vp, _i64, _vp]),
     "phx_probe_mma_f16": (_i32, [_i64, _i32, _i32, _vp, _vp]),
     "phx_selftest_bounded_wait": (_i32, [_u64, _vp]),
+    "phx_selftest_bounded_wait_noalloc": (_i32, [_u64, _vp]),
     "phx_selftest_tuner": (_i32, [_i32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_i32),
                                   ctypes.c_double, ctypes.c_double, _i32, _i32, _u64,
                                   ctypes.POINTER(_i32), ctypes.POINTER(_i64)]),
@@ -241,6 +244,20 @@ def autotune(variant: int, M: int, N: int, K: int, finalists: int = 4, rounds: i
     check(phx_autotune(variant, M, N, K, finalists, rounds, settle_ms, _stream_handle(stream)),
           "phx_autotune")
     return get_config(variant, M, N, K)
+
+
+def device_tag() -> str:
+    """The current device's key in the tuning cache ("<name>:<SMs>", or "none")."""
+    buf = ctypes.create_string_buffer(256)
+    check(phx_device_tag(buf, len(buf)), "phx_device_tag")
+    return buf.value.decode()
+
+
+def autotune_report(variant: int) -> str:
+    """The record of the last autotune of `variant` (finalists, median times and SM clocks)."""
+    buf = ctypes.create_string_buffer(1 << 14)
+    check(phx_autotune_report(variant, buf, len(buf)), "phx_autotune_report")
+    return buf.value.decode()
 
 
 def tune_cache_save(path: str) -> None:

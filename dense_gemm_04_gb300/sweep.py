@@ -130,12 +130,13 @@ def measure_roofs(seconds=2.0):
     for packed in (0, 1):
         t, clk = sustained(lambda: phx.check(phx.phx_probe_ffma(packed, blocks, iters, out.data_ptr(), st)), seconds)
         roofs["fp32_ffma2" if packed else "fp32_ffma"] = {
-            "tflops": blocks * 256 * iters * 16 * (2 if packed else 1) / t / 1e12, "clocks": clk}
+            "tflops": blocks * 256 * iters * 24 / t / 1e12, "clocks": clk}
     sink = torch.empty(sms, device="cuda")
     t, clk = sustained(lambda: phx.check(phx.phx_probe_mma_f16(sms, 4000, 256, sink.data_ptr(), st)), seconds)
     roofs["f16_tensor"] = {"tflops": sms * 4000 * 4 * 2 * 128 * 256 * 16 / t / 1e12, "clocks": clk}
     x = torch.ones(1 << 28, device="cuda")
-    t = steady(lambda: phx.check(phx.phx_probe_stream_read(x.data_ptr(), x.numel(), sink.data_ptr(), sms * 8, st)))
+    fold = torch.empty(sms * 8, dtype=torch.int32, device="cuda")
+    t = steady(lambda: phx.check(phx.phx_probe_stream_read(x.data_ptr(), x.numel(), fold.data_ptr(), sms * 8, st)))
     roofs["hbm_read_gbs"] = x.numel() * 4 / t / 1e9
     del x
     return roofs

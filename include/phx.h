@@ -107,19 +107,22 @@ phx_status phx_gemm_f16tc_f32acc(int64_t M, int64_t N, int64_t K, float alpha,
  * while they run: code in a latency-critical loop that must never wait on an allocator (an
  * allocation can block, grow a pool or fail under memory pressure), or a plug-in whose host
  * application owns the whole device-memory budget.  The paper has no counterpart; this is
- * about this library's memory handling only.  Same arguments, rounding, kernels and
- * results, but the f16 copies of A and B go to one array of static device memory inside the
- * library, so the call allocates nothing:
- *   - Limit: phx_f16tc_workspace_bytes(M, N, K) <= 64 MiB (M = N = K = 4096 fits exactly).
- *     A larger problem returns PHX_ERR_NOMEM before anything is launched.
+ * about this library's memory handling only.  Same arguments, rounding, kernels, schedule
+ * and results (bit for bit, split-K included), but the scratch -- the f16 copies of A and B,
+ * and the partial products of a grid split along K -- goes to one array of static device
+ * memory inside the library, so the call allocates nothing:
+ *   - Limit: the scratch of the call <= 64 MiB.  For shapes that do not split K that is
+ *     phx_f16tc_workspace_bytes(M, N, K) (M = N = K = 4096 fits exactly); few rows of A need
+ *     no copies, only the skinny kernel's partial sums.  A larger problem returns
+ *     PHX_ERR_NOMEM before anything is launched.
  *   - Every GPU that loads this part of the library holds the 64 MiB until the process ends.
  *   - The first call on each device looks up the array's device address (once per device,
  *     with that device current); make that first call before any stream capture begins.
  *   - All calls share the array.  Calls whose GPU work overlaps (different streams, or no
  *     ordering between them) race and corrupt each other's results: keep them ordered.
  *     Nothing needs clearing between calls: each call rewrites all the scratch it reads.
- *   - A device-side wait that gives up records its code in a status word inside that array,
- *     which phx_check_device_status does not read. */
+ *   - A device-side wait that gives up records PHX_ERR_TIMEOUT in a status word inside that
+ *     array; phx_check_device_status reads and clears it, like the pooled calls' word. */
 phx_status phx_gemm_f16tc_f32acc_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
                                          const float* A, const float* B, float beta, float* C,
                                          phx_stream_t stream);
@@ -187,9 +190,11 @@ phx_status phx_f16tc_workspace_bytes(int64_t M, int64_t N, int64_t K, size_t* by
 /* A static, human-readable name for a status code. */
 const char* phx_status_string(phx_status s);
 
-/* Synchronise `stream`, then read and clear the current device's status word: PHX_OK,
+/* Synchronise `stream`, then read and clear the current device's status words -- the one
+ * of the pooled entry points and the one inside phx_gemm_f16tc_f32acc_noalloc's static
+ * array, each if that part of the library has run on this device: PHX_OK,
  * PHX_ERR_TIMEOUT if a kernel gave up a bounded wait since the last check, or
- * PHX_ERR_LAUNCH if the stream reported an error. */
+ * PHX_ERR_LAUNCH if the stream reported an error.  Allocates nothing. */
 phx_status phx_check_device_status(phx_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
@@ -259,26 +264,44 @@ phx_status phx_last_config(int variant, char* buf, size_t buflen);
 phx_status phx_autotune(int variant, int64_t M, int64_t N, int64_t K, int finalists,
                         int rounds, int settle_ms, phx_stream_t stream);
 
-/* Save the tuning cache to a text file (one line per variant and shape) or merge one in. */
+/* The tuning cache is keyed by device as well as by variant and shape: a device's tag is
+ * its name with spaces as underscores, a colon and its SM count ("NVIDIA_GB300:152"; "none"
+ * without a device), and a tuned configuration is only used on a device with the tag it was
+ * tuned on.  phx_device_tag writes the current device's tag to buf. */
+phx_status phx_device_tag(char* buf, size_t buflen);
+
+/* Save the tuning cache to a text file, one line per entry ("<tag> <variant> <M> <N> <K>
+ * <configuration>"), or merge one in (PHX_ERR_CONFIG if a line does not parse; nothing is
+ * merged then).  With the environment variable PHX_TUNE_CACHE=<path>, the first call of the
+ * process merges that file in (if it exists) and every phx_autotune rewrites it. */
 phx_status phx_tune_cache_save(const char* path);
 phx_status phx_tune_cache_load(const char* path);
 
+/* The record of the last phx_autotune of `variant`: the device, the shape, the pick, and
+ * one line per finalist with the median of its second-stage timings and the median SM clock
+ * read (through NVML queries; -1 where NVML is unavailable) right after each of them, as
+ * NUL-terminated text ("NONE" before any tuning). */
+phx_status phx_autotune_report(int variant, char* buf, size_t buflen);
+
 /* ---------------------------------------------------------------------------------------
- * Roof probes, after the lab's Part 1 (a kernel of nothing but independent multiply-adds,
- * and a streaming read); used to measure the denominators of the roofline.
+ * Roof probes: the two roofs of the matrix-multiplication lab's Part 1 (the FP32
+ * multiply-add rate and the memory read rate), measured with kernels designed for sm_103a;
+ * used for the denominators of the roofline.
  * ------------------------------------------------------------------------------------- */
 
-/* FP32 multiply-add probe: `blocks` CTAs of 256 threads, each thread running 8
- * independent chains for `iters` iterations (packed = 1: 8 chains of f32x2 pairs).
- * Floating-point operations performed: blocks * 256 * iters * 16 * (packed ? 2 : 1).
- * `out` (device, blocks * 256 floats) receives one value per thread. */
+/* FP32 multiply-add probe: `blocks` CTAs of 256 threads; each thread keeps 12 independent
+ * recurrences x <- x * rho + tau in registers for `iters` iterations (packed = 1: the same
+ * recurrences two per f32x2 instruction).  Floating-point operations performed:
+ * blocks * 256 * iters * 24, packed or not.  `out` (device, blocks * 256 floats) receives
+ * one value per thread, in [0.5, 1). */
 phx_status phx_probe_ffma(int packed, int64_t blocks, int iters, float* out,
                           phx_stream_t stream);
 
-/* Streaming-read probe: sums n floats of x (device, 16-byte aligned, n % 4 == 0) with
- * `blocks` CTAs of 256 threads; reads 4 * n bytes.  `sink` (device, 1 float) is written
- * only if the sum equals a sentinel, so the read cannot be optimised away. */
-phx_status phx_probe_stream_read(const float* x, int64_t n, float* sink, int64_t blocks,
+/* HBM read probe: reads n floats of x (device, 16-byte aligned, n % 4 == 0; 4 * n bytes)
+ * with `blocks` CTAs of 256 threads, each CTA one contiguous slice.  `fold` (device,
+ * `blocks` 32-bit words) receives, per CTA, the XOR of every 32-bit word of its slice: the
+ * XOR of all `blocks` words equals the XOR of every word of x, which proves the read. */
+phx_status phx_probe_stream_read(const float* x, int64_t n, uint32_t* fold, int64_t blocks,
                                  phx_stream_t stream);
 
 /* Tensor-core probe: `ctas` CTAs each issue `iters` rounds of 4 tcgen05.mma kind::f16
@@ -297,6 +320,11 @@ phx_status phx_probe_mma_f16(int64_t ctas, int iters, int n, float* sink,
  * gives up, records PHX_ERR_TIMEOUT in the status word and the kernel exits normally;
  * phx_check_device_status() then returns PHX_ERR_TIMEOUT.  No fault, trap or hang. */
 phx_status phx_selftest_bounded_wait(uint64_t limit_ns, phx_stream_t stream);
+
+/* The same self-test with the status word of phx_gemm_f16tc_f32acc_noalloc (inside its
+ * static array; the first call on a device sets that device up as the GEMM call does):
+ * phx_check_device_status() then returns PHX_ERR_TIMEOUT from that word.  Allocates nothing. */
+phx_status phx_selftest_bounded_wait_noalloc(uint64_t limit_ns, phx_stream_t stream);
 
 /* Run the autotuner's selection logic (stages 1 and 2 of phx_autotune) on a simulated
  * set of `n` candidates without any GPU: candidate i "takes" base_s[i] seconds scaled by

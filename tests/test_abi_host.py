@@ -2,6 +2,7 @@
 function include/phx.h declares, and its argument checks, configuration table, config
 parsing and tuner selection logic behave as documented."""
 import ctypes
+import os
 
 import pytest
 
@@ -155,42 +156,102 @@ def test_tuner_second_stage_resists_drift():
         assert picked == 0, seed
 
 
-def test_tuner_cache_file_round_trip(tmp_path):
+def test_tuner_cache_is_keyed_by_device(tmp_path):
+    tag = phx.device_tag()          # "none" on a host without a GPU
+    assert tag == "none" or ":" in tag
+    other = "OTHER_GPU:10" if tag != "OTHER_GPU:10" else "OTHER_GPU:11"
     p = tmp_path / "tune.txt"
-    p.write_text("# variant M N K config\n0 4096 4096 4096 TILE_M=128 TILE_N=64 TILE_K=8 STAGES=4 FMA2=0\n"
-                 "1 8192 8192 1024 TILE_M=128 TILE_N=128 TILE_K=64 STAGES=6\n")
+    p.write_text("# device variant M N K config\n"
+                 f"{tag} 0 4096 4096 4096 TILE_M=128 TILE_N=64 TILE_K=8 STAGES=4 FMA2=0\n"
+                 f"{tag} 1 8192 8192 1024 TILE_M=128 TILE_N=128 TILE_K=64 STAGES=6\n"
+                 f"{other} 0 2048 2048 2048 TILE_M=64 TILE_N=64 TILE_K=8 STAGES=4\n")
     phx.set_config(0, None)
     phx.set_config(1, None)
+    default_2048 = phx.get_config(0, 2048, 2048, 2048)
     phx.tune_cache_load(str(p))
     assert phx.get_config(0, 4096, 4096, 4096) == "TILE_M=128 TILE_N=64 TILE_K=8 STAGES=4 FMA2=0"
     assert phx.get_config(1, 8192, 8192, 1024) == "TILE_M=128 TILE_N=128 TILE_K=64 STAGES=6"
+    # another GPU's entry is kept but never applied here
+    assert phx.get_config(0, 2048, 2048, 2048) == default_2048
     out = tmp_path / "out.txt"
     phx.tune_cache_save(str(out))
     text = out.read_text()
-    assert "0 4096 4096 4096 TILE_M=128 TILE_N=64" in text
-    bad = tmp_path / "bad.txt"
-    bad.write_text("0 1 1 1 TILE_M=3 TILE_N=3 TILE_K=3\n")
-    with pytest.raises(phx.PhxError):
-        phx.tune_cache_load(str(bad))
+    assert f"{tag} 0 4096 4096 4096 TILE_M=128 TILE_N=64" in text
+    assert f"{other} 0 2048 2048 2048 TILE_M=64 TILE_N=64" in text
+    for bad_line in ("0 4096 4096 4096 TILE_M=128 TILE_N=64 TILE_K=8\n",      # no device tag
+                     f"{tag} 0 1 1 1 TILE_M=3 TILE_N=3 TILE_K=3\n"):         # no such config
+        bad = tmp_path / "bad.txt"
+        bad.write_text(bad_line)
+        with pytest.raises(phx.PhxError):
+            phx.tune_cache_load(str(bad))
 
 
-def test_cluster_key():
+def _fresh_process(code, env):
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    full_env = dict(os.environ, **env)
+    return subprocess.run([sys.executable, "-c", code], cwd=root, env=full_env,
+                          capture_output=True, text=True, timeout=300)
+
+
+def test_unparsable_env_pin_is_an_error_not_ignored():
+    code = ("from dense_gemm_04_gb300 import phx\n"
+            "try:\n"
+            "    phx.get_config(0, 512, 512, 512)\n"
+            "    print('NO ERROR')\n"
+            "except phx.PhxError as e:\n"
+            "    print('ERR', e.status)\n"
+            "print('F16', phx.get_config(1, 512, 512, 512))\n"
+            "phx.set_config(0, None)\n"
+            "print('AFTER', phx.get_config(0, 512, 512, 512))\n")
+    r = _fresh_process(code, {"PHX_CONFIG_SGEMM": "TILE_M=3 TILE_N=3 TILE_K=3"})
+    assert r.returncode == 0, r.stderr
+    lines = r.stdout.splitlines()
+    assert lines[0] == f"ERR {phx.PHX_ERR_CONFIG}", r.stdout
+    assert lines[1].startswith("F16 TILE_M="), r.stdout       # the other variant is unaffected
+    assert lines[2].startswith("AFTER TILE_M="), r.stdout     # phx_set_config replaces the pin
+    assert "PHX_CONFIG_SGEMM" in r.stderr                     # logged, whatever PHX_LOG says
+
+
+def test_tune_cache_env_file_is_read_at_first_use(tmp_path):
+    p = tmp_path / "cache.txt"
+    code = ("from dense_gemm_04_gb300 import phx\n"
+            "print(phx.device_tag())\n"
+            "print(phx.get_config(0, 3000, 3000, 3000))\n")
+    first = _fresh_process(code, {})
+    tag = first.stdout.splitlines()[0]
+    p.write_text(f"{tag} 0 3000 3000 3000 TILE_M=64 TILE_N=128 TILE_K=8 STAGES=4\n")
+    r = _fresh_process(code, {"PHX_TUNE_CACHE": str(p)})
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.splitlines()[1] == "TILE_M=64 TILE_N=128 TILE_K=8 STAGES=4 FMA2=0", r.stdout
+
+
+def test_no_multicast_configurations():
+    # every f16 configuration is one CTA per 128-row tile or a 2-SM pair (TILE_M = 256); no
+    # CLUSTER key is accepted (CTA pairs that multicast a B tile are not built)
     names = phx.config_names(phx.VARIANT_F16TC)
-    clustered = [n for n in names if n.endswith(" CLUSTER=2")]
-    assert clustered, names
-    for n in clustered:
-        phx.set_config(phx.VARIANT_F16TC, n)
-        assert phx.get_config(phx.VARIANT_F16TC, 4096, 4096, 4096) == n
-    # without the key, the pair-free configuration of the same tile is meant
-    base = clustered[0].replace(" CLUSTER=2", "")
-    phx.set_config(phx.VARIANT_F16TC, base)
-    assert phx.get_config(phx.VARIANT_F16TC, 4096, 4096, 4096) == base
-    for bad in (base + " CLUSTER=3", ):
+    assert not [n for n in names if "CLUSTER" in n], names
+    for n in names:
+        if n != "SKINNY":
+            assert n.split()[0] in ("TILE_M=128", "TILE_M=256"), n
+    for bad in ("TILE_M=256 TILE_N=256 TILE_K=64 STAGES=6 CLUSTER=2",
+                "TILE_M=128 TILE_N=256 TILE_K=64 STAGES=4 CLUSTER=1"):
         with pytest.raises(phx.PhxError):
             phx.set_config(phx.VARIANT_F16TC, bad)
     with pytest.raises(phx.PhxError):
         phx.set_config(phx.VARIANT_SGEMM, "TILE_M=128 TILE_N=128 TILE_K=16 CLUSTER=2")
     phx.set_config(phx.VARIANT_F16TC, None)
+
+
+def test_no_multicast_load_in_the_sources():
+    # a TMA load with cluster multicast is not used anywhere in the library
+    import pathlib
+    csrc = pathlib.Path(__file__).resolve().parents[1] / "dense_gemm_04_gb300" / "csrc"
+    for f in sorted(csrc.iterdir()):
+        if f.suffix in (".cu", ".cuh", ".h", ".inc"):
+            for i, line in enumerate(f.read_text().splitlines(), 1):
+                assert not ("cp.async.bulk" in line and "multicast" in line), f"{f.name}:{i}: {line}"
 
 
 def test_ex_calls_check_the_op_first():

@@ -54,3 +54,43 @@ def test_one_rank_needs_no_process_group():
     import bench
     assert bench.reduce_max(1.25, 1) == 1.25
     assert bench.whole_job_tflops(1, 4, 2e12, 0.5) == pytest.approx(16.0)
+
+
+def _run_stub(argv, env_extra=None, drop_dist_env=True):
+    import json
+    import subprocess
+    env = dict(os.environ)
+    if drop_dist_env:
+        for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT"):
+            env.pop(k, None)
+    env.update(env_extra or {})
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "tests", "bench_stub_rank.py"), *argv],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    return r, [json.loads(ln) for ln in lines]
+
+
+def test_gpus_2_starts_two_ranks_and_reports_the_slowest():
+    # bench.main with --gpus 2 and no outside launcher starts two ranks itself; each runs the
+    # stand-in replica (rank r: steps of 1 + r ms) and rank 0 alone prints the line
+    steps = 5
+    r, lines = _run_stub(["--gpus", "2", "--steps", str(steps), "--warmup", "3", "--no-cpu-baseline"])
+    assert r.returncode == 0, r.stderr[-3000:]
+    assert len(lines) == 1, r.stdout
+    out = lines[0]
+    assert out["n_gpus"] == 2
+    assert out["scaling"] == "weak"
+    assert out["ms_per_step"] == pytest.approx(2.0)                 # the slower rank's step
+    flops_per_step = 2 * 2.0 * 4096 ** 3
+    assert out["value"] == pytest.approx(2 * steps * flops_per_step / (steps * 2e-3) / 1e12)
+    # e2e: the slower rank's median run of 4 steps (4 x 2 x 2 ms), both ranks' work
+    assert out["e2e"]["value"] == pytest.approx(2 * 4 * flops_per_step / 16e-3 / 1e12)
+    assert out["config"]["parallelism"] == "replicas x2 (no collective)"
+
+
+def test_rank_count_must_match_gpus():
+    r, lines = _run_stub(["--gpus", "2", "--steps", "3", "--warmup", "3"],
+                         env_extra={"WORLD_SIZE": "1", "RANK": "0", "LOCAL_RANK": "0"})
+    assert r.returncode != 0
+    assert not lines
+    assert "WORLD_SIZE=1" in r.stderr

@@ -57,9 +57,15 @@ def test_probes_run():
         assert phx.phx_probe_ffma(packed, 64, 1000, out.data_ptr(), s) == phx.PHX_OK
         torch.cuda.synchronize()
         assert torch.isfinite(out).all() and (out > 0).all()
-    x = torch.ones(1 << 20, device="cuda")
-    sink = torch.zeros(1, device="cuda")
-    assert phx.phx_probe_stream_read(x.data_ptr(), x.numel(), sink.data_ptr(), 256, s) == phx.PHX_OK
+    # the read probe's per-block XOR folds combine to the XOR of every word of the buffer
+    # (a ragged length, so the last block's slice is short)
+    n = (1 << 20) + 4 * 37
+    words = np.random.default_rng(3).integers(0, 2 ** 32, size=n, dtype=np.uint64).astype(np.uint32)
+    x = torch.from_numpy(words.view(np.float32)).cuda()
+    fold = torch.zeros(256, dtype=torch.int32, device="cuda")
+    assert phx.phx_probe_stream_read(x.data_ptr(), n, fold.data_ptr(), 256, s) == phx.PHX_OK
+    torch.cuda.synchronize()
+    assert np.bitwise_xor.reduce(fold.cpu().numpy().view(np.uint32)) == np.bitwise_xor.reduce(words)
     sink_mma = torch.full((8,), 7.0, device="cuda")
     for n in (64, 128, 256):
         assert phx.phx_probe_mma_f16(8, 100, n, sink_mma.data_ptr(), s) == phx.PHX_OK
