@@ -264,6 +264,24 @@ def test_results_identical_run_to_run(vname):
             assert np.array_equal(o.view(np.uint32), outs[0].view(np.uint32)), (vname, M, N, K)
 
 
+@pytest.mark.parametrize("shape", [(4096, 4096, 4096), (1000, 1000, 4000), (512, 512, 8192), (4095, 4097, 4093),
+                                   (16384, 128, 1024)])
+def test_new_inputs_in_reused_workspace(shape):
+    # The f16 call's scratch (rounded operand copies, ready flags, split-K planes) comes from a
+    # pool and is reused by the next call of the same shape.  Alternating two problems of one
+    # shape, every result must still be its own problem's: a part of the copies that a call
+    # failed to write, or a flag it failed to set, would surface as the other problem's values
+    # (or as a timeout).
+    M, N, K = shape
+    probs = [synth.problem(M, N, K, seed=s, dist="int3") for s in (31, 32)]
+    wants = [oracle.gemm(A, B, C, 1.0, -1.0, f16_inputs=True, want_mag=False)[0] for A, B, C in probs]
+    for i in (0, 1, 0, 1):
+        A, B, C = probs[i]
+        st, got = run_cuda(phx.VARIANT_F16TC, A, B, C, 1.0, -1.0)
+        assert st == phx.PHX_OK, phx.status_string(st)
+        assert_bits_equal(got, wants[i], f"f16tc {shape} problem {i}")
+
+
 def test_tiling_does_not_change_values():
     # Every configuration computes the same products; only how the k sums are grouped may
     # differ (one k-ordered chain per element, or, where a grid is split along K or its last
