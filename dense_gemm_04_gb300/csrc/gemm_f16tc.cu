@@ -30,7 +30,9 @@
 
 #include <cstdint>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "internal.h"
 #include "sm100_ptx.cuh"
@@ -730,19 +732,46 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// Tensor map of a row-major f16 matrix (rows x Kp) read in boxes of 64 halves x box_rows,
-// 128-byte swizzle, zero fill outside the matrix.
-// A K-major f16 operand: `rows` rows of `Kp` halves (a multiple of 8), `ld` halves apart.
-bool make_map(CUtensorMap* map, const __half* ptr, int64_t rows, int64_t Kp, int box_rows, int64_t ld) {
+// A 2-D tiled tensor map (128-byte swizzle, 256-byte L2 promotion, zero fill), encoded once
+// per (data type, address, extents, row stride, box): a call of the same shape on the same
+// (pooled, hence usually recurring) buffers finds its maps in this small cache.  The map
+// depends on nothing else (not on the device: the address alone names the memory).
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, void* ptr, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+    using Key = std::tuple<int, uintptr_t, uint64_t, uint64_t, uint64_t, uint32_t, uint32_t>;
+    constexpr size_t kMaxEntries = 256;
+    static std::mutex mu;
+    static std::map<Key, CUtensorMap> cache;
+    const Key key(static_cast<int>(dt), reinterpret_cast<uintptr_t>(ptr), inner, outer, row_bytes, box_inner,
+                  box_outer);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) {
+            *map = it->second;
+            return true;
+        }
+    }
     EncodeTiledFn enc = encode_fn();
     if (enc == nullptr) return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(Kp), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+    const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(ptr), dims, strides,
-               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    if (enc(map, dt, 2, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache.size() >= kMaxEntries) cache.clear();
+    cache.emplace(key, *map);
+    return true;
+}
+
+// Tensor map of a K-major f16 operand: `rows` rows of `Kp` halves (a multiple of 8), `ld`
+// halves apart, read in boxes of 64 halves x box_rows.
+bool make_map(CUtensorMap* map, const __half* ptr, int64_t rows, int64_t Kp, int box_rows, int64_t ld) {
+    return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, const_cast<__half*>(ptr), static_cast<uint64_t>(Kp),
+                     static_cast<uint64_t>(rows), static_cast<uint64_t>(ld) * 2, kBK, static_cast<uint32_t>(box_rows));
 }
 
 using TcKernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, float*, int, int, int,
@@ -752,15 +781,8 @@ using TcKernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, 
 // C (M x N f32, rows N floats apart) as 32 x 32 boxes in the 128-byte swizzled layout, for
 // the TMA epilogue.  Needs N % 4 == 0 and a 16-byte aligned C.
 bool make_map_c(CUtensorMap* map, float* C, int64_t M, int64_t N) {
-    EncodeTiledFn enc = encode_fn();
-    if (enc == nullptr) return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * 4};
-    const cuuint32_t box[2] = {32, 32};
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, C, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, static_cast<uint64_t>(N), static_cast<uint64_t>(M),
+                     static_cast<uint64_t>(N) * 4, 32, 32);
 }
 
 struct TcEntry {
@@ -954,8 +976,8 @@ cudaError_t f16tc_gemm_launch_ops(int index, int64_t M, int64_t N, int64_t K, fl
     float* partial = ksplit > 1 ? static_cast<float*>(split_ws) : nullptr;
     const int epi_tma = (c_tma_ok && ksplit == 1) ? 1 : 0;
     if (epi_tma) fn = e.fn_tma;
-    err = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(e.smem));
+    err = set_func_attr_once(reinterpret_cast<const void*>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(e.smem));
     if (err != cudaSuccess) return err;
     err = cudaLaunchKernelEx(&lc, fn, mapA, mapB, mapB_half, mapB_quarter, C, m32, n32, num_kb, alpha,
                              beta, tiles_m, tiles_n, status, full32, tail_split, ksplit, kb_per, partial, Ch,

@@ -17,6 +17,11 @@ namespace phx {
 void note_launches(int n);
 int64_t noted_launches();
 
+// cudaFuncSetAttribute(fn, attr, value) on the current device, once per (device, fn, attr,
+// value): function attributes live with the device's context, so later calls skip the
+// runtime call (phx_api.cu).
+cudaError_t set_func_attr_once(const void* fn, cudaFuncAttribute attr, int value);
+
 // `err` of a kernel launch, noted as one launch when it succeeded.
 inline cudaError_t launched(cudaError_t err) {
     if (err == cudaSuccess) note_launches(1);

@@ -1135,6 +1135,25 @@ namespace phx {
 
 void note_launches(int n) { t_launches += n; }
 
+cudaError_t set_func_attr_once(const void* fn, cudaFuncAttribute attr, int value) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, const void*, int, int>, bool> done;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    const auto key = std::make_tuple(dev, fn, static_cast<int>(attr), value);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (done.count(key)) return cudaSuccess;
+    }
+    err = cudaFuncSetAttribute(fn, attr, value);
+    if (err == cudaSuccess) {
+        std::lock_guard<std::mutex> lock(mu);
+        done[key] = true;
+    }
+    return err;
+}
+
 int64_t noted_launches() { return t_launches; }
 
 }  // namespace phx

@@ -194,9 +194,8 @@ cudaError_t probe_stream_read_launch(const float* x, int64_t n, uint32_t* fold, 
 cudaError_t probe_mma_f16_launch(int64_t ctas, int iters, int n, float* sink, unsigned int* status,
                                  cudaStream_t stream) {
     auto run = [&](auto kernel, uint32_t bytes) {
-        cudaError_t err = cudaFuncSetAttribute(reinterpret_cast<const void*>(kernel),
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(bytes));
+        cudaError_t err = set_func_attr_once(reinterpret_cast<const void*>(kernel),
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
         if (err != cudaSuccess) return err;
         kernel<<<static_cast<unsigned>(ctas), 128, bytes, stream>>>(iters, sink, status);
         return cudaGetLastError();

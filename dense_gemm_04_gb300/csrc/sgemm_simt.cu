@@ -443,22 +443,25 @@ int sgemm_edge(int index, int64_t M, int64_t N, int64_t K, const float* A, const
 
 namespace {
 
-// CTAs of `fn` that fit on one SM at once (cached per kernel).
+// CTAs of `fn` that fit on one SM at once (cached per device and kernel).
 int ctas_per_sm(KernelFn fn, int smem) {
     static std::mutex mu;
-    static std::map<KernelFn, int> cache;
+    static std::map<std::pair<int, KernelFn>, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const auto key = std::make_pair(dev, fn);
     std::lock_guard<std::mutex> lock(mu);
-    auto it = cache.find(fn);
+    auto it = cache.find(key);
     if (it != cache.end()) return it->second;
     int n = 0;
-    if (cudaFuncSetAttribute(reinterpret_cast<const void*>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem) != cudaSuccess ||
+    if (set_func_attr_once(reinterpret_cast<const void*>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreads, smem) != cudaSuccess) {
         cudaGetLastError();
         n = 1;
     }
     if (n < 1) n = 1;
-    cache[fn] = n;
+    cache[key] = n;
     return n;
 }
 
@@ -622,9 +625,8 @@ cudaError_t sgemm_launch(int index, int64_t M, int64_t N, int64_t K, float alpha
     const Entry& e = kEntries[index];
     const int edge = sgemm_edge(index, M, N, K, A, B, C);
     KernelFn fn = e.fn[edge];
-    cudaError_t err = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           e.smem_bytes);
+    cudaError_t err = set_func_attr_once(reinterpret_cast<const void*>(fn),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, e.smem_bytes);
     if (err != cudaSuccess) return err;
     const int64_t tiles = ((M + e.cfg.tile_m - 1) / e.cfg.tile_m) * ((N + e.cfg.tile_n - 1) / e.cfg.tile_n);
     if (tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
@@ -639,8 +641,8 @@ cudaError_t sgemm_launch(int index, int64_t M, int64_t N, int64_t K, float alpha
     if (sk.blocks > 0) {
         // the stream-K blocks first, one per CTA slot: they fill the GPU on their own
         StreamKFn skf = e.sk[edge];
-        err = cudaFuncSetAttribute(reinterpret_cast<const void*>(skf), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   e.smem_bytes);
+        err = set_func_attr_once(reinterpret_cast<const void*>(skf), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 e.smem_bytes);
         if (err != cudaSuccess) return err;
         sk.slots = static_cast<float*>(workspace);
         skf<<<static_cast<unsigned>(sk.blocks), kThreads, e.smem_bytes, stream>>>(
