@@ -52,18 +52,31 @@ bool sgemm_is_aligned(int index, int64_t M, int64_t N, int64_t K, const float* A
 // Scratch bytes config `index` uses for this problem on `num_sms` SMs: the partial
 // products of the K slices when a grid too small for the GPU is split along K (0 if not).
 size_t sgemm_workspace_bytes(int index, int64_t M, int64_t N, int64_t K, const float* A,
-                             const float* B, const float* C, int num_sms);
+                             const float* B, const float* C, int num_sms, int64_t ldb = -1);
 
 // Enqueue config `index` (the aligned kernel when sgemm_is_aligned; else the kernel with
-// 16-byte edge copies when K % 4 == N % 4 == 0 and A, B, C are 16-byte aligned; else the one
-// with 4-byte edge copies).  When sgemm_workspace_bytes is not 0 and `workspace` holds that
+// 16-byte edge copies when K % 4 == ldb % 4 == 0 and A, B are 16-byte aligned, which stores C
+// 16 bytes at a time when N % 4 == 0 and C is 16-byte aligned and 4 bytes at a time otherwise;
+// else the one with 4-byte edge copies).  B's rows are ldb floats apart (ldb = -1: N; a
+// larger ldb for B in a padded copy, whose columns past N must be zero).  When sgemm_workspace_bytes is not 0 and `workspace` holds that
 // many bytes, the last partial wave (or a grid of less than one wave) is spread as stream-K
 // blocks and then fixed up, or a small grid is split along K and then reduced; with
 // workspace == nullptr the grid runs as tiles only.
 // Requires M, N > 0, K > 0 and alpha != 0 (the caller handles the degenerate cases).
 cudaError_t sgemm_launch(int index, int64_t M, int64_t N, int64_t K, float alpha,
                          const float* A, const float* B, float beta, float* C, void* workspace,
-                         int num_sms, cudaStream_t stream);
+                         int num_sms, cudaStream_t stream, int64_t ldb = -1);
+
+// True if config `index` on this problem would copy operands 4 bytes at a time (rows of A or
+// B not 16-byte aligned: K % 4 != 0, N % 4 != 0, or an unaligned base).
+bool sgemm_scalar_edge(int index, int64_t M, int64_t N, int64_t K, const float* A, const float* B,
+                       const float* C);
+
+// dst (rows x dcols, row-major, dcols % 4 == 0, 16-byte aligned) <- src (srows x scols, rows
+// sld floats apart) with zeros past srows and scols: a copy of an operand whose rows start on
+// 16 bytes.
+cudaError_t pad_copy_launch(const float* src, int64_t srows, int64_t scols, int64_t sld, float* dst, int64_t rows,
+                            int64_t dcols, int num_sms, cudaStream_t stream);
 
 // Host check of the f32 GEMM's schedule for config `index` with `per_sm` CTAs per SM on
 // `num_sms` SMs (no device involved): out[0] tiles that run whole (all of them without a

@@ -583,6 +583,58 @@ phx_status launch_skinny(int variant, int trans_a, int trans_b, int64_t M, int64
     return err == cudaSuccess ? PHX_OK : PHX_ERR_LAUNCH;
 }
 
+// A large f32 problem whose rows of A or B do not start on 16 bytes (K % 4 != 0, N % 4 != 0,
+// or an unaligned base) would be copied 4 bytes at a time.  Instead, A (when K % 4 != 0 or A
+// is unaligned) is copied into M x Kp and B into Kp x Np (Kp, Np: K, N rounded up to a
+// multiple of 4), zeros in the new columns and rows, in pooled scratch; the 16-byte-copy
+// kernel then runs on (M, N, Kp) with B's rows Np apart and writes C in place (4-byte stores
+// when C's rows are not 16-byte aligned).  The zeros add exact zeros, so the result is the
+// same (up to the sign of a zero sum), for two copies of A and B (about 2 % of a 4096-class
+// GEMM).
+phx_status launch_sgemm_padded(int cfg, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+                               const float* B, float beta, float* C, DevState* d, cudaStream_t stream) {
+    auto r256 = [](int64_t b) { return (b + 255) / 256 * 256; };
+    auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    const int64_t Kp = (K + 3) / 4 * 4, Np = (N + 3) / 4 * 4;
+    const bool pad_a = K % 4 != 0 || !al16(A);
+    const bool pad_b = K % 4 != 0 || N % 4 != 0 || !al16(B);
+    const int64_t a_bytes = pad_a ? r256(M * Kp * 4) : 0;
+    const int64_t b_bytes = pad_b ? r256(Kp * Np * 4) : 0;
+    const float* Ap = A;
+    const float* Bp = B;
+    const int64_t ldb = pad_b ? Np : N;
+    // the stream-K or split-K scratch of the padded problem follows the copies
+    const size_t sk_bytes = phx::sgemm_workspace_bytes(cfg, M, N, Kp, reinterpret_cast<const float*>(256),
+                                                       reinterpret_cast<const float*>(256), C, d->sm_count, ldb);
+    void* ws = nullptr;
+    if (cudaMallocFromPoolAsync(&ws, static_cast<size_t>(a_bytes + b_bytes) + sk_bytes, d->pool, stream) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return PHX_ERR_NOMEM;
+    }
+    cudaError_t err = cudaSuccess;
+    if (pad_a) {
+        float* Ad = static_cast<float*>(ws);
+        err = timed(kKindTranspose, stream,
+                    [&] { return phx::pad_copy_launch(A, M, K, K, Ad, M, Kp, d->sm_count, stream); });
+        Ap = Ad;
+    }
+    if (err == cudaSuccess && pad_b) {
+        float* Bd = reinterpret_cast<float*>(static_cast<char*>(ws) + a_bytes);
+        err = timed(kKindTranspose, stream,
+                    [&] { return phx::pad_copy_launch(B, K, N, N, Bd, Kp, Np, d->sm_count, stream); });
+        Bp = Bd;
+    }
+    if (err == cudaSuccess) {
+        void* sk_ws = sk_bytes > 0 ? static_cast<char*>(ws) + a_bytes + b_bytes : nullptr;
+        err = timed(kKindSgemm, stream, [&] {
+            return phx::sgemm_launch(cfg, M, N, Kp, alpha, Ap, Bp, beta, C, sk_ws, d->sm_count, stream, ldb);
+        });
+    }
+    cudaFreeAsync(ws, stream);
+    return err == cudaSuccess ? PHX_OK : PHX_ERR_LAUNCH;
+}
+
 phx_status launch_variant(int variant, int cfg, int64_t M, int64_t N, int64_t K, float alpha,
                           const float* A, const float* B, float beta, float* C, DevState* d,
                           cudaStream_t stream, int trans_a = 0, int trans_b = 0) {
@@ -590,6 +642,9 @@ phx_status launch_variant(int variant, int cfg, int64_t M, int64_t N, int64_t K,
         return launch_skinny(variant, trans_a, trans_b, M, N, K, alpha, A, B, beta, C, d, stream);
     if (variant == PHX_VARIANT_SGEMM && (trans_a || trans_b))
         return launch_sgemm_transposed(cfg, trans_a, trans_b, M, N, K, alpha, A, B, beta, C, d, stream);
+    if (variant == PHX_VARIANT_SGEMM && phx::sgemm_scalar_edge(cfg, M, N, K, A, B, C) && M >= 512 && N >= 512 &&
+        M * N * K >= (int64_t(1) << 32))
+        return launch_sgemm_padded(cfg, M, N, K, alpha, A, B, beta, C, d, stream);
     if (variant == PHX_VARIANT_SGEMM) {
         // pooled scratch only for a stream-K spread or a grid split along K
         const size_t bytes = phx::sgemm_workspace_bytes(cfg, M, N, K, A, B, C, d->sm_count);

@@ -153,18 +153,19 @@ __host__ __device__ __forceinline__ int64_t streamk_first_block(int64_t lo, int6
 // at C (element (row, col) at C[(row - m0) * BN + col - n0]).
 template <int BM, int BN, int BK, int STAGES, int TM, int TN, int EDGE, bool FMA2, bool LOCAL>
 __device__ __forceinline__ void sgemm_tile(const float* __restrict__ A, const float* __restrict__ B,
-                                           float* __restrict__ C, int M, int N, int K, float alpha, float beta,
-                                           int k_slice, float* __restrict__ partial, int tile, int kt0, int kt1) {
+                                           float* __restrict__ C, int M, int N, int K, int ldb, float alpha,
+                                           float beta, int k_slice, float* __restrict__ partial, int tile, int kt0,
+                                           int kt1) {
 #include "sgemm_tile_body.inc"
 }
 
 template <int BM, int BN, int BK, int STAGES, int TM, int TN, int EDGE, bool FMA2, int MINB>
 __global__ void __launch_bounds__(kThreads, MINB)
 sgemm_kernel(const float* __restrict__ A, const float* __restrict__ B, float* __restrict__ C,
-             int M, int N, int K, float alpha, float beta, int k_slice, float* __restrict__ partial) {
+             int M, int N, int K, int ldb, float alpha, float beta, int k_slice, float* __restrict__ partial) {
     if constexpr (EDGE != kEdgeScalar) {
-        sgemm_tile<BM, BN, BK, STAGES, TM, TN, EDGE, FMA2, false>(A, B, C, M, N, K, alpha, beta, k_slice, partial, 0,
-                                                                  0, 0);
+        sgemm_tile<BM, BN, BK, STAGES, TM, TN, EDGE, FMA2, false>(A, B, C, M, N, K, ldb, alpha, beta, k_slice, partial,
+                                                                  0, 0, 0);
     } else {
         constexpr bool LOCAL = false;
         int tile = 0;
@@ -178,7 +179,7 @@ sgemm_kernel(const float* __restrict__ A, const float* __restrict__ B, float* __
 // next), each written as a BM x BN tile of partial sums to slot 2s + segment.
 template <int BM, int BN, int BK, int STAGES, int TM, int TN, int EDGE, bool FMA2, int MINB>
 __global__ void __launch_bounds__(kThreads, MINB)
-sgemm_streamk_kernel(const float* __restrict__ A, const float* __restrict__ B, int M, int N, int K,
+sgemm_streamk_kernel(const float* __restrict__ A, const float* __restrict__ B, int M, int N, int K, int ldb,
                      const StreamK sk) {
     const int k_tiles = (K + BK - 1) / BK;
     const int64_t s = blockIdx.x;
@@ -192,7 +193,8 @@ sgemm_streamk_kernel(const float* __restrict__ A, const float* __restrict__ B, i
         const int kt1 = static_cast<int>(min(static_cast<int64_t>(k_tiles), kt0 + (end - it)));
         if (seg > 0) __syncthreads();  // the first segment is done with the shared buffers
         sgemm_tile<BM, BN, BK, STAGES, TM, TN, EDGE, FMA2, true>(A, B, sk.slots + (2 * s + seg) * (BM * BN), M, N, K,
-                                                                   1.f, 0.f, 0, nullptr, sk.dp_tiles + t, kt0, kt1);
+                                                                   ldb, 1.f, 0.f, 0, nullptr, sk.dp_tiles + t, kt0,
+                                                                   kt1);
         it += kt1 - kt0;
         ++seg;
     }
@@ -364,6 +366,23 @@ __global__ void __launch_bounds__(256) transpose_f32_kernel(const float* __restr
 }
 
 // C <- beta * C over M*N elements (beta == 0 writes zeros without reading C).
+// dst[r][c] = src[r * sld + c] for r < srows and c < scols, else 0; one float4 of dst per
+// thread and step (dcols % 4 == 0), grid-stride.
+__global__ void __launch_bounds__(256) pad_copy_kernel(const float* __restrict__ src, int64_t srows, int64_t scols,
+                                                       int64_t sld, float4* __restrict__ dst, int64_t rows,
+                                                       int64_t dcols4) {
+    const int64_t total = rows * dcols4;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
+        const int64_t r = i / dcols4;
+        const int64_t c = (i - r * dcols4) * 4;
+        float v[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[q] = (r < srows && c + q < scols) ? __ldcs(src + r * sld + c + q) : 0.f;
+        dst[i] = make_float4(v[0], v[1], v[2], v[3]);
+    }
+}
+
 __global__ void scale_c_kernel(float* __restrict__ C, int64_t n, float beta) {
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
@@ -376,8 +395,8 @@ __global__ void scale_c_kernel(float* __restrict__ C, int64_t n, float beta) {
 // @autotune row); this build compiles the part of it that a 256-thread CTA with
 // 4x4..8x16 register micro-tiles covers, times STAGES in {3, 4} and the FMA2 switch.
 // ---------------------------------------------------------------------------------------
-using KernelFn = void (*)(const float*, const float*, float*, int, int, int, float, float, int, float*);
-using StreamKFn = void (*)(const float*, const float*, int, int, int, StreamK);
+using KernelFn = void (*)(const float*, const float*, float*, int, int, int, int, float, float, int, float*);
+using StreamKFn = void (*)(const float*, const float*, int, int, int, int, StreamK);
 
 struct Entry {
     SgemmConfig cfg;
@@ -432,11 +451,14 @@ bool sgemm_is_aligned(int index, int64_t M, int64_t N, int64_t K, const float* A
 
 namespace {
 
-// The edge mode of config `index` for this problem (see kEdgeNone).
-int sgemm_edge(int index, int64_t M, int64_t N, int64_t K, const float* A, const float* B, const float* C) {
-    if (sgemm_is_aligned(index, M, N, K, A, B, C)) return kEdgeNone;
+// The edge mode of config `index` for this problem with B's rows ldb floats apart: the aligned
+// kernel for whole tiles; the 16-byte copies whenever the rows of A and B start on 16 bytes
+// (C's rows decide only between 16- and 4-byte accesses in the epilogue); else 4-byte copies.
+int sgemm_edge(int index, int64_t M, int64_t N, int64_t K, const float* A, const float* B, const float* C,
+               int64_t ldb) {
+    if (ldb == N && sgemm_is_aligned(index, M, N, K, A, B, C)) return kEdgeNone;
     auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-    return (K % 4 == 0 && N % 4 == 0 && al16(A) && al16(B) && al16(C)) ? kEdgeVec : kEdgeScalar;
+    return (K % 4 == 0 && ldb % 4 == 0 && al16(A) && al16(B)) ? kEdgeVec : kEdgeScalar;
 }
 
 }  // namespace
@@ -609,9 +631,9 @@ void sgemm_schedule_selftest(int index, int64_t M, int64_t N, int64_t K, int per
 }
 
 size_t sgemm_workspace_bytes(int index, int64_t M, int64_t N, int64_t K, const float* A,
-                             const float* B, const float* C, int num_sms) {
+                             const float* B, const float* C, int num_sms, int64_t ldb) {
     const Entry& e = kEntries[index];
-    const int edge = sgemm_edge(index, M, N, K, A, B, C);
+    const int edge = sgemm_edge(index, M, N, K, A, B, C, ldb < 0 ? N : ldb);
     const StreamK sk = streamk_plan(e, edge, M, N, K, num_sms);
     if (sk.blocks > 0) return static_cast<size_t>(2 * sk.blocks) * e.cfg.tile_m * e.cfg.tile_n * 4;
     const int64_t ks = k_per_slice(e, edge, M, N, K, num_sms);
@@ -621,9 +643,10 @@ size_t sgemm_workspace_bytes(int index, int64_t M, int64_t N, int64_t K, const f
 
 cudaError_t sgemm_launch(int index, int64_t M, int64_t N, int64_t K, float alpha,
                          const float* A, const float* B, float beta, float* C, void* workspace,
-                         int num_sms, cudaStream_t stream) {
+                         int num_sms, cudaStream_t stream, int64_t ldb) {
+    if (ldb < 0) ldb = N;
     const Entry& e = kEntries[index];
-    const int edge = sgemm_edge(index, M, N, K, A, B, C);
+    const int edge = sgemm_edge(index, M, N, K, A, B, C, ldb);
     KernelFn fn = e.fn[edge];
     cudaError_t err = set_func_attr_once(reinterpret_cast<const void*>(fn),
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, e.smem_bytes);
@@ -646,7 +669,7 @@ cudaError_t sgemm_launch(int index, int64_t M, int64_t N, int64_t K, float alpha
         if (err != cudaSuccess) return err;
         sk.slots = static_cast<float*>(workspace);
         skf<<<static_cast<unsigned>(sk.blocks), kThreads, e.smem_bytes, stream>>>(
-            A, B, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), sk);
+            A, B, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), static_cast<int>(ldb), sk);
         err = launched(cudaGetLastError());
         if (err != cudaSuccess) return err;
         // then the tail tiles of C, while the partial tiles are still in L2 (the whole tiles
@@ -662,7 +685,7 @@ cudaError_t sgemm_launch(int index, int64_t M, int64_t N, int64_t K, float alpha
     const int64_t grid = sk.blocks > 0 ? sk.dp_tiles : tiles;
     if (grid == 0) return cudaSuccess;  // the whole grid went to the stream-K blocks
     fn<<<dim3(static_cast<unsigned>(grid), static_cast<unsigned>(slices)), kThreads, e.smem_bytes, stream>>>(
-        A, B, C, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), alpha, beta,
+        A, B, C, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), static_cast<int>(ldb), alpha, beta,
         static_cast<int>(ks), partial);
     err = launched(cudaGetLastError());
     if (err != cudaSuccess || slices == 1) return err;
@@ -706,6 +729,22 @@ cudaError_t transpose_f32_launch(const float* src, float* dst, int64_t rows, int
     const int64_t gx = (cols + 31) / 32, gy = (rows + 31) / 32;
     if (gx * gy > 0x7FFFFFFF) return cudaErrorInvalidValue;
     transpose_f32_kernel<<<static_cast<unsigned>(gx * gy), 256, 0, stream>>>(src, dst, rows, cols, gx);
+    return launched(cudaGetLastError());
+}
+
+bool sgemm_scalar_edge(int index, int64_t M, int64_t N, int64_t K, const float* A, const float* B,
+                       const float* C) {
+    return sgemm_edge(index, M, N, K, A, B, C, N) == kEdgeScalar;
+}
+
+cudaError_t pad_copy_launch(const float* src, int64_t srows, int64_t scols, int64_t sld, float* dst, int64_t rows,
+                            int64_t dcols, int num_sms, cudaStream_t stream) {
+    const int64_t n4 = rows * (dcols / 4);
+    if (n4 == 0) return cudaSuccess;
+    int64_t blocks = (n4 + 255) / 256;
+    if (blocks > static_cast<int64_t>(num_sms) * 8) blocks = static_cast<int64_t>(num_sms) * 8;
+    pad_copy_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(src, srows, scols, sld,
+                                                                        reinterpret_cast<float4*>(dst), rows, dcols / 4);
     return launched(cudaGetLastError());
 }
 

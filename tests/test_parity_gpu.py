@@ -375,3 +375,31 @@ def test_sgemm_vector_edge_path(shape):
                 assert_bits_equal(out[offset], want, what)
             else:
                 assert_within_bound(out[offset], want, mag, C, K, 1.5, -0.5, what)
+
+
+@pytest.mark.parametrize("shape,offset_a", [((1031, 1029, 4100), 0),   # N % 4 != 0: B padded
+                                            ((1030, 1024, 4099), 0),   # K % 4 != 0: A and B padded
+                                            ((1024, 1024, 4096), 1)])  # A not 16-byte aligned: A padded
+def test_sgemm_padded_copies_of_unaligned_operands(shape, offset_a):
+    # Large f32 problems whose rows of A or B do not start on 16 bytes are computed on
+    # zero-padded 16-byte-aligned copies of A and/or B; C (rows unaligned too) is written in
+    # place.  Bit for bit on integer inputs, within the bound on uniform ones.
+    import torch
+    M, N, K = shape
+    for dist in ("int3", "uniform"):
+        A, B, C = synth.problem(M, N, K, seed=41, dist=dist)
+        want, mag = oracle.gemm(A, B, C, 1.5, -0.5)
+        buf = torch.zeros(M * K + 4, device="cuda")
+        dA = buf[offset_a:offset_a + M * K].view(M, K)
+        dA.copy_(torch.from_numpy(A))
+        dB = torch.from_numpy(B).cuda()
+        dC = torch.from_numpy(C.copy()).cuda()
+        st = phx.phx_sgemm(M, N, K, 1.5, dA.data_ptr(), dB.data_ptr(), -0.5, dC.data_ptr(),
+                           torch.cuda.current_stream().cuda_stream)
+        torch.cuda.synchronize()
+        assert st == phx.PHX_OK
+        got = dC.cpu().numpy()
+        if dist == "int3":
+            assert_bits_equal(got, want, f"padded {shape} {dist}")
+        else:
+            assert_within_bound(got, want, mag, C, K, 1.5, -0.5, f"padded {shape} {dist}")
