@@ -34,6 +34,7 @@
 #include <mutex>
 #include <tuple>
 
+#include "debug_checks.cuh"
 #include "internal.h"
 #include "sm100_ptx.cuh"
 
@@ -136,6 +137,7 @@ __global__ void __launch_bounds__(256) cast_kernel(CastJob j0, CastJob j1, int64
                 continue;
             }
             const float* src = static_cast<const float*>(j.src) + r * K + c;
+            PHX_DCHECK(r < j.rows && c + 7 < Kp);
             float v[8];
             if (j.vec && c + 8 <= K) {
                 const float4 x = __ldcs(reinterpret_cast<const float4*>(src));
@@ -214,6 +216,7 @@ __global__ void __launch_bounds__(256) cast_kernel(CastJob j0, CastJob j1, int64
         const int64_t gr = r0 + r;
         const int64_t gk = k0 + kc;
         if (gr < R && gk < Kp) {
+            PHX_DCHECK(gk + 7 < Kp && r < kTT && kc + 7 < kTT);
             const int col = r ^ tt_swizzle(kc);  // the same for the 8 rows kc .. kc+7
             float v[8];
 #pragma unroll
@@ -402,6 +405,8 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, status)) { ok = false; break; }
                     const uint32_t a_dst = sA + stage * L::kABytes;
                     const uint32_t b_dst = sB + stage * L::kBBytes;
+                    PHX_DCHECK(stage < STAGES && kb < num_kb && it.pm * kBM < (kTwoSm ? 2 : 1) * tiles_rows * kBM &&
+                               it.n0 < tiles_n * BN);
                     if constexpr (kTwoSm) {
                         // each CTA: its 128 rows of A and its share of B, counted on the even
                         // CTA's barrier, which expects the pair's bytes
@@ -444,6 +449,7 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, status)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
+                PHX_DCHECK(acc * BN + BN <= L::kTmemCols && it.nkb > 0);
                 for (int kb = 0; kb < it.nkb; ++kb) {
                     if (!mbar_wait(full_bar(stage), phase, abort_flag, status)) { ok = false; break; }
                     tc_fence_after();
@@ -583,6 +589,7 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
+                    PHX_DCHECK(it.n0 + c * 32 < N && row0_of(it) < M);
                     tma_store_2d(&tmC, ebuf + b * 4096, it.n0 + c * 32, row0_of(it));
                     bulk_commit();
                 }
@@ -639,6 +646,7 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                                 o.w = fmaf(b_out, cv[q].w, o.w);
                             }
                             const int64_t off = static_cast<int64_t>(row) * N + col;
+                            PHX_DCHECK(col + 3 < N && c * 32 + cc + 3 < it.width);
                             if (out_h)
                                 store4_h(Ch + off, o);
                             else
@@ -665,6 +673,7 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                             float o = a_out * epi[rr * L::kEpiStride + lane];
                             if (read_c) o = fmaf(b_out, cs[rr], o);
                             const int64_t off = static_cast<int64_t>(row) * N + col;
+                            PHX_DCHECK(c * 32 + lane < it.width);
                             if (out_h)
                                 Ch[off] = __float2half_rn(o);
                             else
@@ -815,6 +824,8 @@ constexpr int kNumTc = sizeof(kTcEntries) / sizeof(kTcEntries[0]);
 int f16tc_num_configs() { return kNumTc; }
 
 const F16Config& f16tc_config(int index) { return kTcEntries[index].cfg; }
+
+int64_t debug_take_f16tc() { return debug_take_local(); }
 
 size_t f16tc_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     const int64_t Kp = round_up(K, 8);

@@ -37,6 +37,7 @@
 #include <mutex>
 #include <utility>
 
+#include "debug_checks.cuh"
 #include "internal.h"
 #include "sm100_ptx.cuh"
 
@@ -244,6 +245,7 @@ __global__ void __launch_bounds__(kSkThreads, 2) skinny_kernel(
         const int64_t n = n0 + c;
         const int mm = m0 + m;
         if (mm >= M || n >= N) continue;
+        PHX_DCHECK(m < MT && cs <= 8);
         const int64_t idx = static_cast<int64_t>(mm) * N + n;
         if (partial != nullptr) {
             partial[static_cast<int64_t>(blockIdx.y) * M * N + idx] = s;
@@ -541,6 +543,7 @@ __global__ void __launch_bounds__(kSkThreads, 2) skinny_nt_kernel(
         const int m = e / kNtRows, cidx = e % kNtRows;
         const int mm = m0 + m, n = n0 + cidx;
         if (mm >= M || n >= N) continue;
+        PHX_DCHECK(m < MT && cs <= 8);
         const int64_t idx = static_cast<int64_t>(mm) * N + n;
         if (partial != nullptr)
             partial[static_cast<int64_t>(blockIdx.y) * M * N + idx] = v;
@@ -668,5 +671,7 @@ cudaError_t skinny_nt_launch(int f16, int a_trans, int64_t M, int64_t N, int64_t
     if (err != cudaSuccess || p.planes == 1) return err;
     return splitk_reduce_launch(partial, p.planes, M, N, alpha, beta, C, num_sms, stream);
 }
+
+int64_t debug_take_skinny() { return debug_take_local(); }
 
 }  // namespace phx

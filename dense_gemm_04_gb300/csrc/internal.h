@@ -22,6 +22,12 @@ int64_t noted_launches();
 // runtime call (phx_api.cu).
 cudaError_t set_func_attr_once(const void* fn, cudaFuncAttribute attr, int value);
 
+// Failed index checks of the bounds-checked build (-DPHX_DEBUG=1) in each translation unit's
+// kernels since the last call, read and cleared (-1 if the read failed); always 0 otherwise.
+int64_t debug_take_sgemm();
+int64_t debug_take_f16tc();
+int64_t debug_take_skinny();
+
 // `err` of a kernel launch, noted as one launch when it succeeded.
 inline cudaError_t launched(cudaError_t err) {
     if (err == cudaSuccess) note_launches(1);

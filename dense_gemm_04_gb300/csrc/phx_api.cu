@@ -927,6 +927,34 @@ phx_status phx_check_device_status(phx_stream_t stream) {
     return ((word | noalloc_word) & phx::kDevTimeout) ? PHX_ERR_TIMEOUT : PHX_OK;
 }
 
+int phx_debug_build(void) {
+#if defined(PHX_DEBUG) && PHX_DEBUG
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+phx_status phx_debug_violations(int64_t* count) {
+    if (count == nullptr) return PHX_ERR_INVALID;
+    *count = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return PHX_ERR_ARCH;
+    }
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return PHX_ERR_LAUNCH;
+    }
+    const int64_t parts[3] = {phx::debug_take_sgemm(), phx::debug_take_f16tc(), phx::debug_take_skinny()};
+    for (int64_t v : parts) {
+        if (v < 0) return PHX_ERR_LAUNCH;
+        *count += v;
+    }
+    return PHX_OK;
+}
+
 phx_status phx_profile_start(void) {
     std::lock_guard<std::mutex> lock(g_prof_mu);
     for (auto& m : g_prof.marks) {

@@ -44,6 +44,7 @@
 #include <mutex>
 #include <vector>
 
+#include "debug_checks.cuh"
 #include "internal.h"
 
 namespace phx {
@@ -235,8 +236,10 @@ __global__ void __launch_bounds__(kFixupThreads) streamk_fixup_kernel(StreamK sk
         int n = 0;
         while (n < kFixupBatch && b < sk.blocks && s0 < hi) {
             const int64_t s1 = streamk_begin(b + 1, sk.work, sk.blocks);
-            if (s1 > s0)  // an empty range wrote nothing
+            if (s1 > s0) {  // an empty range wrote nothing
+                PHX_DCHECK(b < sk.blocks);
                 src[n++] = reinterpret_cast<const float4*>(sk.slots + (2 * b + (s0 < lo ? 1 : 0)) * tile_elems);
+            }
             s0 = s1;
             ++b;
         }
@@ -245,7 +248,10 @@ __global__ void __launch_bounds__(kFixupThreads) streamk_fixup_kernel(StreamK sk
         for (int q = 0; q < kFixupBatch; ++q) {
             if (q < n) {
 #pragma unroll
-                for (int i = 0; i < kFixupVec; ++i) v[q][i] = __ldcs(src[q] + first4 + i * kFixupThreads);
+                for (int i = 0; i < kFixupVec; ++i) {
+                    PHX_DCHECK(4 * (first4 + i * kFixupThreads) + 3 < tile_elems);
+                    v[q][i] = __ldcs(src[q] + first4 + i * kFixupThreads);
+                }
             }
         }
 #pragma unroll
@@ -269,6 +275,7 @@ __global__ void __launch_bounds__(kFixupThreads) streamk_fixup_kernel(StreamK sk
         const int row = m0 + e / bn;
         const int col = n0 + e % bn;
         if (row >= M || col >= N) continue;
+        PHX_DCHECK(!first && (!vec || col + 3 < N));  // every spread tile gets a partial sum
         float* c = C + static_cast<int64_t>(row) * N + col;
         const float a[4] = {acc[i].x, acc[i].y, acc[i].z, acc[i].w};
         if (vec) {
@@ -298,6 +305,7 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ P, int S, int64_t
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const int64_t start = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (vec) {
+        PHX_DCHECK(plane % 4 == 0);
         const int64_t n4 = plane / 4;
         for (int64_t i = start; i < n4; i += stride) {
             float4 acc = __ldcs(reinterpret_cast<const float4*>(P) + i);
@@ -731,6 +739,8 @@ cudaError_t transpose_f32_launch(const float* src, float* dst, int64_t rows, int
     transpose_f32_kernel<<<static_cast<unsigned>(gx * gy), 256, 0, stream>>>(src, dst, rows, cols, gx);
     return launched(cudaGetLastError());
 }
+
+int64_t debug_take_sgemm() { return debug_take_local(); }
 
 bool sgemm_scalar_edge(int index, int64_t M, int64_t N, int64_t K, const float* A, const float* B,
                        const float* C) {

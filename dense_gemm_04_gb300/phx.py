@@ -14,7 +14,8 @@ import os
 import re
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "_lib", "libphx.so")
+# PHX_LIBRARY=<path> loads another build of the same ABI (the bounds-checked one).
+LIB_PATH = os.environ.get("PHX_LIBRARY") or os.path.join(_HERE, "_lib", "libphx.so")
 HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "phx.h")
 
 PHX_OK, PHX_ERR_INVALID, PHX_ERR_ARCH, PHX_ERR_LAUNCH = 0, 1, 2, 3
@@ -64,6 +65,8 @@ _SIGNATURES = {
     "phx_validate_args": (_i32, [_i64, _i64, _i64, _vp, _vp, _vp]),
     "phx_version": (_cp, []),
     "phx_profile_start": (_i32, []),
+    "phx_debug_build": (_i32, []),
+    "phx_debug_violations": (_i32, [ctypes.POINTER(_i64)]),
     "phx_profile_stop": (_i32, [ctypes.POINTER(_i64), ctypes.POINTER(ctypes.c_double)]),
 }
 
@@ -244,6 +247,13 @@ def autotune(variant: int, M: int, N: int, K: int, finalists: int = 4, rounds: i
     check(phx_autotune(variant, M, N, K, finalists, rounds, settle_ms, _stream_handle(stream)),
           "phx_autotune")
     return get_config(variant, M, N, K)
+
+
+def debug_violations() -> int:
+    """Failed index checks since the last call (bounds-checked build; 0 otherwise)."""
+    n = _i64(0)
+    check(phx_debug_violations(ctypes.byref(n)), "phx_debug_violations")
+    return int(n.value)
 
 
 def device_tag() -> str:

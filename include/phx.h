@@ -198,6 +198,23 @@ const char* phx_status_string(phx_status s);
 phx_status phx_check_device_status(phx_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
+ * The bounds-checked build
+ *
+ * Built with PHX_DEBUG=1 (`python dense_gemm_04_gb300/build.py --debug` writes
+ * _lib/libphx_debug.so; the binding loads it when the environment variable PHX_LIBRARY names
+ * it), the kernels check their global-memory and shared-memory indices, tile coordinates and
+ * tensor-memory columns as they go.  A failed check is counted in a device counter and the
+ * kernel carries on (nothing traps; the kernel's own guards still decide what is accessed).
+ * ------------------------------------------------------------------------------------- */
+
+/* 1 if this library was built with the checks, else 0. */
+int phx_debug_build(void);
+
+/* Synchronise the current device, then write the number of failed checks since the last call
+ * (0 in a library built without the checks) and clear it. */
+phx_status phx_debug_violations(int64_t* count);
+
+/* ---------------------------------------------------------------------------------------
  * Per-kernel timing, for roofline reports
  * ------------------------------------------------------------------------------------- */
 
