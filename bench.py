@@ -263,17 +263,29 @@ def reference_arm(args):
     return 0
 
 
-def _traffic_from_profiles(kernel: str):
-    """DRAM bytes per call recorded from ncu captures, if the kernel's source is unchanged
-    since (profiles/dram_traffic.txt: kernel, bytes per call, source hash; a call of the f32
-    GEMM at 4096^3 is three kernels, summed there)."""
+KERNEL_SOURCES = {"sgemm": ("sgemm_simt.cu", "sgemm_tile_body.inc", "internal.h", "debug_checks.cuh"),
+                  "tc_gemm": ("gemm_f16tc.cu", "sm100_ptx.cuh", "internal.h", "debug_checks.cuh"),
+                  "f16_cast": ("gemm_f16tc.cu", "internal.h", "debug_checks.cuh")}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """sha256[:16] over the source files a kernel is compiled from, in a fixed order."""
     import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "dense_gemm_04_gb300", "csrc", name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic_from_profiles(kernel: str):
+    """DRAM bytes per call recorded from ncu captures, if none of the kernel's source files has
+    changed since (profiles/dram_traffic.txt: kernel, bytes per call, hash of its sources; a
+    call of the f32 GEMM at 4096^3 is three kernels, summed there)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    src = {"sgemm": "sgemm_simt.cu", "tc_gemm": "gemm_f16tc.cu", "f16_cast": "gemm_f16tc.cu"}[kernel]
-    with open(os.path.join(ROOT, "dense_gemm_04_gb300", "csrc", src), "rb") as f:
-        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    h = kernel_source_hash(kernel)
     with open(path) as f:
         for line in f:
             p = line.split()

@@ -9,7 +9,9 @@ For every shape of the workload sweep ((8192, 8192, 1024), (1024, 1024, 16384),
 alpha = 1, beta = 0; and 4096^3 with alpha = 1, beta = 0.5) and both precisions, this measures
 the GEMM the way the matrix-multiplication lab's stopwatches do: settle the clock with synced
 calls, then take the median of CUDA-event timings ("steady"), with the shapes visited in a
-freshly shuffled order every round ("sweep").  Each result is placed on its roofline,
+freshly shuffled order every round ("sweep").  Beside each steady time it reports the host
+microseconds spent inside one call and the GPU time per call with 50 calls queued back to
+back (no host gaps).  Each result is placed on its roofline,
 min(peak, bandwidth x intensity), with intensity = 2MNK / minimum bytes (each f32 input
 read once, C written once and read when beta != 0), following the lab's minimum-traffic
 intensity (Part 5, the skinny-matrix sweep).
@@ -100,6 +102,26 @@ def steady(fn, seconds=0.5, min_calls=3):
     return float(np.median(ts))
 
 
+def host_and_queued(fn, queue=50):
+    """(median host seconds spent inside one call, GPU seconds per call with `queue` calls
+    queued back to back between two events).  The first is the library's own cost on the
+    host: argument checks, the configuration lookup and the launches, without waiting for
+    the GPU.  The second is the device time per call without the host's gaps between calls."""
+    import torch
+    fn()
+    _sync()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    host = []
+    ev0.record()
+    for _ in range(queue):
+        t0 = time.perf_counter()
+        fn()
+        host.append(time.perf_counter() - t0)
+    ev1.record()
+    ev1.synchronize()
+    return float(np.median(host)), ev0.elapsed_time(ev1) / 1e3 / queue
+
+
 def sustained(fn, seconds=2.0):
     """Seconds per call under continuous load, with the clocks it ran at."""
     import torch
@@ -152,6 +174,8 @@ def run(quick=False, rounds=3, seed=0):
     shapes = [s for s in SHAPES if not (quick and s[1] * s[2] * s[3] > 2 ** 40)]
     cases = [(s, v) for s in shapes for v in ("sgemm", "f16tc")]
     times = {c: [] for c in range(len(cases))}
+    host = {c: [] for c in range(len(cases))}
+    queued = {c: [] for c in range(len(cases))}
     rng = np.random.default_rng(seed)
     for _ in range(rounds):
         for ci in rng.permutation(len(cases)):
@@ -162,6 +186,9 @@ def run(quick=False, rounds=3, seed=0):
             fn = phx.phx_sgemm if v == "sgemm" else phx.phx_gemm_f16tc_f32acc
             call = lambda: phx.check(fn(M, N, K, alpha, A.data_ptr(), B.data_ptr(), beta, C.data_ptr(), st))
             times[ci].append(steady(call, seconds=0.3 if quick else 0.5))
+            h, q = host_and_queued(call)
+            host[ci].append(h)
+            queued[ci].append(q)
             del A, B, C
             torch.cuda.empty_cache()
     rows = []
@@ -175,6 +202,9 @@ def run(quick=False, rounds=3, seed=0):
         rows.append({"shape": name, "M": M, "N": N, "K": K, "alpha": alpha, "beta": beta, "variant": v,
                      "config": phx.get_config(0 if v == "sgemm" else 1, M, N, K),
                      "seconds": t, "tflops": flops / t / 1e12, "intensity": ai,
+                     "host_us_per_call": 1e6 * float(np.median(host[ci])),
+                     "queued_seconds": float(np.median(queued[ci])),
+                     "queued_tflops": flops / float(np.median(queued[ci])) / 1e12,
                      "roof_tflops": roof / 1e12, "pct_of_roof": 100 * flops / t / roof,
                      "bound": "compute" if roof >= peak * 1e12 else "hbm",
                      "seconds_all": times[ci]})
@@ -368,7 +398,9 @@ def main():
           f"f16 tensor {r['f16_tensor']['tflops']:.0f} TFLOP/s, HBM read {r['hbm_read_gbs']:.0f} GB/s")
     for row in res["rows"]:
         print(f"{row['shape']:>16s} {row['variant']:6s} {row['tflops']:8.1f} TFLOP/s  "
-              f"{row['pct_of_roof']:5.1f}% of {row['bound']} roof ({row['roof_tflops']:.0f})  [{row['config']}]")
+              f"{row['pct_of_roof']:5.1f}% of {row['bound']} roof ({row['roof_tflops']:.0f})  "
+              f"queued {row['queued_tflops']:8.1f} TFLOP/s  host {row['host_us_per_call']:5.1f} us/call  "
+              f"[{row['config']}]")
     if args.out:
         with open(args.out, "w") as f:
             json.dump(res, f, indent=1)
