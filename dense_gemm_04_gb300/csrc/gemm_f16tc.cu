@@ -741,18 +741,20 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// A 2-D tiled tensor map (128-byte swizzle, 256-byte L2 promotion, zero fill), encoded once
-// per (data type, address, extents, row stride, box): a call of the same shape on the same
-// (pooled, hence usually recurring) buffers finds its maps in this small cache.  The map
-// depends on nothing else (not on the device: the address alone names the memory).
+// A 2-D tiled tensor map (128-byte swizzle unless `swizzle` says otherwise, 256-byte L2
+// promotion, zero fill), encoded once per (data type, address, extents, row stride, box,
+// swizzle): a call of the same shape on the same (pooled, hence usually recurring) buffers
+// finds its maps in this small cache.  The map depends on nothing else (not on the device:
+// the address alone names the memory).
 bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, void* ptr, uint64_t inner, uint64_t outer,
-               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
-    using Key = std::tuple<int, uintptr_t, uint64_t, uint64_t, uint64_t, uint32_t, uint32_t>;
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+    using Key = std::tuple<int, uintptr_t, uint64_t, uint64_t, uint64_t, uint32_t, uint32_t, int>;
     constexpr size_t kMaxEntries = 256;
     static std::mutex mu;
     static std::map<Key, CUtensorMap> cache;
     const Key key(static_cast<int>(dt), reinterpret_cast<uintptr_t>(ptr), inner, outer, row_bytes, box_inner,
-                  box_outer);
+                  box_outer, static_cast<int>(swizzle));
     {
         std::lock_guard<std::mutex> lock(mu);
         auto it = cache.find(key);
@@ -767,7 +769,7 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, void* ptr, uint64_t inn
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
-    if (enc(map, dt, 2, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    if (enc(map, dt, 2, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return false;
     std::lock_guard<std::mutex> lock(mu);
@@ -821,9 +823,23 @@ constexpr int kNumTc = sizeof(kTcEntries) / sizeof(kTcEntries[0]);
 
 }  // namespace
 
-int f16tc_num_configs() { return kNumTc; }
+int f16tc_num_configs() { return kNumTc + f16cvt_num_configs(); }
 
-const F16Config& f16tc_config(int index) { return kTcEntries[index].cfg; }
+const F16Config& f16tc_config(int index) {
+    return index < kNumTc ? kTcEntries[index].cfg : f16cvt_config(index - kNumTc);
+}
+
+bool f16tc_is_convert_a(int index) { return index >= kNumTc && index < kNumTc + f16cvt_num_configs(); }
+
+bool f16_operand_map(CUtensorMap* map, const __half* ptr, int64_t rows, int64_t Kp, int box_rows, int64_t ld) {
+    return make_map(map, ptr, rows, Kp, box_rows, ld);
+}
+
+bool f32_rows_map(CUtensorMap* map, const float* ptr, int64_t rows, int64_t cols, int box_cols, int box_rows) {
+    return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, const_cast<float*>(ptr), static_cast<uint64_t>(cols),
+                     static_cast<uint64_t>(rows), static_cast<uint64_t>(cols) * 4, static_cast<uint32_t>(box_cols),
+                     static_cast<uint32_t>(box_rows), CU_TENSOR_MAP_SWIZZLE_NONE);
+}
 
 int64_t debug_take_f16tc() { return debug_take_local(); }
 
@@ -910,6 +926,7 @@ int tc_kb_per_slice(const TcEntry& e, int64_t M, int64_t N, int64_t K, int num_s
 }  // namespace
 
 size_t f16tc_split_bytes(int index, int64_t M, int64_t N, int64_t K, int num_sms) {
+    if (index < 0 || index >= kNumTc) return 0;  // the kernel that rounds A does not split K
     const int64_t num_kb = (K + kBK - 1) / kBK;
     const int kb = tc_kb_per_slice(kTcEntries[index], M, N, K, num_sms);
     if (kb >= num_kb) return 0;
@@ -931,6 +948,7 @@ cudaError_t f16tc_gemm_launch_ops(int index, int64_t M, int64_t N, int64_t K, fl
                                   float* C, __half* Ch, const __half* Ah, int64_t lda, const __half* Bt,
                                   int64_t ldb, void* split_ws, unsigned int* status, int num_sms,
                                   cudaStream_t stream) {
+    if (index < 0 || index >= kNumTc) return cudaErrorInvalidValue;  // not this kernel's configuration
     const TcEntry& e = kTcEntries[index];
     const int64_t Kp = round_up(K, 8);
     CUtensorMap mapA, mapB, mapB_half, mapB_quarter;

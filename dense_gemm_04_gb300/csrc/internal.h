@@ -5,6 +5,7 @@
 // gemm_f16tc.cu and probes.cu.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <cstddef>
@@ -26,6 +27,7 @@ cudaError_t set_func_attr_once(const void* fn, cudaFuncAttribute attr, int value
 // kernels since the last call, read and cleared (-1 if the read failed); always 0 otherwise.
 int64_t debug_take_sgemm();
 int64_t debug_take_f16tc();
+int64_t debug_take_f16cvt();
 int64_t debug_take_skinny();
 
 // `err` of a kernel launch, noted as one launch when it succeeded.
@@ -138,11 +140,33 @@ cudaError_t scale_c_launch(int64_t M, int64_t N, float beta, float* C, cudaStrea
 // ---------------------------------------------------------------------------------------
 struct F16Config {
     int tile_m, tile_n, tile_k, stages;
-    int cluster;  // 1: one CTA per 128-row tile; 2: CTA pairs running the 2-SM MMA (TILE_M = 256)
+    int cluster;        // 1: one CTA per 128-row tile; 2: CTA pairs running the 2-SM MMA (TILE_M = 256)
+    int convert_a = 0;  // 1: A rounded to f16 inside the GEMM kernel (gemm_f16cvt.cu)
 };
 
+// The f16 configurations: the kernel of gemm_f16tc.cu (indices 0 .. n-1), then the kernel
+// that rounds A itself (gemm_f16cvt.cu; f16tc_is_convert_a).
 int f16tc_num_configs();
 const F16Config& f16tc_config(int index);
+bool f16tc_is_convert_a(int index);
+
+// Tensor map of a K-major f16 operand: `rows` rows of `Kp` halves (a multiple of 8), `ld`
+// halves apart, read in 128-byte-swizzled boxes of 64 halves x box_rows (gemm_f16tc.cu).
+bool f16_operand_map(CUtensorMap* map, const __half* ptr, int64_t rows, int64_t Kp, int box_rows, int64_t ld);
+
+// Tensor map of a row-major f32 matrix (rows x cols, cols a multiple of 4, 16-byte aligned),
+// read unswizzled in boxes of box_cols x box_rows; zeros past the edges (gemm_f16tc.cu).
+bool f32_rows_map(CUtensorMap* map, const float* ptr, int64_t rows, int64_t cols, int box_cols, int box_rows);
+
+// The kernel that rounds A itself (gemm_f16cvt.cu): its configurations, and one GEMM of
+// configuration `index` (0 .. f16cvt_num_configs() - 1) on A (M x K f32, row-major) and Bt
+// (N x Kp f16, K-major, ldb halves apart, from the rounding pass), launched as a
+// programmatic dependent of that pass.  Requires M, N, K > 0 and alpha != 0.
+int f16cvt_num_configs();
+const F16Config& f16cvt_config(int index);
+cudaError_t f16cvt_gemm_launch(int index, int64_t M, int64_t N, int64_t K, float alpha, float beta, float* C,
+                               const float* A, const __half* Bt, int64_t ldb, unsigned int* status, int num_sms,
+                               cudaStream_t stream);
 
 // Bytes of workspace for the rounded operands: A as M x Kp f16 and B transposed as
 // N x Kp f16, Kp = K rounded up to a multiple of 8, each part 256-byte aligned.

@@ -242,16 +242,17 @@ std::string config_name(int variant, int i) {
                       c.tile_n, c.tile_k, c.stages, c.fma2);
     } else {
         const F16Config& c = phx::f16tc_config(i);
-        // a 256-row tile is a 2-SM pair; a 128-row tile one CTA
-        std::snprintf(buf, sizeof buf, "TILE_M=%d TILE_N=%d TILE_K=%d STAGES=%d", c.tile_m, c.tile_n,
-                      c.tile_k, c.stages);
+        // a 256-row tile is a 2-SM pair; a 128-row tile one CTA; CONVERT_A=1 the kernel that
+        // rounds A itself
+        std::snprintf(buf, sizeof buf, "TILE_M=%d TILE_N=%d TILE_K=%d STAGES=%d%s", c.tile_m, c.tile_n,
+                      c.tile_k, c.stages, c.convert_a ? " CONVERT_A=1" : "");
     }
     return buf;
 }
 
 // Parse "KEY=value KEY=value ..." and return the first compiled config that matches every
-// given key (TILE_M, TILE_N, TILE_K required; STAGES optional; FMA2 for the f32 variant
-// optional, default 0), or -1.
+// given key (TILE_M, TILE_N, TILE_K required; STAGES optional; FMA2 for the f32 variant and
+// CONVERT_A for the f16 one optional, default 0), or -1.
 int parse_config(int variant, const char* spec) {
     if (spec == nullptr || num_configs(variant) < 0) return -1;
     std::map<std::string, int> kv;
@@ -270,26 +271,29 @@ int parse_config(int variant, const char* spec) {
         char* end = nullptr;
         const long v = std::strtol(val.c_str(), &end, 10);
         if (end == nullptr || *end != '\0') return -1;
-        if (key != "TILE_M" && key != "TILE_N" && key != "TILE_K" && key != "STAGES" && key != "FMA2")
+        if (key != "TILE_M" && key != "TILE_N" && key != "TILE_K" && key != "STAGES" && key != "FMA2" &&
+            key != "CONVERT_A")
             return -1;
         if (variant == PHX_VARIANT_F16TC && key == "FMA2") return -1;
+        if (variant == PHX_VARIANT_SGEMM && key == "CONVERT_A") return -1;
         kv[key] = static_cast<int>(v);
     }
     if (!kv.count("TILE_M") || !kv.count("TILE_N") || !kv.count("TILE_K")) return -1;
     const int n = tile_configs(variant);
     for (int i = 0; i < n; ++i) {
-        int tm, tn, tk, st, f2 = 0;
+        int tm, tn, tk, st, f2 = 0, cv = 0;
         if (variant == PHX_VARIANT_SGEMM) {
             const SgemmConfig& c = phx::sgemm_config(i);
             tm = c.tile_m; tn = c.tile_n; tk = c.tile_k; st = c.stages; f2 = c.fma2;
         } else {
             const F16Config& c = phx::f16tc_config(i);
-            tm = c.tile_m; tn = c.tile_n; tk = c.tile_k; st = c.stages;
+            tm = c.tile_m; tn = c.tile_n; tk = c.tile_k; st = c.stages; cv = c.convert_a;
         }
         if (kv["TILE_M"] != tm || kv["TILE_N"] != tn || kv["TILE_K"] != tk) continue;
         if (kv.count("STAGES") && kv["STAGES"] != st) continue;
         if (kv.count("FMA2") && kv["FMA2"] != f2) continue;
         if (!kv.count("FMA2") && variant == PHX_VARIANT_SGEMM && f2 != 0) continue;
+        if ((kv.count("CONVERT_A") ? kv["CONVERT_A"] : 0) != cv) continue;
         return i;
     }
     return -1;
@@ -339,29 +343,82 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // Defaults when nothing is pinned or tuned: the largest tile that still gives every SM
 // work (the trade-off "gemm, f32" section "Tuning" describes: larger tiles reuse more,
 // but leave fewer CTAs to spread over the card).
-int default_tile_config(int variant, int64_t M, int64_t N, int sms);
+int default_tile_config(int variant, int64_t M, int64_t N, int64_t K, int sms, bool convert_a = true);
 
-int default_config(int variant, int64_t M, int64_t N, int sms) {
+int default_config(int variant, int64_t M, int64_t N, int64_t K, int sms) {
     if (M <= skinny_default_max_m(variant)) return skinny_index(variant);
-    return default_tile_config(variant, M, N, sms);
+    return default_tile_config(variant, M, N, K, sms);
 }
 
-int default_tile_config(int variant, int64_t M, int64_t N, int sms) {
+// The compiled configurations the defaults name, resolved once (parsing a name per call
+// would cost a microsecond of host time).
+struct DefaultConfigs {
+    int s128x128 = -1, s128x64 = -1, s64x64 = -1;                // f32
+    int t256x256 = -1, t128x256 = -1, t128x128 = -1, t128x64 = -1;  // f16 tensor cores
+    int c64 = -1, c128 = -1, c256 = -1;  // f16, A rounded in the kernel, TILE_N = 64, 128, 256
+};
+
+const DefaultConfigs& default_configs() {
+    static const DefaultConfigs d = [] {
+        DefaultConfigs c;
+        c.s128x128 = parse_config(PHX_VARIANT_SGEMM, "TILE_M=128 TILE_N=128 TILE_K=16 STAGES=4 FMA2=1");
+        c.s128x64 = parse_config(PHX_VARIANT_SGEMM, "TILE_M=128 TILE_N=64 TILE_K=8 STAGES=4");
+        c.s64x64 = parse_config(PHX_VARIANT_SGEMM, "TILE_M=64 TILE_N=64 TILE_K=8 STAGES=4");
+        c.t256x256 = parse_config(PHX_VARIANT_F16TC, "TILE_M=256 TILE_N=256 TILE_K=64 STAGES=6");
+        c.t128x256 = parse_config(PHX_VARIANT_F16TC, "TILE_M=128 TILE_N=256 TILE_K=64 STAGES=4");
+        c.t128x128 = parse_config(PHX_VARIANT_F16TC, "TILE_M=128 TILE_N=128 TILE_K=64 STAGES=6");
+        c.t128x64 = parse_config(PHX_VARIANT_F16TC, "TILE_M=128 TILE_N=64 TILE_K=64 STAGES=8");
+        c.c64 = parse_config(PHX_VARIANT_F16TC, "TILE_M=128 TILE_N=64 TILE_K=64 STAGES=4 CONVERT_A=1");
+        c.c128 = parse_config(PHX_VARIANT_F16TC, "TILE_M=128 TILE_N=128 TILE_K=64 STAGES=3 CONVERT_A=1");
+        c.c256 = parse_config(PHX_VARIANT_F16TC, "TILE_M=128 TILE_N=256 TILE_K=64 STAGES=2 CONVERT_A=1");
+        return c;
+    }();
+    return d;
+}
+
+// Problems of at most this many multiply-adds (2^28: 512 x 512 x 1024) take the small f32
+// tiles: their time is the latency of a few k steps, and more, smaller CTAs spread it over
+// more SMs (measured on GB300, queued calls: 512^3 16.5 us with 128 x 64 tiles against 22.8
+// with 128 x 128; 256^3 14.4 us with 64 x 64 against 22.7).
+constexpr int64_t kSmallSgemmWork = int64_t(1) << 28;
+
+// With convert_a, the f16 default may be the kernel that rounds A itself; callers whose A is
+// not a row-major f32 matrix pass false.
+int default_tile_config(int variant, int64_t M, int64_t N, int64_t K, int sms, bool convert_a) {
+    const DefaultConfigs& dc = default_configs();
     if (variant == PHX_VARIANT_SGEMM) {
         const int64_t slots = 2 * static_cast<int64_t>(sms);  // two CTAs per SM
+        if (static_cast<double>(M) * static_cast<double>(N) * static_cast<double>(K) <=
+            static_cast<double>(kSmallSgemmWork))
+            return ceil_div(M, 128) * ceil_div(N, 64) >= 32 ? dc.s128x64 : dc.s64x64;
         // 128 x 128 tiles whenever they exist: a grid too small for the GPU is then spread as
         // stream-K blocks or split along K, which keeps the larger, more efficient tile
-        if (M >= 128 && N >= 128) return parse_config(variant, "TILE_M=128 TILE_N=128 TILE_K=16 STAGES=4 FMA2=1");
-        if (ceil_div(M, 128) * ceil_div(N, 128) >= slots) return parse_config(variant, "TILE_M=128 TILE_N=128 TILE_K=16 STAGES=4 FMA2=1");
-        if (ceil_div(M, 128) * ceil_div(N, 64) >= slots) return parse_config(variant, "TILE_M=128 TILE_N=64 TILE_K=8 STAGES=4");
-        return parse_config(variant, "TILE_M=64 TILE_N=64 TILE_K=8 STAGES=4");
+        if (M >= 128 && N >= 128) return dc.s128x128;
+        if (ceil_div(M, 128) * ceil_div(N, 128) >= slots) return dc.s128x128;
+        if (ceil_div(M, 128) * ceil_div(N, 64) >= slots) return dc.s128x64;
+        return dc.s64x64;
     }
-    // the 2-SM 256 x 256 tile whenever it fits the problem: a grid too small for the GPU is
-    // then split along K (when K is long enough), which keeps the efficient tile
-    if (M >= 256 && N >= 256) return parse_config(variant, "TILE_M=256 TILE_N=256 TILE_K=64 STAGES=6");
-    if (ceil_div(M, 128) * ceil_div(N, 256) >= sms) return parse_config(variant, "TILE_M=128 TILE_N=256 TILE_K=64 STAGES=4");
-    if (ceil_div(M, 128) * ceil_div(N, 128) >= sms) return parse_config(variant, "TILE_M=128 TILE_N=128 TILE_K=64 STAGES=6");
-    return parse_config(variant, "TILE_M=128 TILE_N=64 TILE_K=64 STAGES=8");
+    // Few columns, many rows: A is most of the bytes, and rounding it inside the GEMM saves
+    // writing and reading back its f16 copy.  One tile of N, and 128-row tiles for at least
+    // half the SMs (fewer rows leave SMs idle; the other kernel splits such grids along K).
+    if (convert_a && N <= 256 && ceil_div(M, 128) >= sms / 2)
+        return N <= 64 ? dc.c64 : N <= 128 ? dc.c128 : dc.c256;
+    if (M >= 256 && N >= 256) {
+        // the 2-SM 256 x 256 tile when it fills the CTA pairs, or when a grid too small for
+        // the GPU is split along K (32 or more k blocks of 64); else the one-CTA tile that gives more
+        // SMs work (measured on GB300, queued calls: 2048^3 24.8 us with 128 x 256 against
+        // 26.3 with 2-SM 256 x 256 on 128 SMs; 1024^3 14.4 against 16.5; 512^3 10.4 against
+        // 12.5)
+        const int64_t pairs = ceil_div(M, 256) * ceil_div(N, 256);
+        const int64_t workers = sms / 2;
+        const bool k_split = 2 * pairs <= workers && ceil_div(K, 64) >= 32;
+        if (pairs >= workers || k_split) return dc.t256x256;
+        if (ceil_div(M, 128) * ceil_div(N, 256) >= 3 * static_cast<int64_t>(sms) / 4) return dc.t128x256;
+        return dc.t128x128;
+    }
+    if (ceil_div(M, 128) * ceil_div(N, 256) >= sms) return dc.t128x256;
+    if (ceil_div(M, 128) * ceil_div(N, 128) >= sms) return dc.t128x128;
+    return dc.t128x64;
 }
 
 // The configuration for a call: the pin, else the tuned one for this device and shape, else
@@ -373,7 +430,7 @@ int choose_config(int variant, int64_t M, int64_t N, int64_t K, int sms) {
     if (g_pin[variant] >= 0 || g_pin[variant] == kBadPin) return g_pin[variant];
     auto it = g_tuned.find(ShapeKey(tag, variant, M, N, K));
     if (it != g_tuned.end()) return it->second;
-    return default_config(variant, M, N, sms);
+    return default_config(variant, M, N, K, sms);
 }
 
 phx_status config_error(int cfg) { return cfg == kBadPin ? PHX_ERR_CONFIG : PHX_ERR_INTERNAL; }
@@ -659,6 +716,12 @@ phx_status launch_variant(int variant, int cfg, int64_t M, int64_t N, int64_t K,
         if (ws != nullptr) cudaFreeAsync(ws, stream);
         return err == cudaSuccess ? PHX_OK : PHX_ERR_LAUNCH;
     }
+    // the kernel that rounds A reads A stored M x K only: a transposed A takes the default
+    // of the other kernel
+    if (trans_a && phx::f16tc_is_convert_a(cfg)) {
+        cfg = default_tile_config(PHX_VARIANT_F16TC, M, N, K, d->sm_count, false);
+        g_last_cfg[PHX_VARIANT_F16TC].store(cfg);
+    }
     // one pooled block holds the call's scratch (phx::f16tc_run_bytes)
     void* ws = nullptr;
     if (cudaMallocFromPoolAsync(&ws, phx::f16tc_run_bytes(cfg, M, N, K, d->sm_count), d->pool, stream) !=
@@ -743,7 +806,9 @@ phx_status f16in_entry(int trans_a, int trans_b, int64_t M, int64_t N, int64_t K
         return err == cudaSuccess ? PHX_OK : PHX_ERR_LAUNCH;
     }
     int cfg = choose_config(PHX_VARIANT_F16TC, M, N, K, d->sm_count);
-    if (cfg == skinny_index(PHX_VARIANT_F16TC)) cfg = default_tile_config(PHX_VARIANT_F16TC, M, N, d->sm_count);
+    // the skinny kernel and the kernel that rounds A read f32 operands: the default tile then
+    if (cfg == skinny_index(PHX_VARIANT_F16TC) || (cfg >= 0 && phx::f16tc_is_convert_a(cfg)))
+        cfg = default_tile_config(PHX_VARIANT_F16TC, M, N, K, d->sm_count, false);
     if (cfg < 0) return config_error(cfg);
     g_last_cfg[PHX_VARIANT_F16TC].store(cfg);
     const int64_t Kp = (K + 7) / 8 * 8;
@@ -790,6 +855,8 @@ phx_status copy_name(const std::string& s, char* buf, size_t buflen) {
 
 namespace phx {
 size_t f16tc_run_bytes(int cfg, int64_t M, int64_t N, int64_t K, int num_sms) {
+    // the kernel that rounds A itself: only B's f16 copy
+    if (f16tc_is_convert_a(cfg)) return static_cast<size_t>(((N * ((K + 7) / 8 * 8) * 2) + 255) / 256 * 256);
     // the f16 operand copies, then (for a grid split along K) the partial products of the
     // slices
     return f16tc_workspace_bytes(M, N, K) + f16tc_split_bytes(cfg, M, N, K, num_sms);
@@ -798,6 +865,20 @@ size_t f16tc_run_bytes(int cfg, int64_t M, int64_t N, int64_t K, int num_sms) {
 cudaError_t f16tc_run(int cfg, int trans_a, int trans_b, int64_t M, int64_t N, int64_t K, float alpha,
                       const float* A, const float* B, float beta, float* C, void* ws, unsigned int* status,
                       int num_sms, cudaStream_t stream) {
+    if (f16tc_is_convert_a(cfg)) {
+        // B's f16 copy (N x Kp) at the start of ws, then the GEMM that rounds A as it reads it
+        if (trans_a) return cudaErrorInvalidValue;  // it reads A stored M x K only
+        __half* Bt = static_cast<__half*>(ws);
+        cudaError_t err = timed(kKindCast, stream, [&] {
+            return f16tc_prepare_launch(0, 0, trans_b, M, N, K, A, B, nullptr, Bt, num_sms, stream);
+        });
+        if (err == cudaSuccess)
+            err = timed(kKindTcGemm, stream, [&] {
+                return f16cvt_gemm_launch(cfg - (f16tc_num_configs() - f16cvt_num_configs()), M, N, K, alpha, beta,
+                                          C, A, Bt, (K + 7) / 8 * 8, status, num_sms, stream);
+            });
+        return err;
+    }
     const size_t cast_bytes = f16tc_workspace_bytes(M, N, K);
     const size_t split_bytes = f16tc_split_bytes(cfg, M, N, K, num_sms);
     void* split_ws = split_bytes > 0 ? static_cast<char*>(ws) + cast_bytes : nullptr;
@@ -947,7 +1028,8 @@ phx_status phx_debug_violations(int64_t* count) {
         cudaGetLastError();
         return PHX_ERR_LAUNCH;
     }
-    const int64_t parts[3] = {phx::debug_take_sgemm(), phx::debug_take_f16tc(), phx::debug_take_skinny()};
+    const int64_t parts[4] = {phx::debug_take_sgemm(), phx::debug_take_f16tc(), phx::debug_take_f16cvt(),
+                              phx::debug_take_skinny()};
     for (int64_t v : parts) {
         if (v < 0) return PHX_ERR_LAUNCH;
         *count += v;

@@ -39,14 +39,27 @@ def main():
     # the schedules: stream-K tail and whole-grid stream-K, split-K, the TMA epilogue, half-width
     # tail items, the skinny kernels (few rows), ragged and padded edges
     shapes |= {(256, 256, 256), (1024, 1024, 4096), (300, 500, 3000), (2048, 2048, 256), (3000, 2000, 700),
-               (8, 4096, 4096), (2, 128, 65536), (40, 1000, 3000), (1031, 1029, 4100), (1030, 1024, 4099)}
+               (8, 4096, 4096), (2, 128, 65536), (40, 1000, 3000), (1031, 1029, 4100), (1030, 1024, 4099),
+               (10000, 100, 300)}  # the last: few columns, many rows (the kernel that rounds A)
     failures = []
+    runs = 0
     for variant, f16 in ((phx.VARIANT_SGEMM, False), (phx.VARIANT_F16TC, True)):
         for i, (M, N, K) in enumerate(sorted(shapes)):
+            runs += 1
             if not run(variant, f16, M, N, K, 1.5, 0.5, i):
                 failures.append((variant, M, N, K))
+    # the kernel that rounds A, pinned, on the edge shapes
+    for cfg in [n for n in phx.config_names(phx.VARIANT_F16TC) if "CONVERT_A=1" in n]:
+        phx.set_config(phx.VARIANT_F16TC, cfg)
+        for i, (M, N, K) in enumerate(sorted(shapes)):
+            if M * N * K > 2 ** 31:
+                continue
+            runs += 1
+            if not run(phx.VARIANT_F16TC, True, M, N, K, 1.5, 0.5, 100 + i):
+                failures.append((cfg, M, N, K))
+        phx.set_config(phx.VARIANT_F16TC, None)
     count = phx.debug_violations()
-    print(f"shapes {2 * len(shapes)} failures {len(failures)} violations {count}")
+    print(f"shapes {runs} failures {len(failures)} violations {count}")
     if failures:
         print("failed:", failures[:10])
     return 0 if not failures and count == 0 else 1

@@ -108,6 +108,24 @@ def test_default_config_follows_grid_size():
     assert small.startswith("TILE_M=128 TILE_N=128")   # a small grid is split along K instead
     assert skinny.startswith("TILE_M=64 TILE_N=64")
     assert phx.get_config(phx.VARIANT_F16TC, 4096, 4096, 4096).startswith("TILE_M=256 TILE_N=256")
+    # small problems: smaller tiles give more SMs work (152 SMs assumed without a GPU)
+    assert phx.get_config(phx.VARIANT_SGEMM, 512, 512, 512).startswith("TILE_M=128 TILE_N=64 TILE_K=8 ")
+    assert phx.get_config(phx.VARIANT_SGEMM, 256, 256, 256).startswith("TILE_M=64 TILE_N=64 TILE_K=8 ")
+    assert phx.get_config(phx.VARIANT_SGEMM, 1024, 1024, 1024).startswith("TILE_M=128 TILE_N=128")
+    assert phx.get_config(phx.VARIANT_F16TC, 512, 512, 512).startswith("TILE_M=128 TILE_N=128")
+    assert phx.get_config(phx.VARIANT_F16TC, 1024, 1024, 1024).startswith("TILE_M=128 TILE_N=128")
+    assert phx.get_config(phx.VARIANT_F16TC, 2048, 2048, 2048).startswith("TILE_M=128 TILE_N=256")
+    # ... but a grid split along K keeps the 2-SM tile
+    assert phx.get_config(phx.VARIANT_F16TC, 1024, 1024, 16384).startswith("TILE_M=256 TILE_N=256")
+    # few columns, many rows: the kernel that rounds A itself, its tile as wide as N needs
+    for n, tile_n in ((64, 64), (100, 128), (128, 128), (200, 256), (256, 256)):
+        cfg = phx.get_config(phx.VARIANT_F16TC, 16384, n, 4096)
+        assert cfg.startswith(f"TILE_M=128 TILE_N={tile_n} ") and cfg.endswith(" CONVERT_A=1"), (n, cfg)
+    assert "CONVERT_A" not in phx.get_config(phx.VARIANT_F16TC, 16384, 257, 4096)
+    assert "CONVERT_A" not in phx.get_config(phx.VARIANT_F16TC, 4096, 128, 4096)   # rows for 32 SMs only
+    # the f32 variant has no such key
+    with pytest.raises(phx.PhxError):
+        phx.set_config(phx.VARIANT_SGEMM, "TILE_M=128 TILE_N=128 TILE_K=16 CONVERT_A=1")
     # few rows of A: the skinny kernel (B streamed once) up to 48 rows (f32) and 16 (f16)
     assert phx.get_config(phx.VARIANT_SGEMM, 1, 4096, 4096) == "SKINNY"
     assert phx.get_config(phx.VARIANT_SGEMM, 48, 4096, 4096) == "SKINNY"

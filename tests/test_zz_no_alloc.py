@@ -44,6 +44,7 @@ PROBLEMS = [
     (8, 4096, 4096, 1.0, 0.5, 14),       # few rows of A: the skinny kernel, K split in a cluster
     (2, 128, 65536, 1.0, 0.5, 15),       # ... and in planes of partial sums in the scratch
     (8, 8192, 4096, 1.0, 0.5, 17),       # skinny: more than 64 MiB of f16 copies, which it never makes
+    (16384, 128, 1024, 1.0, 0.5, 18),    # few columns: A rounded inside the GEMM, only B's copy in the array
 ]
 
 
