@@ -169,8 +169,9 @@ typedef uint16_t phx_f16;
  * alignment is read in place; otherwise it is copied into the K-major layout the tensor
  * cores read, and B always is (N x K halves, padded to a multiple of 8), in scratch taken in
  * stream order from the library's pooled device memory (PHX_ERR_NOMEM if that fails).  The
- * tile configuration is the f16 variant's (pins and tuning apply); where that is "SKINNY",
- * which reads f32 operands, the default tile configuration is used instead. */
+ * tile configuration is the f16 variant's (pins and tuning apply); where that is "SKINNY"
+ * or a CONVERT_A=1 configuration, which read f32 operands, the default tile configuration
+ * is used instead. */
 phx_status phx_gemm_f16in_f32acc(phx_op op_a, phx_op op_b, int64_t M, int64_t N, int64_t K,
                                  float alpha, const phx_f16* A, const phx_f16* B, float beta,
                                  float* C, phx_stream_t stream);
@@ -242,7 +243,13 @@ phx_status phx_profile_stop(int64_t* launches, double* ms);
  * A configuration is one compiled kernel shape, written as in "gemm, f32" section
  * "Tuning": "TILE_M=128 TILE_N=128 TILE_K=8 STAGES=4" (f32 variant; an optional
  * "FMA2=1" selects packed f32x2 multiply-adds) or "TILE_M=128 TILE_N=256 TILE_K=64
- * STAGES=4" (f16 variant).  The order of keys does not matter.  The last configuration of
+ * STAGES=4" (f16 variant).  The order of keys does not matter.  An f16 configuration
+ * ending in "CONVERT_A=1" (TILE_M=128, TILE_N 64, 128 or 256) is the kernel that rounds A to
+ * f16 itself as it stages A's f32 tiles, so that only B goes through the separate rounding
+ * pass; it is the default where N <= 256 and A has 128-row tiles for at least half the SMs,
+ * and it computes the same rounded products, summed in f32 in the same order per tile.  A
+ * stored K x M (op_a = PHX_OP_T) and the half-precision entry points take the default of the
+ * other kernel instead.  The last configuration of
  * each variant, "SKINNY", is the kernel for few rows of A (the lab's skinny-matrix sweep,
  * Part 5): B is streamed once from HBM with 16-byte loads and the products are summed with
  * f32 multiply-adds on the CUDA cores (for the f16 variant, of operands rounded to f16 as
