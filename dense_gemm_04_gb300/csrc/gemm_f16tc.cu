@@ -494,11 +494,13 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                          (partial == nullptr || (reinterpret_cast<uintptr_t>(partial) & 15u) == 0);
         // an f16 result (Ch) moves 4 halves = 8 bytes per lane on the vector path
         const bool vec_h = (N % 4 == 0) && ((reinterpret_cast<uintptr_t>(Ch) & 7u) == 0);
-        // The TMA epilogue (f32 C, whole tiles, N % 4 == 0, C 16-byte aligned): each 32 x 32
-        // chunk's c_old arrives by TMA in one of the warp's two swizzled buffers (the next
-        // chunk's while this one is finished), lane = row finishes the row in place from the
-        // accumulator, and the chunk leaves by TMA store.
-        const bool tma_c = EPI_TMA && !OUT_H && epi_tma != 0 && ksplit == 1;
+        // The TMA epilogue (whole tiles; an f32 C with N % 4 == 0 or an f16 C with N % 8 == 0,
+        // 16-byte aligned): each 32 x 32 chunk's c_old arrives by TMA in one of the warp's two
+        // buffers (the next chunk's while this one is finished), lane = row finishes the row in
+        // place from the accumulator, and the chunk leaves by TMA store.  An f32 chunk is a
+        // 128-byte swizzled box of 4 KB; an f16 chunk an unswizzled box of 2 KB (64-byte rows).
+        const bool tma_c = EPI_TMA && epi_tma != 0 && ksplit == 1;
+        constexpr uint32_t kChunkBytes = OUT_H ? 32 * 32 * 2 : 32 * 32 * 4;
         const bool load_c = tma_c && beta != 0.f;
         const uint32_t ebuf = smem_u32(epi);
         auto swz = [](int r, int u) { return r * 32 + ((u ^ (r & 7)) << 2); };
@@ -510,7 +512,7 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             if (w_req >= num_items) return;
             const Item nx = decode(w_req);
             if (!live(nx, c_req)) return;
-            mbar_arrive_expect_tx(cold_bar(warp, b), 32 * 32 * 4);
+            mbar_arrive_expect_tx(cold_bar(warp, b), kChunkBytes);
             tma_load_2d(ebuf + b * 4096, &tmC, nx.n0 + c_req * 32, nx.pm * kBM + warp * 32, cold_bar(warp, b));
             cpend |= 1u << b;
         };
@@ -569,22 +571,45 @@ gemm_f16tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     continue;
                 }
                 float* buf = epi + b * 32 * 32;
+                if constexpr (OUT_H) {
+                    // row `lane`: 32 halves = 4 x 16 bytes; alpha * acc + beta * c_old in f32,
+                    // rounded to f16 once
+                    uint4* row4 = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(buf) + lane * 64);
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    float4* p4 = reinterpret_cast<float4*>(buf + swz(lane, u));
-                    float4 o;
-                    o.x = alpha * __uint_as_float(r[u * 4 + 0]);
-                    o.y = alpha * __uint_as_float(r[u * 4 + 1]);
-                    o.z = alpha * __uint_as_float(r[u * 4 + 2]);
-                    o.w = alpha * __uint_as_float(r[u * 4 + 3]);
-                    if (load_c) {
-                        const float4 co = *p4;
-                        o.x = fmaf(beta, co.x, o.x);
-                        o.y = fmaf(beta, co.y, o.y);
-                        o.z = fmaf(beta, co.z, o.z);
-                        o.w = fmaf(beta, co.w, o.w);
+                    for (int u = 0; u < 4; ++u) {
+                        float o[8];
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) o[q] = alpha * __uint_as_float(r[u * 8 + q]);
+                        if (load_c) {
+                            const uint4 raw = row4[u];
+                            const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const __half2 h2 = *reinterpret_cast<const __half2*>(&wv[q]);
+                                o[2 * q] = fmaf(beta, __low2float(h2), o[2 * q]);
+                                o[2 * q + 1] = fmaf(beta, __high2float(h2), o[2 * q + 1]);
+                            }
+                        }
+                        row4[u] = pack8(o);
                     }
-                    *p4 = o;
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        float4* p4 = reinterpret_cast<float4*>(buf + swz(lane, u));
+                        float4 o;
+                        o.x = alpha * __uint_as_float(r[u * 4 + 0]);
+                        o.y = alpha * __uint_as_float(r[u * 4 + 1]);
+                        o.z = alpha * __uint_as_float(r[u * 4 + 2]);
+                        o.w = alpha * __uint_as_float(r[u * 4 + 3]);
+                        if (load_c) {
+                            const float4 co = *p4;
+                            o.x = fmaf(beta, co.x, o.x);
+                            o.y = fmaf(beta, co.y, o.y);
+                            o.z = fmaf(beta, co.z, o.z);
+                            o.w = fmaf(beta, co.w, o.w);
+                        }
+                        *p4 = o;
+                    }
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -796,11 +821,19 @@ bool make_map_c(CUtensorMap* map, float* C, int64_t M, int64_t N) {
                      static_cast<uint64_t>(N) * 4, 32, 32);
 }
 
+// An f16 C as 32 x 32 boxes of 64-byte rows, unswizzled.  Needs N % 8 == 0 and a 16-byte
+// aligned C.
+bool make_map_ch(CUtensorMap* map, __half* Ch, int64_t M, int64_t N) {
+    return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Ch, static_cast<uint64_t>(N), static_cast<uint64_t>(M),
+                     static_cast<uint64_t>(N) * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 struct TcEntry {
     F16Config cfg;
     TcKernelFn fn;      // f32 result
     TcKernelFn fn_tma;  // f32 result through the TMA epilogue
     TcKernelFn fn_h;    // f16 result
+    TcKernelFn fn_h_tma;  // f16 result through the TMA epilogue
     uint32_t smem;
 };
 
@@ -811,7 +844,8 @@ TcEntry make_tc_entry() {
     static_assert(PAIR == 0 || PAIR == 2, "one CTA per tile, or the 2-SM pair");
     return TcEntry{F16Config{PAIR == 2 ? 2 * kBM : kBM, BN, kBK, STAGES, PAIR == 0 ? 1 : 2},
                    &gemm_f16tc_kernel<BN, STAGES, PAIR, false, false>, &gemm_f16tc_kernel<BN, STAGES, PAIR, false, true>,
-                   &gemm_f16tc_kernel<BN, STAGES, PAIR, true, false>, TcLayout<BN, STAGES, PAIR>::kDynSmem};
+                   &gemm_f16tc_kernel<BN, STAGES, PAIR, true, false>, &gemm_f16tc_kernel<BN, STAGES, PAIR, true, true>,
+                   TcLayout<BN, STAGES, PAIR>::kDynSmem};
 }
 
 const TcEntry kTcEntries[] = {
@@ -956,12 +990,14 @@ cudaError_t f16tc_gemm_launch_ops(int index, int64_t M, int64_t N, int64_t K, fl
         !make_map(&mapB_half, Bt, N, Kp, e.cfg.tile_n / 2, ldb) ||
         !make_map(&mapB_quarter, Bt, N, Kp, e.cfg.tile_n / 4, ldb))
         return cudaErrorInvalidValue;
-    // the TMA epilogue for an f32 C whose rows are 16-byte aligned (whole tiles: decided
-    // below, once the split is known)
+    // the TMA epilogue for an f32 C whose rows are 16-byte aligned, or an f16 C with N % 8 == 0
+    // and a 16-byte aligned base (whole tiles: decided below, once the split is known)
     CUtensorMap mapC;
     std::memset(&mapC, 0, sizeof mapC);
-    const bool c_tma_ok = Ch == nullptr && N % 4 == 0 && (reinterpret_cast<uintptr_t>(C) & 15u) == 0 &&
-                          make_map_c(&mapC, C, M, N);
+    const bool c_tma_ok = Ch == nullptr ? N % 4 == 0 && (reinterpret_cast<uintptr_t>(C) & 15u) == 0 &&
+                                              make_map_c(&mapC, C, M, N)
+                                        : N % 8 == 0 && (reinterpret_cast<uintptr_t>(Ch) & 15u) == 0 &&
+                                              make_map_ch(&mapC, Ch, M, N);
     TcKernelFn fn = Ch != nullptr ? e.fn_h : e.fn;
     cudaError_t err = cudaSuccess;
     const int tiles_m = static_cast<int>((M + kBM - 1) / kBM);  // 128-row tiles (one per CTA)
@@ -1004,7 +1040,7 @@ cudaError_t f16tc_gemm_launch_ops(int index, int64_t M, int64_t N, int64_t K, fl
     const int m32 = static_cast<int>(M), n32 = static_cast<int>(N), full32 = static_cast<int>(full);
     float* partial = ksplit > 1 ? static_cast<float*>(split_ws) : nullptr;
     const int epi_tma = (c_tma_ok && ksplit == 1) ? 1 : 0;
-    if (epi_tma) fn = e.fn_tma;
+    if (epi_tma) fn = Ch != nullptr ? e.fn_h_tma : e.fn_tma;
     err = set_func_attr_once(reinterpret_cast<const void*>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(e.smem));
     if (err != cudaSuccess) return err;

@@ -124,6 +124,28 @@ def test_f16_inputs_layouts_and_alignment(out_f16):
     _check(200, 136, 77, 1.0, 0.5, "int3", out_f16, seed=10)
 
 
+@pytest.mark.parametrize("N,c_offset", [(264, 0), (264, 1), (262, 0)])
+def test_f16_output_epilogues(N, c_offset):
+    # an f16 C with N % 8 == 0 on 16 bytes leaves through the TMA epilogue (c_old loaded a chunk
+    # ahead); one 2 bytes off, or with N % 8 != 0, through the register epilogue: the same bits
+    import torch
+    M, K = 300, 200
+    A, B, C = synth.problem(M, N, K, seed=12, dist="int3")
+    C = C.astype(np.float16).astype(np.float32)
+    want, _ = oracle.gemm_f16out(A, B, C, 1.5, 0.5)
+    flat = torch.zeros(M * N + c_offset, dtype=torch.float16)
+    flat[c_offset:] = torch.from_numpy(C.reshape(-1).astype(np.float16))
+    dC = flat.cuda()
+    dA = torch.from_numpy(A.astype(np.float16)).cuda()
+    dB = torch.from_numpy(B.astype(np.float16)).cuda()
+    st = phx.phx_gemm_f16in_f16out(phx.OP_N, phx.OP_N, M, N, K, 1.5, dA.data_ptr(), dB.data_ptr(), 0.5,
+                                   dC.data_ptr() + 2 * c_offset, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert st == phx.PHX_OK, phx.status_string(st)
+    got = dC.cpu()[c_offset:].numpy().view(np.uint16).reshape(M, N)
+    assert np.array_equal(got, want), (N, c_offset, int((got != want).sum()))
+
+
 @pytest.mark.parametrize("out_f16", [False, True])
 def test_f16_inputs_degenerate(out_f16):
     A, B, C = synth.problem(9, 7, 5, seed=11, dist="int3")
