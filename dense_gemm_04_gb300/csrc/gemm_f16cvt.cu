@@ -1,39 +1,47 @@
-// gemm_f16cvt.cu -- the f16 tensor-core GEMM with A rounded to f16 inside the kernel.
+// gemm_f16cvt.cu -- the f16 tensor-core GEMM with one operand rounded to f16 inside the kernel.
 //
 // The arithmetic is that of gemm_f16tc.cu: every element of A and B rounded to the nearest
 // f16 (ties to even), the f16 x f16 products summed in f32 by tcgen05.mma.kind::f16, then
 // alpha * acc + beta * c_old ("gemm on tensor cores", phobos-lang.dev/docs/examples/
-// gemm-fp16tc-fp32acc/, section "What changes").  The difference is where A is rounded.
+// gemm-fp16tc-fp32acc/, section "What changes").  The difference is where the large operand
+// is rounded.
 //
-// For a problem with many rows and few columns (N within one or two tiles) A is most of the
-// bytes, and the GEMM is bound by memory.  The separate rounding pass would read A, write
-// its f16 copy (half of A's bytes), and the GEMM would read that copy back: 1.5 x A's f32
-// bytes on top of the one read of A the problem needs.  Here the kernel reads A (f32) once,
-// rounds it on the way into shared memory, in the layout the MMA reads.  Only B, which is
-// small on such shapes, still goes through the rounding pass (N x Kp f16, K-major) and
-// arrives by TMA.
+// When one operand is most of a problem's bytes, the GEMM is bound by memory, and the
+// separate rounding pass would read that operand, write its f16 copy (half its bytes) and
+// the GEMM would read the copy back: 1.5 x its f32 bytes on top of the one read the problem
+// needs.  Here the kernel reads that operand (f32) once and rounds it on the way into shared
+// memory, in the layout the MMA reads; the other, small operand still goes through the
+// rounding pass (K-major f16) and arrives by TMA.
+//   CONVERT_A (CB = false): many rows, few columns (N within a tile or two).  A is staged as
+//     128 x 64 f32 boxes; B comes from the pass as N x Kp f16.
+//   CONVERT_B (CB = true): few rows (up to a tile or two), many columns.  B is staged as
+//     64 x TILE_N f32 boxes (k rows of n) and transposed while it is rounded; A comes from
+//     the pass as M x Kp f16.  A grid of few tiles is split along K into slices that write
+//     f32 partial planes, added in slice order by a separate reduction.
 //
 // A persistent kernel, one CTA per SM, 320 threads (10 warps):
-//   warp 4      TMA producer: per 64-wide k block of a 128-row tile, the 128 x 64 f32 box of A
-//               (unswizzled, zeros past M and K) into a staging ring three k blocks deep, and
-//               the TILE_N x 64 f16 tile of B into the MMA ring.
-//   warps 6-9   converters: warp 6 + w takes rows 32w .. 32w+31 of the staged box; each lane
-//               reads 8 (row, 16-byte chunk) pairs of 8 floats, hands the staging slot back,
-//               rounds them with cvt.rn.f16x2.f32 and stores the 8 halves at chunk c ^ (r % 8)
-//               of row r of the MMA ring's A slot: the 128-byte swizzle that TMA's
-//               CU_TENSOR_MAP_SWIZZLE_128B writes.  (When A's rows do not start on 16 bytes
-//               there is no tensor map of A: the converters then load A from global memory
-//               themselves, 4 bytes at a time.)
+//   warp 4      TMA producer: per 64-deep k block, the f32 box of the converted operand into
+//               a staging ring three k blocks deep (unswizzled, zeros past the edges), and
+//               the f16 tile of the other operand into the MMA ring.
+//   warps 6-9   converters.  Each lane reads 8 (row, 16-byte chunk) pairs of 8 floats from
+//               the staged box, hands the staging slot back, rounds them with
+//               cvt.rn.f16x2.f32 and stores the 8 halves at chunk c ^ (r % 8) of row r of
+//               the MMA ring's slot: the 128-byte swizzle TMA's CU_TENSOR_MAP_SWIZZLE_128B
+//               writes, so the MMA descriptors are those of gemm_f16tc.cu.  For A a row of
+//               the slot is a row of the box; for B a row of the slot (one n) is a column of
+//               the box, read 8 k rows apart.  (Without a tensor map of the operand, rows not
+//               on 16 bytes, the converters load it from global memory themselves.)
 //   warp 5      MMA issuer: tcgen05.mma.cta_group::1 (M = 128, N = TILE_N, K = 16).
 //   warps 0-3   epilogue: tcgen05.ld of the accumulator (warp w: rows 32w..32w+31), through
-//               a per-warp shared-memory buffer to coalesced rows of C.
-// An MMA ring slot is full when B's bytes have landed and the four converter warps have
+//               a per-warp shared-memory buffer to coalesced rows of C (or of a k slice's
+//               partial plane).
+// An MMA ring slot is full when the TMA bytes have landed and the four converter warps have
 // arrived (after a proxy fence that makes their generic stores visible to the tensor cores).
 // The accumulator is double-buffered in tensor memory.  Every wait is bounded (sm100_ptx.cuh).
 //
-// The kernel is launched as a programmatic dependent of the pass that rounds B.  A does not
-// depend on that pass: the producer issues A's first staging load, then waits for the pass
-// (griddepcontrol.wait) before its first load of B.
+// The kernel is launched as a programmatic dependent of the rounding pass.  The converted
+// operand does not depend on that pass: the producer issues its first staging load, then
+// waits for the pass (griddepcontrol.wait) before the first load of the other operand.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -58,17 +66,22 @@ constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kFirstConvWarp = 6;
 constexpr int kConvWarps = 4;   // warps 6-9
+constexpr int kConvThreads = 32 * kConvWarps;
 constexpr int kThreads = 32 * (kFirstConvWarp + kConvWarps);
 
-// How the converters get A: 0 four bytes at a time from global memory, 1 sixteen bytes at a
-// time from global memory (rows on 16 bytes), 2 from the TMA staging ring.
-enum AMode : int { kAScalar = 0, kAVector = 1, kATma = 2 };
+// How the converters get their operand: 0 four bytes at a time from global memory, 1
+// sixteen bytes at a time from global memory (A's rows on 16 bytes), 2 from the TMA
+// staging ring.
+enum SrcMode : int { kSrcScalar = 0, kSrcVector = 1, kSrcTma = 2 };
 
-template <int BN, int STAGES, int STG>
+template <int BN, int STAGES, int STG, bool CB>
 struct CvtLayout {
     static constexpr uint32_t kABytes = kBM * kBK * 2;      // f16 A slot of the MMA ring
     static constexpr uint32_t kBBytes = BN * kBK * 2;       // f16 B slot
-    static constexpr uint32_t kStgBytes = kBM * kBK * 4;    // f32 A slot of the staging ring
+    // f32 slot of the staging ring: 128 rows of A x 64 k, or 64 k x TILE_N columns of B
+    static constexpr uint32_t kStgBytes = (CB ? BN : kBM) * kBK * 4;
+    // 16-byte chunks a converter thread writes per k block (the converted slot / 16 / 128)
+    static constexpr int kChunks = (CB ? kBBytes : kABytes) / 16 / kConvThreads;
     // offsets from the 1024-byte aligned base
     static constexpr uint32_t kA = 0;
     static constexpr uint32_t kB = STAGES * kABytes;
@@ -86,6 +99,7 @@ struct CvtLayout {
     static constexpr uint32_t kTmemCols = 2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512);
     static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "tcgen05 N, and whole 32-column chunks");
     static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "swizzle atoms stay 1024-aligned");
+    static_assert(kChunks * 16 * kConvThreads == (CB ? kBBytes : kABytes), "the converters cover the slot");
     static_assert(kDynSmem <= 227 * 1024, "fits one CTA's shared memory");
 };
 
@@ -102,12 +116,18 @@ __device__ __forceinline__ uint32_t half2_bits(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-template <int BN, int STAGES, int STG>
+// src: the operand the converters round (A for CONVERT_A, B for CONVERT_B), f32 row-major
+// (A: M x K, B: K x N).  tm_stg: its f32 tensor map for the staging ring (src_mode kSrcTma).
+// tm_f16: the other operand's K-major f16 tensor map (B: N x Kp for CONVERT_A, A: M x Kp for
+// CONVERT_B).  With ksplit > 1 the items are (tile, k slice) pairs and each writes its slice's
+// partial products (alpha = 1, beta = 0) to plane `slice` of `partial` (M x N f32 each).
+template <int BN, int STAGES, int STG, bool CB>
 __global__ void __launch_bounds__(kThreads, 1)
-gemm_f16cvt_kernel(const float* __restrict__ A, const __grid_constant__ CUtensorMap tmA,
-                   const __grid_constant__ CUtensorMap tmB, float* __restrict__ C, int M, int N, int K, int num_kb,
-                   float alpha, float beta, int tiles_m, int tiles_n, unsigned int* status, int a_mode) {
-    using L = CvtLayout<BN, STAGES, STG>;
+gemm_f16cvt_kernel(const float* __restrict__ src, const __grid_constant__ CUtensorMap tm_stg,
+                   const __grid_constant__ CUtensorMap tm_f16, float* __restrict__ C, int M, int N, int K,
+                   int num_kb, float alpha, float beta, int tiles_m, int tiles_n, unsigned int* status,
+                   int src_mode, int ksplit, int kb_per_slice, float* __restrict__ partial) {
+    using L = CvtLayout<BN, STAGES, STG, CB>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -129,18 +149,26 @@ gemm_f16cvt_kernel(const float* __restrict__ A, const __grid_constant__ CUtensor
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    const bool staged = a_mode == kATma;
-    const int num_items = tiles_m * tiles_n;
-    // item w: tile row w % tiles_m, tile column w / tiles_m (the CTAs at work at one time
-    // share B's tile)
-    auto tile_of = [&](int w, int& pm, int& pn) {
-        pn = w / tiles_m;
-        pm = w - pn * tiles_m;
+    const bool staged = src_mode == kSrcTma;
+    const int num_items = tiles_m * tiles_n * ksplit;
+    // item w: slice w % ksplit of tile t = w / ksplit, tile row t % tiles_m, tile column
+    // t / tiles_m (the CTAs at work at one time share the column's tile of B); k blocks
+    // kb0 .. kb0 + nkb - 1
+    struct Item { int pm, pn, slice, kb0, nkb; };
+    auto decode = [&](int w) {
+        Item it;
+        const int t = w / ksplit;
+        it.slice = w - t * ksplit;
+        it.pn = t / tiles_m;
+        it.pm = t - it.pn * tiles_m;
+        it.kb0 = it.slice * kb_per_slice;
+        it.nkb = min(kb_per_slice, num_kb - it.kb0);
+        return it;
     };
 
     if (warp == kProducerWarp && lane == 0) {
-        tma_prefetch_desc(&tmB);
-        if (staged) tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tm_f16);
+        if (staged) tma_prefetch_desc(&tm_stg);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1 + kConvWarps);  // the producer's expect_tx + the converters
             mbar_init(empty_bar(s), 1);
@@ -169,32 +197,39 @@ gemm_f16cvt_kernel(const float* __restrict__ A, const __grid_constant__ CUtensor
             uint32_t issued_mask = 0, issued_phase = 0, sissued_mask = 0, sissued_phase = 0;
             uint32_t stage = 0, phase = 0, sstage = 0, sphase = 0;
             bool ok = true;
-            bool b_ready = false;  // the rounding pass of B has been waited for
+            bool pass_done = false;  // the rounding pass has been waited for
             for (int w = blockIdx.x; w < num_items && ok; w += gridDim.x) {
-                int pm, pn;
-                tile_of(w, pm, pn);
-                for (int kb = 0; kb < num_kb; ++kb) {
+                const Item it = decode(w);
+                for (int kb = it.kb0; kb < it.kb0 + it.nkb; ++kb) {
                     if (staged) {
-                        // A does not depend on the rounding pass: its first loads go out
-                        // before the wait for that pass
+                        // the converted operand does not depend on the rounding pass: its
+                        // first loads go out before the wait for that pass
                         if (!mbar_wait(sempty_bar(sstage), sphase ^ 1u, abort_flag, status)) { ok = false; break; }
-                        PHX_DCHECK(sstage < STG && pm < tiles_m);
+                        PHX_DCHECK(sstage < STG && it.pm < tiles_m && it.pn < tiles_n && kb < num_kb);
                         mbar_arrive_expect_tx(sfull_bar(sstage), L::kStgBytes);
-                        tma_load_2d(sStg + sstage * L::kStgBytes, &tmA, kb * kBK, pm * kBM, sfull_bar(sstage));
+                        if constexpr (CB)
+                            tma_load_2d(sStg + sstage * L::kStgBytes, &tm_stg, it.pn * BN, kb * kBK, sfull_bar(sstage));
+                        else
+                            tma_load_2d(sStg + sstage * L::kStgBytes, &tm_stg, kb * kBK, it.pm * kBM, sfull_bar(sstage));
                         sissued_mask |= 1u << sstage;
                         sissued_phase = (sissued_phase & ~(1u << sstage)) | (sphase << sstage);
                         if (++sstage == STG) { sstage = 0; sphase ^= 1u; }
                     }
-                    if (!b_ready) {
-                        // B comes from the rounding pass just before this kernel, which may
-                        // still be running
+                    if (!pass_done) {
+                        // the other operand comes from the rounding pass just before this
+                        // kernel, which may still be running
                         asm volatile("griddepcontrol.wait;" ::: "memory");
-                        b_ready = true;
+                        pass_done = true;
                     }
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, status)) { ok = false; break; }
-                    PHX_DCHECK(stage < STAGES && pn < tiles_n);
-                    mbar_arrive_expect_tx(full_bar(stage), L::kBBytes);
-                    tma_load_2d(sB + stage * L::kBBytes, &tmB, kb * kBK, pn * BN, full_bar(stage));
+                    PHX_DCHECK(stage < STAGES);
+                    if constexpr (CB) {
+                        mbar_arrive_expect_tx(full_bar(stage), L::kABytes);
+                        tma_load_2d(sA + stage * L::kABytes, &tm_f16, kb * kBK, it.pm * kBM, full_bar(stage));
+                    } else {
+                        mbar_arrive_expect_tx(full_bar(stage), L::kBBytes);
+                        tma_load_2d(sB + stage * L::kBBytes, &tm_f16, kb * kBK, it.pn * BN, full_bar(stage));
+                    }
                     issued_mask |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -209,19 +244,28 @@ gemm_f16cvt_kernel(const float* __restrict__ A, const __grid_constant__ CUtensor
             }
         }
     } else if (warp >= kFirstConvWarp) {
-        const int cw = warp - kFirstConvWarp;  // rows 32cw .. 32cw+31 of each tile
-        const int chunk = lane & 7;             // 16-byte chunk of a 128-byte f16 row
+        const int ct = threadIdx.x - 32 * kFirstConvWarp;  // 0 .. 127
+        // chunk i of this thread: row r_i of the converted slot (a row of A, or one n of B),
+        // and its 16-byte chunk c_i (8 consecutive k).
+        //   A: warp w owns rows 32w .. 32w+31; lane takes chunk lane % 8 of rows 4i + lane / 8.
+        //   B: chunk id ct + 128 i: n = id % TILE_N, chunk = id / TILE_N, so the 32 lanes of a
+        //      warp read 32 consecutive n of one staged k row (one 128-byte line).
+        auto row_of = [&](int i) {
+            if constexpr (CB) return (ct + kConvThreads * i) % BN;
+            else return (ct / 32) * 32 + 4 * i + (lane >> 3);
+        };
+        auto chunk_of = [&](int i) {
+            if constexpr (CB) return (ct + kConvThreads * i) / BN;
+            else return lane & 7;
+        };
         uint32_t stage = 0, phase = 0, sstage = 0, sphase = 0;
         bool ok = true;
         for (int w = blockIdx.x; w < num_items && ok; w += gridDim.x) {
-            int pm, pn;
-            tile_of(w, pm, pn);
-            const int64_t row_base = static_cast<int64_t>(pm) * kBM + cw * 32;
-            for (int kb = 0; kb < num_kb; ++kb) {
-                const int k = kb * kBK + chunk * 8;
-                float4 v[8][2];
+            const Item it = decode(w);
+            for (int kb = it.kb0; kb < it.kb0 + it.nkb; ++kb) {
+                float v[L::kChunks][8];
                 if (staged) {
-                    // the f32 box (zeros past M and K) from the staging slot, then the slot
+                    // the f32 box (zeros past the edges) from the staging slot, then the slot
                     // goes back to the producer
                     if (!__all_sync(0xffffffffu, mbar_wait(sfull_bar(sstage), sphase, abort_flag, status))) {
                         ok = false;
@@ -229,29 +273,45 @@ gemm_f16cvt_kernel(const float* __restrict__ A, const __grid_constant__ CUtensor
                     }
                     const float* stg = reinterpret_cast<const float*>(base_ptr + L::kStg + sstage * L::kStgBytes);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int r = cw * 32 + 4 * i + (lane >> 3);
-                        v[i][0] = *reinterpret_cast<const float4*>(stg + r * kBK + chunk * 8);
-                        v[i][1] = *reinterpret_cast<const float4*>(stg + r * kBK + chunk * 8 + 4);
+                    for (int i = 0; i < L::kChunks; ++i) {
+                        const int r = row_of(i), c = chunk_of(i);
+                        if constexpr (CB) {
+                            // column r of the 64 x TILE_N box, k rows 8c .. 8c+7
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) v[i][q] = stg[(8 * c + q) * BN + r];
+                        } else {
+                            const float4 x = *reinterpret_cast<const float4*>(stg + r * kBK + c * 8);
+                            const float4 y = *reinterpret_cast<const float4*>(stg + r * kBK + c * 8 + 4);
+                            v[i][0] = x.x; v[i][1] = x.y; v[i][2] = x.z; v[i][3] = x.w;
+                            v[i][4] = y.x; v[i][5] = y.y; v[i][6] = y.z; v[i][7] = y.w;
+                        }
                     }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(sempty_bar(sstage));
                     if (++sstage == STG) { sstage = 0; sphase ^= 1u; }
                 } else {
-                    // straight from global memory, all 8 chunks' loads in flight together
+                    // straight from global memory, all chunks' loads in flight together
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int64_t grow = row_base + 4 * i + (lane >> 3);
-                        const float* src = A + grow * K + k;
-                        if (grow < M && a_mode == kAVector && k + 8 <= K) {
-                            v[i][0] = ld_stream4(src);
-                            v[i][1] = ld_stream4(src + 4);
+                    for (int i = 0; i < L::kChunks; ++i) {
+                        const int r = row_of(i), c = chunk_of(i);
+                        const int k = kb * kBK + c * 8;
+                        if constexpr (CB) {
+                            const int64_t n = static_cast<int64_t>(it.pn) * BN + r;
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                v[i][q] = (n < N && k + q < K) ? __ldg(src + static_cast<int64_t>(k + q) * N + n) : 0.f;
                         } else {
-                            float t[8];
+                            const int64_t grow = static_cast<int64_t>(it.pm) * kBM + r;
+                            const float* p = src + grow * K + k;
+                            if (grow < M && src_mode == kSrcVector && k + 8 <= K) {
+                                const float4 x = ld_stream4(p);
+                                const float4 y = ld_stream4(p + 4);
+                                v[i][0] = x.x; v[i][1] = x.y; v[i][2] = x.z; v[i][3] = x.w;
+                                v[i][4] = y.x; v[i][5] = y.y; v[i][6] = y.z; v[i][7] = y.w;
+                            } else {
 #pragma unroll
-                            for (int q = 0; q < 8; ++q) t[q] = (grow < M && k + q < K) ? __ldg(src + q) : 0.f;
-                            v[i][0] = make_float4(t[0], t[1], t[2], t[3]);
-                            v[i][1] = make_float4(t[4], t[5], t[6], t[7]);
+                                for (int q = 0; q < 8; ++q) v[i][q] = (grow < M && k + q < K) ? __ldg(p + q) : 0.f;
+                            }
                         }
                     }
                 }
@@ -259,17 +319,17 @@ gemm_f16cvt_kernel(const float* __restrict__ A, const __grid_constant__ CUtensor
                     ok = false;
                     break;
                 }
-                uint8_t* a_stage = base_ptr + L::kA + stage * L::kABytes;
+                uint8_t* slot = base_ptr + (CB ? L::kB + stage * L::kBBytes : L::kA + stage * L::kABytes);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int r = cw * 32 + 4 * i + (lane >> 3);  // row within the tile
+                for (int i = 0; i < L::kChunks; ++i) {
+                    const int r = row_of(i), c = chunk_of(i);
                     uint4 h;
-                    h.x = half2_bits(v[i][0].x, v[i][0].y);
-                    h.y = half2_bits(v[i][0].z, v[i][0].w);
-                    h.z = half2_bits(v[i][1].x, v[i][1].y);
-                    h.w = half2_bits(v[i][1].z, v[i][1].w);
-                    PHX_DCHECK(r < kBM && chunk < 8);
-                    *reinterpret_cast<uint4*>(a_stage + r * 128 + ((chunk ^ (r & 7)) << 4)) = h;
+                    h.x = half2_bits(v[i][0], v[i][1]);
+                    h.y = half2_bits(v[i][2], v[i][3]);
+                    h.z = half2_bits(v[i][4], v[i][5]);
+                    h.w = half2_bits(v[i][6], v[i][7]);
+                    PHX_DCHECK(r < (CB ? BN : kBM) && c < 8);
+                    *reinterpret_cast<uint4*>(slot + r * 128 + ((c ^ (r & 7)) << 4)) = h;
                 }
                 // the stores become visible to the tensor cores' reads of the slot
                 fence_proxy_async_smem();
@@ -285,11 +345,12 @@ gemm_f16cvt_kernel(const float* __restrict__ A, const __grid_constant__ CUtensor
             uint32_t acc = 0, acc_phase = 0;
             bool ok = true;
             for (int w = blockIdx.x; w < num_items && ok; w += gridDim.x) {
+                const Item it = decode(w);
                 if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, status)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                PHX_DCHECK(acc * BN + BN <= L::kTmemCols);
-                for (int kb = 0; kb < num_kb; ++kb) {
+                PHX_DCHECK(acc * BN + BN <= L::kTmemCols && it.nkb > 0);
+                for (int kb = 0; kb < it.nkb; ++kb) {
                     if (!mbar_wait(full_bar(stage), phase, abort_flag, status)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t a0 = sA + stage * L::kABytes;
@@ -315,20 +376,24 @@ gemm_f16cvt_kernel(const float* __restrict__ A, const __grid_constant__ CUtensor
     } else {
         // epilogue, warps 0-3: warp w owns TMEM lanes (rows) 32w .. 32w+31
         float* epi = reinterpret_cast<float*>(base_ptr + L::kEpi) + warp * L::kEpiWarpFloats;
-        const bool vec = (N % 4 == 0) && ((reinterpret_cast<uintptr_t>(C) & 15u) == 0);
-        const bool read_c = beta != 0.f;
+        const bool vec = (N % 4 == 0) && ((reinterpret_cast<uintptr_t>(C) & 15u) == 0) &&
+                         (partial == nullptr || (reinterpret_cast<uintptr_t>(partial) & 15u) == 0);
         uint32_t acc = 0, acc_phase = 0;
         for (int w = blockIdx.x; w < num_items; w += gridDim.x) {
-            int pm, pn;
-            tile_of(w, pm, pn);
+            const Item it = decode(w);
+            // a k slice writes its plane of partial products; a whole tile writes C
+            float* Cout = ksplit > 1 ? partial + static_cast<int64_t>(it.slice) * M * N : C;
+            const float a_out = ksplit > 1 ? 1.f : alpha;
+            const float b_out = ksplit > 1 ? 0.f : beta;
+            const bool read_c = b_out != 0.f;
             // warp-uniform outcome: tcgen05.ld below is .sync.aligned
             if (!__all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), acc_phase, abort_flag, status))) break;
             tc_fence_after();
-            const int row0 = pm * kBM + warp * 32;
+            const int row0 = it.pm * kBM + warp * 32;
             const uint32_t t_base = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + acc * BN;
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
-                const int col0 = pn * BN + c * 32;
+                const int col0 = it.pn * BN + c * 32;
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(t_base + c * 32, r);
                 tmem_ld_wait();
@@ -350,7 +415,7 @@ gemm_f16cvt_kernel(const float* __restrict__ A, const __grid_constant__ CUtensor
                             const int row = row0 + q * 4 + lane / 8;
                             cv[q] = make_float4(0.f, 0.f, 0.f, 0.f);
                             if (row < M && col < N)
-                                cv[q] = *reinterpret_cast<const float4*>(C + static_cast<int64_t>(row) * N + col);
+                                cv[q] = *reinterpret_cast<const float4*>(Cout + static_cast<int64_t>(row) * N + col);
                         }
                     }
 #pragma unroll
@@ -359,15 +424,15 @@ gemm_f16cvt_kernel(const float* __restrict__ A, const __grid_constant__ CUtensor
                         const int row = row0 + rr;
                         if (row < M && col < N) {
                             const float4 a = *reinterpret_cast<const float4*>(epi + rr * L::kEpiStride + cc);
-                            float4 o = make_float4(alpha * a.x, alpha * a.y, alpha * a.z, alpha * a.w);
+                            float4 o = make_float4(a_out * a.x, a_out * a.y, a_out * a.z, a_out * a.w);
                             if (read_c) {
-                                o.x = fmaf(beta, cv[q].x, o.x);
-                                o.y = fmaf(beta, cv[q].y, o.y);
-                                o.z = fmaf(beta, cv[q].z, o.z);
-                                o.w = fmaf(beta, cv[q].w, o.w);
+                                o.x = fmaf(b_out, cv[q].x, o.x);
+                                o.y = fmaf(b_out, cv[q].y, o.y);
+                                o.z = fmaf(b_out, cv[q].z, o.z);
+                                o.w = fmaf(b_out, cv[q].w, o.w);
                             }
                             PHX_DCHECK(col + 3 < N);
-                            *reinterpret_cast<float4*>(C + static_cast<int64_t>(row) * N + col) = o;
+                            *reinterpret_cast<float4*>(Cout + static_cast<int64_t>(row) * N + col) = o;
                         }
                     }
                 } else {
@@ -378,16 +443,16 @@ gemm_f16cvt_kernel(const float* __restrict__ A, const __grid_constant__ CUtensor
 #pragma unroll
                         for (int rr = 0; rr < 32; ++rr) {
                             const int row = row0 + rr;
-                            cs[rr] = (row < M && col < N) ? C[static_cast<int64_t>(row) * N + col] : 0.f;
+                            cs[rr] = (row < M && col < N) ? Cout[static_cast<int64_t>(row) * N + col] : 0.f;
                         }
                     }
 #pragma unroll
                     for (int rr = 0; rr < 32; ++rr) {
                         const int row = row0 + rr;
                         if (row < M && col < N) {
-                            float o = alpha * epi[rr * L::kEpiStride + lane];
-                            if (read_c) o = fmaf(beta, cs[rr], o);
-                            C[static_cast<int64_t>(row) * N + col] = o;
+                            float o = a_out * epi[rr * L::kEpiStride + lane];
+                            if (read_c) o = fmaf(b_out, cs[rr], o);
+                            Cout[static_cast<int64_t>(row) * N + col] = o;
                         }
                     }
                 }
@@ -410,7 +475,7 @@ gemm_f16cvt_kernel(const float* __restrict__ A, const __grid_constant__ CUtensor
 }
 
 using CvtKernelFn = void (*)(const float*, CUtensorMap, CUtensorMap, float*, int, int, int, int, float, float,
-                             int, int, unsigned int*, int);
+                             int, int, unsigned int*, int, int, int, float*);
 
 struct CvtEntry {
     F16Config cfg;
@@ -418,20 +483,40 @@ struct CvtEntry {
     uint32_t smem;
 };
 
-template <int BN, int STAGES, int STG>
+template <int BN, int STAGES, int STG, bool CB>
 CvtEntry make_cvt_entry() {
-    return CvtEntry{F16Config{kBM, BN, kBK, STAGES, 1, 1}, &gemm_f16cvt_kernel<BN, STAGES, STG>,
-                    CvtLayout<BN, STAGES, STG>::kDynSmem};
+    return CvtEntry{F16Config{kBM, BN, kBK, STAGES, 1, CB ? 0 : 1, CB ? 1 : 0}, &gemm_f16cvt_kernel<BN, STAGES, STG, CB>,
+                    CvtLayout<BN, STAGES, STG, CB>::kDynSmem};
 }
 
-// At each width 96 KB of MMA ring (4 slots of 24 KB, 3 of 32 KB, 2 of 48 KB) and 96 KB of
-// f32 staging (3 k blocks of A in flight per SM).
+// CONVERT_A: at each width 96 KB of MMA ring (4 slots of 24 KB, 3 of 32 KB, 2 of 48 KB) and
+// 96 KB of f32 staging (3 k blocks of A in flight per SM).  CONVERT_B: the same at TILE_N = 64
+// (3 staged k blocks of B are 48 KB) and 128 (96 KB).
 const CvtEntry kCvtEntries[] = {
-    make_cvt_entry<64, 4, 3>(),
-    make_cvt_entry<128, 3, 3>(),
-    make_cvt_entry<256, 2, 3>(),
+    make_cvt_entry<64, 4, 3, false>(),
+    make_cvt_entry<128, 3, 3, false>(),
+    make_cvt_entry<256, 2, 3, false>(),
+    make_cvt_entry<64, 4, 3, true>(),
+    make_cvt_entry<128, 3, 3, true>(),
 };
 constexpr int kNumCvt = sizeof(kCvtEntries) / sizeof(kCvtEntries[0]);
+
+constexpr int kCvtMaxSplit = 8;
+constexpr int kCvtMinKbPerSlice = 8;
+
+// K blocks per slice for CONVERT_B: enough slices to give every SM an item when the tiles
+// alone do not (at most 8, at least 8 k blocks each); num_kb when not split.
+int cvt_kb_per_slice(const CvtEntry& e, int64_t M, int64_t N, int64_t K, int num_sms) {
+    const int64_t num_kb = (K + kBK - 1) / kBK;
+    if (!e.cfg.convert_b) return static_cast<int>(num_kb);
+    const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + e.cfg.tile_n - 1) / e.cfg.tile_n);
+    if (tiles <= 0 || 2 * tiles > num_sms) return static_cast<int>(num_kb);
+    int64_t split = num_sms / tiles;
+    if (split > kCvtMaxSplit) split = kCvtMaxSplit;
+    if (split > num_kb / kCvtMinKbPerSlice) split = num_kb / kCvtMinKbPerSlice;
+    if (split < 2) return static_cast<int>(num_kb);
+    return static_cast<int>((num_kb + split - 1) / split);
+}
 
 }  // namespace
 
@@ -441,32 +526,50 @@ const F16Config& f16cvt_config(int index) { return kCvtEntries[index].cfg; }
 
 int64_t debug_take_f16cvt() { return debug_take_local(); }
 
+size_t f16cvt_split_bytes(int index, int64_t M, int64_t N, int64_t K, int num_sms) {
+    if (index < 0 || index >= kNumCvt) return 0;
+    const int64_t num_kb = (K + kBK - 1) / kBK;
+    const int kb = cvt_kb_per_slice(kCvtEntries[index], M, N, K, num_sms);
+    if (kb >= num_kb) return 0;
+    return static_cast<size_t>((num_kb + kb - 1) / kb) * static_cast<size_t>(M * N) * 4;
+}
+
 cudaError_t f16cvt_gemm_launch(int index, int64_t M, int64_t N, int64_t K, float alpha, float beta, float* C,
-                               const float* A, const __half* Bt, int64_t ldb, unsigned int* status, int num_sms,
-                               cudaStream_t stream) {
+                               const float* A, const float* B, const __half* other, int64_t ld_other,
+                               void* split_ws, unsigned int* status, int num_sms, cudaStream_t stream) {
     if (index < 0 || index >= kNumCvt || M <= 0 || N <= 0 || K <= 0 || num_sms <= 0) return cudaErrorInvalidValue;
     const CvtEntry& e = kCvtEntries[index];
+    const bool cb = e.cfg.convert_b != 0;
     const int bn = e.cfg.tile_n;
     const int64_t Kp = (K + 7) / 8 * 8;
-    CUtensorMap mapB;
-    if (!f16_operand_map(&mapB, Bt, N, Kp, bn, ldb)) return cudaErrorInvalidValue;
+    if (M > 0x7FFFFFFF || N > 0x7FFFFFFF || K > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    // the f16 operand from the rounding pass: B (N x Kp) for CONVERT_A, A (M x Kp) for CONVERT_B
+    CUtensorMap map_f16;
+    if (!f16_operand_map(&map_f16, other, cb ? M : N, Kp, cb ? kBM : bn, ld_other)) return cudaErrorInvalidValue;
     const int64_t tiles_m = (M + kBM - 1) / kBM;
     const int64_t tiles_n = (N + bn - 1) / bn;
-    const int64_t items = tiles_m * tiles_n;
-    if (items > 0x7FFFFFFF || M > 0x7FFFFFFF || N > 0x7FFFFFFF || K > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    const int64_t num_kb64 = (K + kBK - 1) / kBK;
+    int kb_per = cvt_kb_per_slice(e, M, N, K, num_sms);
+    if (split_ws == nullptr) kb_per = static_cast<int>(num_kb64);
+    const int64_t ksplit = (num_kb64 + kb_per - 1) / kb_per;
+    const int64_t items = tiles_m * tiles_n * ksplit;
+    if (items > 0x7FFFFFFF) return cudaErrorInvalidValue;
     const int grid = static_cast<int>(items < num_sms ? items : num_sms);
-    const int num_kb = static_cast<int>((K + kBK - 1) / kBK);
-    // A through the TMA staging ring when its rows can be a tensor map (K % 4 == 0, 16-byte
-    // aligned); else the converters load it themselves
-    const bool a_al = (K % 4 == 0) && ((reinterpret_cast<uintptr_t>(A) & 15u) == 0);
-    CUtensorMap mapA;
-    std::memset(&mapA, 0, sizeof mapA);
-    int a_mode = a_al ? kAVector : kAScalar;
-    if (a_al && f32_rows_map(&mapA, A, M, K, kBK, kBM)) a_mode = kATma;
+    // the converted operand through the TMA staging ring when its rows can be a tensor map
+    // (16-byte aligned rows and base); else the converters load it themselves
+    const float* src = cb ? B : A;
+    const int64_t src_cols = cb ? N : K;
+    const bool al = (src_cols % 4 == 0) && ((reinterpret_cast<uintptr_t>(src) & 15u) == 0);
+    CUtensorMap map_stg;
+    std::memset(&map_stg, 0, sizeof map_stg);
+    int src_mode = (al && !cb) ? kSrcVector : kSrcScalar;
+    if (al && (cb ? f32_rows_map(&map_stg, B, K, N, bn, kBK) : f32_rows_map(&map_stg, A, M, K, kBK, kBM)))
+        src_mode = kSrcTma;
+    float* partial = ksplit > 1 ? static_cast<float*>(split_ws) : nullptr;
     cudaError_t err = set_func_attr_once(reinterpret_cast<const void*>(e.fn),
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(e.smem));
     if (err != cudaSuccess) return err;
-    // a programmatic dependent of the pass that rounds B (see the top of this file)
+    // a programmatic dependent of the rounding pass (see the top of this file)
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(static_cast<unsigned>(grid));
     lc.blockDim = dim3(kThreads);
@@ -478,17 +581,20 @@ cudaError_t f16cvt_gemm_launch(int index, int64_t M, int64_t N, int64_t K, float
     lc.attrs = attr;
     lc.numAttrs = 1;
     const int m32 = static_cast<int>(M), n32 = static_cast<int>(N), k32 = static_cast<int>(K);
-    const int tm32 = static_cast<int>(tiles_m), tn32 = static_cast<int>(tiles_n);
-    err = cudaLaunchKernelEx(&lc, e.fn, A, mapA, mapB, C, m32, n32, k32, num_kb, alpha, beta, tm32, tn32, status,
-                             a_mode);
+    const int tm32 = static_cast<int>(tiles_m), tn32 = static_cast<int>(tiles_n), nkb = static_cast<int>(num_kb64);
+    const int ks32 = static_cast<int>(ksplit);
+    err = cudaLaunchKernelEx(&lc, e.fn, src, map_stg, map_f16, C, m32, n32, k32, nkb, alpha, beta, tm32, tn32, status,
+                             src_mode, ks32, kb_per, partial);
     if (err != cudaSuccess) {
         // a stream that does not take programmatic launches: launch normally
         cudaGetLastError();
         lc.numAttrs = 0;
-        err = cudaLaunchKernelEx(&lc, e.fn, A, mapA, mapB, C, m32, n32, k32, num_kb, alpha, beta, tm32, tn32,
-                                 status, a_mode);
+        err = cudaLaunchKernelEx(&lc, e.fn, src, map_stg, map_f16, C, m32, n32, k32, nkb, alpha, beta, tm32, tn32,
+                                 status, src_mode, ks32, kb_per, partial);
     }
-    return launched(err);
+    err = launched(err);
+    if (err != cudaSuccess || ksplit == 1) return err;
+    return splitk_reduce_launch(partial, ks32, M, N, alpha, beta, C, num_sms, stream);
 }
 
 }  // namespace phx

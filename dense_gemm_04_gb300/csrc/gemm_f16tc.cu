@@ -863,7 +863,13 @@ const F16Config& f16tc_config(int index) {
     return index < kNumTc ? kTcEntries[index].cfg : f16cvt_config(index - kNumTc);
 }
 
-bool f16tc_is_convert_a(int index) { return index >= kNumTc && index < kNumTc + f16cvt_num_configs(); }
+bool f16tc_is_convert_a(int index) {
+    return index >= kNumTc && index < kNumTc + f16cvt_num_configs() && f16cvt_config(index - kNumTc).convert_a;
+}
+
+bool f16tc_is_convert_b(int index) {
+    return index >= kNumTc && index < kNumTc + f16cvt_num_configs() && f16cvt_config(index - kNumTc).convert_b;
+}
 
 bool f16_operand_map(CUtensorMap* map, const __half* ptr, int64_t rows, int64_t Kp, int box_rows, int64_t ld) {
     return make_map(map, ptr, rows, Kp, box_rows, ld);
@@ -960,7 +966,8 @@ int tc_kb_per_slice(const TcEntry& e, int64_t M, int64_t N, int64_t K, int num_s
 }  // namespace
 
 size_t f16tc_split_bytes(int index, int64_t M, int64_t N, int64_t K, int num_sms) {
-    if (index < 0 || index >= kNumTc) return 0;  // the kernel that rounds A does not split K
+    if (index >= kNumTc) return f16cvt_split_bytes(index - kNumTc, M, N, K, num_sms);
+    if (index < 0) return 0;
     const int64_t num_kb = (K + kBK - 1) / kBK;
     const int kb = tc_kb_per_slice(kTcEntries[index], M, N, K, num_sms);
     if (kb >= num_kb) return 0;

@@ -142,13 +142,16 @@ struct F16Config {
     int tile_m, tile_n, tile_k, stages;
     int cluster;        // 1: one CTA per 128-row tile; 2: CTA pairs running the 2-SM MMA (TILE_M = 256)
     int convert_a = 0;  // 1: A rounded to f16 inside the GEMM kernel (gemm_f16cvt.cu)
+    int convert_b = 0;  // 1: B rounded to f16 inside the GEMM kernel (gemm_f16cvt.cu)
 };
 
 // The f16 configurations: the kernel of gemm_f16tc.cu (indices 0 .. n-1), then the kernel
-// that rounds A itself (gemm_f16cvt.cu; f16tc_is_convert_a).
+// that rounds A or B itself (gemm_f16cvt.cu; f16tc_is_convert_a / _b).
 int f16tc_num_configs();
 const F16Config& f16tc_config(int index);
 bool f16tc_is_convert_a(int index);
+bool f16tc_is_convert_b(int index);
+inline bool f16tc_is_convert(int index) { return f16tc_is_convert_a(index) || f16tc_is_convert_b(index); }
 
 // Tensor map of a K-major f16 operand: `rows` rows of `Kp` halves (a multiple of 8), `ld`
 // halves apart, read in 128-byte-swizzled boxes of 64 halves x box_rows (gemm_f16tc.cu).
@@ -158,15 +161,19 @@ bool f16_operand_map(CUtensorMap* map, const __half* ptr, int64_t rows, int64_t 
 // read unswizzled in boxes of box_cols x box_rows; zeros past the edges (gemm_f16tc.cu).
 bool f32_rows_map(CUtensorMap* map, const float* ptr, int64_t rows, int64_t cols, int box_cols, int box_rows);
 
-// The kernel that rounds A itself (gemm_f16cvt.cu): its configurations, and one GEMM of
-// configuration `index` (0 .. f16cvt_num_configs() - 1) on A (M x K f32, row-major) and Bt
-// (N x Kp f16, K-major, ldb halves apart, from the rounding pass), launched as a
-// programmatic dependent of that pass.  Requires M, N, K > 0 and alpha != 0.
+// The kernel that rounds A or B itself (gemm_f16cvt.cu): its configurations, the scratch
+// bytes of a CONVERT_B grid split along K (0 if not split), and one GEMM of configuration
+// `index` (0 .. f16cvt_num_configs() - 1) on A (M x K f32) and B (K x N f32), row-major, with
+// `other` the operand the kernel does not round, K-major f16 from the rounding pass (Bt,
+// N x Kp, for CONVERT_A; Ah, M x Kp, for CONVERT_B), ld_other halves apart; split_ws holds
+// the split's partial planes (nullptr: no split).  Launched as a programmatic dependent of
+// the rounding pass.  Requires M, N, K > 0 and alpha != 0.
 int f16cvt_num_configs();
 const F16Config& f16cvt_config(int index);
+size_t f16cvt_split_bytes(int index, int64_t M, int64_t N, int64_t K, int num_sms);
 cudaError_t f16cvt_gemm_launch(int index, int64_t M, int64_t N, int64_t K, float alpha, float beta, float* C,
-                               const float* A, const __half* Bt, int64_t ldb, unsigned int* status, int num_sms,
-                               cudaStream_t stream);
+                               const float* A, const float* B, const __half* other, int64_t ld_other,
+                               void* split_ws, unsigned int* status, int num_sms, cudaStream_t stream);
 
 // Bytes of workspace for the rounded operands: A as M x Kp f16 and B transposed as
 // N x Kp f16, Kp = K rounded up to a multiple of 8, each part 256-byte aligned.

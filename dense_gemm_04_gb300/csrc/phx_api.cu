@@ -242,17 +242,17 @@ std::string config_name(int variant, int i) {
                       c.tile_n, c.tile_k, c.stages, c.fma2);
     } else {
         const F16Config& c = phx::f16tc_config(i);
-        // a 256-row tile is a 2-SM pair; a 128-row tile one CTA; CONVERT_A=1 the kernel that
-        // rounds A itself
+        // a 256-row tile is a 2-SM pair; a 128-row tile one CTA; CONVERT_A=1 / CONVERT_B=1 the
+        // kernel that rounds A / B itself
         std::snprintf(buf, sizeof buf, "TILE_M=%d TILE_N=%d TILE_K=%d STAGES=%d%s", c.tile_m, c.tile_n,
-                      c.tile_k, c.stages, c.convert_a ? " CONVERT_A=1" : "");
+                      c.tile_k, c.stages, c.convert_a ? " CONVERT_A=1" : c.convert_b ? " CONVERT_B=1" : "");
     }
     return buf;
 }
 
 // Parse "KEY=value KEY=value ..." and return the first compiled config that matches every
 // given key (TILE_M, TILE_N, TILE_K required; STAGES optional; FMA2 for the f32 variant and
-// CONVERT_A for the f16 one optional, default 0), or -1.
+// CONVERT_A, CONVERT_B for the f16 one optional, default 0), or -1.
 int parse_config(int variant, const char* spec) {
     if (spec == nullptr || num_configs(variant) < 0) return -1;
     std::map<std::string, int> kv;
@@ -272,28 +272,29 @@ int parse_config(int variant, const char* spec) {
         const long v = std::strtol(val.c_str(), &end, 10);
         if (end == nullptr || *end != '\0') return -1;
         if (key != "TILE_M" && key != "TILE_N" && key != "TILE_K" && key != "STAGES" && key != "FMA2" &&
-            key != "CONVERT_A")
+            key != "CONVERT_A" && key != "CONVERT_B")
             return -1;
         if (variant == PHX_VARIANT_F16TC && key == "FMA2") return -1;
-        if (variant == PHX_VARIANT_SGEMM && key == "CONVERT_A") return -1;
+        if (variant == PHX_VARIANT_SGEMM && (key == "CONVERT_A" || key == "CONVERT_B")) return -1;
         kv[key] = static_cast<int>(v);
     }
     if (!kv.count("TILE_M") || !kv.count("TILE_N") || !kv.count("TILE_K")) return -1;
     const int n = tile_configs(variant);
     for (int i = 0; i < n; ++i) {
-        int tm, tn, tk, st, f2 = 0, cv = 0;
+        int tm, tn, tk, st, f2 = 0, cv = 0, cvb = 0;
         if (variant == PHX_VARIANT_SGEMM) {
             const SgemmConfig& c = phx::sgemm_config(i);
             tm = c.tile_m; tn = c.tile_n; tk = c.tile_k; st = c.stages; f2 = c.fma2;
         } else {
             const F16Config& c = phx::f16tc_config(i);
-            tm = c.tile_m; tn = c.tile_n; tk = c.tile_k; st = c.stages; cv = c.convert_a;
+            tm = c.tile_m; tn = c.tile_n; tk = c.tile_k; st = c.stages; cv = c.convert_a; cvb = c.convert_b;
         }
         if (kv["TILE_M"] != tm || kv["TILE_N"] != tn || kv["TILE_K"] != tk) continue;
         if (kv.count("STAGES") && kv["STAGES"] != st) continue;
         if (kv.count("FMA2") && kv["FMA2"] != f2) continue;
         if (!kv.count("FMA2") && variant == PHX_VARIANT_SGEMM && f2 != 0) continue;
         if ((kv.count("CONVERT_A") ? kv["CONVERT_A"] : 0) != cv) continue;
+        if ((kv.count("CONVERT_B") ? kv["CONVERT_B"] : 0) != cvb) continue;
         return i;
     }
     return -1;
@@ -343,11 +344,20 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // Defaults when nothing is pinned or tuned: the largest tile that still gives every SM
 // work (the trade-off "gemm, f32" section "Tuning" describes: larger tiles reuse more,
 // but leave fewer CTAs to spread over the card).
-int default_tile_config(int variant, int64_t M, int64_t N, int64_t K, int sms, bool convert_a = true);
+int default_tile_config(int variant, int64_t M, int64_t N, int64_t K, int sms, bool convert = true);
+int default_config(int variant, int64_t M, int64_t N, int64_t K, int sms, bool convert = true);
 
-int default_config(int variant, int64_t M, int64_t N, int64_t K, int sms) {
-    if (M <= skinny_default_max_m(variant)) return skinny_index(variant);
-    return default_tile_config(variant, M, N, K, sms);
+// The kernel that rounds B itself is the f16 default for few rows and a large B (see
+// default_tile_config); it beats the skinny kernel from about 12 rows (measured on GB300,
+// queued calls, K = N = 4096: 20.9 us against 27.0 at M = 12, 16.7 against 20.9 at M = 8).
+bool f16_convert_b_fits(int64_t M, int64_t N, int64_t K) {
+    return M <= 256 && N >= 1024 && static_cast<double>(K) * static_cast<double>(N) >= 8388608.0;
+}
+
+int default_config(int variant, int64_t M, int64_t N, int64_t K, int sms, bool convert) {
+    const bool skip_skinny = variant == PHX_VARIANT_F16TC && convert && M > 8 && f16_convert_b_fits(M, N, K);
+    if (M <= skinny_default_max_m(variant) && !skip_skinny) return skinny_index(variant);
+    return default_tile_config(variant, M, N, K, sms, convert);
 }
 
 // The compiled configurations the defaults name, resolved once (parsing a name per call
@@ -356,6 +366,7 @@ struct DefaultConfigs {
     int s128x128 = -1, s128x64 = -1, s64x64 = -1;                // f32
     int t256x256 = -1, t128x256 = -1, t128x128 = -1, t128x64 = -1;  // f16 tensor cores
     int c64 = -1, c128 = -1, c256 = -1;  // f16, A rounded in the kernel, TILE_N = 64, 128, 256
+    int cb64 = -1, cb128 = -1;           // f16, B rounded in the kernel, TILE_N = 64, 128
 };
 
 const DefaultConfigs& default_configs() {
@@ -371,6 +382,8 @@ const DefaultConfigs& default_configs() {
         c.c64 = parse_config(PHX_VARIANT_F16TC, "TILE_M=128 TILE_N=64 TILE_K=64 STAGES=4 CONVERT_A=1");
         c.c128 = parse_config(PHX_VARIANT_F16TC, "TILE_M=128 TILE_N=128 TILE_K=64 STAGES=3 CONVERT_A=1");
         c.c256 = parse_config(PHX_VARIANT_F16TC, "TILE_M=128 TILE_N=256 TILE_K=64 STAGES=2 CONVERT_A=1");
+        c.cb64 = parse_config(PHX_VARIANT_F16TC, "TILE_M=128 TILE_N=64 TILE_K=64 STAGES=4 CONVERT_B=1");
+        c.cb128 = parse_config(PHX_VARIANT_F16TC, "TILE_M=128 TILE_N=128 TILE_K=64 STAGES=3 CONVERT_B=1");
         return c;
     }();
     return d;
@@ -382,9 +395,9 @@ const DefaultConfigs& default_configs() {
 // with 128 x 128; 256^3 14.4 us with 64 x 64 against 22.7).
 constexpr int64_t kSmallSgemmWork = int64_t(1) << 28;
 
-// With convert_a, the f16 default may be the kernel that rounds A itself; callers whose A is
-// not a row-major f32 matrix pass false.
-int default_tile_config(int variant, int64_t M, int64_t N, int64_t K, int sms, bool convert_a) {
+// With `convert`, the f16 default may be the kernel that rounds A or B itself; callers whose
+// operands are not row-major f32 matrices pass false.
+int default_tile_config(int variant, int64_t M, int64_t N, int64_t K, int sms, bool convert) {
     const DefaultConfigs& dc = default_configs();
     if (variant == PHX_VARIANT_SGEMM) {
         const int64_t slots = 2 * static_cast<int64_t>(sms);  // two CTAs per SM
@@ -401,8 +414,14 @@ int default_tile_config(int variant, int64_t M, int64_t N, int64_t K, int sms, b
     // Few columns, many rows: A is most of the bytes, and rounding it inside the GEMM saves
     // writing and reading back its f16 copy.  One tile of N, and 128-row tiles for at least
     // half the SMs (fewer rows leave SMs idle; the other kernel splits such grids along K).
-    if (convert_a && N <= 256 && ceil_div(M, 128) >= sms / 2)
+    if (convert && N <= 256 && ceil_div(M, 128) >= sms / 2)
         return N <= 64 ? dc.c64 : N <= 128 ? dc.c128 : dc.c256;
+    // Few rows, a large B (2^23 elements or more): B is most of the bytes; the kernel rounds
+    // B itself, and splits K to give every SM work.  (Few enough rows take the skinny kernel
+    // before this.)  Measured on GB300, queued calls: (64, 4096, 4096) 21.1 us against 32.9
+    // for the best tile of the other kernel, (64, 8192, 8192) 55 against 105; with a small B,
+    // (64, 1024, 1024), 16.6 against 12.7.
+    if (convert && f16_convert_b_fits(M, N, K)) return dc.cb128;
     if (M >= 256 && N >= 256) {
         // the 2-SM 256 x 256 tile when it fills the CTA pairs, or when a grid too small for
         // the GPU is split along K (32 or more k blocks of 64); else the one-CTA tile that gives more
@@ -695,6 +714,13 @@ phx_status launch_sgemm_padded(int cfg, int64_t M, int64_t N, int64_t K, float a
 phx_status launch_variant(int variant, int cfg, int64_t M, int64_t N, int64_t K, float alpha,
                           const float* A, const float* B, float beta, float* C, DevState* d,
                           cudaStream_t stream, int trans_a = 0, int trans_b = 0) {
+    // the kernel that rounds A (B) reads A stored M x K (B stored K x N) only: an operand
+    // given transposed takes the default without that kernel (the skinny kernel included)
+    if (variant == PHX_VARIANT_F16TC &&
+        ((trans_a && phx::f16tc_is_convert_a(cfg)) || (trans_b && phx::f16tc_is_convert_b(cfg)))) {
+        cfg = default_config(PHX_VARIANT_F16TC, M, N, K, d->sm_count, false);
+        g_last_cfg[PHX_VARIANT_F16TC].store(cfg);
+    }
     if (cfg == skinny_index(variant))
         return launch_skinny(variant, trans_a, trans_b, M, N, K, alpha, A, B, beta, C, d, stream);
     if (variant == PHX_VARIANT_SGEMM && (trans_a || trans_b))
@@ -715,12 +741,6 @@ phx_status launch_variant(int variant, int cfg, int64_t M, int64_t N, int64_t K,
         });
         if (ws != nullptr) cudaFreeAsync(ws, stream);
         return err == cudaSuccess ? PHX_OK : PHX_ERR_LAUNCH;
-    }
-    // the kernel that rounds A reads A stored M x K only: a transposed A takes the default
-    // of the other kernel
-    if (trans_a && phx::f16tc_is_convert_a(cfg)) {
-        cfg = default_tile_config(PHX_VARIANT_F16TC, M, N, K, d->sm_count, false);
-        g_last_cfg[PHX_VARIANT_F16TC].store(cfg);
     }
     // one pooled block holds the call's scratch (phx::f16tc_run_bytes)
     void* ws = nullptr;
@@ -807,7 +827,7 @@ phx_status f16in_entry(int trans_a, int trans_b, int64_t M, int64_t N, int64_t K
     }
     int cfg = choose_config(PHX_VARIANT_F16TC, M, N, K, d->sm_count);
     // the skinny kernel and the kernel that rounds A read f32 operands: the default tile then
-    if (cfg == skinny_index(PHX_VARIANT_F16TC) || (cfg >= 0 && phx::f16tc_is_convert_a(cfg)))
+    if (cfg == skinny_index(PHX_VARIANT_F16TC) || (cfg >= 0 && phx::f16tc_is_convert(cfg)))
         cfg = default_tile_config(PHX_VARIANT_F16TC, M, N, K, d->sm_count, false);
     if (cfg < 0) return config_error(cfg);
     g_last_cfg[PHX_VARIANT_F16TC].store(cfg);
@@ -855,8 +875,12 @@ phx_status copy_name(const std::string& s, char* buf, size_t buflen) {
 
 namespace phx {
 size_t f16tc_run_bytes(int cfg, int64_t M, int64_t N, int64_t K, int num_sms) {
-    // the kernel that rounds A itself: only B's f16 copy
-    if (f16tc_is_convert_a(cfg)) return static_cast<size_t>(((N * ((K + 7) / 8 * 8) * 2) + 255) / 256 * 256);
+    const int64_t Kp = (K + 7) / 8 * 8;
+    // the kernel that rounds A itself: only B's f16 copy; B itself: A's copy, then the
+    // partial planes of a split along K
+    if (f16tc_is_convert_a(cfg)) return static_cast<size_t>((N * Kp * 2 + 255) / 256 * 256);
+    if (f16tc_is_convert_b(cfg))
+        return static_cast<size_t>((M * Kp * 2 + 255) / 256 * 256) + f16tc_split_bytes(cfg, M, N, K, num_sms);
     // the f16 operand copies, then (for a grid split along K) the partial products of the
     // slices
     return f16tc_workspace_bytes(M, N, K) + f16tc_split_bytes(cfg, M, N, K, num_sms);
@@ -865,17 +889,25 @@ size_t f16tc_run_bytes(int cfg, int64_t M, int64_t N, int64_t K, int num_sms) {
 cudaError_t f16tc_run(int cfg, int trans_a, int trans_b, int64_t M, int64_t N, int64_t K, float alpha,
                       const float* A, const float* B, float beta, float* C, void* ws, unsigned int* status,
                       int num_sms, cudaStream_t stream) {
-    if (f16tc_is_convert_a(cfg)) {
-        // B's f16 copy (N x Kp) at the start of ws, then the GEMM that rounds A as it reads it
-        if (trans_a) return cudaErrorInvalidValue;  // it reads A stored M x K only
-        __half* Bt = static_cast<__half*>(ws);
+    if (f16tc_is_convert(cfg)) {
+        // The other operand's f16 copy at the start of ws (B as N x Kp, or A as M x Kp), the
+        // partial planes of a split after it, then the GEMM that rounds its operand as it
+        // reads it (stored M x K for A, K x N for B: not transposed)
+        const bool cb = f16tc_is_convert_b(cfg);
+        if (cb ? trans_b : trans_a) return cudaErrorInvalidValue;
+        const int64_t Kp = (K + 7) / 8 * 8;
+        __half* other = static_cast<__half*>(ws);
+        void* split = cb && f16tc_split_bytes(cfg, M, N, K, num_sms) > 0
+                          ? static_cast<char*>(ws) + (M * Kp * 2 + 255) / 256 * 256
+                          : nullptr;
         cudaError_t err = timed(kKindCast, stream, [&] {
-            return f16tc_prepare_launch(0, 0, trans_b, M, N, K, A, B, nullptr, Bt, num_sms, stream);
+            return cb ? f16tc_prepare_launch(0, trans_a, 0, M, N, K, A, B, other, nullptr, num_sms, stream)
+                      : f16tc_prepare_launch(0, 0, trans_b, M, N, K, A, B, nullptr, other, num_sms, stream);
         });
         if (err == cudaSuccess)
             err = timed(kKindTcGemm, stream, [&] {
                 return f16cvt_gemm_launch(cfg - (f16tc_num_configs() - f16cvt_num_configs()), M, N, K, alpha, beta,
-                                          C, A, Bt, (K + 7) / 8 * 8, status, num_sms, stream);
+                                          C, A, B, other, Kp, split, status, num_sms, stream);
             });
         return err;
     }

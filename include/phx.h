@@ -246,15 +246,18 @@ phx_status phx_profile_stop(int64_t* launches, double* ms);
  * STAGES=4" (f16 variant).  The order of keys does not matter.  An f16 configuration
  * ending in "CONVERT_A=1" (TILE_M=128, TILE_N 64, 128 or 256) is the kernel that rounds A to
  * f16 itself as it stages A's f32 tiles, so that only B goes through the separate rounding
- * pass; it is the default where N <= 256 and A has 128-row tiles for at least half the SMs,
- * and it computes the same rounded products, summed in f32 in the same order per tile.  A
- * stored K x M (op_a = PHX_OP_T) and the half-precision entry points take the default of the
- * other kernel instead.  The last configuration of
+ * pass; it is the default where N <= 256 and A has 128-row tiles for at least half the SMs.
+ * One ending in "CONVERT_B=1" (TILE_M=128, TILE_N 64 or 128) rounds B itself the same way
+ * (and splits K when its tiles cannot fill the SMs); it is the default for M <= 256, N >= 1024
+ * and K * N >= 2^23.  Both compute the same rounded products, summed in f32 in the same order
+ * per tile.  An operand they round given transposed (op_a or op_b = PHX_OP_T), and the
+ * half-precision entry points, take the default without them instead.  The last configuration of
  * each variant, "SKINNY", is the kernel for few rows of A (the lab's skinny-matrix sweep,
  * Part 5): B is streamed once from HBM with 16-byte loads and the products are summed with
  * f32 multiply-adds on the CUDA cores (for the f16 variant, of operands rounded to f16 as
  * they are loaded: the same rounded products, summed in f32).  It takes any M, in blocks
- * of 16 rows, and is the default for M <= 48 (f32) and M <= 16 (f16).
+ * of 16 rows, and is the default for M <= 48 (f32) and M <= 16 (f16; M <= 8 where B has
+ * 2^23 elements or more, N >= 1024, and the kernel that rounds B itself takes over).
  * ------------------------------------------------------------------------------------- */
 
 /* Number of compiled configurations of a variant (or -1 for a bad variant). */

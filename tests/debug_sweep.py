@@ -40,7 +40,7 @@ def main():
     # tail items, the skinny kernels (few rows), ragged and padded edges
     shapes |= {(256, 256, 256), (1024, 1024, 4096), (300, 500, 3000), (2048, 2048, 256), (3000, 2000, 700),
                (8, 4096, 4096), (2, 128, 65536), (40, 1000, 3000), (1031, 1029, 4100), (1030, 1024, 4099),
-               (10000, 100, 300)}  # the last: few columns, many rows (the kernel that rounds A)
+               (10000, 100, 300), (64, 3000, 2000)}  # few columns / few rows (the kernel that rounds A / B)
     failures = []
     runs = 0
     for variant, f16 in ((phx.VARIANT_SGEMM, False), (phx.VARIANT_F16TC, True)):
@@ -48,8 +48,8 @@ def main():
             runs += 1
             if not run(variant, f16, M, N, K, 1.5, 0.5, i):
                 failures.append((variant, M, N, K))
-    # the kernel that rounds A, pinned, on the edge shapes
-    for cfg in [n for n in phx.config_names(phx.VARIANT_F16TC) if "CONVERT_A=1" in n]:
+    # the kernel that rounds A or B, pinned, on the edge shapes
+    for cfg in [n for n in phx.config_names(phx.VARIANT_F16TC) if "CONVERT" in n]:
         phx.set_config(phx.VARIANT_F16TC, cfg)
         for i, (M, N, K) in enumerate(sorted(shapes)):
             if M * N * K > 2 ** 31:

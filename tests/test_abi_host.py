@@ -123,15 +123,27 @@ def test_default_config_follows_grid_size():
         assert cfg.startswith(f"TILE_M=128 TILE_N={tile_n} ") and cfg.endswith(" CONVERT_A=1"), (n, cfg)
     assert "CONVERT_A" not in phx.get_config(phx.VARIANT_F16TC, 16384, 257, 4096)
     assert "CONVERT_A" not in phx.get_config(phx.VARIANT_F16TC, 4096, 128, 4096)   # rows for 32 SMs only
+    # few rows, many columns: the kernel that rounds B itself (up to 16 rows: the skinny kernel)
+    for m in (9, 16, 17, 64, 256):
+        assert phx.get_config(phx.VARIANT_F16TC, m, 4096, 4096).endswith(" CONVERT_B=1")
+    assert phx.get_config(phx.VARIANT_F16TC, 8, 4096, 4096) == "SKINNY"
+    assert phx.get_config(phx.VARIANT_F16TC, 16, 1024, 1024) == "SKINNY"       # a small B
+    assert "CONVERT" not in phx.get_config(phx.VARIANT_F16TC, 64, 1024, 1024)
+    assert "CONVERT" not in phx.get_config(phx.VARIANT_F16TC, 257, 4096, 4096)
+    with pytest.raises(phx.PhxError):
+        phx.set_config(phx.VARIANT_SGEMM, "TILE_M=128 TILE_N=128 TILE_K=16 CONVERT_B=1")
     # the f32 variant has no such key
     with pytest.raises(phx.PhxError):
         phx.set_config(phx.VARIANT_SGEMM, "TILE_M=128 TILE_N=128 TILE_K=16 CONVERT_A=1")
-    # few rows of A: the skinny kernel (B streamed once) up to 48 rows (f32) and 16 (f16)
+    # few rows of A: the skinny kernel (B streamed once) up to 48 rows (f32) and 16 (f16), or 8
+    # (f16) where B is large enough for the kernel that rounds B itself
     assert phx.get_config(phx.VARIANT_SGEMM, 1, 4096, 4096) == "SKINNY"
     assert phx.get_config(phx.VARIANT_SGEMM, 48, 4096, 4096) == "SKINNY"
     assert phx.get_config(phx.VARIANT_SGEMM, 49, 4096, 4096) != "SKINNY"
-    assert phx.get_config(phx.VARIANT_F16TC, 16, 4096, 4096) == "SKINNY"
-    assert phx.get_config(phx.VARIANT_F16TC, 17, 4096, 4096) != "SKINNY"
+    assert phx.get_config(phx.VARIANT_F16TC, 8, 4096, 4096) == "SKINNY"
+    assert phx.get_config(phx.VARIANT_F16TC, 9, 4096, 4096) != "SKINNY"
+    assert phx.get_config(phx.VARIANT_F16TC, 16, 2048, 2048) == "SKINNY"
+    assert phx.get_config(phx.VARIANT_F16TC, 17, 2048, 2048) != "SKINNY"
 
 
 def test_workspace_bytes():

@@ -45,6 +45,7 @@ PROBLEMS = [
     (2, 128, 65536, 1.0, 0.5, 15),       # ... and in planes of partial sums in the scratch
     (8, 8192, 4096, 1.0, 0.5, 17),       # skinny: more than 64 MiB of f16 copies, which it never makes
     (16384, 128, 1024, 1.0, 0.5, 18),    # few columns: A rounded inside the GEMM, only B's copy in the array
+    (64, 4096, 4096, 1.0, 0.5, 19),      # few rows: B rounded inside the GEMM, A's copy and K-split planes
 ]
 
 
