@@ -82,8 +82,10 @@ __device__ __forceinline__ float ld_shared_cluster(uint32_t addr) {
 // Grid: x = (tile, rank) with the cluster's ranks innermost (tile = column strip x row
 // block of A, row blocks innermost so that CTAs sharing B rows run together); y = plane.
 // The CTA's slice of K is slice = y * cs + rank, rows [slice * k_cta, +k_cta) clipped to K.
+// Up to 8 rows a tile: 2 CTAs per SM.  16 rows: 1 CTA per SM, so that the 64 accumulators
+// and the f32x2 operand pairs stay in registers (at 128 registers they spilled).
 template <int MT, bool F16, bool VEC>
-__global__ void __launch_bounds__(kSkThreads, 2) skinny_kernel(
+__global__ void __launch_bounds__(kSkThreads, MT > 8 ? 1 : 2) skinny_kernel(
     const float* __restrict__ A, const float* __restrict__ B, float* __restrict__ C, float* __restrict__ partial,
     int M, int64_t N, int K, int k_cta, int cs, int mchunks, int64_t strips, int a_trans, float alpha,
     float beta) {
@@ -145,9 +147,18 @@ __global__ void __launch_bounds__(kSkThreads, 2) skinny_kernel(
         asm volatile("cp.async.commit_group;\n" ::: "memory");
     };
 
-    float2 acc[MT][2];  // columns (0, 1) and (2, 3) of the lane's four
+    // Accumulators in pairs for packed f32x2 multiply-adds (the same IEEE fma in each half):
+    //   MT <= 8: acc[m][h] = columns (2h, 2h+1) of the lane's four, row m (pairs along N, each
+    //            A value duplicated into a register pair);
+    //   MT > 8:  acc[p][c] = rows (2p, 2p+1), column c (pairs along M: the A pairs come straight
+    //            from the 16-byte loads, and only the four B values are duplicated).
+    constexpr int AR = MT <= 8 ? MT : MT / 2;
+    constexpr int AC = MT <= 8 ? 2 : 4;
+    float2 acc[AR][AC];
 #pragma unroll
-    for (int m = 0; m < MT; ++m) acc[m][0] = acc[m][1] = make_float2(0.f, 0.f);
+    for (int i = 0; i < AR; ++i)
+#pragma unroll
+        for (int j = 0; j < AC; ++j) acc[i][j] = make_float2(0.f, 0.f);
 
 #pragma unroll
     for (int g = 0; g < S - 1; ++g) issue(g);
@@ -185,9 +196,7 @@ __global__ void __launch_bounds__(kSkThreads, 2) skinny_kernel(
 #pragma unroll
                 for (int m = 0; m < MT; ++m) av[m] = ak[m];
             }
-            if (MT <= 8) {
-                // packed f32x2 multiply-adds: the same IEEE fma in each lane, half the issue
-                // slots (with 16 rows the register pairs they need would spill)
+            if constexpr (MT <= 8) {
                 const float2 bxy = make_float2(bq.x, bq.y), bzw = make_float2(bq.z, bq.w);
 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
@@ -196,12 +205,13 @@ __global__ void __launch_bounds__(kSkThreads, 2) skinny_kernel(
                     acc[m][1] = __ffma2_rn(aa, bzw, acc[m][1]);
                 }
             } else {
+                const float2 bc[4] = {make_float2(bq.x, bq.x), make_float2(bq.y, bq.y), make_float2(bq.z, bq.z),
+                                      make_float2(bq.w, bq.w)};
 #pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    acc[m][0].x = fmaf(av[m], bq.x, acc[m][0].x);
-                    acc[m][0].y = fmaf(av[m], bq.y, acc[m][0].y);
-                    acc[m][1].x = fmaf(av[m], bq.z, acc[m][1].x);
-                    acc[m][1].y = fmaf(av[m], bq.w, acc[m][1].y);
+                for (int p = 0; p < MT / 2; ++p) {
+                    const float2 aa = make_float2(av[2 * p], av[2 * p + 1]);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) acc[p][c] = __ffma2_rn(aa, bc[c], acc[p][c]);
                 }
             }
         }
@@ -213,7 +223,11 @@ __global__ void __launch_bounds__(kSkThreads, 2) skinny_kernel(
 #pragma unroll
     for (int m = 0; m < MT; ++m)
         reinterpret_cast<float4*>(red + (warp * MT + m) * kSkBN)[lane] =
-            make_float4(acc[m][0].x, acc[m][0].y, acc[m][1].x, acc[m][1].y);
+            MT <= 8 ? make_float4(acc[m % AR][0].x, acc[m % AR][0].y, acc[m % AR][1].x, acc[m % AR][1].y)
+                    : (m % 2 == 0 ? make_float4(acc[(m / 2) % AR][0].x, acc[(m / 2) % AR][1].x,
+                                                acc[(m / 2) % AR][2 % AC].x, acc[(m / 2) % AR][3 % AC].x)
+                                  : make_float4(acc[(m / 2) % AR][0].y, acc[(m / 2) % AR][1].y,
+                                                acc[(m / 2) % AR][2 % AC].y, acc[(m / 2) % AR][3 % AC].y));
     __syncthreads();
     constexpr int E = MT * kSkBN;
     for (int e = tid; e < E; e += kSkThreads) {
