@@ -354,9 +354,21 @@ bool f16_convert_b_fits(int64_t M, int64_t N, int64_t K) {
     return M <= 256 && N >= 1024 && static_cast<double>(K) * static_cast<double>(N) >= 8388608.0;
 }
 
+// f32 problems the skinny kernel also takes, beyond few rows: small ones, where its one
+// launch and its K slices beat the tiles' grid, and 64 rows against a B that L2 holds while
+// the four 16-row chunks read it (measured on GB300, queued calls: 256^3 8.3 us against 14.5
+// with 64 x 64 tiles, 384^3 10.4 against 14.5, (128, 1024, 1024) 16.5 against 18.7,
+// (64, 2048, 2048) 24.7 against 39.2; 512^3 16.5 against 16.6; 768^3 37.0 against 31.4).
+bool sgemm_skinny_fits(int64_t M, int64_t N, int64_t K) {
+    const double mnk = static_cast<double>(M) * static_cast<double>(N) * static_cast<double>(K);
+    const double kn = static_cast<double>(K) * static_cast<double>(N);
+    return (M <= 512 && mnk <= 134217728.0) || (M <= 64 && kn <= 4194304.0);
+}
+
 int default_config(int variant, int64_t M, int64_t N, int64_t K, int sms, bool convert) {
     const bool skip_skinny = variant == PHX_VARIANT_F16TC && convert && M > 8 && f16_convert_b_fits(M, N, K);
     if (M <= skinny_default_max_m(variant) && !skip_skinny) return skinny_index(variant);
+    if (variant == PHX_VARIANT_SGEMM && sgemm_skinny_fits(M, N, K)) return skinny_index(variant);
     return default_tile_config(variant, M, N, K, sms, convert);
 }
 

@@ -109,8 +109,14 @@ def test_default_config_follows_grid_size():
     assert skinny.startswith("TILE_M=64 TILE_N=64")
     assert phx.get_config(phx.VARIANT_F16TC, 4096, 4096, 4096).startswith("TILE_M=256 TILE_N=256")
     # small problems: smaller tiles give more SMs work (152 SMs assumed without a GPU)
-    assert phx.get_config(phx.VARIANT_SGEMM, 512, 512, 512).startswith("TILE_M=128 TILE_N=64 TILE_K=8 ")
-    assert phx.get_config(phx.VARIANT_SGEMM, 256, 256, 256).startswith("TILE_M=64 TILE_N=64 TILE_K=8 ")
+    assert phx.get_config(phx.VARIANT_SGEMM, 512, 512, 1024).startswith("TILE_M=128 TILE_N=64 TILE_K=8 ")
+    assert phx.get_config(phx.VARIANT_SGEMM, 1024, 256, 256).startswith("TILE_M=128 TILE_N=64 TILE_K=8 ")
+    # ... and smaller f32 problems, or 64 rows against a B that L2 holds, the skinny kernel
+    assert phx.get_config(phx.VARIANT_SGEMM, 512, 512, 512) == "SKINNY"
+    assert phx.get_config(phx.VARIANT_SGEMM, 256, 256, 256) == "SKINNY"
+    assert phx.get_config(phx.VARIANT_SGEMM, 64, 2048, 2048) == "SKINNY"
+    assert phx.get_config(phx.VARIANT_SGEMM, 64, 4096, 4096) != "SKINNY"
+    assert phx.get_config(phx.VARIANT_SGEMM, 768, 768, 768) != "SKINNY"
     assert phx.get_config(phx.VARIANT_SGEMM, 1024, 1024, 1024).startswith("TILE_M=128 TILE_N=128")
     assert phx.get_config(phx.VARIANT_F16TC, 512, 512, 512).startswith("TILE_M=128 TILE_N=128")
     assert phx.get_config(phx.VARIANT_F16TC, 1024, 1024, 1024).startswith("TILE_M=128 TILE_N=128")
@@ -240,7 +246,7 @@ def test_unparsable_env_pin_is_an_error_not_ignored():
     lines = r.stdout.splitlines()
     assert lines[0] == f"ERR {phx.PHX_ERR_CONFIG}", r.stdout
     assert lines[1].startswith("F16 TILE_M="), r.stdout       # the other variant is unaffected
-    assert lines[2].startswith("AFTER TILE_M="), r.stdout     # phx_set_config replaces the pin
+    assert lines[2] == "AFTER SKINNY", r.stdout               # phx_set_config replaces the pin
     assert "PHX_CONFIG_SGEMM" in r.stderr                     # logged, whatever PHX_LOG says
 
 
