@@ -257,7 +257,9 @@ phx_status phx_profile_stop(int64_t* launches, double* ms);
  * f32 multiply-adds on the CUDA cores (for the f16 variant, of operands rounded to f16 as
  * they are loaded: the same rounded products, summed in f32).  It takes any M, in blocks
  * of 16 rows, and is the default for M <= 48 (f32) and M <= 16 (f16; M <= 8 where B has
- * 2^23 elements or more, N >= 1024, and the kernel that rounds B itself takes over).
+ * 2^23 elements or more, N >= 1024, and the kernel that rounds B itself takes over).  For
+ * f32 it is also the default for small problems (M <= 512 and M * N * K <= 2^27) and for
+ * M <= 64 with K * N <= 2^22.
  * ------------------------------------------------------------------------------------- */
 
 /* Number of compiled configurations of a variant (or -1 for a bad variant). */
