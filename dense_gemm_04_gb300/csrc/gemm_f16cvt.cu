@@ -1,4 +1,4 @@
-// gemm_f16cvt.cu -- the f16 tensor-core GEMM with one operand rounded to f16 inside the kernel.
+// gemm_f16cvt.cu -- the f16 tensor-core GEMM with operands rounded to f16 inside the kernel.
 //
 // The arithmetic is that of gemm_f16tc.cu: every element of A and B rounded to the nearest
 // f16 (ties to even), the f16 x f16 products summed in f32 by tcgen05.mma.kind::f16, then
@@ -12,17 +12,21 @@
 // needs.  Here the kernel reads that operand (f32) once and rounds it on the way into shared
 // memory, in the layout the MMA reads; the other, small operand still goes through the
 // rounding pass (K-major f16) and arrives by TMA.
-//   CONVERT_A (CB = false): many rows, few columns (N within a tile or two).  A is staged as
-//     128 x 64 f32 boxes; B comes from the pass as N x Kp f16.
-//   CONVERT_B (CB = true): few rows (up to a tile or two), many columns.  B is staged as
-//     64 x TILE_N f32 boxes (k rows of n) and transposed while it is rounded; A comes from
-//     the pass as M x Kp f16.  A grid of few tiles is split along K into slices that write
-//     f32 partial planes, added in slice order by a separate reduction.
+//   CONVERT_A: many rows, few columns (N within a tile or two).  A is staged as 128 x 64 f32
+//     boxes; B comes from the pass as N x Kp f16.
+//   CONVERT_B: few rows (up to a tile or two), many columns.  B is staged as 64 x TILE_N f32
+//     boxes (k rows of n) and transposed while it is rounded; A comes from the pass as M x Kp
+//     f16.
+//   CONVERT_A + CONVERT_B: both operands staged and rounded here, no pass at all: one launch,
+//     no scratch (for small problems, where the launches and the pass are most of the time).
+// With B rounded here, a grid of few tiles is split along K into slices that write f32
+// partial planes, added in slice order by a separate reduction.
 //
 // A persistent kernel, one CTA per SM, 320 threads (10 warps):
-//   warp 4      TMA producer: per 64-deep k block, the f32 box of the converted operand into
-//               a staging ring three k blocks deep (unswizzled, zeros past the edges), and
-//               the f16 tile of the other operand into the MMA ring.
+//   warp 4      TMA producer: per 64-deep k block, the f32 box of each converted operand into
+//               a staging ring (unswizzled, zeros past the edges; one slot holds both boxes
+//               when both are converted), and the f16 tile of the other operand, if any, into
+//               the MMA ring.
 //   warps 6-9   converters.  Each lane reads 8 (row, 16-byte chunk) pairs of 8 floats from
 //               the staged box, hands the staging slot back, rounds them with
 //               cvt.rn.f16x2.f32 and stores the 8 halves at chunk c ^ (r % 8) of row r of
@@ -35,13 +39,15 @@
 //   warps 0-3   epilogue: tcgen05.ld of the accumulator (warp w: rows 32w..32w+31), through
 //               a per-warp shared-memory buffer to coalesced rows of C (or of a k slice's
 //               partial plane).
-// An MMA ring slot is full when the TMA bytes have landed and the four converter warps have
-// arrived (after a proxy fence that makes their generic stores visible to the tensor cores).
+// An MMA ring slot is full when the TMA bytes of the other operand (if any) have landed and
+// the four converter warps have arrived (after a proxy fence that makes their generic stores
+// visible to the tensor cores).
 // The accumulator is double-buffered in tensor memory.  Every wait is bounded (sm100_ptx.cuh).
 //
-// The kernel is launched as a programmatic dependent of the rounding pass.  The converted
-// operand does not depend on that pass: the producer issues its first staging load, then
-// waits for the pass (griddepcontrol.wait) before the first load of the other operand.
+// With one operand converted, the kernel is launched as a programmatic dependent of the
+// rounding pass.  The converted operand does not depend on that pass: the producer issues its
+// first staging load, then waits for the pass (griddepcontrol.wait) before the first load of
+// the other operand.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -69,19 +75,26 @@ constexpr int kConvWarps = 4;   // warps 6-9
 constexpr int kConvThreads = 32 * kConvWarps;
 constexpr int kThreads = 32 * (kFirstConvWarp + kConvWarps);
 
-// How the converters get their operand: 0 four bytes at a time from global memory, 1
-// sixteen bytes at a time from global memory (A's rows on 16 bytes), 2 from the TMA
-// staging ring.
-enum SrcMode : int { kSrcScalar = 0, kSrcVector = 1, kSrcTma = 2 };
+// Which operands the kernel rounds itself.
+enum CvtMode : int { kModeA = 0, kModeB = 1, kModeAB = 2 };
 
-template <int BN, int STAGES, int STG, bool CB>
+// How the converters get their operands: 0 from global memory (4 bytes at a time, A 16
+// bytes at a time when its rows start on 16 bytes), 1 from the TMA staging ring.
+enum SrcMode : int { kSrcGlobal = 0, kSrcTma = 1 };
+
+template <int BN, int STAGES, int STG, int MODE>
 struct CvtLayout {
+    static constexpr bool kCvtA = MODE != kModeB;           // A rounded here
+    static constexpr bool kCvtB = MODE != kModeA;           // B rounded here
     static constexpr uint32_t kABytes = kBM * kBK * 2;      // f16 A slot of the MMA ring
     static constexpr uint32_t kBBytes = BN * kBK * 2;       // f16 B slot
-    // f32 slot of the staging ring: 128 rows of A x 64 k, or 64 k x TILE_N columns of B
-    static constexpr uint32_t kStgBytes = (CB ? BN : kBM) * kBK * 4;
-    // 16-byte chunks a converter thread writes per k block (the converted slot / 16 / 128)
-    static constexpr int kChunks = (CB ? kBBytes : kABytes) / 16 / kConvThreads;
+    // f32 part of a staging slot: 128 rows of A x 64 k, then 64 k x TILE_N columns of B
+    static constexpr uint32_t kStgA = kCvtA ? kBM * kBK * 4 : 0;
+    static constexpr uint32_t kStgB = kCvtB ? BN * kBK * 4 : 0;
+    static constexpr uint32_t kStgBytes = kStgA + kStgB;
+    // 16-byte chunks a converter thread writes per k block into each converted slot
+    static constexpr int kChunksA = kABytes / 16 / kConvThreads;
+    static constexpr int kChunksB = kBBytes / 16 / kConvThreads;
     // offsets from the 1024-byte aligned base
     static constexpr uint32_t kA = 0;
     static constexpr uint32_t kB = STAGES * kABytes;
@@ -99,7 +112,8 @@ struct CvtLayout {
     static constexpr uint32_t kTmemCols = 2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512);
     static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "tcgen05 N, and whole 32-column chunks");
     static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "swizzle atoms stay 1024-aligned");
-    static_assert(kChunks * 16 * kConvThreads == (CB ? kBBytes : kABytes), "the converters cover the slot");
+    static_assert(kChunksA == 8 && (!kCvtB || (kChunksB * 16 * kConvThreads == kBBytes && kChunksB <= 8)),
+                  "the converters cover the slots, at most 8 chunks a thread");
     static_assert(kDynSmem <= 227 * 1024, "fits one CTA's shared memory");
 };
 
@@ -116,18 +130,21 @@ __device__ __forceinline__ uint32_t half2_bits(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// src: the operand the converters round (A for CONVERT_A, B for CONVERT_B), f32 row-major
-// (A: M x K, B: K x N).  tm_stg: its f32 tensor map for the staging ring (src_mode kSrcTma).
-// tm_f16: the other operand's K-major f16 tensor map (B: N x Kp for CONVERT_A, A: M x Kp for
-// CONVERT_B).  With ksplit > 1 the items are (tile, k slice) pairs and each writes its slice's
-// partial products (alpha = 1, beta = 0) to plane `slice` of `partial` (M x N f32 each).
-template <int BN, int STAGES, int STG, bool CB>
+// A (M x K) and B (K x N): the f32 operands, row-major.  tm_a32 / tm_b32: the tensor maps
+// of the converted ones for the staging ring (src_mode kSrcTma); a_vec: A's rows start on 16
+// bytes (loads from global memory).  tm_f16: the other operand's K-major f16 tensor map (B:
+// N x Kp for CONVERT_A, A: M x Kp for CONVERT_B; unused when both are converted).  With
+// ksplit > 1 the items are (tile, k slice) pairs and each writes its slice's partial products
+// (alpha = 1, beta = 0) to plane `slice` of `partial` (M x N f32 each).
+template <int BN, int STAGES, int STG, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
-gemm_f16cvt_kernel(const float* __restrict__ src, const __grid_constant__ CUtensorMap tm_stg,
+gemm_f16cvt_kernel(const float* __restrict__ A, const float* __restrict__ B,
+                   const __grid_constant__ CUtensorMap tm_a32, const __grid_constant__ CUtensorMap tm_b32,
                    const __grid_constant__ CUtensorMap tm_f16, float* __restrict__ C, int M, int N, int K,
                    int num_kb, float alpha, float beta, int tiles_m, int tiles_n, unsigned int* status,
-                   int src_mode, int ksplit, int kb_per_slice, float* __restrict__ partial) {
-    using L = CvtLayout<BN, STAGES, STG, CB>;
+                   int src_mode, int a_vec, int ksplit, int kb_per_slice, float* __restrict__ partial) {
+    using L = CvtLayout<BN, STAGES, STG, MODE>;
+    constexpr bool kCvtA = L::kCvtA, kCvtB = L::kCvtB;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -167,10 +184,12 @@ gemm_f16cvt_kernel(const float* __restrict__ src, const __grid_constant__ CUtens
     };
 
     if (warp == kProducerWarp && lane == 0) {
-        tma_prefetch_desc(&tm_f16);
-        if (staged) tma_prefetch_desc(&tm_stg);
+        if (MODE != kModeAB) tma_prefetch_desc(&tm_f16);
+        if (staged && kCvtA) tma_prefetch_desc(&tm_a32);
+        if (staged && kCvtB) tma_prefetch_desc(&tm_b32);
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full_bar(s), 1 + kConvWarps);  // the producer's expect_tx + the converters
+            // the converters, and the producer's expect_tx for the other operand's f16 tile
+            mbar_init(full_bar(s), (MODE == kModeAB ? 0 : 1) + kConvWarps);
             mbar_init(empty_bar(s), 1);
         }
         for (int s = 0; s < STG; ++s) {
@@ -198,41 +217,44 @@ gemm_f16cvt_kernel(const float* __restrict__ src, const __grid_constant__ CUtens
             uint32_t stage = 0, phase = 0, sstage = 0, sphase = 0;
             bool ok = true;
             bool pass_done = false;  // the rounding pass has been waited for
+            (void)pass_done;
             for (int w = blockIdx.x; w < num_items && ok; w += gridDim.x) {
                 const Item it = decode(w);
                 for (int kb = it.kb0; kb < it.kb0 + it.nkb; ++kb) {
                     if (staged) {
-                        // the converted operand does not depend on the rounding pass: its
+                        // the converted operands do not depend on the rounding pass: their
                         // first loads go out before the wait for that pass
                         if (!mbar_wait(sempty_bar(sstage), sphase ^ 1u, abort_flag, status)) { ok = false; break; }
                         PHX_DCHECK(sstage < STG && it.pm < tiles_m && it.pn < tiles_n && kb < num_kb);
                         mbar_arrive_expect_tx(sfull_bar(sstage), L::kStgBytes);
-                        if constexpr (CB)
-                            tma_load_2d(sStg + sstage * L::kStgBytes, &tm_stg, it.pn * BN, kb * kBK, sfull_bar(sstage));
-                        else
-                            tma_load_2d(sStg + sstage * L::kStgBytes, &tm_stg, kb * kBK, it.pm * kBM, sfull_bar(sstage));
+                        const uint32_t slot = sStg + sstage * L::kStgBytes;
+                        if constexpr (kCvtA) tma_load_2d(slot, &tm_a32, kb * kBK, it.pm * kBM, sfull_bar(sstage));
+                        if constexpr (kCvtB)
+                            tma_load_2d(slot + L::kStgA, &tm_b32, it.pn * BN, kb * kBK, sfull_bar(sstage));
                         sissued_mask |= 1u << sstage;
                         sissued_phase = (sissued_phase & ~(1u << sstage)) | (sphase << sstage);
                         if (++sstage == STG) { sstage = 0; sphase ^= 1u; }
                     }
-                    if (!pass_done) {
-                        // the other operand comes from the rounding pass just before this
-                        // kernel, which may still be running
-                        asm volatile("griddepcontrol.wait;" ::: "memory");
-                        pass_done = true;
+                    if constexpr (MODE != kModeAB) {
+                        if (!pass_done) {
+                            // the other operand comes from the rounding pass just before this
+                            // kernel, which may still be running
+                            asm volatile("griddepcontrol.wait;" ::: "memory");
+                            pass_done = true;
+                        }
+                        if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, status)) { ok = false; break; }
+                        PHX_DCHECK(stage < STAGES);
+                        if constexpr (MODE == kModeB) {
+                            mbar_arrive_expect_tx(full_bar(stage), L::kABytes);
+                            tma_load_2d(sA + stage * L::kABytes, &tm_f16, kb * kBK, it.pm * kBM, full_bar(stage));
+                        } else {
+                            mbar_arrive_expect_tx(full_bar(stage), L::kBBytes);
+                            tma_load_2d(sB + stage * L::kBBytes, &tm_f16, kb * kBK, it.pn * BN, full_bar(stage));
+                        }
+                        issued_mask |= 1u << stage;
+                        issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                     }
-                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, status)) { ok = false; break; }
-                    PHX_DCHECK(stage < STAGES);
-                    if constexpr (CB) {
-                        mbar_arrive_expect_tx(full_bar(stage), L::kABytes);
-                        tma_load_2d(sA + stage * L::kABytes, &tm_f16, kb * kBK, it.pm * kBM, full_bar(stage));
-                    } else {
-                        mbar_arrive_expect_tx(full_bar(stage), L::kBBytes);
-                        tma_load_2d(sB + stage * L::kBBytes, &tm_f16, kb * kBK, it.pn * BN, full_bar(stage));
-                    }
-                    issued_mask |= 1u << stage;
-                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
-                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
             }
             if (!ok) {
@@ -245,65 +267,67 @@ gemm_f16cvt_kernel(const float* __restrict__ src, const __grid_constant__ CUtens
         }
     } else if (warp >= kFirstConvWarp) {
         const int ct = threadIdx.x - 32 * kFirstConvWarp;  // 0 .. 127
-        // chunk i of this thread: row r_i of the converted slot (a row of A, or one n of B),
-        // and its 16-byte chunk c_i (8 consecutive k).
+        // Chunk i of this thread in each converted slot: row r (a row of A, or one n of B) and
+        // 16-byte chunk c (8 consecutive k).
         //   A: warp w owns rows 32w .. 32w+31; lane takes chunk lane % 8 of rows 4i + lane / 8.
         //   B: chunk id ct + 128 i: n = id % TILE_N, chunk = id / TILE_N, so the 32 lanes of a
         //      warp read 32 consecutive n of one staged k row (one 128-byte line).
-        auto row_of = [&](int i) {
-            if constexpr (CB) return (ct + kConvThreads * i) % BN;
-            else return (ct / 32) * 32 + 4 * i + (lane >> 3);
-        };
-        auto chunk_of = [&](int i) {
-            if constexpr (CB) return (ct + kConvThreads * i) / BN;
-            else return lane & 7;
+        auto a_row = [&](int i) { return (ct / 32) * 32 + 4 * i + (lane >> 3); };
+        auto a_chunk = [&](int) { return lane & 7; };
+        auto b_row = [&](int i) { return (ct + kConvThreads * i) % BN; };
+        auto b_chunk = [&](int i) { return (ct + kConvThreads * i) / BN; };
+        // round chunk i (8 floats) to f16 and store it at chunk c ^ (r % 8) of row r of the slot
+        auto store1 = [&](uint8_t* slot, const float (&x)[8], int r, int c) {
+            uint4 h;
+            h.x = half2_bits(x[0], x[1]);
+            h.y = half2_bits(x[2], x[3]);
+            h.z = half2_bits(x[4], x[5]);
+            h.w = half2_bits(x[6], x[7]);
+            PHX_DCHECK(r < 256 && c < 8);
+            *reinterpret_cast<uint4*>(slot + r * 128 + ((c ^ (r & 7)) << 4)) = h;
         };
         uint32_t stage = 0, phase = 0, sstage = 0, sphase = 0;
         bool ok = true;
         for (int w = blockIdx.x; w < num_items && ok; w += gridDim.x) {
             const Item it = decode(w);
             for (int kb = it.kb0; kb < it.kb0 + it.nkb; ++kb) {
-                float v[L::kChunks][8];
+                float v[8][8];
+                const float* stg = nullptr;
                 if (staged) {
-                    // the f32 box (zeros past the edges) from the staging slot, then the slot
-                    // goes back to the producer
+                    // the f32 boxes (zeros past the edges) of the staging slot
                     if (!__all_sync(0xffffffffu, mbar_wait(sfull_bar(sstage), sphase, abort_flag, status))) {
                         ok = false;
                         break;
                     }
-                    const float* stg = reinterpret_cast<const float*>(base_ptr + L::kStg + sstage * L::kStgBytes);
+                    stg = reinterpret_cast<const float*>(base_ptr + L::kStg + sstage * L::kStgBytes);
+                }
+                // the staging slot goes back to the producer once this warp has read it all
+                auto release = [&] {
+                    if (!staged) return;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(sempty_bar(sstage));
+                    if (++sstage == STG) { sstage = 0; sphase ^= 1u; }
+                };
+                bool slot_free = false;  // the MMA ring's slot has been waited for
+                auto wait_slot = [&] {
+                    if (slot_free) return true;
+                    slot_free = __all_sync(0xffffffffu, mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, status));
+                    return slot_free;
+                };
+                if constexpr (kCvtA) {
 #pragma unroll
-                    for (int i = 0; i < L::kChunks; ++i) {
-                        const int r = row_of(i), c = chunk_of(i);
-                        if constexpr (CB) {
-                            // column r of the 64 x TILE_N box, k rows 8c .. 8c+7
-#pragma unroll
-                            for (int q = 0; q < 8; ++q) v[i][q] = stg[(8 * c + q) * BN + r];
-                        } else {
+                    for (int i = 0; i < L::kChunksA; ++i) {
+                        const int r = a_row(i), c = a_chunk(i);
+                        if (staged) {
                             const float4 x = *reinterpret_cast<const float4*>(stg + r * kBK + c * 8);
                             const float4 y = *reinterpret_cast<const float4*>(stg + r * kBK + c * 8 + 4);
                             v[i][0] = x.x; v[i][1] = x.y; v[i][2] = x.z; v[i][3] = x.w;
                             v[i][4] = y.x; v[i][5] = y.y; v[i][6] = y.z; v[i][7] = y.w;
-                        }
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(sempty_bar(sstage));
-                    if (++sstage == STG) { sstage = 0; sphase ^= 1u; }
-                } else {
-                    // straight from global memory, all chunks' loads in flight together
-#pragma unroll
-                    for (int i = 0; i < L::kChunks; ++i) {
-                        const int r = row_of(i), c = chunk_of(i);
-                        const int k = kb * kBK + c * 8;
-                        if constexpr (CB) {
-                            const int64_t n = static_cast<int64_t>(it.pn) * BN + r;
-#pragma unroll
-                            for (int q = 0; q < 8; ++q)
-                                v[i][q] = (n < N && k + q < K) ? __ldg(src + static_cast<int64_t>(k + q) * N + n) : 0.f;
                         } else {
+                            const int k = kb * kBK + c * 8;
                             const int64_t grow = static_cast<int64_t>(it.pm) * kBM + r;
-                            const float* p = src + grow * K + k;
-                            if (grow < M && src_mode == kSrcVector && k + 8 <= K) {
+                            const float* p = A + grow * K + k;
+                            if (grow < M && a_vec && k + 8 <= K) {
                                 const float4 x = ld_stream4(p);
                                 const float4 y = ld_stream4(p + 4);
                                 v[i][0] = x.x; v[i][1] = x.y; v[i][2] = x.z; v[i][3] = x.w;
@@ -314,22 +338,34 @@ gemm_f16cvt_kernel(const float* __restrict__ src, const __grid_constant__ CUtens
                             }
                         }
                     }
-                }
-                if (!__all_sync(0xffffffffu, mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, status))) {
-                    ok = false;
-                    break;
-                }
-                uint8_t* slot = base_ptr + (CB ? L::kB + stage * L::kBBytes : L::kA + stage * L::kABytes);
+                    if (!kCvtB) release();
+                    if (!wait_slot()) { ok = false; break; }
 #pragma unroll
-                for (int i = 0; i < L::kChunks; ++i) {
-                    const int r = row_of(i), c = chunk_of(i);
-                    uint4 h;
-                    h.x = half2_bits(v[i][0], v[i][1]);
-                    h.y = half2_bits(v[i][2], v[i][3]);
-                    h.z = half2_bits(v[i][4], v[i][5]);
-                    h.w = half2_bits(v[i][6], v[i][7]);
-                    PHX_DCHECK(r < (CB ? BN : kBM) && c < 8);
-                    *reinterpret_cast<uint4*>(slot + r * 128 + ((c ^ (r & 7)) << 4)) = h;
+                    for (int i = 0; i < L::kChunksA; ++i)
+                        store1(base_ptr + L::kA + stage * L::kABytes, v[i], a_row(i), a_chunk(i));
+                }
+                if constexpr (kCvtB) {
+#pragma unroll
+                    for (int i = 0; i < L::kChunksB; ++i) {
+                        const int r = b_row(i), c = b_chunk(i);
+                        if (staged) {
+                            // column r of the 64 x TILE_N box, k rows 8c .. 8c+7
+                            const float* sb = stg + L::kStgA / 4;
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) v[i][q] = sb[(8 * c + q) * BN + r];
+                        } else {
+                            const int k = kb * kBK + c * 8;
+                            const int64_t n = static_cast<int64_t>(it.pn) * BN + r;
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                v[i][q] = (n < N && k + q < K) ? __ldg(B + static_cast<int64_t>(k + q) * N + n) : 0.f;
+                        }
+                    }
+                    release();
+                    if (!wait_slot()) { ok = false; break; }
+#pragma unroll
+                    for (int i = 0; i < L::kChunksB; ++i)
+                        store1(base_ptr + L::kB + stage * L::kBBytes, v[i], b_row(i), b_chunk(i));
                 }
                 // the stores become visible to the tensor cores' reads of the slot
                 fence_proxy_async_smem();
@@ -474,41 +510,45 @@ gemm_f16cvt_kernel(const float* __restrict__ src, const __grid_constant__ CUtens
     }
 }
 
-using CvtKernelFn = void (*)(const float*, CUtensorMap, CUtensorMap, float*, int, int, int, int, float, float,
-                             int, int, unsigned int*, int, int, int, float*);
+using CvtKernelFn = void (*)(const float*, const float*, CUtensorMap, CUtensorMap, CUtensorMap, float*, int, int, int,
+                             int, float, float, int, int, unsigned int*, int, int, int, int, float*);
 
 struct CvtEntry {
     F16Config cfg;
+    int mode;
     CvtKernelFn fn;
     uint32_t smem;
 };
 
-template <int BN, int STAGES, int STG, bool CB>
+template <int BN, int STAGES, int STG, int MODE>
 CvtEntry make_cvt_entry() {
-    return CvtEntry{F16Config{kBM, BN, kBK, STAGES, 1, CB ? 0 : 1, CB ? 1 : 0}, &gemm_f16cvt_kernel<BN, STAGES, STG, CB>,
-                    CvtLayout<BN, STAGES, STG, CB>::kDynSmem};
+    return CvtEntry{F16Config{kBM, BN, kBK, STAGES, 1, MODE != kModeB ? 1 : 0, MODE != kModeA ? 1 : 0}, MODE,
+                    &gemm_f16cvt_kernel<BN, STAGES, STG, MODE>, CvtLayout<BN, STAGES, STG, MODE>::kDynSmem};
 }
 
 // CONVERT_A: at each width 96 KB of MMA ring (4 slots of 24 KB, 3 of 32 KB, 2 of 48 KB) and
 // 96 KB of f32 staging (3 k blocks of A in flight per SM).  CONVERT_B: the same at TILE_N = 64
-// (3 staged k blocks of B are 48 KB) and 128 (96 KB).
+// (3 staged k blocks of B are 48 KB) and 128 (96 KB).  Both: 2 staging slots of A and B
+// (96 KB at TILE_N = 64, 128 KB at 128) and 3 or 2 MMA slots.
 const CvtEntry kCvtEntries[] = {
-    make_cvt_entry<64, 4, 3, false>(),
-    make_cvt_entry<128, 3, 3, false>(),
-    make_cvt_entry<256, 2, 3, false>(),
-    make_cvt_entry<64, 4, 3, true>(),
-    make_cvt_entry<128, 3, 3, true>(),
+    make_cvt_entry<64, 4, 3, kModeA>(),
+    make_cvt_entry<128, 3, 3, kModeA>(),
+    make_cvt_entry<256, 2, 3, kModeA>(),
+    make_cvt_entry<64, 4, 3, kModeB>(),
+    make_cvt_entry<128, 3, 3, kModeB>(),
+    make_cvt_entry<64, 3, 2, kModeAB>(),
+    make_cvt_entry<128, 2, 2, kModeAB>(),
 };
 constexpr int kNumCvt = sizeof(kCvtEntries) / sizeof(kCvtEntries[0]);
 
 constexpr int kCvtMaxSplit = 8;
 constexpr int kCvtMinKbPerSlice = 8;
 
-// K blocks per slice for CONVERT_B: enough slices to give every SM an item when the tiles
-// alone do not (at most 8, at least 8 k blocks each); num_kb when not split.
+// K blocks per slice when B is rounded here: enough slices to give every SM an item when the
+// tiles alone do not (at most 8, at least 8 k blocks each); num_kb when not split.
 int cvt_kb_per_slice(const CvtEntry& e, int64_t M, int64_t N, int64_t K, int num_sms) {
     const int64_t num_kb = (K + kBK - 1) / kBK;
-    if (!e.cfg.convert_b) return static_cast<int>(num_kb);
+    if (e.mode == kModeA) return static_cast<int>(num_kb);
     const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + e.cfg.tile_n - 1) / e.cfg.tile_n);
     if (tiles <= 0 || 2 * tiles > num_sms) return static_cast<int>(num_kb);
     int64_t split = num_sms / tiles;
@@ -539,13 +579,15 @@ cudaError_t f16cvt_gemm_launch(int index, int64_t M, int64_t N, int64_t K, float
                                void* split_ws, unsigned int* status, int num_sms, cudaStream_t stream) {
     if (index < 0 || index >= kNumCvt || M <= 0 || N <= 0 || K <= 0 || num_sms <= 0) return cudaErrorInvalidValue;
     const CvtEntry& e = kCvtEntries[index];
-    const bool cb = e.cfg.convert_b != 0;
     const int bn = e.cfg.tile_n;
     const int64_t Kp = (K + 7) / 8 * 8;
     if (M > 0x7FFFFFFF || N > 0x7FFFFFFF || K > 0x7FFFFFFF) return cudaErrorInvalidValue;
     // the f16 operand from the rounding pass: B (N x Kp) for CONVERT_A, A (M x Kp) for CONVERT_B
     CUtensorMap map_f16;
-    if (!f16_operand_map(&map_f16, other, cb ? M : N, Kp, cb ? kBM : bn, ld_other)) return cudaErrorInvalidValue;
+    std::memset(&map_f16, 0, sizeof map_f16);
+    if (e.mode != kModeAB &&
+        !f16_operand_map(&map_f16, other, e.mode == kModeB ? M : N, Kp, e.mode == kModeB ? kBM : bn, ld_other))
+        return cudaErrorInvalidValue;
     const int64_t tiles_m = (M + kBM - 1) / kBM;
     const int64_t tiles_n = (N + bn - 1) / bn;
     const int64_t num_kb64 = (K + kBK - 1) / kBK;
@@ -555,21 +597,25 @@ cudaError_t f16cvt_gemm_launch(int index, int64_t M, int64_t N, int64_t K, float
     const int64_t items = tiles_m * tiles_n * ksplit;
     if (items > 0x7FFFFFFF) return cudaErrorInvalidValue;
     const int grid = static_cast<int>(items < num_sms ? items : num_sms);
-    // the converted operand through the TMA staging ring when its rows can be a tensor map
-    // (16-byte aligned rows and base); else the converters load it themselves
-    const float* src = cb ? B : A;
-    const int64_t src_cols = cb ? N : K;
-    const bool al = (src_cols % 4 == 0) && ((reinterpret_cast<uintptr_t>(src) & 15u) == 0);
-    CUtensorMap map_stg;
-    std::memset(&map_stg, 0, sizeof map_stg);
-    int src_mode = (al && !cb) ? kSrcVector : kSrcScalar;
-    if (al && (cb ? f32_rows_map(&map_stg, B, K, N, bn, kBK) : f32_rows_map(&map_stg, A, M, K, kBK, kBM)))
-        src_mode = kSrcTma;
+    // the converted operands through the TMA staging ring when their rows can be tensor maps
+    // (16-byte aligned rows and bases, all of them); else the converters load them themselves
+    auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    const bool cvt_a = e.mode != kModeB, cvt_b = e.mode != kModeA;
+    const bool a_al = K % 4 == 0 && al16(A), b_al = N % 4 == 0 && al16(B);
+    CUtensorMap map_a32, map_b32;
+    std::memset(&map_a32, 0, sizeof map_a32);
+    std::memset(&map_b32, 0, sizeof map_b32);
+    bool tma = (!cvt_a || a_al) && (!cvt_b || b_al);
+    if (tma && cvt_a) tma = f32_rows_map(&map_a32, A, M, K, kBK, kBM);
+    if (tma && cvt_b) tma = f32_rows_map(&map_b32, B, K, N, bn, kBK);
+    const int src_mode = tma ? kSrcTma : kSrcGlobal;
+    const int a_vec = a_al ? 1 : 0;
     float* partial = ksplit > 1 ? static_cast<float*>(split_ws) : nullptr;
     cudaError_t err = set_func_attr_once(reinterpret_cast<const void*>(e.fn),
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(e.smem));
     if (err != cudaSuccess) return err;
-    // a programmatic dependent of the rounding pass (see the top of this file)
+    // with one operand from the rounding pass, a programmatic dependent of that pass (see the
+    // top of this file)
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(static_cast<unsigned>(grid));
     lc.blockDim = dim3(kThreads);
@@ -579,18 +625,18 @@ cudaError_t f16cvt_gemm_launch(int index, int64_t M, int64_t N, int64_t K, float
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     lc.attrs = attr;
-    lc.numAttrs = 1;
+    lc.numAttrs = e.mode == kModeAB ? 0 : 1;
     const int m32 = static_cast<int>(M), n32 = static_cast<int>(N), k32 = static_cast<int>(K);
     const int tm32 = static_cast<int>(tiles_m), tn32 = static_cast<int>(tiles_n), nkb = static_cast<int>(num_kb64);
     const int ks32 = static_cast<int>(ksplit);
-    err = cudaLaunchKernelEx(&lc, e.fn, src, map_stg, map_f16, C, m32, n32, k32, nkb, alpha, beta, tm32, tn32, status,
-                             src_mode, ks32, kb_per, partial);
-    if (err != cudaSuccess) {
+    err = cudaLaunchKernelEx(&lc, e.fn, A, B, map_a32, map_b32, map_f16, C, m32, n32, k32, nkb, alpha, beta, tm32,
+                             tn32, status, src_mode, a_vec, ks32, kb_per, partial);
+    if (err != cudaSuccess && lc.numAttrs > 0) {
         // a stream that does not take programmatic launches: launch normally
         cudaGetLastError();
         lc.numAttrs = 0;
-        err = cudaLaunchKernelEx(&lc, e.fn, src, map_stg, map_f16, C, m32, n32, k32, nkb, alpha, beta, tm32, tn32,
-                                 status, src_mode, ks32, kb_per, partial);
+        err = cudaLaunchKernelEx(&lc, e.fn, A, B, map_a32, map_b32, map_f16, C, m32, n32, k32, nkb, alpha, beta,
+                                 tm32, tn32, status, src_mode, a_vec, ks32, kb_per, partial);
     }
     err = launched(err);
     if (err != cudaSuccess || ksplit == 1) return err;

@@ -244,8 +244,8 @@ std::string config_name(int variant, int i) {
         const F16Config& c = phx::f16tc_config(i);
         // a 256-row tile is a 2-SM pair; a 128-row tile one CTA; CONVERT_A=1 / CONVERT_B=1 the
         // kernel that rounds A / B itself
-        std::snprintf(buf, sizeof buf, "TILE_M=%d TILE_N=%d TILE_K=%d STAGES=%d%s", c.tile_m, c.tile_n,
-                      c.tile_k, c.stages, c.convert_a ? " CONVERT_A=1" : c.convert_b ? " CONVERT_B=1" : "");
+        std::snprintf(buf, sizeof buf, "TILE_M=%d TILE_N=%d TILE_K=%d STAGES=%d%s%s", c.tile_m, c.tile_n,
+                      c.tile_k, c.stages, c.convert_a ? " CONVERT_A=1" : "", c.convert_b ? " CONVERT_B=1" : "");
     }
     return buf;
 }
@@ -379,6 +379,7 @@ struct DefaultConfigs {
     int t256x256 = -1, t128x256 = -1, t128x128 = -1, t128x64 = -1;  // f16 tensor cores
     int c64 = -1, c128 = -1, c256 = -1;  // f16, A rounded in the kernel, TILE_N = 64, 128, 256
     int cb64 = -1, cb128 = -1;           // f16, B rounded in the kernel, TILE_N = 64, 128
+    int cab64 = -1;                      // f16, both rounded in the kernel, TILE_N = 64
 };
 
 const DefaultConfigs& default_configs() {
@@ -396,6 +397,7 @@ const DefaultConfigs& default_configs() {
         c.c256 = parse_config(PHX_VARIANT_F16TC, "TILE_M=128 TILE_N=256 TILE_K=64 STAGES=2 CONVERT_A=1");
         c.cb64 = parse_config(PHX_VARIANT_F16TC, "TILE_M=128 TILE_N=64 TILE_K=64 STAGES=4 CONVERT_B=1");
         c.cb128 = parse_config(PHX_VARIANT_F16TC, "TILE_M=128 TILE_N=128 TILE_K=64 STAGES=3 CONVERT_B=1");
+        c.cab64 = parse_config(PHX_VARIANT_F16TC, "TILE_M=128 TILE_N=64 TILE_K=64 STAGES=3 CONVERT_A=1 CONVERT_B=1");
         return c;
     }();
     return d;
@@ -434,6 +436,12 @@ int default_tile_config(int variant, int64_t M, int64_t N, int64_t K, int sms, b
     // for the best tile of the other kernel, (64, 8192, 8192) 55 against 105; with a small B,
     // (64, 1024, 1024), 16.6 against 12.7.
     if (convert && f16_convert_b_fits(M, N, K)) return dc.cb128;
+    // Tiny problems (2^25 multiply-adds or fewer): both operands rounded in the kernel, one
+    // launch and no scratch (measured on GB300, synced calls: 256^3 15.5 us against 17.3 for
+    // the rounding pass and the 128 x 128 tile; even at 512^3, slower from 768^3 on, where
+    // every tile rounding its own A and B boxes costs more than one pass).
+    if (convert && static_cast<double>(M) * static_cast<double>(N) * static_cast<double>(K) <= 33554432.0)
+        return dc.cab64;
     if (M >= 256 && N >= 256) {
         // the 2-SM 256 x 256 tile when it fills the CTA pairs, or when a grid too small for
         // the GPU is split along K (32 or more k blocks of 64); else the one-CTA tile that gives more
@@ -754,16 +762,17 @@ phx_status launch_variant(int variant, int cfg, int64_t M, int64_t N, int64_t K,
         if (ws != nullptr) cudaFreeAsync(ws, stream);
         return err == cudaSuccess ? PHX_OK : PHX_ERR_LAUNCH;
     }
-    // one pooled block holds the call's scratch (phx::f16tc_run_bytes)
+    // one pooled block holds the call's scratch (phx::f16tc_run_bytes; none for the kernel
+    // that rounds both operands without a split)
+    const size_t bytes = phx::f16tc_run_bytes(cfg, M, N, K, d->sm_count);
     void* ws = nullptr;
-    if (cudaMallocFromPoolAsync(&ws, phx::f16tc_run_bytes(cfg, M, N, K, d->sm_count), d->pool, stream) !=
-        cudaSuccess) {
+    if (bytes > 0 && cudaMallocFromPoolAsync(&ws, bytes, d->pool, stream) != cudaSuccess) {
         cudaGetLastError();
         return PHX_ERR_NOMEM;
     }
     const cudaError_t err = phx::f16tc_run(cfg, trans_a, trans_b, M, N, K, alpha, A, B, beta, C, ws, d->status,
                                            d->sm_count, stream);
-    cudaFreeAsync(ws, stream);
+    if (ws != nullptr) cudaFreeAsync(ws, stream);
     return err == cudaSuccess ? PHX_OK : PHX_ERR_LAUNCH;
 }
 
@@ -888,8 +897,9 @@ phx_status copy_name(const std::string& s, char* buf, size_t buflen) {
 namespace phx {
 size_t f16tc_run_bytes(int cfg, int64_t M, int64_t N, int64_t K, int num_sms) {
     const int64_t Kp = (K + 7) / 8 * 8;
-    // the kernel that rounds A itself: only B's f16 copy; B itself: A's copy, then the
-    // partial planes of a split along K
+    // the kernel that rounds both itself: only the partial planes of a split along K; A
+    // itself: only B's f16 copy; B itself: A's copy, then the planes
+    if (f16tc_is_convert_a(cfg) && f16tc_is_convert_b(cfg)) return f16tc_split_bytes(cfg, M, N, K, num_sms);
     if (f16tc_is_convert_a(cfg)) return static_cast<size_t>((N * Kp * 2 + 255) / 256 * 256);
     if (f16tc_is_convert_b(cfg))
         return static_cast<size_t>((M * Kp * 2 + 255) / 256 * 256) + f16tc_split_bytes(cfg, M, N, K, num_sms);
@@ -905,9 +915,18 @@ cudaError_t f16tc_run(int cfg, int trans_a, int trans_b, int64_t M, int64_t N, i
         // The other operand's f16 copy at the start of ws (B as N x Kp, or A as M x Kp), the
         // partial planes of a split after it, then the GEMM that rounds its operand as it
         // reads it (stored M x K for A, K x N for B: not transposed)
-        const bool cb = f16tc_is_convert_b(cfg);
-        if (cb ? trans_b : trans_a) return cudaErrorInvalidValue;
+        const bool ca = f16tc_is_convert_a(cfg), cb = f16tc_is_convert_b(cfg);
+        if ((ca && trans_a) || (cb && trans_b)) return cudaErrorInvalidValue;
         const int64_t Kp = (K + 7) / 8 * 8;
+        const int ci = cfg - (f16tc_num_configs() - f16cvt_num_configs());
+        if (ca && cb) {
+            // both rounded in the kernel: one launch, scratch only for a split's planes
+            void* split = f16tc_split_bytes(cfg, M, N, K, num_sms) > 0 ? ws : nullptr;
+            return timed(kKindTcGemm, stream, [&] {
+                return f16cvt_gemm_launch(ci, M, N, K, alpha, beta, C, A, B, nullptr, 0, split, status, num_sms,
+                                          stream);
+            });
+        }
         __half* other = static_cast<__half*>(ws);
         void* split = cb && f16tc_split_bytes(cfg, M, N, K, num_sms) > 0
                           ? static_cast<char*>(ws) + (M * Kp * 2 + 255) / 256 * 256
@@ -918,8 +937,8 @@ cudaError_t f16tc_run(int cfg, int trans_a, int trans_b, int64_t M, int64_t N, i
         });
         if (err == cudaSuccess)
             err = timed(kKindTcGemm, stream, [&] {
-                return f16cvt_gemm_launch(cfg - (f16tc_num_configs() - f16cvt_num_configs()), M, N, K, alpha, beta,
-                                          C, A, B, other, Kp, split, status, num_sms, stream);
+                return f16cvt_gemm_launch(ci, M, N, K, alpha, beta, C, A, B, other, Kp, split, status, num_sms,
+                                          stream);
             });
         return err;
     }

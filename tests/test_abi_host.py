@@ -119,6 +119,7 @@ def test_default_config_follows_grid_size():
     assert phx.get_config(phx.VARIANT_SGEMM, 768, 768, 768) != "SKINNY"
     assert phx.get_config(phx.VARIANT_SGEMM, 1024, 1024, 1024).startswith("TILE_M=128 TILE_N=128")
     assert phx.get_config(phx.VARIANT_F16TC, 512, 512, 512).startswith("TILE_M=128 TILE_N=128")
+    assert phx.get_config(phx.VARIANT_F16TC, 256, 256, 256).endswith(" CONVERT_A=1 CONVERT_B=1")
     assert phx.get_config(phx.VARIANT_F16TC, 1024, 1024, 1024).startswith("TILE_M=128 TILE_N=128")
     assert phx.get_config(phx.VARIANT_F16TC, 2048, 2048, 2048).startswith("TILE_M=128 TILE_N=256")
     # ... but a grid split along K keeps the 2-SM tile

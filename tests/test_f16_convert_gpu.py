@@ -18,8 +18,10 @@ from tests.gpu_util import assert_bits_equal, assert_within_bound
 
 pytestmark = pytest.mark.gpu
 
-CVT = [n for n in phx.config_names(phx.VARIANT_F16TC) if "CONVERT_A=1" in n]
-CVTB = [n for n in phx.config_names(phx.VARIANT_F16TC) if "CONVERT_B=1" in n]
+_NAMES = phx.config_names(phx.VARIANT_F16TC)
+CVT = [n for n in _NAMES if "CONVERT_A=1" in n and "CONVERT_B=1" not in n]      # A rounded here
+CVTB = [n for n in _NAMES if "CONVERT_B=1" in n and "CONVERT_A=1" not in n]     # B rounded here
+CVTAB = [n for n in _NAMES if "CONVERT_A=1" in n and "CONVERT_B=1" in n]        # both
 
 
 @pytest.fixture(autouse=True)
@@ -76,11 +78,21 @@ SHAPES_B = [
 ]
 
 
-@pytest.mark.parametrize("cfg", CVT + CVTB)
+SHAPES_AB = [
+    (300, 200, 700, 1.5, 0.5),     # ragged in every dimension
+    (256, 256, 4096, 1.0, 0.5),    # 4 tiles: K split into 8 slices of partial planes
+    (257, 130, 130, 2.0, -1.0),    # K % 4 != 0: A's rows not on 16 bytes; N % 4 != 0
+    (5, 7, 3, 1.0, 0.5),           # smaller than a tile in every dimension
+    (1024, 1024, 1024, 1.0, 0.0),  # a whole wave of tiles, beta = 0
+]
+
+
+@pytest.mark.parametrize("cfg", CVT + CVTB + CVTAB)
 @pytest.mark.parametrize("dist", ["int3", "uniform"])
 def test_matches_the_oracle(cfg, dist):
     phx.set_config(phx.VARIANT_F16TC, cfg)
-    for i, (M, N, K, alpha, beta) in enumerate(SHAPES if cfg in CVT else SHAPES_B):
+    shapes = SHAPES if cfg in CVT else SHAPES_B if cfg in CVTB else SHAPES_AB
+    for i, (M, N, K, alpha, beta) in enumerate(shapes):
         A, B, C = synth.problem(M, N, K, seed=40 + i, dist=dist)
         want, mag = oracle.gemm(A, B, C, alpha, beta, f16_inputs=True)
         st, got = _run(A, B, C, alpha, beta)
@@ -170,6 +182,44 @@ def test_b_rounded_in_the_kernel_same_bits_as_the_tma_kernel(tile_n, stages):
     st, cvt = _run(A, B, C, 1.25, -0.5)
     assert st == phx.PHX_OK and "CONVERT_B=1" in phx.last_config(phx.VARIANT_F16TC)
     assert_bits_equal(cvt, tma, f"TILE_N={tile_n}: B rounded in the kernel vs by the pass")
+
+
+@pytest.mark.parametrize("cfg", CVTAB)
+def test_both_rounded_unaligned_and_transposed(cfg):
+    phx.set_config(phx.VARIANT_F16TC, cfg)
+    M, N, K = 300, 264, 516
+    A, B, C = synth.problem(M, N, K, seed=9, dist="int3")
+    want, _ = oracle.gemm(A, B, C, 1.0, 0.5, f16_inputs=True)
+    # either operand off 16 bytes: no tensor maps, the converters load both themselves
+    for a_off, b_off in ((1, 0), (0, 1)):
+        st, got = _run(A, B, C, 1.0, 0.5, a_offset=a_off, b_offset=b_off)
+        assert st == phx.PHX_OK
+        assert phx.last_config(phx.VARIANT_F16TC) == cfg
+        assert_bits_equal(got, want, f"[{cfg}] offsets {a_off}, {b_off}")
+    # an operand stored transposed takes the kernels without this one
+    for op_a, op_b in ((phx.OP_T, phx.OP_N), (phx.OP_N, phx.OP_T)):
+        st, got = _run(A, B, C, 1.0, 0.5, op_a=op_a, op_b=op_b)
+        assert st == phx.PHX_OK
+        assert "CONVERT" not in phx.last_config(phx.VARIANT_F16TC)
+        assert_bits_equal(got, want, f"[{cfg}] ops {op_a}, {op_b}")
+
+
+@pytest.mark.parametrize("tile_n,stages", [(64, 8), (128, 6)])
+def test_both_rounded_same_bits_as_the_tma_kernel(tile_n, stages):
+    # 152 tiles of 128 x TILE_N, one whole wave, K short enough not to split
+    import torch
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("the single-wave shape is sized for 152 SMs")
+    M, N, K = 8 * 128, 19 * tile_n, 512
+    A, B, C = synth.problem(M, N, K, seed=6, dist="uniform")
+    base = f"TILE_M=128 TILE_N={tile_n} TILE_K=64 STAGES={stages}"
+    phx.set_config(phx.VARIANT_F16TC, base)
+    st, tma = _run(A, B, C, 1.25, -0.5)
+    assert st == phx.PHX_OK and phx.last_config(phx.VARIANT_F16TC) == base
+    phx.set_config(phx.VARIANT_F16TC, f"TILE_M=128 TILE_N={tile_n} TILE_K=64 CONVERT_A=1 CONVERT_B=1")
+    st, cvt = _run(A, B, C, 1.25, -0.5)
+    assert st == phx.PHX_OK and "CONVERT_A=1 CONVERT_B=1" in phx.last_config(phx.VARIANT_F16TC)
+    assert_bits_equal(cvt, tma, f"TILE_N={tile_n}: both rounded in the kernel vs by the pass")
 
 
 def test_default_routes_few_rows_here():
