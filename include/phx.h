@@ -249,8 +249,9 @@ phx_status phx_profile_stop(int64_t* launches, double* ms);
  * pass; it is the default where N <= 256 and A has 128-row tiles for at least half the SMs.
  * One ending in "CONVERT_B=1" (TILE_M=128, TILE_N 64 or 128) rounds B itself the same way
  * (and splits K when its tiles cannot fill the SMs); it is the default for M <= 256, N >= 1024
- * and K * N >= 2^23.  Both compute the same rounded products, summed in f32 in the same order
- * per tile.  An operand they round given transposed (op_a or op_b = PHX_OP_T), and the
+ * and K * N >= 2^23.  One ending in "CONVERT_A=1 CONVERT_B=1" rounds both operands itself: one
+ * launch, no rounding pass (the default for at most 2^25 multiply-adds).  All of them compute
+ * the same rounded products, summed in f32 in the same order per tile.  An operand they round given transposed (op_a or op_b = PHX_OP_T), and the
  * half-precision entry points, take the default without them instead.  The last configuration of
  * each variant, "SKINNY", is the kernel for few rows of A (the lab's skinny-matrix sweep,
  * Part 5): B is streamed once from HBM with 16-byte loads and the products are summed with
