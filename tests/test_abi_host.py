@@ -106,7 +106,7 @@ def test_default_config_follows_grid_size():
     skinny = phx.get_config(phx.VARIANT_SGEMM, 64, 4096, 4096)
     assert big.startswith("TILE_M=128 TILE_N=128")
     assert small.startswith("TILE_M=128 TILE_N=128")   # a small grid is split along K instead
-    assert skinny.startswith("TILE_M=64 TILE_N=64")
+    assert skinny.startswith("TILE_M=64 TILE_N=128")
     assert phx.get_config(phx.VARIANT_F16TC, 4096, 4096, 4096).startswith("TILE_M=256 TILE_N=256")
     # small problems: smaller tiles give more SMs work (152 SMs assumed without a GPU)
     assert phx.get_config(phx.VARIANT_SGEMM, 512, 512, 1024).startswith("TILE_M=128 TILE_N=64 TILE_K=8 ")
@@ -117,6 +117,9 @@ def test_default_config_follows_grid_size():
     assert phx.get_config(phx.VARIANT_SGEMM, 64, 2048, 2048) == "SKINNY"
     assert phx.get_config(phx.VARIANT_SGEMM, 64, 4096, 4096) != "SKINNY"
     assert phx.get_config(phx.VARIANT_SGEMM, 768, 768, 768) != "SKINNY"
+    # fewer than 128 rows, many columns: 64 x 128 tiles up to 64 rows, 128 x 128 above
+    assert phx.get_config(phx.VARIANT_SGEMM, 64, 4096, 4096).startswith("TILE_M=64 TILE_N=128 TILE_K=16 ")
+    assert phx.get_config(phx.VARIANT_SGEMM, 96, 4096, 4096).startswith("TILE_M=128 TILE_N=128 TILE_K=16 ")
     assert phx.get_config(phx.VARIANT_SGEMM, 1024, 1024, 1024).startswith("TILE_M=128 TILE_N=128")
     assert phx.get_config(phx.VARIANT_F16TC, 512, 512, 512).startswith("TILE_M=128 TILE_N=128")
     assert phx.get_config(phx.VARIANT_F16TC, 256, 256, 256).endswith(" CONVERT_A=1 CONVERT_B=1")
