@@ -375,7 +375,7 @@ int default_config(int variant, int64_t M, int64_t N, int64_t K, int sms, bool c
 // The compiled configurations the defaults name, resolved once (parsing a name per call
 // would cost a microsecond of host time).
 struct DefaultConfigs {
-    int s128x128 = -1, s128x64 = -1, s64x64 = -1, s64x128 = -1;  // f32
+    int s128x128 = -1, s128x64 = -1, s64x64 = -1, s64x128 = -1, s128x64f2 = -1;  // f32
     int t256x256 = -1, t128x256 = -1, t128x128 = -1, t128x64 = -1;  // f16 tensor cores
     int c64 = -1, c128 = -1, c256 = -1;  // f16, A rounded in the kernel, TILE_N = 64, 128, 256
     int cb64 = -1, cb128 = -1;           // f16, B rounded in the kernel, TILE_N = 64, 128
@@ -389,6 +389,7 @@ const DefaultConfigs& default_configs() {
         c.s128x64 = parse_config(PHX_VARIANT_SGEMM, "TILE_M=128 TILE_N=64 TILE_K=8 STAGES=4");
         c.s64x64 = parse_config(PHX_VARIANT_SGEMM, "TILE_M=64 TILE_N=64 TILE_K=8 STAGES=4");
         c.s64x128 = parse_config(PHX_VARIANT_SGEMM, "TILE_M=64 TILE_N=128 TILE_K=16 STAGES=4 FMA2=1");
+        c.s128x64f2 = parse_config(PHX_VARIANT_SGEMM, "TILE_M=128 TILE_N=64 TILE_K=16 STAGES=4 FMA2=1");
         c.t256x256 = parse_config(PHX_VARIANT_F16TC, "TILE_M=256 TILE_N=256 TILE_K=64 STAGES=6");
         c.t128x256 = parse_config(PHX_VARIANT_F16TC, "TILE_M=128 TILE_N=256 TILE_K=64 STAGES=4");
         c.t128x128 = parse_config(PHX_VARIANT_F16TC, "TILE_M=128 TILE_N=128 TILE_K=64 STAGES=6");
@@ -426,6 +427,10 @@ int default_tile_config(int variant, int64_t M, int64_t N, int64_t K, int sms, b
         // tiles below (measured on GB300, queued calls, K = N = 4096: M = 96 98.9 us against
         // 134.5 with 64 x 64 tiles; M = 64 62.4 against 74.5; (64, 8192, 4096) 104 against 141)
         if (N >= 128) return M > 64 ? dc.s128x128 : dc.s64x128;
+        // ... and the same across: 128 rows or more against fewer than 128 columns ((4096, 64,
+        // 4096) 64.0 us against 74.5; (4096, 96, 4096) 99.0 against 137.9; (8192, 32, 4096)
+        // 108.3 against 138.3)
+        if (M >= 128) return N > 64 ? dc.s128x128 : dc.s128x64f2;
         if (ceil_div(M, 128) * ceil_div(N, 128) >= slots) return dc.s128x128;
         if (ceil_div(M, 128) * ceil_div(N, 64) >= slots) return dc.s128x64;
         return dc.s64x64;

@@ -120,6 +120,8 @@ def test_default_config_follows_grid_size():
     # fewer than 128 rows, many columns: 64 x 128 tiles up to 64 rows, 128 x 128 above
     assert phx.get_config(phx.VARIANT_SGEMM, 64, 4096, 4096).startswith("TILE_M=64 TILE_N=128 TILE_K=16 ")
     assert phx.get_config(phx.VARIANT_SGEMM, 96, 4096, 4096).startswith("TILE_M=128 TILE_N=128 TILE_K=16 ")
+    assert phx.get_config(phx.VARIANT_SGEMM, 4096, 64, 4096).startswith("TILE_M=128 TILE_N=64 TILE_K=16 ")
+    assert phx.get_config(phx.VARIANT_SGEMM, 4096, 96, 4096).startswith("TILE_M=128 TILE_N=128 TILE_K=16 ")
     assert phx.get_config(phx.VARIANT_SGEMM, 1024, 1024, 1024).startswith("TILE_M=128 TILE_N=128")
     assert phx.get_config(phx.VARIANT_F16TC, 512, 512, 512).startswith("TILE_M=128 TILE_N=128")
     assert phx.get_config(phx.VARIANT_F16TC, 256, 256, 256).endswith(" CONVERT_A=1 CONVERT_B=1")
