@@ -544,11 +544,10 @@ constexpr int kNumCvt = sizeof(kCvtEntries) / sizeof(kCvtEntries[0]);
 constexpr int kCvtMaxSplit = 8;
 constexpr int kCvtMinKbPerSlice = 8;
 
-// K blocks per slice when B is rounded here: enough slices to give every SM an item when the
-// tiles alone do not (at most 8, at least 8 k blocks each); num_kb when not split.
+// K blocks per slice: enough slices to give every SM an item when the tiles alone do not (at
+// most 8, at least 8 k blocks each); num_kb when not split.
 int cvt_kb_per_slice(const CvtEntry& e, int64_t M, int64_t N, int64_t K, int num_sms) {
     const int64_t num_kb = (K + kBK - 1) / kBK;
-    if (e.mode == kModeA) return static_cast<int>(num_kb);
     const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + e.cfg.tile_n - 1) / e.cfg.tile_n);
     if (tiles <= 0 || 2 * tiles > num_sms) return static_cast<int>(num_kb);
     int64_t split = num_sms / tiles;

@@ -437,8 +437,11 @@ int default_tile_config(int variant, int64_t M, int64_t N, int64_t K, int sms, b
     }
     // Few columns, many rows: A is most of the bytes, and rounding it inside the GEMM saves
     // writing and reading back its f16 copy.  One tile of N, and 128-row tiles for at least
-    // half the SMs (fewer rows leave SMs idle; the other kernel splits such grids along K).
-    if (convert && N <= 256 && ceil_div(M, 128) >= sms / 2)
+    // half the SMs, or 2048 rows or more with K long enough to split (the kernel then splits
+    // K to give every SM work).  Measured on GB300, queued calls: (4096, 128, 4096) 25.1 us
+    // against 33.1 for the other kernel, (8192, 128, 4096) 42.2 against 53.7, (2048, 128,
+    // 4096) 19.0 against 20.9.
+    if (convert && N <= 256 && (ceil_div(M, 128) >= sms / 2 || (M >= 2048 && K >= 1024)))
         return N <= 64 ? dc.c64 : N <= 128 ? dc.c128 : dc.c256;
     // Few rows, a large B (2^23 elements or more): B is most of the bytes; the kernel rounds
     // B itself, and splits K to give every SM work.  (Few enough rows take the skinny kernel
@@ -907,10 +910,11 @@ phx_status copy_name(const std::string& s, char* buf, size_t buflen) {
 namespace phx {
 size_t f16tc_run_bytes(int cfg, int64_t M, int64_t N, int64_t K, int num_sms) {
     const int64_t Kp = (K + 7) / 8 * 8;
-    // the kernel that rounds both itself: only the partial planes of a split along K; A
-    // itself: only B's f16 copy; B itself: A's copy, then the planes
+    // the kernel that rounds both itself: only the partial planes of a split along K; A (B)
+    // itself: B's (A's) f16 copy, then the planes
     if (f16tc_is_convert_a(cfg) && f16tc_is_convert_b(cfg)) return f16tc_split_bytes(cfg, M, N, K, num_sms);
-    if (f16tc_is_convert_a(cfg)) return static_cast<size_t>((N * Kp * 2 + 255) / 256 * 256);
+    if (f16tc_is_convert_a(cfg))
+        return static_cast<size_t>((N * Kp * 2 + 255) / 256 * 256) + f16tc_split_bytes(cfg, M, N, K, num_sms);
     if (f16tc_is_convert_b(cfg))
         return static_cast<size_t>((M * Kp * 2 + 255) / 256 * 256) + f16tc_split_bytes(cfg, M, N, K, num_sms);
     // the f16 operand copies, then (for a grid split along K) the partial products of the
@@ -938,8 +942,9 @@ cudaError_t f16tc_run(int cfg, int trans_a, int trans_b, int64_t M, int64_t N, i
             });
         }
         __half* other = static_cast<__half*>(ws);
-        void* split = cb && f16tc_split_bytes(cfg, M, N, K, num_sms) > 0
-                          ? static_cast<char*>(ws) + (M * Kp * 2 + 255) / 256 * 256
+        // the partial planes of a split follow the other operand's copy (A's, or B's)
+        void* split = f16tc_split_bytes(cfg, M, N, K, num_sms) > 0
+                          ? static_cast<char*>(ws) + ((cb ? M : N) * Kp * 2 + 255) / 256 * 256
                           : nullptr;
         cudaError_t err = timed(kKindCast, stream, [&] {
             return cb ? f16tc_prepare_launch(0, trans_a, 0, M, N, K, A, B, other, nullptr, num_sms, stream)

@@ -134,7 +134,9 @@ def test_default_config_follows_grid_size():
         cfg = phx.get_config(phx.VARIANT_F16TC, 16384, n, 4096)
         assert cfg.startswith(f"TILE_M=128 TILE_N={tile_n} ") and cfg.endswith(" CONVERT_A=1"), (n, cfg)
     assert "CONVERT_A" not in phx.get_config(phx.VARIANT_F16TC, 16384, 257, 4096)
-    assert "CONVERT_A" not in phx.get_config(phx.VARIANT_F16TC, 4096, 128, 4096)   # rows for 32 SMs only
+    assert phx.get_config(phx.VARIANT_F16TC, 4096, 128, 4096).endswith(" CONVERT_A=1")  # K split
+    assert "CONVERT_A" not in phx.get_config(phx.VARIANT_F16TC, 4096, 128, 512)   # too short to split
+    assert "CONVERT_A" not in phx.get_config(phx.VARIANT_F16TC, 1024, 128, 4096)  # too few rows
     # few rows, many columns: the kernel that rounds B itself (up to 16 rows: the skinny kernel)
     for m in (9, 16, 17, 64, 256):
         assert phx.get_config(phx.VARIANT_F16TC, m, 4096, 4096).endswith(" CONVERT_B=1")
