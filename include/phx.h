@@ -95,10 +95,12 @@ phx_status phx_sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float* 
 /* f16 tensor cores with f32 accumulation ("gemm on tensor cores", section "What
  * changes"): every element of A and B is rounded to the nearest f16 (ties to even), the
  * f16 x f16 products are summed in f32 by tcgen05.mma into tensor memory, and the
- * epilogue computes alpha * acc + beta * c_old in f32.  The rounded operands go to a
- * workspace of phx_f16tc_workspace_bytes(M, N, K) bytes taken, in stream order, from a
- * memory pool the library owns for the current device, and returned to it after the
- * GEMM (PHX_ERR_NOMEM if that fails). */
+ * epilogue computes alpha * acc + beta * c_old in f32.  The call's scratch -- the f16 copies
+ * the rounding pass writes (at most phx_f16tc_workspace_bytes(M, N, K) bytes; none of an
+ * operand the chosen configuration rounds itself) and, for a grid split along K, slices x
+ * M x N x 4 bytes of f32 partial products -- is taken, in stream order, from a memory pool
+ * the library owns for the current device, and returned to it after the GEMM
+ * (PHX_ERR_NOMEM if that fails). */
 phx_status phx_gemm_f16tc_f32acc(int64_t M, int64_t N, int64_t K, float alpha,
                                  const float* A, const float* B, float beta, float* C,
                                  phx_stream_t stream);
@@ -179,9 +181,12 @@ phx_status phx_gemm_f16in_f16out(phx_op op_a, phx_op op_b, int64_t M, int64_t N,
                                  float alpha, const phx_f16* A, const phx_f16* B, float beta,
                                  phx_f16* C, phx_stream_t stream);
 
-/* Workspace bytes phx_gemm_f16tc_f32acc takes for this shape: the rounded A (M rows) and
- * the rounded, transposed B (N rows), each row padded with zeros to a multiple of 8
- * halves. */
+/* Bytes of the f16 copies the rounding pass of phx_gemm_f16tc_f32acc writes for this shape
+ * when it rounds both operands: the rounded A (M rows) and the rounded, transposed B (N
+ * rows), each row padded with zeros to a multiple of 8 halves, each part rounded up to 256
+ * bytes.  That is the whole scratch of a call that neither splits K nor rounds an operand
+ * inside the GEMM, and a bound on the copies of any call; a split along K takes its partial
+ * products besides. */
 phx_status phx_f16tc_workspace_bytes(int64_t M, int64_t N, int64_t K, size_t* bytes);
 
 /* ---------------------------------------------------------------------------------------
