@@ -437,11 +437,13 @@ int default_tile_config(int variant, int64_t M, int64_t N, int64_t K, int sms, b
     }
     // Few columns, many rows: A is most of the bytes, and rounding it inside the GEMM saves
     // writing and reading back its f16 copy.  One tile of N, and 128-row tiles for at least
-    // half the SMs, or 2048 rows or more with K long enough to split (the kernel then splits
-    // K to give every SM work).  Measured on GB300, queued calls: (4096, 128, 4096) 25.1 us
-    // against 33.1 for the other kernel, (8192, 128, 4096) 42.2 against 53.7, (2048, 128,
-    // 4096) 19.0 against 20.9.
-    if (convert && N <= 256 && (ceil_div(M, 128) >= sms / 2 || (M >= 2048 && K >= 1024)))
+    // half the SMs; or fewer row tiles, with K split to give every SM work, where the copy
+    // saved outweighs the split's extra launch and planes: A of 2^23 elements or more, and
+    // K >= 2048.  Measured on GB300, queued calls: (4096, 128, 4096) 25.1 us against 33.1 for
+    // the other kernel, (8192, 128, 4096) 42.2 against 53.7, (2048, 128, 4096) 19.0 against
+    // 20.9, (8192, 64, 2048) 22.9 against 27.9; but (4096, 128, 1024) 18.7 against about 13.
+    if (convert && N <= 256 &&
+        (ceil_div(M, 128) >= sms / 2 || (M >= 1024 && K >= 2048 && M * K >= (int64_t(1) << 23))))
         return N <= 64 ? dc.c64 : N <= 128 ? dc.c128 : dc.c256;
     // Few rows, a large B (2^23 elements or more): B is most of the bytes; the kernel rounds
     // B itself, and splits K to give every SM work.  (Few enough rows take the skinny kernel

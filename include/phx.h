@@ -252,7 +252,7 @@ phx_status phx_profile_stop(int64_t* launches, double* ms);
  * ending in "CONVERT_A=1" (TILE_M=128, TILE_N 64, 128 or 256) is the kernel that rounds A to
  * f16 itself as it stages A's f32 tiles, so that only B goes through the separate rounding
  * pass; it is the default where N <= 256 and A has 128-row tiles for at least half the SMs, or
- * 2048 rows or more with K >= 1024 (K is then split to give every SM work).
+ * M >= 1024, K >= 2048 and M * K >= 2^23 (K is then split to give every SM work).
  * One ending in "CONVERT_B=1" (TILE_M=128, TILE_N 64 or 128) rounds B itself the same way
  * (and splits K when its tiles cannot fill the SMs); it is the default for M <= 256, N >= 1024
  * and K * N >= 2^23.  One ending in "CONVERT_A=1 CONVERT_B=1" rounds both operands itself: one

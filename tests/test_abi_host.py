@@ -135,7 +135,9 @@ def test_default_config_follows_grid_size():
         assert cfg.startswith(f"TILE_M=128 TILE_N={tile_n} ") and cfg.endswith(" CONVERT_A=1"), (n, cfg)
     assert "CONVERT_A" not in phx.get_config(phx.VARIANT_F16TC, 16384, 257, 4096)
     assert phx.get_config(phx.VARIANT_F16TC, 4096, 128, 4096).endswith(" CONVERT_A=1")  # K split
-    assert "CONVERT_A" not in phx.get_config(phx.VARIANT_F16TC, 4096, 128, 512)   # too short to split
+    assert "CONVERT_A" not in phx.get_config(phx.VARIANT_F16TC, 4096, 128, 1024)  # too short to split
+    assert phx.get_config(phx.VARIANT_F16TC, 8192, 64, 2048).endswith(" CONVERT_A=1")
+    assert "CONVERT_A" not in phx.get_config(phx.VARIANT_F16TC, 2048, 128, 2048)  # A below 2^23
     assert "CONVERT_A" not in phx.get_config(phx.VARIANT_F16TC, 1024, 128, 4096)  # too few rows
     # few rows, many columns: the kernel that rounds B itself (up to 16 rows: the skinny kernel)
     for m in (9, 16, 17, 64, 256):

@@ -252,16 +252,17 @@ def test_default_routes_tall_narrow_problems_here():
 
 
 def test_default_routes_fewer_rows_split_k_here():
-    # (2085, 96, 1100): 17 row tiles, too few for the SMs; the kernel that rounds A splits K
-    # (18 k blocks: 2 slices) into partial planes.  Whole result, bit for bit on integers.
-    M, N, K = 2085, 96, 1100
+    # (2085, 96, 4100): 17 row tiles, too few for the SMs; the kernel that rounds A splits K
+    # (65 k blocks: 8 slices of 9, the last of 2) into partial planes.  Whole result, bit for
+    # bit on integers.
+    M, N, K = 2085, 96, 4100
     assert phx.get_config(phx.VARIANT_F16TC, M, N, K).endswith(" CONVERT_A=1")
     A, B, C = synth.problem(M, N, K, seed=17, dist="int3")
     want, _ = oracle.gemm(A, B, C, 2.0, -1.0, f16_inputs=True)
     st, got = _run(A, B, C, 2.0, -1.0)
     assert st == phx.PHX_OK
     assert phx.last_config(phx.VARIANT_F16TC).endswith(" CONVERT_A=1")
-    assert_bits_equal(got, want, "(2085, 96, 1100)")
+    assert_bits_equal(got, want, "(2085, 96, 4100)")
 
 
 def test_f16_operand_entry_points_take_the_tma_kernel():
