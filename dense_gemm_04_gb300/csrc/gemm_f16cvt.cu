@@ -217,7 +217,7 @@ gemm_f16cvt_kernel(const float* __restrict__ A, const float* __restrict__ B,
             uint32_t stage = 0, phase = 0, sstage = 0, sphase = 0;
             bool ok = true;
             bool pass_done = false;  // the rounding pass has been waited for
-            (void)pass_done;
+            (void)pass_done;         // (unused when both operands are rounded here)
             for (int w = blockIdx.x; w < num_items && ok; w += gridDim.x) {
                 const Item it = decode(w);
                 for (int kb = it.kb0; kb < it.kb0 + it.nkb; ++kb) {
