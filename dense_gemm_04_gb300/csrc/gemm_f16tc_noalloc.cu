@@ -124,10 +124,12 @@ extern "C" phx_status phx_gemm_f16tc_f32acc_noalloc(int64_t M, int64_t N, int64_
     unsigned int* status_word = reinterpret_cast<unsigned int*>(d->base);
     void* workspace = d->base + kStatusBytes;
     if (phx::is_skinny_config(PHX_VARIANT_F16TC, cfg)) {
-        // few rows of A: no rounded copies; the scratch holds the K slices' partial sums
-        if (phx::skinny_workspace_bytes(1, M, N, K, B, d->sm_count) > kNoAllocScratchBytes) return PHX_ERR_NOMEM;
-        return phx::skinny_launch(1, 0, M, N, K, alpha, A, B, beta, C, workspace, d->sm_count, stream) ==
-                       cudaSuccess
+        // few rows of A (or few columns): no rounded copies; the scratch holds the K slices'
+        // partial sums
+        if (phx::skinny_run_bytes(PHX_VARIANT_F16TC, 0, 0, M, N, K, A, B, d->sm_count) > kNoAllocScratchBytes)
+            return PHX_ERR_NOMEM;
+        return phx::skinny_run(PHX_VARIANT_F16TC, 0, 0, M, N, K, alpha, A, B, beta, C, workspace, d->sm_count,
+                               stream) == cudaSuccess
                    ? PHX_OK : PHX_ERR_LAUNCH;
     }
     // the same scratch layout and kernels as the pooled entry point (split-K planes included),

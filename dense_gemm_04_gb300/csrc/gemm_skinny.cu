@@ -385,6 +385,9 @@ bool skinny_plan(int f16, int64_t M, int64_t N, int64_t K, const float* B, int n
 //     one lane) and the A values in place once they land (all warps use them).
 //   - The K slices of a tile are added through distributed shared memory in rank order, as
 //     in the kernel above, or, past 8 slices, through partial planes.
+//   - out_t: C (and the partial planes) stored transposed, N x M: output (m, n) at n * M + m.
+//     With it the kernel also serves few columns against many rows: C = A @ B is
+//     C^T = B^T @ A^T, a few-row product whose W is A itself, stored M x K.
 // ---------------------------------------------------------------------------------------
 constexpr int kNtRows = 32;    // rows of W (output columns) per CTA
 constexpr int kNtKc = 128;     // k per chunk
@@ -399,7 +402,8 @@ __host__ __device__ constexpr size_t nt_smem(int mt) {
 template <int MT, bool F16, bool VEC>
 __global__ void __launch_bounds__(kSkThreads, 2) skinny_nt_kernel(
     const float* __restrict__ A, const float* __restrict__ W, float* __restrict__ C, float* __restrict__ partial,
-    int M, int N, int K, int k_cta, int cs, int mchunks, int strips, int a_trans, float alpha, float beta) {
+    int M, int N, int K, int k_cta, int cs, int mchunks, int strips, int a_trans, int out_t, float alpha,
+    float beta) {
     constexpr int S = kNtStages;
     // A stored M x K with rows on 16-byte boundaries (the host passes a_trans = 2 for that)
     const bool a_vec = a_trans == 2;
@@ -558,7 +562,7 @@ __global__ void __launch_bounds__(kSkThreads, 2) skinny_nt_kernel(
         const int mm = m0 + m, n = n0 + cidx;
         if (mm >= M || n >= N) continue;
         PHX_DCHECK(m < MT && cs <= 8);
-        const int64_t idx = static_cast<int64_t>(mm) * N + n;
+        const int64_t idx = out_t ? static_cast<int64_t>(n) * M + mm : static_cast<int64_t>(mm) * N + n;
         if (partial != nullptr)
             partial[static_cast<int64_t>(blockIdx.y) * M * N + idx] = v;
         else
@@ -568,7 +572,7 @@ __global__ void __launch_bounds__(kSkThreads, 2) skinny_nt_kernel(
 }
 
 using SkinnyNtFn = void (*)(const float*, const float*, float*, float*, int, int, int, int, int, int, int, int,
-                            float, float);
+                            int, float, float);
 
 template <int MT, bool F16>
 SkinnyNtFn pick_nt_vec(bool vec) {
@@ -659,7 +663,7 @@ size_t skinny_nt_workspace_bytes(int f16, int64_t M, int64_t N, int64_t K, const
 
 cudaError_t skinny_nt_launch(int f16, int a_trans, int64_t M, int64_t N, int64_t K, float alpha,
                              const float* A, const float* W, float beta, float* C, void* workspace,
-                             int num_sms, cudaStream_t stream) {
+                             int num_sms, cudaStream_t stream, int out_t) {
     SkinnyNtPlan p;
     if (!skinny_nt_plan(f16, M, N, K, W, num_sms, &p)) return cudaErrorInvalidValue;
     if (p.planes > 1 && workspace == nullptr) return cudaErrorInvalidValue;
@@ -679,8 +683,8 @@ cudaError_t skinny_nt_launch(int f16, int a_trans, int64_t M, int64_t N, int64_t
     // a_trans = 2: A stored M x K with 16-byte aligned rows, copied 16 bytes at a time
     const int a_mode = a_trans ? 1 : (K % 4 == 0 && (reinterpret_cast<uintptr_t>(A) & 15u) == 0) ? 2 : 0;
     cudaError_t err = cudaLaunchKernelEx(&cfg, p.fn, A, W, C, partial, static_cast<int>(M), static_cast<int>(N),
-                                         static_cast<int>(K), p.k_cta, p.cs, p.mchunks, p.strips, a_mode, alpha,
-                                         beta);
+                                         static_cast<int>(K), p.k_cta, p.cs, p.mchunks, p.strips, a_mode,
+                                         out_t ? 1 : 0, alpha, beta);
     err = launched(err);
     if (err != cudaSuccess || p.planes == 1) return err;
     return splitk_reduce_launch(partial, p.planes, M, N, alpha, beta, C, num_sms, stream);

@@ -127,10 +127,11 @@ cudaError_t skinny_launch(int f16, int a_trans, int64_t M, int64_t N, int64_t K,
                           int num_sms, cudaStream_t stream);
 
 // The same with B stored transposed as W (N x K): C <- alpha * op(A) @ W^T + beta * C.
+// out_t: C stored transposed (N x M, output (m, n) at n * M + m).
 size_t skinny_nt_workspace_bytes(int f16, int64_t M, int64_t N, int64_t K, const float* W, int num_sms);
 cudaError_t skinny_nt_launch(int f16, int a_trans, int64_t M, int64_t N, int64_t K, float alpha,
                              const float* A, const float* W, float beta, float* C, void* workspace,
-                             int num_sms, cudaStream_t stream);
+                             int num_sms, cudaStream_t stream, int out_t = 0);
 
 // C <- beta * C (beta == 0: C <- 0 without reading C).  Used for K == 0 or alpha == 0.
 cudaError_t scale_c_launch(int64_t M, int64_t N, float beta, float* C, cudaStream_t stream);
@@ -236,6 +237,14 @@ cudaError_t noalloc_take_status(unsigned int* word);
 // PHX_CONFIG_* environment pin does not parse (the call then returns PHX_ERR_CONFIG).
 constexpr int kBadConfigPin = -2;
 int choose_config_for(int variant, int64_t M, int64_t N, int64_t K, int sms);
+// The skinny configuration's scratch and launch for a call (phx_api.cu): few rows of op(A),
+// or few columns with A stored M x K (the transposed product on the kernel that streams
+// rows).  f16 variant: both operands rounded to f16 as they are loaded.
+size_t skinny_run_bytes(int variant, int trans_a, int trans_b, int64_t M, int64_t N, int64_t K, const float* A,
+                        const float* B, int num_sms);
+cudaError_t skinny_run(int variant, int trans_a, int trans_b, int64_t M, int64_t N, int64_t K, float alpha,
+                       const float* A, const float* B, float beta, float* C, void* ws, int num_sms,
+                       cudaStream_t stream);
 
 // True if configuration `cfg` of `variant` is the skinny kernel rather than a GEMM tile.
 bool is_skinny_config(int variant, int cfg);

@@ -233,6 +233,14 @@ int skinny_index(int variant) { return tile_configs(variant); }
 // f16: 27 against 31 us at M = 16, 47 against 33 at M = 32, where the tensor cores win).
 int64_t skinny_default_max_m(int variant) { return variant == PHX_VARIANT_SGEMM ? 48 : 16; }
 
+// Few columns against many rows, A stored M x K: the skinny kernels run the transposed
+// product, C^T = op(B)^T @ A^T, a few-row product that streams A (each row of A one
+// contiguous row of the operand the kernel streams) and writes C^T transposed, which is C.
+int64_t skinny_columns_max_n(int variant) { return variant == PHX_VARIANT_SGEMM ? 16 : 8; }
+bool skinny_by_columns(int variant, int trans_a, int64_t M, int64_t N) {
+    return !trans_a && M >= 1024 && N < M && N <= skinny_columns_max_n(variant);
+}
+
 std::string config_name(int variant, int i) {
     char buf[128];
     if (i == skinny_index(variant)) return "SKINNY";
@@ -345,7 +353,7 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // work (the trade-off "gemm, f32" section "Tuning" describes: larger tiles reuse more,
 // but leave fewer CTAs to spread over the card).
 int default_tile_config(int variant, int64_t M, int64_t N, int64_t K, int sms, bool convert = true);
-int default_config(int variant, int64_t M, int64_t N, int64_t K, int sms, bool convert = true);
+int default_config(int variant, int64_t M, int64_t N, int64_t K, int sms, bool convert = true, bool a_rows = true);
 
 // The kernel that rounds B itself is the f16 default for few rows and a large B (see
 // default_tile_config); it beats the skinny kernel from about 12 rows (measured on GB300,
@@ -365,9 +373,21 @@ bool sgemm_skinny_fits(int64_t M, int64_t N, int64_t K) {
     return (M <= 512 && mnk <= 134217728.0) || (M <= 64 && kn <= 4194304.0);
 }
 
-int default_config(int variant, int64_t M, int64_t N, int64_t K, int sms, bool convert) {
+// a_rows: A is stored M x K (the skinny kernels' few-columns form needs that).
+int default_config(int variant, int64_t M, int64_t N, int64_t K, int sms, bool convert, bool a_rows) {
     const bool skip_skinny = variant == PHX_VARIANT_F16TC && convert && M > 8 && f16_convert_b_fits(M, N, K);
     if (M <= skinny_default_max_m(variant) && !skip_skinny) return skinny_index(variant);
+    // Few columns, an A of 2^22 elements or more: one pass over A.  For f16, where the kernel
+    // that rounds A inside the GEMM takes over (A of 2^23 elements or more), only up to 4
+    // columns and 4096 rows.  Measured on GB300, queued calls, K = 4096: f32 N = 1 12.4 us
+    // against 88.2 with tiles, N = 8 26.8 against 78.1, N = 16 45.2 against 78.1, (16384, 8,
+    // 4096) 90 against 230; f16 (4096, 1, 4096) 14.5 against 22.7 for the kernel that rounds A,
+    // N = 4 20.6 against 22.6, but N = 8 28.8 against 22.7 and (16384, 8, 4096) 100.7 against
+    // 57.0; (1024, 4, 4096) 10.4 against 18.3 for the kernel that rounds both.
+    const double mk = static_cast<double>(M) * static_cast<double>(K);
+    if (a_rows && skinny_by_columns(variant, 0, M, N) && mk >= 4194304.0 &&
+        (variant == PHX_VARIANT_SGEMM || mk < 8388608.0 || (N <= 4 && M <= 4096)))
+        return skinny_index(variant);
     if (variant == PHX_VARIANT_SGEMM && sgemm_skinny_fits(M, N, K)) return skinny_index(variant);
     return default_tile_config(variant, M, N, K, sms, convert);
 }
@@ -477,14 +497,14 @@ int default_tile_config(int variant, int64_t M, int64_t N, int64_t K, int sms, b
 
 // The configuration for a call: the pin, else the tuned one for this device and shape, else
 // the default; kBadPin when the variant's PHX_CONFIG_* pin does not parse.
-int choose_config(int variant, int64_t M, int64_t N, int64_t K, int sms) {
+int choose_config(int variant, int64_t M, int64_t N, int64_t K, int sms, int trans_a = 0) {
     const std::string tag = device_tag();
     std::lock_guard<std::mutex> lock(g_mu);
     load_env_once_locked();
     if (g_pin[variant] >= 0 || g_pin[variant] == kBadPin) return g_pin[variant];
     auto it = g_tuned.find(ShapeKey(tag, variant, M, N, K));
     if (it != g_tuned.end()) return it->second;
-    return default_config(variant, M, N, K, sms);
+    return default_config(variant, M, N, K, sms, true, !trans_a);
 }
 
 phx_status config_error(int cfg) { return cfg == kBadPin ? PHX_ERR_CONFIG : PHX_ERR_INTERNAL; }
@@ -673,22 +693,17 @@ phx_status launch_sgemm_transposed(int cfg, int trans_a, int trans_b, int64_t M,
                                    float alpha, const float* A, const float* B, float beta, float* C,
                                    DevState* d, cudaStream_t stream);
 
-// The skinny kernels read A in either storage order; B stored transposed (N x K) has a
-// kernel of its own, which streams B's rows.
 phx_status launch_skinny(int variant, int trans_a, int trans_b, int64_t M, int64_t N, int64_t K,
                          float alpha, const float* A, const float* B, float beta, float* C,
                          DevState* d, cudaStream_t stream) {
-    const int f16 = variant == PHX_VARIANT_F16TC ? 1 : 0;
-    const size_t bytes = trans_b ? phx::skinny_nt_workspace_bytes(f16, M, N, K, B, d->sm_count)
-                                 : phx::skinny_workspace_bytes(f16, M, N, K, B, d->sm_count);
+    const size_t bytes = phx::skinny_run_bytes(variant, trans_a, trans_b, M, N, K, A, B, d->sm_count);
     void* ws = nullptr;
     if (bytes > 0 && cudaMallocFromPoolAsync(&ws, bytes, d->pool, stream) != cudaSuccess) {
         cudaGetLastError();
         return PHX_ERR_NOMEM;
     }
     const cudaError_t err = timed(kKindSkinny, stream, [&] {
-        return trans_b ? phx::skinny_nt_launch(f16, trans_a, M, N, K, alpha, A, B, beta, C, ws, d->sm_count, stream)
-                       : phx::skinny_launch(f16, trans_a, M, N, K, alpha, A, B, beta, C, ws, d->sm_count, stream);
+        return phx::skinny_run(variant, trans_a, trans_b, M, N, K, alpha, A, B, beta, C, ws, d->sm_count, stream);
     });
     if (ws != nullptr) cudaFreeAsync(ws, stream);
     return err == cudaSuccess ? PHX_OK : PHX_ERR_LAUNCH;
@@ -753,7 +768,7 @@ phx_status launch_variant(int variant, int cfg, int64_t M, int64_t N, int64_t K,
     // given transposed takes the default without that kernel (the skinny kernel included)
     if (variant == PHX_VARIANT_F16TC &&
         ((trans_a && phx::f16tc_is_convert_a(cfg)) || (trans_b && phx::f16tc_is_convert_b(cfg)))) {
-        cfg = default_config(PHX_VARIANT_F16TC, M, N, K, d->sm_count, false);
+        cfg = default_config(PHX_VARIANT_F16TC, M, N, K, d->sm_count, false, !trans_a);
         g_last_cfg[PHX_VARIANT_F16TC].store(cfg);
     }
     if (cfg == skinny_index(variant))
@@ -832,7 +847,7 @@ phx_status gemm_entry(int variant, int64_t M, int64_t N, int64_t K, float alpha,
                        cudaSuccess
                    ? PHX_OK : PHX_ERR_LAUNCH;
     }
-    const int cfg = choose_config(variant, M, N, K, d->sm_count);
+    const int cfg = choose_config(variant, M, N, K, d->sm_count, trans_a);
     if (cfg < 0) return config_error(cfg);
     g_last_cfg[variant].store(cfg);
     if (log_level() >= 2)
@@ -910,6 +925,31 @@ phx_status copy_name(const std::string& s, char* buf, size_t buflen) {
 }  // namespace
 
 namespace phx {
+// The skinny kernels read A in either storage order; B stored transposed (N x K) has a
+// kernel of its own, which streams B's rows; few columns against many rows, with A stored
+// M x K, run as the transposed product on that kernel, streaming A's rows
+// (skinny_by_columns).
+size_t skinny_run_bytes(int variant, int trans_a, int trans_b, int64_t M, int64_t N, int64_t K, const float* A,
+                        const float* B, int num_sms) {
+    const int f16 = variant == PHX_VARIANT_F16TC ? 1 : 0;
+    if (skinny_by_columns(variant, trans_a, M, N)) return skinny_nt_workspace_bytes(f16, N, M, K, A, num_sms);
+    return trans_b ? skinny_nt_workspace_bytes(f16, M, N, K, B, num_sms)
+                   : skinny_workspace_bytes(f16, M, N, K, B, num_sms);
+}
+
+cudaError_t skinny_run(int variant, int trans_a, int trans_b, int64_t M, int64_t N, int64_t K, float alpha,
+                       const float* A, const float* B, float beta, float* C, void* ws, int num_sms,
+                       cudaStream_t stream) {
+    const int f16 = variant == PHX_VARIANT_F16TC ? 1 : 0;
+    if (skinny_by_columns(variant, trans_a, M, N))
+        // C^T (N x M) = op(B)^T @ A^T: the few rows are op(B)^T, which is B stored transposed
+        // (B stored K x N) or plain (B stored N x K); A (M x K) is the streamed operand; C^T
+        // written transposed is C
+        return skinny_nt_launch(f16, trans_b ? 0 : 1, N, M, K, alpha, B, A, beta, C, ws, num_sms, stream, 1);
+    return trans_b ? skinny_nt_launch(f16, trans_a, M, N, K, alpha, A, B, beta, C, ws, num_sms, stream)
+                   : skinny_launch(f16, trans_a, M, N, K, alpha, A, B, beta, C, ws, num_sms, stream);
+}
+
 size_t f16tc_run_bytes(int cfg, int64_t M, int64_t N, int64_t K, int num_sms) {
     const int64_t Kp = (K + 7) / 8 * 8;
     // the kernel that rounds both itself: only the partial planes of a split along K; A (B)

@@ -1,6 +1,7 @@
 """Shape and arithmetic-intensity sweep of both GEMM precisions, placed on the roofline.
 
-    python -m dense_gemm_04_gb300.sweep [--out results.json] [--quick] [--layouts] [--skinny] [--f16in]
+    python -m dense_gemm_04_gb300.sweep [--out results.json] [--quick] [--layouts] [--skinny] [--narrow]
+        [--f16in]
     python -m dense_gemm_04_gb300.sweep --one M,N,K [--variant sgemm|f16tc|f16in|f16out] [--calls 5]
         [--alpha 1] [--beta 0] [--b-transposed]
 
@@ -286,6 +287,51 @@ def run_skinny(rounds=3, seed=0, seconds=0.3, queue=50, b_transposed=False):
     return rows
 
 
+def run_narrow(rounds=3, seed=0, seconds=0.3, queue=50):
+    """The skinny sweep turned on its side: few columns of B and C.  (M x 4096) @ (4096 x N)
+    for N = 1 .. 2048 at M = 4096, and N = 128 at M = 1024 .. 16384, both precisions,
+    alpha = 1, beta = 0, with the default configuration (for the f16 variant, the kernel that
+    rounds A inside the GEMM where A is most of the bytes).  Timed as run_skinny times: the
+    median over shuffled rounds of `queue` back-to-back calls between two events; the least
+    traffic 4 (MK + KN + MN) bytes gives the bandwidth each call reached."""
+    import torch
+    st = torch.cuda.current_stream().cuda_stream
+    K = 4096
+    shapes = [(4096, n) for n in (1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024, 2048)]
+    shapes += [(m, 128) for m in (1024, 2048, 8192, 16384)]
+    A = {m: torch.rand(m, K, device="cuda") * 2 - 1 for m in sorted({m for m, _ in shapes})}
+    B = {n: torch.rand(K, n, device="cuda") * 2 - 1 for n in sorted({n for _, n in shapes})}
+    Cs = {sh: torch.zeros(*sh, device="cuda") for sh in shapes}
+    cases = [(v, sh) for v in ("sgemm", "f16tc") for sh in shapes]
+    times = {c: [] for c in cases}
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    rng = np.random.default_rng(seed)
+    for _ in range(rounds):
+        for ci in rng.permutation(len(cases)):
+            v, (M, N) = cases[ci]
+            a, b, c = A[M], B[N], Cs[(M, N)]
+            fn = phx.phx_sgemm if v == "sgemm" else phx.phx_gemm_f16tc_f32acc
+            call = lambda: phx.check(fn(M, N, K, 1.0, a.data_ptr(), b.data_ptr(), 0.0, c.data_ptr(), st))
+            t0 = time.perf_counter()
+            while time.perf_counter() - t0 < seconds / 2:
+                call()
+                _sync()
+            ev0.record()
+            for _ in range(queue):
+                call()
+            ev1.record()
+            ev1.synchronize()
+            times[cases[ci]].append(ev0.elapsed_time(ev1) / 1e3 / queue)
+    rows = []
+    for v, (M, N) in cases:
+        t = float(np.median(times[(v, (M, N))]))
+        nbytes = 4.0 * (M * K + K * N + M * N)
+        rows.append({"variant": v, "M": M, "N": N, "K": K, "seconds": t, "tflops": 2.0 * M * N * K / t / 1e12,
+                     "gbs": nbytes / t / 1e9, "intensity": 2.0 * M * N * K / nbytes,
+                     "config": phx.get_config(0 if v == "sgemm" else 1, M, N, K)})
+    return rows
+
+
 def run_f16in(rounds=3, seed=0, seconds=0.5):
     """Half-precision operands against the f32-operand tensor-core path (the lab's Part 4
     precision study: cuBLAS f16 GEMM), squares 2048 .. 8192 with alpha = 1, beta = 0.5:
@@ -354,6 +400,7 @@ def main():
     ap.add_argument("--quick", action="store_true", help="skip shapes above 2^40 MNK and shorten timings")
     ap.add_argument("--layouts", action="store_true", help="time the four storage orders at 4096^3 only")
     ap.add_argument("--skinny", action="store_true", help="time M = 1 .. 2048 rows against K = N = 4096 only")
+    ap.add_argument("--narrow", action="store_true", help="time N = 1 .. 2048 columns against M = K = 4096 only")
     ap.add_argument("--b-transposed", action="store_true", help="with --skinny or --one: B stored N x K")
     ap.add_argument("--f16in", action="store_true", help="time half-precision operands against f32 ones only")
     ap.add_argument("--one", default=None, metavar="M,N,K", help="only run a few calls of this shape (for profilers)")
@@ -383,6 +430,15 @@ def main():
         if args.out:
             with open(args.out, "w") as f:
                 json.dump({"skinny": rows}, f, indent=1)
+        return 0
+    if args.narrow:
+        rows = run_narrow()
+        for row in rows:
+            print(f"{row['variant']:6s} M={row['M']:5d} N={row['N']:5d} {row['seconds'] * 1e6:9.1f} us "
+                  f"{row['tflops']:8.2f} TFLOP/s {row['gbs']:7.0f} GB/s  I={row['intensity']:7.1f}  [{row['config']}]")
+        if args.out:
+            with open(args.out, "w") as f:
+                json.dump({"narrow": rows}, f, indent=1)
         return 0
     if args.layouts:
         rows = run_layouts()

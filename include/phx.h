@@ -266,7 +266,11 @@ phx_status phx_profile_stop(int64_t* launches, double* ms);
  * of 16 rows, and is the default for M <= 48 (f32) and M <= 16 (f16; M <= 8 where B has
  * 2^23 elements or more, N >= 1024, and the kernel that rounds B itself takes over).  For
  * f32 it is also the default for small problems (M <= 512 and M * N * K <= 2^27) and for
- * M <= 64 with K * N <= 2^22.
+ * M <= 64 with K * N <= 2^22.  Few columns against many rows (M >= 1024 and N <= 16 for
+ * f32, N <= 8 for f16), with A stored M x K, it runs as the transposed product
+ * C^T = op(B)^T @ A^T, streaming A once and writing C^T transposed, which is C; that is the
+ * default there when A has 2^22 elements or more (for f16 only up to 4 columns and 4096
+ * rows, or an A below 2^23 elements, where the kernel that rounds A is slower).
  * ------------------------------------------------------------------------------------- */
 
 /* Number of compiled configurations of a variant (or -1 for a bad variant). */

@@ -41,10 +41,12 @@ def main():
     shapes |= {(256, 256, 256), (1024, 1024, 4096), (300, 500, 3000), (2048, 2048, 256), (3000, 2000, 700),
                (8, 4096, 4096), (2, 128, 65536), (40, 1000, 3000), (1031, 1029, 4100), (1030, 1024, 4099),
                (10000, 100, 300), (64, 3000, 2000)}  # few columns / few rows (the kernel that rounds A / B)
+    # few columns against many rows: the skinny kernel on the transposed product (default routes)
+    narrow = [(2085, 7, 2050), (1024, 3, 65536)]
     failures = []
     runs = 0
     for variant, f16 in ((phx.VARIANT_SGEMM, False), (phx.VARIANT_F16TC, True)):
-        for i, (M, N, K) in enumerate(sorted(shapes)):
+        for i, (M, N, K) in enumerate(sorted(shapes) + narrow):
             runs += 1
             if not run(variant, f16, M, N, K, 1.5, 0.5, i):
                 failures.append((variant, M, N, K))

@@ -160,6 +160,17 @@ def test_default_config_follows_grid_size():
     assert phx.get_config(phx.VARIANT_F16TC, 9, 4096, 4096) != "SKINNY"
     assert phx.get_config(phx.VARIANT_F16TC, 16, 2048, 2048) == "SKINNY"
     assert phx.get_config(phx.VARIANT_F16TC, 17, 2048, 2048) != "SKINNY"
+    # few columns against many rows (A of 2^22 elements or more): the skinny kernel, on the
+    # transposed product
+    assert phx.get_config(phx.VARIANT_SGEMM, 4096, 16, 4096) == "SKINNY"
+    assert phx.get_config(phx.VARIANT_SGEMM, 4096, 17, 4096) != "SKINNY"
+    assert phx.get_config(phx.VARIANT_F16TC, 4096, 4, 4096) == "SKINNY"
+    assert phx.get_config(phx.VARIANT_F16TC, 2048, 8, 2048) == "SKINNY"
+    assert phx.get_config(phx.VARIANT_F16TC, 4096, 8, 4096).endswith(" CONVERT_A=1")
+    assert phx.get_config(phx.VARIANT_F16TC, 16384, 4, 4096).endswith(" CONVERT_A=1")
+    assert phx.get_config(phx.VARIANT_SGEMM, 16384, 16, 4096) == "SKINNY"
+    assert phx.get_config(phx.VARIANT_SGEMM, 1000, 4, 8192) != "SKINNY"    # fewer than 1024 rows
+    assert phx.get_config(phx.VARIANT_SGEMM, 4096, 4, 512) != "SKINNY"     # A below 2^22
 
 
 def test_workspace_bytes():

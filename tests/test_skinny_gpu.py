@@ -1,7 +1,9 @@
 """The skinny kernel (few rows of A; the matrix-multiplication lab's skinny-matrix sweep,
 Part 5), both precisions, through the C ABI on a GB300, against the oracle.
 
-It is the default for small M and can be pinned ("SKINNY") for any M.  Covered here: M from
+It is the default for small M, and for few columns against many rows with A stored M x K (as
+the transposed product, streaming A's rows), and can be pinned ("SKINNY") for any M.  Covered
+here: few columns (1 to 8, ragged, long and short K, every storage order); M from
 1 to 64 at the sweep's K = N = 4096 in both precisions; ragged N (scalar loads, partial
 column strips), K shorter than one slice and K split into many slices; A stored transposed
 (read in place); B stored transposed (N x K, the layout of W in x @ W^T: the kernel that
@@ -188,6 +190,60 @@ def test_skinny_is_deterministic(vname):
     _, r1 = run_cuda(variant, A, B, C, 1.0, 0.5)
     _, r2 = run_cuda(variant, A, B, C, 1.0, 0.5)
     assert_bits_equal(r1, r2, "two runs")
+
+
+@pytest.mark.parametrize("vname", list(VARIANTS))
+@pytest.mark.parametrize("shape", [(4096, 1, 4096), (2085, 7, 2050), (1030, 8, 333), (1024, 3, 65536),
+                                   (1500, 5, 3000), (5000, 2, 64)])
+def test_few_columns_transposed_product(vname, shape):
+    # few columns against many rows: C^T = B^T @ A^T on the kernel that streams rows (of A
+    # here), C^T written transposed.  Ragged M and K; K % 4 != 0 (A's rows not on 16 bytes);
+    # K split across a cluster, and into planes at K = 65536; one chunk of K.
+    M, N, K = shape
+    _check(vname, M, N, K, 1.5, 0.5, "int3", seed=31)
+    _check(vname, M, N, K, 2.0, -1.0, "uniform", seed=32)
+    # beta = 0 with NaN in C: C is not read
+    variant, f16 = VARIANTS[vname]
+    A, B, C = synth.problem(M, N, K, seed=33, dist="int3")
+    want, _ = oracle.gemm(A, B, C, 1.0, 0.0, f16_inputs=f16)
+    st, got = run_cuda(variant, A, B, np.full_like(C, np.nan), 1.0, 0.0)
+    assert st == phx.PHX_OK
+    assert_bits_equal(got, want, f"{vname} few columns {shape}, beta = 0")
+
+
+@pytest.mark.parametrize("vname", list(VARIANTS))
+def test_few_columns_storage_orders(vname):
+    # B stored N x K (plain rows of the few-row operand) and A stored at a 4-byte offset (its
+    # rows copied 4 bytes at a time) take the transposed product; A stored K x M takes the
+    # rows of A in blocks of 16 instead.  All against the oracle.
+    variant, f16 = VARIANTS[vname]
+    M, N, K = 1500, 5, 3000
+    A, B, C = synth.problem(M, N, K, seed=34, dist="int3")
+    want, _ = oracle.gemm(A, B, C, 1.0, 0.5, f16_inputs=f16)
+    for op_a, op_b, off in ((phx.OP_N, phx.OP_T, 0), (phx.OP_N, phx.OP_N, 1), (phx.OP_N, phx.OP_T, 1),
+                            (phx.OP_T, phx.OP_N, 0), (phx.OP_T, phx.OP_T, 0)):
+        st, got = _run_ex(variant, op_a, op_b, A, B, C, 1.0, 0.5, offset=off)
+        assert st == phx.PHX_OK, phx.status_string(st)
+        assert_bits_equal(got, want, f"{vname} few columns ops ({op_a},{op_b}) offset {off}")
+
+
+def test_default_routes_few_columns_to_skinny():
+    for v in (phx.VARIANT_SGEMM, phx.VARIANT_F16TC):
+        phx.set_config(v, None)
+    assert phx.get_config(phx.VARIANT_SGEMM, 4096, 16, 4096) == "SKINNY"
+    assert phx.get_config(phx.VARIANT_F16TC, 4096, 4, 4096) == "SKINNY"
+    assert phx.get_config(phx.VARIANT_F16TC, 4096, 8, 4096) != "SKINNY"
+    for vname, n in (("sgemm", 16), ("f16tc", 4)):
+        _check(vname, 4096, n, 4096, 1.0, 0.5, "int3", seed=35)
+        assert phx.last_config(VARIANTS[vname][0]) == "SKINNY"
+    # A stored K x M: the default tile instead
+    variant, f16 = VARIANTS["sgemm"]
+    A, B, C = synth.problem(2048, 4, 2048, seed=36, dist="int3")
+    want, _ = oracle.gemm(A, B, C, 1.0, 0.5, f16_inputs=f16)
+    st, got = _run_ex(variant, phx.OP_T, phx.OP_N, A, B, C, 1.0, 0.5)
+    assert st == phx.PHX_OK
+    assert phx.last_config(variant) != "SKINNY"
+    assert_bits_equal(got, want, "few columns, A stored K x M")
 
 
 def test_default_routes_small_m_to_skinny():

@@ -47,6 +47,7 @@ PROBLEMS = [
     (16384, 128, 1024, 1.0, 0.5, 18),    # few columns: A rounded inside the GEMM, only B's copy in the array
     (64, 4096, 4096, 1.0, 0.5, 19),      # few rows: B rounded inside the GEMM, A's copy and K-split planes
     (2085, 96, 4100, 2.0, -1.0, 20),     # fewer row tiles than SMs: A rounded inside, B's copy and K-split planes
+    (4096, 3, 4096, 1.0, 0.5, 21),       # few columns: the skinny kernel on the transposed product
 ]
 
 
