@@ -18,9 +18,11 @@
 //     boxes (k rows of n) and transposed while it is rounded; A comes from the pass as M x Kp
 //     f16.
 //   CONVERT_A + CONVERT_B: both operands staged and rounded here, no pass at all: one launch,
-//     no scratch (for small problems, where the launches and the pass are most of the time).
-// With B rounded here, a grid of few tiles is split along K into slices that write f32
-// partial planes, added in slice order by a separate reduction.
+//     no scratch unless K is split (for small problems, where the launches and the pass are
+//     most of the time).
+// In every mode, a grid whose tiles cannot give every SM work is split along K (at most 8
+// slices of at least 8 k blocks) into slices that write f32 partial planes, added in slice
+// order by a separate reduction.
 //
 // A persistent kernel, one CTA per SM, 320 threads (10 warps):
 //   warp 4      TMA producer: per 64-deep k block, the f32 box of each converted operand into
