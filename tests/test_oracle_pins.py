@@ -156,7 +156,7 @@ def test_k_zero_scales_c(oracle_mod):
 # ----------------------------------------------------------------------------------------
 
 @pytest.mark.parametrize("shape", [(1, 1, 1), (3, 5, 7), (65, 33, 129), (128, 96, 300),
-                                   (40, 257, 64)])
+                                   (40, 257, 64), (257, 1, 1000), (1, 300, 517)])
 @pytest.mark.parametrize("ab", [(1.5, 0.5), (2.0, -1.0), (1.0, 0.0)])
 @pytest.mark.parametrize("f16", [False, True])
 def test_integer_inputs_exact(oracle_mod, shape, ab, f16):
@@ -210,7 +210,7 @@ def test_brute_force_tiny_shapes_exact_rationals(oracle_mod, f16):
 # GEMM: float64 library matmul on non-square, non-symmetric inputs (catches transposes)
 # ----------------------------------------------------------------------------------------
 
-@pytest.mark.parametrize("shape", [(31, 47, 53), (128, 64, 200), (5, 300, 17)])
+@pytest.mark.parametrize("shape", [(31, 47, 53), (128, 64, 200), (5, 300, 17), (300, 3, 517), (1, 130, 999)])
 def test_matches_numpy_float64(oracle_mod, shape):
     M, N, K = shape
     A, B, C = synth.problem(M, N, K, seed=21)
